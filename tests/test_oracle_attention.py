@@ -1,0 +1,140 @@
+"""Pins of the oracle's attention stage and of the whole decode/prefill step.
+
+Attention: all 64 query heads attend to one 512-wide latent per position used
+as both key and value (miles.radixark.com "DeepSeek-V4.1 Flash", §1
+"Architecture"), over the selected latents and the 128-position window
+(recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse attention"),
+under one softmax.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+
+
+def sdpa(q, kv, tau):
+    qt = torch.from_numpy(q)[None, None]          # [1, 1, H, D]
+    kt = torch.from_numpy(kv)[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, kt, scale=tau)
+    return o[0, 0].numpy()
+
+
+def test_attend_matches_torch_sdpa():
+    rng = np.random.default_rng(20)
+    q, kv = rng.standard_normal((64, 512)), rng.standard_normal((640, 512))
+    for tau in (1 / np.sqrt(512), 1.0, 0.05):
+        o, lse = O.attend(q, kv, tau)
+        assert np.allclose(o, sdpa(q, kv, tau), rtol=1e-10, atol=1e-12)
+        z = tau * q @ kv.T
+        assert np.allclose(lse, np.log(np.exp(z - z.max(1, keepdims=True)).sum(1))
+                           + z.max(1), rtol=1e-12)
+
+
+def test_attend_special_cases():
+    rng = np.random.default_rng(21)
+    q, kv = rng.standard_normal((4, 32)), rng.standard_normal((9, 32))
+    # tau = 0: the plain mean of the rows, lse = log(rows)
+    o, lse = O.attend(q, kv, 0.0)
+    assert np.allclose(o, np.tile(kv.mean(0), (4, 1)))
+    assert np.allclose(lse, np.log(9.0))
+    # one row: that row
+    o, _ = O.attend(q, kv[:1], 0.3)
+    assert np.allclose(o, np.tile(kv[0], (4, 1)))
+    # a large tau and one key planted along q: that key
+    kv2 = rng.standard_normal((50, 32)) * 0.01
+    kv2[17] = q[2] / np.linalg.norm(q[2])
+    o, _ = O.attend(q[2:3], kv2, 1e4)
+    assert np.allclose(o[0], kv2[17], atol=1e-9)
+    # probabilities: non-negative rows summing to 1
+    p = O.attention_probs(q, kv, 0.7)
+    assert (p >= 0).all() and np.abs(p.sum(1) - 1).max() < 1e-12
+    # row order does not matter
+    perm = rng.permutation(9)
+    assert np.allclose(O.attend(q, kv, 0.7)[0], O.attend(q, kv[perm], 0.7)[0], rtol=1e-13)
+
+
+def _cfg(**kw):
+    return O.StepConfig(**kw)
+
+
+def test_decode_all_selected_equals_dense_attention():
+    # k_tokens >= L: every latent is selected, so the step is dense attention
+    # over all latents followed by the window, under one softmax.
+    inp = synth.decode_inputs([600], 2, "bf16", seed=7)      # L = 300 latents
+    cfg = _cfg(ratio=2, k_tokens=512)
+    r = O.decode_sequence(cfg, inp, 0)
+    assert list(r["token_ids"][:300]) == list(range(300))
+    kv = np.concatenate([O.bf16_to_f64(inp.latents[0, :300]),
+                         O.bf16_to_f64(inp.swa[0, :128])])
+    q = O.bf16_to_f64(inp.q[0])
+    assert np.allclose(r["out"], sdpa(q, kv, 1 / np.sqrt(512)), rtol=1e-10, atol=1e-13)
+
+
+def test_decode_short_sequence_window_and_latents():
+    # T = 5 at ratio 2: 2 latents (positions 0-3), window holds positions 0..4.
+    inp = synth.decode_inputs([5], 2, "bf16", seed=8)
+    assert inp.n_latents[0] == 2 and inp.swa_len[0] == 5
+    r = O.decode_sequence(_cfg(ratio=2), inp, 0)
+    assert list(r["token_ids"][:2]) == [0, 1] and (r["token_ids"][2:] == -1).all()
+    kv = np.concatenate([O.bf16_to_f64(inp.latents[0, :2]), O.bf16_to_f64(inp.swa[0, :5])])
+    assert np.allclose(r["out"], sdpa(O.bf16_to_f64(inp.q[0]), kv, 1 / np.sqrt(512)),
+                       rtol=1e-10, atol=1e-13)
+
+
+def test_decode_one_token_ratio_two_has_no_latent():
+    inp = synth.decode_inputs([1], 2, "bf16", seed=9)
+    r = O.decode_sequence(_cfg(ratio=2), inp, 0)
+    assert (r["token_ids"] == -1).all()
+    # one window row: the output is that row
+    assert np.allclose(r["out"], np.tile(O.bf16_to_f64(inp.swa[0, 0]), (64, 1)))
+
+
+def test_prefill_window_rows_closed_form():
+    # row r of the prefill window buffer holds position ctx - 127 + r
+    assert O.prefill_window_rows(1000, 0, 128) == (0, 128)
+    assert O.prefill_window_rows(1000, 5, 128) == (5, 133)
+    assert O.prefill_window_rows(10, 0, 128) == (117, 128)      # positions 0..10
+    assert O.prefill_visible(1000, 0, 2) == 500 and O.prefill_visible(1000, 1, 2) == 501
+    assert O.prefill_visible(1001, 0, 2) == 501
+
+
+@pytest.mark.parametrize("fmt,ratio", [("bf16", 2), ("mxfp8", 1), ("bf16", 1)])
+def test_prefill_last_query_equals_decode(fmt, ratio):
+    ctx, n_q = 333, 20
+    cfg = _cfg(ratio=ratio, k_blocks=6, k_tokens=40)
+    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, seed=11)
+    kv, pooled, _ = O.prefill_caches(cfg, pf)
+    T = ctx + n_q
+    L = T // ratio
+    # the same sequence as a decode batch of one
+    dec = synth.decode_inputs([T], ratio, fmt, seed=11)
+    dec.q[0], dec.q_idx[0], dec.w[0] = pf.q[-1], pf.q_idx[-1], pf.w[-1]
+    dec.latents[0, :L] = pf.latents[:L]
+    dec.keys.data[0, :L] = pf.keys.data[:L]
+    if fmt == "mxfp8":
+        dec.keys.scales[0, :L] = pf.keys.scales[:L]
+    lo, hi = O.prefill_window_rows(ctx, n_q - 1, 128)
+    dec.swa[0, : hi - lo] = pf.swa[lo:hi]
+    rp = O.prefill_query(cfg, pf, n_q - 1, kv, pooled)
+    rd = O.decode_sequence(cfg, dec, 0)
+    assert np.array_equal(rp["block_ids"], rd["block_ids"])
+    assert np.array_equal(rp["token_ids"], rd["token_ids"])
+    assert np.array_equal(rp["out"], rd["out"])
+
+
+def test_prefill_partial_block_is_mean_of_visible_members():
+    ctx, n_q, ratio = 100, 12, 1
+    cfg = _cfg(ratio=ratio, k_blocks=3, k_tokens=16)
+    pf = synth.prefill_inputs(n_q, ctx, ratio, "bf16", seed=12)
+    kv, pooled, _ = O.prefill_caches(cfg, pf)
+    for i in range(n_q):
+        n_vis = O.prefill_visible(ctx, i, ratio)
+        # recompute this query's block keys independently by decoding its own pool
+        pd, _ = O.pool_keys(kv[:n_vis], n_vis, "bf16")
+        r = O.select_query(cfg, pf.q_idx[i], pf.w[i], kv, O.bf16_to_f64(pd), n_vis)
+        rp = O.prefill_query(cfg, pf, i, kv, pooled, with_attention=False)
+        assert np.array_equal(r["block_ids"], rp["block_ids"])
+        assert np.array_equal(r["token_ids"], rp["token_ids"])
+        assert (rp["token_ids"][rp["token_ids"] >= 0] < n_vis).all()

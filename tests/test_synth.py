@@ -1,0 +1,47 @@
+"""The seeded input generator: determinism, distributions and layout."""
+import numpy as np
+
+import oracle as O
+import synth
+
+
+def test_deterministic_and_counter_based():
+    a = synth.normal_bf16(3, 1, 0, 1000, 1.0)
+    b = synth.normal_bf16(3, 1, 0, 1000, 1.0)
+    assert np.array_equal(a, b)
+    # element i depends only on its counter: a window of the stream matches
+    c = synth.normal_bf16(3, 1, 333, 100, 1.0)
+    assert np.array_equal(a[333:433], c)
+    assert not np.array_equal(a, synth.normal_bf16(4, 1, 0, 1000, 1.0))
+    assert not np.array_equal(a, synth.normal_bf16(3, 2, 0, 1000, 1.0))
+
+
+def test_distributions():
+    z = synth.normal_f32(0, 9, 0, 400000, 1.0).astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1) < 0.01
+    assert abs((np.abs(z) < 1).mean() - 0.6827) < 0.005
+    u = synth.uniform_f32(0, 9, 0, 200000).astype(np.float64)
+    assert u.min() >= 0 and u.max() < 1 and abs(u.mean() - 0.5) < 0.005
+    assert np.array_equal(u * 2 ** 24, np.floor(u * 2 ** 24))
+
+
+def test_mxfp8_generator_is_close_to_its_normals():
+    codes, scales = synth.normal_mxfp8(1, 5, 0, 300, 128, 1 / np.sqrt(128))
+    ref = synth.normal_f32(1, 5, 0, 300 * 128, 1 / np.sqrt(128)).reshape(300, 128)
+    dec = O.mxfp8_decode(codes, scales)
+    big = np.abs(ref) > 1e-3
+    assert (np.abs(dec - ref)[big] / np.abs(ref)[big]).max() < 0.13
+    # the generator's encoding is the OCP MX conversion
+    c2, s2 = O.mxfp8_encode(ref)
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
+
+
+def test_decode_inputs_layout():
+    inp = synth.decode_inputs([100, 37], 2, "mxfp8", seed=3)
+    assert inp.q.shape == (2, 64, 512) and inp.q_idx.shape == (2, 16, 128)
+    assert list(inp.n_latents) == [50, 18] and list(inp.swa_len) == [100, 37]
+    assert inp.cap == 56 and inp.keys.scales.shape == (2, 56, 4)
+    assert (inp.latents[1, 18:] == 0x7F80).all()      # poisoned tail
+    assert (inp.swa[1, 37:] == 0).all()
+    lat = O.bf16_to_f64(inp.latents[0, :50])
+    assert abs(lat.std() * np.sqrt(512) - 1) < 0.02
