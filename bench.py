@@ -1,0 +1,397 @@
+"""Benchmark of the two-tier sparse-attention decode step on GB300.
+
+Default workload: decode, batch 64, 131072 tokens per sequence at compression
+ratio 1 (131072 latents, 16384 blocks of 8; the candidate stage keeps 2048
+blocks), MXFP8 index keys, bf16 latents, top-512 plus a 128-position window.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one whole decode step: pooling of each sequence's newest block,
+block scores + top-2048 blocks, token scores + top-512 latents, and attention,
+for every query of the batch. Inputs (caches and queries) are resident in HBM
+when the timed region starts; the L2 is flushed (a 512 MiB write) before every
+timed step, outside its events. `value` is queries/s over the whole job.
+`e2e` repeats the step through the C ABI with host buffers: each step copies
+its queries in from pinned host memory and its outputs back.
+The reference arm times the CPU oracle on the host cores on a bounded sample.
+Multi-GPU: one process per GPU (torchrun); decode shards by sequence, so each
+rank runs its own batch with no collective (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode queries/s at 128K ctx; achieved HBM GB/s vs roofline"
+DEFAULT_WORKLOAD = "decode_b64_t131072_r1_mxfp8"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=0,
+                   help="sequences in the CPU-oracle sample (0: automatic)")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_rate(workload: str, n_seq: int, steps: int = 1):
+    """Times the oracle, as it stands, on n_seq sequences of the workload's shape.
+    Returns (queries/s, seconds per step, threads, sample description)."""
+    import oracle as O
+    import synth
+    spec = dict(synth.WORKLOADS[workload])
+    assert spec.pop("kind") == "decode"
+    inp = synth.decode_inputs([spec["T"]] * n_seq, spec["ratio"], spec["key_fmt"], spec["seed"])
+    cfg = O.StepConfig(ratio=spec["ratio"])
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for b in range(n_seq):
+            O.decode_sequence(cfg, inp, b)
+        times.append(time.perf_counter() - t0)
+    threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or os.cpu_count() or 1
+    sample = (f"{n_seq} sequence(s) of the workload ({spec['T']} tokens, ratio {spec['ratio']}, "
+              f"{spec['key_fmt']} keys); the oracle pools each sequence's keys as part of its step")
+    t = float(np.median(times))
+    return n_seq / t, t, threads, sample
+
+
+def auto_cpu_sample(workload: str) -> int:
+    import synth
+    T = synth.WORKLOADS[workload]["T"]
+    return max(1, min(16, int(2 ** 21 // max(T, 1))))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    spec = synth.WORKLOADS[args.workload]
+    n = args.cpu_sample or auto_cpu_sample(args.workload)
+    for _ in range(args.warmup):
+        cpu_oracle_rate(args.workload, n)
+    qps, t, threads, sample = cpu_oracle_rate(args.workload, n, steps=max(1, args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": qps, "unit": "queries/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": spec["B"], "tokens": spec["T"],
+                   "ratio": spec["ratio"], "key_fmt": spec["key_fmt"]},
+        "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import two_tier_sparse_gb300 as dsa
+
+    spec = dict(synth.WORKLOADS[args.workload])
+    if spec["kind"] != "decode":
+        raise SystemExit("bench.py times the decode step; prefill is measured by bench_prefill")
+    B, T, ratio, fmt = spec["B"], spec["T"], spec["ratio"], spec["key_fmt"]
+    # Every rank decodes its own batch: seeds differ per rank.
+    t0 = time.time()
+    inp = synth.decode_inputs([T] * B, ratio, fmt, spec["seed"] + 1000 * rank)
+    gen_s = time.time() - t0
+    cfg = dsa.config(ratio=ratio)
+    cap = inp.cap
+    L = int(inp.n_latents.max())
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, q_idx, w = d(inp.q), d(inp.q_idx), d(inp.w)
+    latents, swa = d(inp.latents), d(inp.swa)
+    n_lat, swa_len = d(inp.n_latents), d(inp.swa_len)
+    keys = dsa.Keys(fmt, d(inp.keys.data), None if inp.keys.scales is None else
+                    d(inp.keys.scales))
+    del inp
+    nbc = cap // 8
+    if fmt == "bf16":
+        pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.int16, device=dev))
+    else:
+        pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.uint8, device=dev),
+                          torch.empty((B, nbc, 4), dtype=torch.uint8, device=dev))
+    ws = dsa.workspace(cfg, B, cap, dev)
+    out = torch.empty((B, 64, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # The pooled-key cache is built once (cache build, outside the step).
+    dsa.pool_index_keys(cfg, keys, n_lat, cap, pooled, ws)
+    torch.cuda.synchronize()
+
+    def step():
+        dsa.decode_step(cfg, q, q_idx, w, keys, pooled, latents, n_lat, cap, swa, swa_len, out,
+                        ws, lse=lse, update_pool=True)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # live per-launch timing of the scan kernel (two launches per step)
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    dsa.profile_events("scan", ks, ke)
+    dsa.launch_counts(reset=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(K):
+            flush.zero_()
+            ev_s[i].record()
+            step()
+            ev_e[i].record()
+        torch.cuda.synchronize()
+    dsa.profile_events("scan", [], [])
+    counts = dsa.launch_counts(reset=True)
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
+    scan_ms = [s.elapsed_time(e) for s, e in zip(ks, ke)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * B / (ms_per_step * 1e-3)
+
+    # Roofline of the dominant kernel: the indexer scan. Algorithmic bytes per
+    # launch = rows scanned x bytes per key row (MXFP8: 128 codes + 4 scale
+    # bytes; bf16: 256); both launches of a step scan 2048 x 8 = 16384 rows per
+    # query (16384 block keys, then 16384 candidate latents).
+    row_bytes = 132 if fmt == "mxfp8" else 256
+    nb = -(-L // 8)
+    blk_rows = nb if nb > cfg.k_blocks else 0
+    tok_rows = 8 * cfg.k_blocks if nb > cfg.k_blocks else L
+    per_launch = [B * blk_rows * row_bytes, B * tok_rows * row_bytes] if blk_rows else \
+        [B * tok_rows * row_bytes]
+    launches_per_step = len(per_launch)
+    bytes_per_launch = float(np.mean(per_launch))
+    scan_avg_ms = float(np.mean(scan_ms)) if scan_ms else float("nan")
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved = bytes_per_launch / (scan_avg_ms * 1e-3) / 1e9
+    # whole-step algorithmic bytes (keys scanned + latent rows gathered + window + q/out)
+    step_bytes = B * (blk_rows * row_bytes + tok_rows * row_bytes + 512 * 1024 + 128 * 1024
+                      + 64 * 512 * 2 * 2 + 16 * 128 * 2)
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "scan_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            tr = json.load(open(tr_path))
+            if tr.get("workload") == args.workload:
+                traffic = tr.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # End to end through the C ABI with host buffers.
+    q_h = q.cpu().pin_memory()
+    qi_h = q_idx.cpu().pin_memory()
+    w_h = w.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, qi_d, w_d = torch.empty_like(q), torch.empty_like(q_idx), torch.empty_like(w)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        qi_d.copy_(qi_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        dsa.decode_step(cfg, q_d, qi_d, w_d, keys, pooled, latents, n_lat, cap, swa, swa_len, out,
+                        ws, lse=lse, update_pool=True)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        e_s[i].record()
+        e2e_step()
+        e_e[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = q.numel() * 2 + q_idx.numel() * 2 + w.numel() * 4
+    d2h = out.numel() * 2 + lse.numel() * 4
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        n = args.cpu_sample or auto_cpu_sample(args.workload)
+        qps, t, threads, sample = cpu_oracle_rate(args.workload, n)
+        cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
+               "sample": sample}
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch_per_gpu": B, "tokens": T, "ratio": ratio,
+                   "latents": L, "blocks": nb, "k_blocks": cfg.k_blocks,
+                   "k_tokens": cfg.k_tokens, "window": cfg.window, "key_fmt": fmt,
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "step_algorithmic_bytes": step_bytes,
+                   "step_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                   "step_hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+                   "input_gen_s": round(gen_s, 1)},
+        "roofline": {"kernel": "scan (indexer scores, tcgen05)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "avg_launch_ms": scan_avg_ms, "launches_per_step": launches_per_step},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "queries/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": int(sum(counts.values())),
+        "gpu_launches_by_kind": counts,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

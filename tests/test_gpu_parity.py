@@ -1,0 +1,333 @@
+"""GPU parity: every call of the C ABI against the CPU oracle on the same seeded inputs.
+
+Sizes span several 128-row tiles with ragged tails, partial blocks, sequences
+shorter than the window, empty selections, and the maximum k_blocks/k_tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+import two_tier_sparse_gb300 as dsa
+from parity import (DecodeOnDevice, check_ids, check_out, check_scores, dev, host_u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    from two_tier_sparse_gb300 import build
+    build.build()
+    dsa.load()
+    torch.cuda.set_device(cuda_device)
+
+
+def oracle_cfg(cfg):
+    return O.StepConfig(k_blocks=cfg.k_blocks, k_tokens=cfg.k_tokens, window=cfg.window,
+                        ratio=cfg.ratio, sm_scale=cfg.sm_scale if cfg.sm_scale > 0 else None)
+
+
+# ---------------------------------------------------------------------------
+# S0: pooled keys, bit-exact
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_pool_bit_exact(fmt):
+    inp = synth.decode_inputs([1003, 77, 8, 1, 2051], 1, fmt, seed=21)
+    cfg = dsa.config(ratio=1)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    assert d.status()[0] == 0
+    pdat = d.pooled.data.cpu().numpy()
+    psc = None if d.pooled.scales is None else d.pooled.scales.cpu().numpy()
+    for b in range(inp.B):
+        n = int(inp.n_latents[b])
+        kv = O.decode_keys(fmt, inp.keys.data[b][:n],
+                           None if inp.keys.scales is None else inp.keys.scales[b][:n])
+        want, want_s = O.pool_keys(kv, n, fmt)
+        nb = want.shape[0]
+        got = pdat[b, :nb].view(np.uint16) if fmt == "bf16" else pdat[b, :nb]
+        assert np.array_equal(got, want), f"seq {b}"
+        if fmt == "mxfp8":
+            assert np.array_equal(psc[b, :nb], want_s), f"seq {b} scales"
+
+
+def test_pool_tail_only_writes_the_last_block():
+    inp = synth.decode_inputs([1003, 64], 1, "mxfp8", seed=22)
+    d = DecodeOnDevice(inp, dsa.config())
+    d.pooled.data.fill_(0x55)
+    d.pool(tail_only=True)
+    got = d.pooled.data.cpu().numpy()
+    for b, n in enumerate(inp.n_latents):
+        last = (int(n) - 1) // 8
+        kv = O.decode_keys("mxfp8", inp.keys.data[b][:n], inp.keys.scales[b][:n])
+        want, _ = O.pool_keys(kv, int(n), "mxfp8")
+        assert np.array_equal(got[b, last], want[last])
+        assert (got[b, :last] == 0x55).all()
+
+
+# ---------------------------------------------------------------------------
+# S1 + S2: candidate-block stage
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("fmt,k_blocks", [("bf16", 64), ("mxfp8", 64), ("mxfp8", 4096),
+                                          ("bf16", 1)])
+def test_index_blocks(fmt, k_blocks):
+    T = [5000, 3001, 700, 9]
+    inp = synth.decode_inputs(T, 1, fmt, seed=23)
+    cfg = dsa.config(k_blocks=k_blocks, ratio=1)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    nbc = d.cap // 8
+    bids = torch.empty((inp.B, k_blocks), dtype=torch.int32, device="cuda")
+    bsc = torch.empty((inp.B, nbc), dtype=torch.float32, device="cuda")
+    dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws, block_scores=bsc)
+    assert d.status()[0] == 0
+    bids, bsc = bids.cpu().numpy(), bsc.cpu().numpy()
+    oc = oracle_cfg(cfg)
+    for b in range(inp.B):
+        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        nb = len(r["block_scores"])
+        check_scores(bsc[b, :nb], r["block_scores"], f"block scores {b}")
+        assert np.isneginf(bsc[b, nb:]).all()
+        check_ids(bids[b], r["block_ids"], lambda i: r["block_scores"][i], k_blocks, f"blocks {b}")
+
+
+# ---------------------------------------------------------------------------
+# S3 + S4: token stage (over the GPU's block set, and over every block)
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("fmt,ratio", [("bf16", 2), ("mxfp8", 1)])
+def test_topk_over_gpu_blocks(fmt, ratio):
+    T = [12000, 4099, 2000]
+    inp = synth.decode_inputs(T, ratio, fmt, seed=24)
+    cfg = dsa.config(k_blocks=96, k_tokens=512, ratio=ratio)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    bids = torch.empty((inp.B, 96), dtype=torch.int32, device="cuda")
+    dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws)
+    tok = torch.empty((inp.B, 512), dtype=torch.int32, device="cuda")
+    tsc = torch.empty((inp.B, 96 * 8), dtype=torch.float32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, bids, d.n_lat, d.cap, tok, d.ws, token_scores=tsc)
+    assert d.status()[0] == 0
+    bids_h, tok_h, tsc_h = bids.cpu().numpy(), tok.cpu().numpy(), tsc.cpu().numpy()
+    oc = oracle_cfg(cfg)
+    for b in range(inp.B):
+        r = O.decode_sequence(oc, inp, b, with_attention=False, block_ids=bids_h[b])
+        # candidate i is latent 8 * bids[i // 8] + i % 8
+        ref = np.full(96 * 8, -np.inf)
+        pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
+        for i in range(96 * 8):
+            blk = bids_h[b, i // 8]
+            t = blk * 8 + i % 8
+            if blk >= 0 and t in pos:
+                ref[i] = pos[t]
+        check_scores(tsc_h[b], ref, f"token scores {b}")
+        check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_topk_all_blocks(fmt):
+    T = [4096, 1000, 513, 30]
+    inp = synth.decode_inputs(T, 2, fmt, seed=25)
+    cfg = dsa.config(k_tokens=512, ratio=2)
+    d = DecodeOnDevice(inp, cfg)
+    tok = torch.empty((inp.B, 512), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, None, d.n_lat, d.cap, tok, d.ws)
+    assert d.status()[0] == 0
+    tok_h = tok.cpu().numpy()
+    oc = oracle_cfg(cfg)
+    for b in range(inp.B):
+        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
+        check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
+
+
+# ---------------------------------------------------------------------------
+# S5 - S7: attention given ids
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("T,ratio,q_scale,sm_scale", [
+    ([4096, 1000, 300, 100, 5], 2, 1.0, 0.0),     # default scale (near-uniform softmax)
+    ([4096, 1000, 300, 100, 5], 2, 8.0, 1.0),     # sharpened: logit std about 3
+    ([70000, 1], 1, 8.0, 1.0),                    # 512 selected of many; a 1-token sequence
+    ([2], 2, 1.0, 0.0),                           # one latent, two window rows
+])
+def test_attention_given_oracle_ids(T, ratio, q_scale, sm_scale):
+    inp = synth.decode_inputs(T, ratio, "bf16", seed=26, q_scale=q_scale)
+    cfg = dsa.config(ratio=ratio, sm_scale=sm_scale)
+    oc = oracle_cfg(cfg)
+    d = DecodeOnDevice(inp, cfg)
+    refs = [O.decode_sequence(oc, inp, b) for b in range(inp.B)]
+    ids = np.stack([r["token_ids"] for r in refs]).astype(np.int32)
+    out = torch.empty((inp.B, 64, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((inp.B, 64), dtype=torch.float32, device="cuda")
+    dsa.sparse_attn_decode(cfg, d.q, d.latents, d.n_lat, dev(ids), d.swa, d.swa_len, out, d.ws,
+                           lse=lse)
+    assert d.status()[0] == 0
+    out_h, lse_h = host_u16(out), lse.cpu().numpy()
+    for b, r in enumerate(refs):
+        check_out(out_h[b], lse_h[b], r["out"], r["lse"], f"seq {b}")
+
+
+def test_attention_no_rows_and_bad_ids():
+    # T = 1 at ratio 2: no latent; with swa_len forced to 0 the query has no rows.
+    inp = synth.decode_inputs([1, 300], 2, "bf16", seed=27)
+    inp.swa_len[0] = 0
+    cfg = dsa.config(ratio=2)
+    d = DecodeOnDevice(inp, cfg)
+    ids = np.full((2, 512), -1, np.int32)
+    ids[1, :3] = [0, 5, 149]
+    out = torch.empty((2, 64, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((2, 64), dtype=torch.float32, device="cuda")
+    dsa.sparse_attn_decode(cfg, d.q, d.latents, d.n_lat, dev(ids), d.swa, d.swa_len, out, d.ws,
+                           lse=lse)
+    assert d.status()[0] == 0
+    assert (out[0] == 0).all() and torch.isneginf(lse[0]).all()
+    r = O.decode_sequence(O.StepConfig(ratio=2), inp, 1, token_ids=ids[1])
+    check_out(host_u16(out)[1], lse.cpu().numpy()[1], r["out"], r["lse"])
+    # an id past the sequence's latents is flagged and skipped
+    ids[1, 3] = 150
+    dsa.sparse_attn_decode(cfg, d.q, d.latents, d.n_lat, dev(ids), d.swa, d.swa_len, out, d.ws,
+                           lse=lse)
+    code, info = d.status()
+    assert code == 6 and (info >> 24) == 4 and (info & 0xFFFFFF) == 150
+    check_out(host_u16(out)[1], lse.cpu().numpy()[1], r["out"], r["lse"])
+    assert d.status()[0] == 0  # reading clears it
+
+
+# ---------------------------------------------------------------------------
+# The whole decode step
+# ---------------------------------------------------------------------------
+
+
+def run_step(d, cfg, update_pool=False):
+    inp = d.inp
+    B = inp.B
+    out = torch.empty((B, 64, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((B, 64), dtype=torch.float32, device="cuda")
+    bids = torch.empty((B, cfg.k_blocks), dtype=torch.int32, device="cuda")
+    tok = torch.empty((B, cfg.k_tokens), dtype=torch.int32, device="cuda")
+    dsa.decode_step(cfg, d.q, d.q_idx, d.w, d.keys, d.pooled, d.latents, d.n_lat, d.cap, d.swa,
+                    d.swa_len, out, d.ws, lse=lse, block_ids=bids, token_ids=tok,
+                    update_pool=update_pool)
+    return out, lse, bids, tok
+
+
+def check_step(inp, cfg, outs, seqs):
+    out, lse, bids, tok = (x.cpu().numpy() for x in outs)
+    out = out.view(np.uint16)
+    oc = oracle_cfg(cfg)
+    for b in seqs:
+        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        check_ids(bids[b], r["block_ids"], lambda i: r["block_scores"][i], cfg.k_blocks,
+                  f"blocks {b}")
+        r2 = O.decode_sequence(oc, inp, b, block_ids=bids[b], token_ids=tok[b])
+        pos = {int(t): s for t, s in zip(r2["cand"], r2["token_scores"])}
+        check_ids(tok[b], r2["token_ids"], lambda i: pos[i], cfg.k_tokens, f"tokens {b}")
+        check_out(out[b], lse[b], r2["out"], r2["lse"], f"out {b}")
+
+
+@pytest.mark.parametrize("T,ratio,fmt,k_blocks,q_scale,sm", [
+    ([4096], 2, "bf16", 2048, 1.0, 0.0),                       # decode, 4096 tokens, batch 1
+    ([20000, 9001, 777, 64, 3], 1, "mxfp8", 128, 8.0, 1.0),     # both tiers, ragged, sharpened
+    ([20000, 9001, 777], 2, "bf16", 200, 1.0, 0.0),
+])
+def test_decode_step(T, ratio, fmt, k_blocks, q_scale, sm):
+    inp = synth.decode_inputs(T, ratio, fmt, seed=28, q_scale=q_scale)
+    cfg = dsa.config(k_blocks=k_blocks, ratio=ratio, sm_scale=sm)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    outs = run_step(d, cfg)
+    assert d.status()[0] == 0
+    check_step(inp, cfg, outs, range(inp.B))
+
+
+def test_decode_step_is_deterministic_and_updates_the_pool():
+    inp = synth.decode_inputs([30000, 17], 1, "mxfp8", seed=29)
+    cfg = dsa.config(k_blocks=256)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    ref_pool = d.pooled.data.clone()
+    # clobber each sequence's newest block, then let the step rebuild it
+    for b, n in enumerate(inp.n_latents):
+        d.pooled.data[b, (int(n) - 1) // 8] = 0
+    a = run_step(d, cfg, update_pool=True)
+    assert torch.equal(d.pooled.data, ref_pool)
+    b_ = run_step(d, cfg, update_pool=True)
+    for x, y in zip(a, b_):
+        assert torch.equal(x, y)
+    assert d.status()[0] == 0
+
+
+def test_decode_32_sequences_of_32768_tokens():
+    """Decode, batch 32, 32768 tokens at ratio 2 (16384 latents, 2048 blocks, all kept)."""
+    inp = synth.workload_inputs("decode_b32_t32768_r2_bf16")
+    cfg = dsa.config(ratio=2)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    outs = run_step(d, cfg)
+    assert d.status()[0] == 0
+    check_step(inp, cfg, outs, range(inp.B))
+
+
+# ---------------------------------------------------------------------------
+# Prefill
+# ---------------------------------------------------------------------------
+
+
+def block_near_tie(scores, k):
+    """True when the block tier's k-th and (k+1)-th best oracle scores are a near-tie."""
+    if len(scores) <= k:
+        return False
+    srt = np.sort(scores)[::-1]
+    return abs(srt[k - 1] - srt[k]) <= 1e-5 * abs(srt[k - 1])
+
+
+def run_prefill(pf, cfg):
+    n_q = pf.n_q
+    fmt = pf.keys.fmt
+    n_lat = (pf.ctx + n_q) // pf.ratio
+    keys = dsa.Keys(fmt, dev(pf.keys.data), None if pf.keys.scales is None else dev(pf.keys.scales))
+    # pooled keys of complete blocks, built on the GPU (the pool call over one sequence)
+    nbf = n_lat // 8
+    if fmt == "bf16":
+        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.int16, device="cuda"))
+    else:
+        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.uint8, device="cuda"),
+                          torch.zeros((1, max(nbf, 1), 4), dtype=torch.uint8, device="cuda"))
+    ws = dsa.workspace(cfg, n_q, n_lat)
+    keys1 = dsa.Keys(fmt, keys.data[None], None if keys.scales is None else keys.scales[None])
+    n1 = torch.tensor([nbf * 8], dtype=torch.int32, device="cuda")
+    dsa.pool_index_keys(cfg, keys1, n1, nbf * 8, pooled, ws)
+    pooled2 = dsa.Keys(fmt, pooled.data[0], None if pooled.scales is None else pooled.scales[0])
+    out = torch.empty((n_q, 64, 512), dtype=torch.int16, device="cuda")
+    lse = torch.empty((n_q, 64), dtype=torch.float32, device="cuda")
+    tok = torch.empty((n_q, cfg.k_tokens), dtype=torch.int32, device="cuda")
+    dsa.sparse_attn_prefill(cfg, pf.ctx, dev(pf.q), dev(pf.q_idx), dev(pf.w), dev(pf.latents),
+                            keys, pooled2, dev(pf.swa), out, ws, lse=lse, token_ids=tok)
+    code, info = dsa.read_device_status(ws)
+    assert code == 0, hex(info)
+    return host_u16(out), lse.cpu().numpy(), tok.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,ratio,ctx,n_q", [("bf16", 2, 333, 50), ("mxfp8", 1, 1000, 37),
+                                               ("bf16", 1, 5, 130)])
+def test_prefill(fmt, ratio, ctx, n_q):
+    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, seed=30, q_scale=8.0)
+    cfg = dsa.config(k_blocks=12, k_tokens=40, ratio=ratio, sm_scale=1.0)
+    out, lse, tok = run_prefill(pf, cfg)
+    oc = oracle_cfg(cfg)
+    kv, pooled, _ = O.prefill_caches(oc, pf)
+    for i in range(n_q):
+        r = O.prefill_query(oc, pf, i, kv, pooled, with_attention=False)
+        pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
+        if not block_near_tie(r["block_scores"], cfg.k_blocks):
+            check_ids(tok[i], r["token_ids"], lambda j: pos[j], cfg.k_tokens, f"q{i}")
+        r2 = O.prefill_query(oc, pf, i, kv, pooled, token_ids=tok[i])
+        check_out(out[i], lse[i], r2["out"], r2["lse"], f"q{i}")

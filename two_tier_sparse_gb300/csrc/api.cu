@@ -1,0 +1,596 @@
+// C-ABI entry points (declared in include/dsa.h): argument checks on the host,
+// workspace layout, and the launch sequence of each call on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace regions for n queries over sequences of at most max_latents latents.
+struct Layout {
+  size_t status, block_scores, token_scores, block_ids, token_ids, partial, total;
+  int64_t nb_max, n_cand;
+};
+
+Layout layout(const dsa_config_t& c, int n, int64_t max_latents) {
+  Layout L{};
+  L.nb_max = (max_latents + kBlock - 1) / kBlock;
+  const int64_t gathered = static_cast<int64_t>(c.k_blocks) * kBlock;
+  const int64_t all = (max_latents + 7) / 8 * 8;
+  L.n_cand = std::max(gathered, all);
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + sizeof(DeviceStatus));
+  L.block_scores = off;
+  off = align_up(off + static_cast<size_t>(n) * L.nb_max * 4);
+  L.token_scores = off;
+  off = align_up(off + static_cast<size_t>(n) * L.n_cand * 4);
+  L.block_ids = off;
+  off = align_up(off + static_cast<size_t>(n) * c.k_blocks * 4);
+  L.token_ids = off;
+  off = align_up(off + static_cast<size_t>(n) * c.k_tokens * 4);
+  L.partial = off;  // prefill partial blocks: n rows of 128 B/256 B + scales
+  off = align_up(off + static_cast<size_t>(n) * (kIdxDim * 2 + 4));
+  L.total = off;
+  return L;
+}
+
+dsa_status_t check_config(const dsa_config_t* c) {
+  if (c == nullptr) return DSA_ERR_INVALID_ARG;
+  if (c->n_heads != kHeads || c->latent_dim != kLatent || c->n_idx_heads != kIdxHeads ||
+      c->idx_dim != kIdxDim || c->block != kBlock) {
+    return DSA_ERR_UNSUPPORTED;
+  }
+  if (c->k_blocks < 1 || c->k_blocks > kMaxKBlocks || c->k_tokens < 1 ||
+      c->k_tokens > kMaxKTokens || c->window < 1 || c->window > kMaxWindow || c->ratio < 1 ||
+      !(c->sm_scale == c->sm_scale) || isinf(c->sm_scale)) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  return DSA_OK;
+}
+
+float tau(const dsa_config_t& c) {
+  return c.sm_scale > 0.f ? c.sm_scale : 1.0f / sqrtf(static_cast<float>(c.latent_dim));
+}
+
+dsa_status_t check_keys(const dsa_keys_t* k, int64_t min_stride, bool need_stride) {
+  if (k == nullptr || k->data == nullptr) return DSA_ERR_INVALID_ARG;
+  if (k->fmt != DSA_FMT_BF16 && k->fmt != DSA_FMT_MXFP8) return DSA_ERR_INVALID_ARG;
+  if (k->fmt == DSA_FMT_MXFP8 && k->scales == nullptr) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(k->data)) return DSA_ERR_MISALIGNED;
+  if (k->fmt == DSA_FMT_MXFP8 && (reinterpret_cast<uintptr_t>(k->scales) & 3u)) {
+    return DSA_ERR_MISALIGNED;
+  }
+  if (need_stride && k->seq_stride_rows < min_stride) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t check_ws(const dsa_config_t& c, int n, int64_t max_latents, void* ws, size_t bytes,
+                      Layout* L) {
+  *L = layout(c, n, max_latents);
+  if (ws == nullptr || bytes < L->total) return DSA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return DSA_ERR_MISALIGNED;
+  return DSA_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+#define DSA_TRY(expr)                  \
+  do {                                 \
+    dsa_status_t _s = (expr);          \
+    if (_s != DSA_OK) return _s;       \
+  } while (0)
+#define DSA_CUDA(expr) DSA_TRY(cuda_status(expr))
+
+constexpr int64_t kMaxLatents = int64_t(1) << 30;
+
+// Timing hook and launch counters (dsa_profile_events, dsa_launch_counts).
+struct Profile {
+  void* const* starts = nullptr;
+  void* const* ends = nullptr;
+  int n = 0;
+  uint64_t next = 0;
+};
+Profile g_profile[DSA_KERNEL_KINDS];
+uint64_t g_launches[DSA_KERNEL_KINDS] = {0};
+
+template <typename F>
+cudaError_t launch(int kind, cudaStream_t s, F&& f) {
+  Profile& p = g_profile[kind];
+  const bool timed = p.n > 0;
+  const int slot = timed ? static_cast<int>(p.next % static_cast<uint64_t>(p.n)) : 0;
+  if (timed) {
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(p.starts[slot]), s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = f();
+  if (e != cudaSuccess) return e;
+  ++g_launches[kind];
+  if (timed) {
+    ++p.next;
+    return cudaEventRecord(static_cast<cudaEvent_t>(p.ends[slot]), s);
+  }
+  return cudaSuccess;
+}
+
+// Launch sequences shared by the public calls.
+dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
+                             const dsa_keys_t& pooled, const int32_t* n_lat, int B,
+                             int64_t max_latents, int32_t* block_ids, float* scores,
+                             DeviceStatus* st, cudaStream_t s, int prefill, int64_t ctx,
+                             const void* partial, const uint8_t* partial_scales) {
+  const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
+  ScanArgs sa{};
+  sa.fmt = pooled.fmt;
+  sa.key_data = pooled.data;
+  sa.key_scales = pooled.scales;
+  sa.key_stride = prefill ? 0 : pooled.seq_stride_rows;
+  sa.q_idx = q_idx;
+  sa.w = w;
+  sa.n_latents = n_lat;
+  sa.max_latents = max_latents;
+  sa.mode = ROWS_BLOCKS;
+  sa.n_rows = nb_max;
+  sa.scores = scores;
+  sa.B = B;
+  sa.prefill = prefill;
+  sa.ctx = ctx;
+  sa.ratio = c.ratio;
+  sa.partial_data = partial;
+  sa.partial_scales = partial_scales;
+  sa.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&] { return launch_scan(sa, device_sm_count(), s); }));
+  SelectArgs se{};
+  se.scores = scores;
+  se.n = nb_max;
+  se.k = c.k_blocks;
+  se.B = B;
+  se.out_ids = block_ids;
+  se.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&] { return launch_select(se, s); }));
+  return DSA_OK;
+}
+
+dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
+                             const dsa_keys_t& keys, const int32_t* block_ids,
+                             const int32_t* n_lat, int B, int64_t max_latents, int32_t* token_ids,
+                             float* scores, DeviceStatus* st, cudaStream_t s, int prefill,
+                             int64_t ctx) {
+  ScanArgs sa{};
+  sa.fmt = keys.fmt;
+  sa.key_data = keys.data;
+  sa.key_scales = keys.scales;
+  sa.key_stride = prefill ? 0 : keys.seq_stride_rows;
+  sa.q_idx = q_idx;
+  sa.w = w;
+  sa.n_latents = n_lat;
+  sa.max_latents = max_latents;
+  if (block_ids) {
+    sa.mode = ROWS_GATHER;
+    sa.block_ids = block_ids;
+    sa.k_blocks = c.k_blocks;
+    sa.n_rows = static_cast<int64_t>(c.k_blocks) * kBlock;
+  } else {
+    sa.mode = ROWS_LATENTS;
+    sa.n_rows = (max_latents + 7) / 8 * 8;
+  }
+  sa.scores = scores;
+  sa.B = B;
+  sa.prefill = prefill;
+  sa.ctx = ctx;
+  sa.ratio = c.ratio;
+  sa.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&] { return launch_scan(sa, device_sm_count(), s); }));
+  SelectArgs se{};
+  se.scores = scores;
+  se.n = sa.n_rows;
+  se.k = c.k_tokens;
+  se.B = B;
+  se.block_ids = block_ids;
+  se.k_blocks = c.k_blocks;
+  se.out_ids = token_ids;
+  se.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&] { return launch_select(se, s); }));
+  return DSA_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      n = 148;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+__global__ void identity_blocks_kernel(const int32_t* n_latents, int k_blocks, int32_t* out) {
+  const int b = blockIdx.x;
+  const int nb = (n_latents[b] + 7) / 8;
+  for (int i = threadIdx.x; i < k_blocks; i += blockDim.x) {
+    out[static_cast<int64_t>(b) * k_blocks + i] = i < nb ? i : -1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks,
+                                   int32_t* block_ids, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  identity_blocks_kernel<<<B, 256, 0, s>>>(n_latents, k_blocks, block_ids);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+void dsa_default_config(dsa_config_t* c) {
+  if (c == nullptr) return;
+  c->n_heads = kHeads;
+  c->latent_dim = kLatent;
+  c->n_idx_heads = kIdxHeads;
+  c->idx_dim = kIdxDim;
+  c->block = kBlock;
+  c->k_blocks = 2048;
+  c->k_tokens = 512;
+  c->window = 128;
+  c->ratio = 1;
+  c->sm_scale = 0.f;
+}
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int n_queries, int64_t max_latents,
+                                size_t* bytes) {
+  DSA_TRY(check_config(cfg));
+  if (bytes == nullptr || n_queries < 0 || max_latents < 0 || max_latents > kMaxLatents) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  *bytes = layout(*cfg, n_queries, max_latents).total;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys,
+                                 const int32_t* n_latents, int B, int64_t max_latents,
+                                 int tail_only, const dsa_keys_out_t* pooled, void* workspace,
+                                 size_t workspace_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || pooled == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  DSA_TRY(check_keys(keys, max_latents, true));
+  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows};
+  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true));
+  if (pooled->fmt != keys->fmt || n_latents == nullptr) return DSA_ERR_INVALID_ARG;
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0 || max_latents == 0) return DSA_OK;
+  PoolArgs a{};
+  a.fmt = keys->fmt;
+  a.key_data = keys->data;
+  a.key_scales = keys->scales;
+  a.key_stride = keys->seq_stride_rows;
+  a.n_latents = n_latents;
+  a.max_latents = max_latents;
+  a.B = B;
+  a.tail_only = tail_only;
+  a.out_data = pooled->data;
+  a.out_scales = pooled->scales;
+  a.out_stride = pooled->seq_stride_rows;
+  a.status = at<DeviceStatus>(workspace, L.status);
+  DSA_CUDA(launch(DSA_KERNEL_POOL, static_cast<cudaStream_t>(stream), [&] { return launch_pool(a, static_cast<cudaStream_t>(stream)); }));
+  return DSA_OK;
+}
+
+dsa_status_t dsa_index_blocks(const dsa_config_t* cfg, const void* q_idx, const float* w,
+                              const dsa_keys_t* pooled, const int32_t* n_latents, int B,
+                              int64_t max_latents, int32_t* block_ids, float* block_scores,
+                              void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents) return DSA_ERR_INVALID_ARG;
+  if (q_idx == nullptr || w == nullptr || n_latents == nullptr || block_ids == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(block_ids) ||
+      (block_scores && !aligned16(block_scores))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(pooled, (max_latents + 7) / 8, true));
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  float* scores = block_scores ? block_scores : at<float>(workspace, L.block_scores);
+  return run_block_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *pooled, n_latents, B,
+                         max_latents, block_ids, scores, at<DeviceStatus>(workspace, L.status),
+                         static_cast<cudaStream_t>(stream), 0, 0, nullptr, nullptr);
+}
+
+dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w,
+                      const dsa_keys_t* keys, const int32_t* block_ids,
+                      const int32_t* n_latents, int B, int64_t max_latents, int32_t* token_ids,
+                      float* token_scores, void* workspace, size_t workspace_bytes,
+                      dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents) return DSA_ERR_INVALID_ARG;
+  if (q_idx == nullptr || w == nullptr || n_latents == nullptr || token_ids == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(token_ids) ||
+      (block_ids && !aligned16(block_ids)) || (token_scores && !aligned16(token_scores))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(keys, max_latents, true));
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  float* scores = token_scores ? token_scores : at<float>(workspace, L.token_scores);
+  return run_token_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *keys, block_ids,
+                         n_latents, B, max_latents, token_ids, scores,
+                         at<DeviceStatus>(workspace, L.status), static_cast<cudaStream_t>(stream),
+                         0, 0);
+}
+
+dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, const void* latents,
+                                    int64_t latent_seq_stride_rows, const int32_t* n_latents,
+                                    const int32_t* token_ids, const void* swa,
+                                    const int32_t* swa_len, int B, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || latent_seq_stride_rows < 0) return DSA_ERR_INVALID_ARG;
+  if (q == nullptr || latents == nullptr || n_latents == nullptr || token_ids == nullptr ||
+      swa == nullptr || swa_len == nullptr || out == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q) || !aligned16(latents) || !aligned16(swa) || !aligned16(out) ||
+      !aligned16(token_ids) || (lse && !aligned16(lse))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, 0, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.latents = static_cast<const uint16_t*>(latents);
+  a.lat_stride = latent_seq_stride_rows;
+  a.n_latents = n_latents;
+  a.token_ids = token_ids;
+  a.k_tokens = cfg->k_tokens;
+  a.swa = static_cast<const uint16_t*>(swa);
+  a.swa_len = swa_len;
+  a.window = cfg->window;
+  a.B = B;
+  a.scale_log2 = tau(*cfg) * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.status = at<DeviceStatus>(workspace, L.status);
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, static_cast<cudaStream_t>(stream), [&] { return launch_attn(a, static_cast<cudaStream_t>(stream)); }));
+  return DSA_OK;
+}
+
+dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void* q_idx,
+                             const float* w, const dsa_keys_t* keys, const dsa_keys_out_t* pooled,
+                             int update_pool, const void* latents,
+                             int64_t latent_seq_stride_rows, const int32_t* n_latents,
+                             int64_t max_latents, const void* swa, const int32_t* swa_len, int B,
+                             int32_t* block_ids, int32_t* token_ids, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || pooled == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (latent_seq_stride_rows < max_latents) return DSA_ERR_INVALID_ARG;
+  if (q == nullptr || q_idx == nullptr || w == nullptr || latents == nullptr ||
+      n_latents == nullptr || swa == nullptr || swa_len == nullptr || out == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(w) || !aligned16(latents) ||
+      !aligned16(swa) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (block_ids && !aligned16(block_ids)) || (token_ids && !aligned16(token_ids))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(keys, max_latents, true));
+  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows};
+  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true));
+  if (pooled->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
+  if (update_pool && max_latents > 0) {
+    PoolArgs a{};
+    a.fmt = keys->fmt;
+    a.key_data = keys->data;
+    a.key_scales = keys->scales;
+    a.key_stride = keys->seq_stride_rows;
+    a.n_latents = n_latents;
+    a.max_latents = max_latents;
+    a.B = B;
+    a.tail_only = 1;
+    a.out_data = pooled->data;
+    a.out_scales = pooled->scales;
+    a.out_stride = pooled->seq_stride_rows;
+    a.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_pool(a, s); }));
+  }
+  const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
+  int32_t* bids = block_ids ? block_ids : at<int32_t>(workspace, L.block_ids);
+  const int32_t* gather_ids = nullptr;
+  if (L.nb_max > cfg->k_blocks) {
+    DSA_TRY(run_block_stage(*cfg, qi, w, pk, n_latents, B, max_latents, bids,
+                            at<float>(workspace, L.block_scores), st, s, 0, 0, nullptr, nullptr));
+    gather_ids = bids;
+  } else if (block_ids) {
+    DSA_CUDA(launch(DSA_KERNEL_OTHER, s, [&] { return launch_identity_blocks(n_latents, B, cfg->k_blocks, block_ids, s); }));
+  }
+  int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
+  DSA_TRY(run_token_stage(*cfg, qi, w, *keys, gather_ids, n_latents, B, max_latents, tids,
+                          at<float>(workspace, L.token_scores), st, s, 0, 0));
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.latents = static_cast<const uint16_t*>(latents);
+  a.lat_stride = latent_seq_stride_rows;
+  a.n_latents = n_latents;
+  a.token_ids = tids;
+  a.k_tokens = cfg->k_tokens;
+  a.swa = static_cast<const uint16_t*>(swa);
+  a.swa_len = swa_len;
+  a.window = cfg->window;
+  a.B = B;
+  a.scale_log2 = tau(*cfg) * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t ctx_len,
+                                     const void* q, const void* q_idx, const float* w,
+                                     const void* latents, const dsa_keys_t* keys,
+                                     const dsa_keys_t* pooled, const void* swa, void* out,
+                                     float* lse, int32_t* token_ids, void* workspace,
+                                     size_t workspace_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (n_q < 0 || ctx_len < 0) return DSA_ERR_INVALID_ARG;
+  const int64_t n_lat = (ctx_len + n_q) / cfg->ratio;
+  if (n_lat > kMaxLatents) return DSA_ERR_INVALID_ARG;
+  if (q == nullptr || q_idx == nullptr || w == nullptr || latents == nullptr || swa == nullptr ||
+      out == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(w) || !aligned16(latents) ||
+      !aligned16(swa) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (token_ids && !aligned16(token_ids))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(keys, 0, false));
+  DSA_TRY(check_keys(pooled, 0, false));
+  if (pooled->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  Layout L;
+  DSA_TRY(check_ws(*cfg, n_q, n_lat, workspace, workspace_bytes, &L));
+  if (n_q == 0) return DSA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
+  const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
+  uint8_t* part = at<uint8_t>(workspace, L.partial);
+  const size_t row_bytes = keys->fmt == DSA_FMT_BF16 ? 256 : 128;
+  uint8_t* part_scales = part + static_cast<size_t>(n_q) * row_bytes;
+  {
+    PoolArgs a{};
+    a.fmt = keys->fmt;
+    a.key_data = keys->data;
+    a.key_scales = keys->scales;
+    a.key_stride = 0;
+    a.max_latents = n_lat;
+    a.B = n_q;
+    a.out_data = part;
+    a.out_scales = part_scales;
+    a.prefill = 1;
+    a.ctx = ctx_len;
+    a.ratio = cfg->ratio;
+    a.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_pool(a, s); }));
+  }
+  int32_t* bids = at<int32_t>(workspace, L.block_ids);
+  DSA_TRY(run_block_stage(*cfg, qi, w, *pooled, nullptr, n_q, n_lat, bids,
+                          at<float>(workspace, L.block_scores), st, s, 1, ctx_len, part,
+                          part_scales));
+  int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
+  DSA_TRY(run_token_stage(*cfg, qi, w, *keys, bids, nullptr, n_q, n_lat, tids,
+                          at<float>(workspace, L.token_scores), st, s, 1, ctx_len));
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.latents = static_cast<const uint16_t*>(latents);
+  a.lat_stride = n_lat;
+  a.token_ids = tids;
+  a.k_tokens = cfg->k_tokens;
+  a.swa = static_cast<const uint16_t*>(swa);
+  a.window = cfg->window;
+  a.B = n_q;
+  a.scale_log2 = tau(*cfg) * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.prefill = 1;
+  a.ctx = ctx_len;
+  a.ratio = cfg->ratio;
+  a.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
+  return DSA_OK;
+}
+
+dsa_status_t dsa_profile_events(int kind, void* const* starts, void* const* ends, int n) {
+  if (kind < 0 || kind >= DSA_KERNEL_KINDS || n < 0) return DSA_ERR_INVALID_ARG;
+  if (n > 0 && (starts == nullptr || ends == nullptr)) return DSA_ERR_INVALID_ARG;
+  Profile& p = g_profile[kind];
+  p.starts = n > 0 ? starts : nullptr;
+  p.ends = n > 0 ? ends : nullptr;
+  p.n = n;
+  p.next = 0;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_launch_counts(uint64_t* counts, int reset) {
+  if (counts == nullptr) return DSA_ERR_INVALID_ARG;
+  for (int k = 0; k < DSA_KERNEL_KINDS; ++k) {
+    counts[k] = g_launches[k];
+    if (reset) g_launches[k] = 0;
+  }
+  return DSA_OK;
+}
+
+dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* info) {
+  if (workspace == nullptr) return DSA_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus h{};
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    return DSA_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  if (h.code != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  if (info) *info = h.info;
+  return static_cast<dsa_status_t>(h.code);
+}
+
+}  // extern "C"
