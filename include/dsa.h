@@ -236,6 +236,36 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
                                      float* lse, int32_t* token_ids, void* workspace,
                                      size_t workspace_bytes, dsa_stream_t stream);
 
+/*
+ * dsa_topk without a workspace. The pages have no counterpart to this call; it
+ * serves callers that cannot allocate device memory: a plugin that runs inside
+ * a host framework which owns all device memory and lends it none, or a
+ * serving loop under a fixed memory budget that forbids allocation once it has
+ * started. It computes exactly what dsa_topk computes (same kernels, same
+ * arguments, bit-identical token_ids) but keeps its candidate scores in a
+ * scratch array that the library defines statically in device memory:
+ * DSA_TOPK_NOALLOC_MAX_SCORES fp32 values (8 MiB), held on every GPU that
+ * loads the library until the process exits. It calls no allocator.
+ *   - Limit: B * n_cand <= DSA_TOPK_NOALLOC_MAX_SCORES, where n_cand is
+ *     8 * k_blocks (block_ids given) or max_latents rounded up to 8 (block_ids
+ *     NULL); larger requests return DSA_ERR_WORKSPACE before any launch.
+ *   - Set-up: the first call on each device looks up that device's address of
+ *     the scratch array (the calling thread's current device must be the one
+ *     the stream belongs to); make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same scratch array, which keeps
+ *     the last call's contents (every score the kernels read is written first
+ *     by the same call, so nothing needs clearing). Calls that may overlap on
+ *     the GPU (different streams without ordering) race on it: serialise them.
+ *   - Device-side input checks (ids outside a sequence, unordered block ids)
+ *     have no status word to write here: the offending elements are skipped
+ *     and nothing is reported. Use dsa_topk to have them reported.
+ */
+#define DSA_TOPK_NOALLOC_MAX_SCORES (1 << 21)
+dsa_status_t dsa_topk_noalloc(const dsa_config_t* cfg, const void* q_idx, const float* w,
+                              const dsa_keys_t* keys, const int32_t* block_ids,
+                              const int32_t* n_latents, int B, int64_t max_latents,
+                              int32_t* token_ids, dsa_stream_t stream);
+
 /* Kernel kinds, for the timing hook and the launch counters below. */
 typedef enum {
   DSA_KERNEL_POOL = 0,    /* block-key pooling */

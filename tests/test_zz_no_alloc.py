@@ -1,0 +1,74 @@
+"""dsa_topk_noalloc, the token stage for callers that cannot allocate device
+memory (its candidate scores live in a scratch array the library defines
+statically), gives the same token ids as dsa_topk with a caller workspace, on
+two calls in a row (the shared scratch keeps the previous call's contents).
+
+This file is collected last on purpose, so that a run stopping at the first
+failure has run every other test first; it also passes alone in a fresh
+process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import two_tier_sparse_gb300 as dsa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    from two_tier_sparse_gb300 import build
+    build.build()
+    dsa.load()
+    torch.cuda.set_device(cuda_device)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("fmt,ratio,T,k_blocks,gathered", [
+    ("mxfp8", 1, [20000, 9001, 777, 5], 96, True),
+    ("bf16", 2, [4096, 1000, 30], 2048, False),
+])
+def test_noalloc_topk_matches_topk(fmt, ratio, T, k_blocks, gathered):
+    inp = synth.decode_inputs(T, ratio, fmt, seed=40)
+    cfg = dsa.config(k_blocks=k_blocks, ratio=ratio)
+    B, cap = inp.B, inp.cap
+    keys = dsa.Keys(fmt, _dev(inp.keys.data),
+                    None if inp.keys.scales is None else _dev(inp.keys.scales))
+    q_idx, w, n_lat = _dev(inp.q_idx), _dev(inp.w), _dev(inp.n_latents)
+    ws = dsa.workspace(cfg, B, cap)
+    bids = None
+    if gathered:
+        nbc = cap // 8
+        shape = (B, nbc, 128)
+        pdat = torch.zeros(shape, dtype=torch.int16 if fmt == "bf16" else torch.uint8,
+                           device="cuda")
+        psc = None if fmt == "bf16" else torch.zeros((B, nbc, 4), dtype=torch.uint8,
+                                                     device="cuda")
+        pooled = dsa.Keys(fmt, pdat, psc)
+        dsa.pool_index_keys(cfg, keys, n_lat, cap, pooled, ws)
+        bids = torch.empty((B, k_blocks), dtype=torch.int32, device="cuda")
+        dsa.index_blocks(cfg, q_idx, w, pooled, n_lat, cap, bids, ws)
+    ref = torch.empty((B, cfg.k_tokens), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, q_idx, w, keys, bids, n_lat, cap, ref, ws)
+    assert dsa.read_device_status(ws)[0] == 0
+    for _ in range(2):
+        got = torch.full((B, cfg.k_tokens), -7, dtype=torch.int32, device="cuda")
+        dsa.topk_noalloc(cfg, q_idx, w, keys, bids, n_lat, cap, got)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+
+
+def test_noalloc_topk_rejects_requests_beyond_its_scratch():
+    cfg = dsa.config(k_blocks=2048)
+    lib = dsa.load()
+    # 129 queries x 16384 candidates > 2^21 scores: refused before any launch.
+    keys = dsa._Keys(0, 16, None, 1 << 20)
+    code = lib.dsa_topk_noalloc(ctypes.byref(cfg), 16, 16, ctypes.byref(keys), 16, 16, 129,
+                                1 << 20, 16, None)
+    assert dsa.STATUS[code] == "DSA_ERR_WORKSPACE"

@@ -31,7 +31,9 @@ STATUS = {
 EXPORTS = ("dsa_default_config", "dsa_status_string", "dsa_workspace_size",
            "dsa_pool_index_keys", "dsa_index_blocks", "dsa_topk", "dsa_sparse_attn_decode",
            "dsa_decode_step", "dsa_sparse_attn_prefill", "dsa_read_device_status",
-           "dsa_profile_events", "dsa_launch_counts")
+           "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc")
+
+TOPK_NOALLOC_MAX_SCORES = 1 << 21
 
 KERNEL_KINDS = ("pool", "scan", "select", "attn", "other")
 
@@ -87,6 +89,7 @@ def load() -> ctypes.CDLL:
         lib.dsa_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.dsa_profile_events.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32]
         lib.dsa_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
+        lib.dsa_topk_noalloc.argtypes = [cp, vp, vp, kp, vp, vp, i32, i64, vp, vp]
         for f in EXPORTS:
             if f not in ("dsa_default_config", "dsa_status_string"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -167,6 +170,18 @@ def topk(cfg, q_idx, w, keys: Keys, block_ids, n_latents, max_latents, token_ids
     _check(load().dsa_topk(ctypes.byref(cfg), _p(q_idx), _p(w), ctypes.byref(keys.c()),
                            _p(block_ids), _p(n_latents), B, max_latents, _p(token_ids),
                            _p(token_scores), _p(ws), ws.numel(), _stream(stream)), "dsa_topk")
+
+
+def topk_noalloc(cfg, q_idx, w, keys: Keys, block_ids, n_latents, max_latents, token_ids,
+                 stream=None):
+    """dsa_topk without a workspace: for callers that cannot allocate device
+    memory. Candidate scores go to a scratch array the library defines
+    statically (at most TOPK_NOALLOC_MAX_SCORES values for the whole batch);
+    calls that may overlap on the GPU share it and must be serialised."""
+    B = q_idx.shape[0]
+    _check(load().dsa_topk_noalloc(ctypes.byref(cfg), _p(q_idx), _p(w), ctypes.byref(keys.c()),
+                                   _p(block_ids), _p(n_latents), B, max_latents, _p(token_ids),
+                                   _stream(stream)), "dsa_topk_noalloc")
 
 
 def sparse_attn_decode(cfg, q, latents, n_latents, token_ids, swa, swa_len, out, ws, lse=None,

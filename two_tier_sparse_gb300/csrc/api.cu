@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -594,3 +595,65 @@ dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dsa_topk_noalloc: the token stage with its candidate scores in a statically
+// defined device array, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Candidate-score scratch of dsa_topk_noalloc (8 MiB on every device that
+// loads the library). Device code could name it directly; host code must use
+// the address cudaGetSymbolAddress returns for the current device, since the
+// symbol itself is only a host-side stand-in.
+static __device__ __align__(256) float g_topk_scratch[DSA_TOPK_NOALLOC_MAX_SCORES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_topk_scratch on the current device, looked up once per
+// device (the first call on a device does this set-up).
+dsa_status_t topk_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) {
+      return DSA_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" dsa_status_t dsa_topk_noalloc(const dsa_config_t* cfg, const void* q_idx,
+                                         const float* w, const dsa_keys_t* keys,
+                                         const int32_t* block_ids, const int32_t* n_latents,
+                                         int B, int64_t max_latents, int32_t* token_ids,
+                                         dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents) return DSA_ERR_INVALID_ARG;
+  if (q_idx == nullptr || w == nullptr || n_latents == nullptr || token_ids == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(token_ids) ||
+      (block_ids && !aligned16(block_ids))) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(keys, max_latents, true));
+  const int64_t n_cand = block_ids ? static_cast<int64_t>(cfg->k_blocks) * kBlock
+                                   : (max_latents + 7) / 8 * 8;
+  if (static_cast<int64_t>(B) * n_cand > DSA_TOPK_NOALLOC_MAX_SCORES) return DSA_ERR_WORKSPACE;
+  if (B == 0) return DSA_OK;
+  float* scores = nullptr;
+  DSA_TRY(topk_scratch(&scores));
+  return run_token_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *keys, block_ids,
+                         n_latents, B, max_latents, token_ids, scores, nullptr,
+                         static_cast<cudaStream_t>(stream), 0, 0);
+}
