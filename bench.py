@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import shutil
 import subprocess
 import sys
 import threading
@@ -43,6 +44,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--batch", type=int, default=0,
+                   help="override the workload's batch (smaller cases for profiling)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0,
@@ -69,53 +72,55 @@ def measured_peaks():
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """Samples SM clocks, power and throttle reasons with single-shot
+    nvidia-smi queries from a background thread (about every 100 ms) while the
+    timed region runs."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
-        self.proc = None
         self.lines = []
+        self.stop = threading.Event()
+        self.t = None
+
+    def _run(self):
+        while not self.stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                     "--format=csv,noheader,nounits"],
+                    capture_output=True, text=True, timeout=5).stdout
+                self.lines.extend(x.strip() for x in out.splitlines() if x.strip())
+            except Exception:
+                pass
+            self.stop.wait(0.1)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
+        if shutil.which("nvidia-smi"):
+            self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
-        except Exception:
-            self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.t.join(timeout=2)
+        self.stop.set()
+        if self.t is not None:
+            self.t.join(timeout=10)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 7:
                 continue
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            for n, v in zip(names, parts[3:7]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
@@ -203,6 +208,8 @@ def run_ours(args):
     if spec["kind"] != "decode":
         raise SystemExit("bench.py times the decode step; prefill is measured by bench_prefill")
     B, T, ratio, fmt = spec["B"], spec["T"], spec["ratio"], spec["key_fmt"]
+    if args.batch:
+        B = args.batch
     # Every rank decodes its own batch: seeds differ per rank.
     t0 = time.time()
     inp = synth.decode_inputs([T] * B, ratio, fmt, spec["seed"] + 1000 * rank)
@@ -257,6 +264,17 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # nvidia-smi samples every 100 ms: keep the GPU under the same load for
+        # 1.5 s before the timed steps so the samples describe the timed region.
+        dsa.profile_events("scan", [], [])
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        dsa.profile_events("scan", ks, ke)
+        dsa.launch_counts(reset=True)
         for i in range(K):
             flush.zero_()
             ev_s[i].record()
@@ -368,6 +386,8 @@ def run_ours(args):
                    "step_hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
                    "input_gen_s": round(gen_s, 1)},
         "roofline": {"kernel": "scan (indexer scores, tcgen05)", "bound": "hbm",
+                     "launch_ms_block_stage": float(np.mean(scan_ms[0::2])) if blk_rows else None,
+                     "launch_ms_token_stage": float(np.mean(scan_ms[1::2] if blk_rows else scan_ms)),
                      "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": bytes_per_launch,

@@ -331,3 +331,34 @@ def test_prefill(fmt, ratio, ctx, n_q):
             check_ids(tok[i], r["token_ids"], lambda j: pos[j], cfg.k_tokens, f"q{i}")
         r2 = O.prefill_query(oc, pf, i, kv, pooled, token_ids=tok[i])
         check_out(out[i], lse[i], r2["out"], r2["lse"], f"q{i}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_scan_many_short_queries(fmt):
+    """One or two tiles per query, so the scan pipeline switches query on
+    almost every tile (the per-query operand slots are rebuilt constantly)."""
+    rng = np.random.default_rng(41)
+    T = [int(t) for t in rng.integers(1, 300, 200)]
+    inp = synth.decode_inputs(T, 1, fmt, seed=41)
+    cfg = dsa.config(k_blocks=4, k_tokens=24)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    bids = torch.empty((inp.B, 4), dtype=torch.int32, device="cuda")
+    bsc = torch.empty((inp.B, d.cap // 8), dtype=torch.float32, device="cuda")
+    dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws, block_scores=bsc)
+    tok = torch.empty((inp.B, 24), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, None, d.n_lat, d.cap, tok, d.ws)
+    assert d.status()[0] == 0
+    bids, bsc, tok = bids.cpu().numpy(), bsc.cpu().numpy(), tok.cpu().numpy()
+    oc = oracle_cfg(cfg)
+    for b in range(inp.B):
+        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        nb = len(r["block_scores"])
+        check_scores(bsc[b, :nb], r["block_scores"], f"block scores {b}")
+        check_ids(bids[b], r["block_ids"], lambda i: r["block_scores"][i], 4, f"blocks {b}")
+        single = O.select_query(O.StepConfig(k_blocks=1 << 20, k_tokens=24), inp.q_idx[b],
+                                inp.w[b], O.decode_keys(fmt, inp.keys.data[b][:T[b]],
+                                None if inp.keys.scales is None else inp.keys.scales[b][:T[b]]),
+                                np.zeros(((T[b] + 7) // 8, 128)), T[b])
+        pos = {int(t): s for t, s in zip(single["cand"], single["token_scores"])}
+        check_ids(tok[b], single["token_ids"], lambda i: pos[i], 24, f"tokens {b}")

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -18,7 +20,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace regions for n queries over sequences of at most max_latents latents.
 struct Layout {
-  size_t status, block_scores, token_scores, block_ids, token_ids, partial, total;
+  size_t status, block_scores, token_scores, block_ids, token_ids, total;
   int64_t nb_max, n_cand;
 };
 
@@ -39,8 +41,6 @@ Layout layout(const dsa_config_t& c, int n, int64_t max_latents) {
   off = align_up(off + static_cast<size_t>(n) * c.k_blocks * 4);
   L.token_ids = off;
   off = align_up(off + static_cast<size_t>(n) * c.k_tokens * 4);
-  L.partial = off;  // prefill partial blocks: n rows of 128 B/256 B + scales
-  off = align_up(off + static_cast<size_t>(n) * (kIdxDim * 2 + 4));
   L.total = off;
   return L;
 }
@@ -133,7 +133,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              const dsa_keys_t& pooled, const int32_t* n_lat, int B,
                              int64_t max_latents, int32_t* block_ids, float* scores,
                              DeviceStatus* st, cudaStream_t s, int prefill, int64_t ctx,
-                             const void* partial, const uint8_t* partial_scales) {
+                             const dsa_keys_t* partial_keys) {
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
   ScanArgs sa{};
   sa.fmt = pooled.fmt;
@@ -151,10 +151,22 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
   sa.prefill = prefill;
   sa.ctx = ctx;
   sa.ratio = c.ratio;
-  sa.partial_data = partial;
-  sa.partial_scales = partial_scales;
   sa.status = st;
   DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&] { return launch_scan(sa, device_sm_count(), s); }));
+  if (prefill) {
+    PartialArgs pa{};
+    pa.fmt = pooled.fmt;
+    pa.key_data = partial_keys->data;
+    pa.key_scales = partial_keys->scales;
+    pa.q_idx = q_idx;
+    pa.w = w;
+    pa.n_q = B;
+    pa.ctx = ctx;
+    pa.ratio = c.ratio;
+    pa.scores = scores;
+    pa.n_rows = nb_max;
+    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_prefill_partial(pa, s); }));
+  }
   SelectArgs se{};
   se.scores = scores;
   se.n = nb_max;
@@ -210,6 +222,32 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
 }
 
 }  // namespace
+
+cudaError_t encode_tma_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                          uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                          uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      return cudaErrorNotSupported;
+    }
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 int device_sm_count() {
   static int cached[64] = {0};
@@ -340,7 +378,7 @@ dsa_status_t dsa_index_blocks(const dsa_config_t* cfg, const void* q_idx, const 
   float* scores = block_scores ? block_scores : at<float>(workspace, L.block_scores);
   return run_block_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *pooled, n_latents, B,
                          max_latents, block_ids, scores, at<DeviceStatus>(workspace, L.status),
-                         static_cast<cudaStream_t>(stream), 0, 0, nullptr, nullptr);
+                         static_cast<cudaStream_t>(stream), 0, 0, nullptr);
 }
 
 dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w,
@@ -457,7 +495,7 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   const int32_t* gather_ids = nullptr;
   if (L.nb_max > cfg->k_blocks) {
     DSA_TRY(run_block_stage(*cfg, qi, w, pk, n_latents, B, max_latents, bids,
-                            at<float>(workspace, L.block_scores), st, s, 0, 0, nullptr, nullptr));
+                            at<float>(workspace, L.block_scores), st, s, 0, 0, nullptr));
     gather_ids = bids;
   } else if (block_ids) {
     DSA_CUDA(launch(DSA_KERNEL_OTHER, s, [&] { return launch_identity_blocks(n_latents, B, cfg->k_blocks, block_ids, s); }));
@@ -512,29 +550,9 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
   const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
-  uint8_t* part = at<uint8_t>(workspace, L.partial);
-  const size_t row_bytes = keys->fmt == DSA_FMT_BF16 ? 256 : 128;
-  uint8_t* part_scales = part + static_cast<size_t>(n_q) * row_bytes;
-  {
-    PoolArgs a{};
-    a.fmt = keys->fmt;
-    a.key_data = keys->data;
-    a.key_scales = keys->scales;
-    a.key_stride = 0;
-    a.max_latents = n_lat;
-    a.B = n_q;
-    a.out_data = part;
-    a.out_scales = part_scales;
-    a.prefill = 1;
-    a.ctx = ctx_len;
-    a.ratio = cfg->ratio;
-    a.status = st;
-    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_pool(a, s); }));
-  }
   int32_t* bids = at<int32_t>(workspace, L.block_ids);
   DSA_TRY(run_block_stage(*cfg, qi, w, *pooled, nullptr, n_q, n_lat, bids,
-                          at<float>(workspace, L.block_scores), st, s, 1, ctx_len, part,
-                          part_scales));
+                          at<float>(workspace, L.block_scores), st, s, 1, ctx_len, keys));
   int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
   DSA_TRY(run_token_stage(*cfg, qi, w, *keys, bids, nullptr, n_q, n_lat, tids,
                           at<float>(workspace, L.token_scores), st, s, 1, ctx_len));

@@ -33,12 +33,6 @@ struct PoolArgs {
   void* out_data;
   uint8_t* out_scales;
   int64_t out_stride;
-  // Prefill: query b sees (ctx + b + 1) / ratio latents of one shared key
-  // array (key_stride 0); only a partially visible last block is pooled, into
-  // output row b. Queries whose last block is complete write nothing.
-  int prefill;
-  int64_t ctx;
-  int ratio;
   DeviceStatus* status;
 };
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s);
@@ -68,16 +62,41 @@ struct ScanArgs {
   int64_t n_rows;  // rows per query (score row stride)
   float* scores;   // [B, n_rows]
   int B;
-  // Prefill: query b sees n_latents = (ctx + b + 1) / ratio and, in
-  // ROWS_BLOCKS mode, a partially visible last block is pooled on the fly.
+  // Prefill: query b sees n_latents = (ctx + b + 1) / ratio latents of one
+  // shared key array (key_stride 0).
   int prefill;
   int64_t ctx;
   int ratio;
-  const void* partial_data;       // prefill ROWS_BLOCKS: pooled partial block of query b
-  const uint8_t* partial_scales;  // at row b
   DeviceStatus* status;
 };
+// In prefill ROWS_BLOCKS mode only complete blocks are scored; a query's
+// partially visible last block is left at -inf for launch_prefill_partial.
 cudaError_t launch_scan(const ScanArgs& a, int num_sms, cudaStream_t s);
+
+// Prefill: for each query whose last visible block is incomplete, pool that
+// block over its visible members (fp32 sum in order, / count, rounded to the
+// key format), score it against the query's index heads and store the score
+// at scores[b * n_rows + block].
+struct PartialArgs {
+  int fmt;
+  const void* key_data;
+  const uint8_t* key_scales;
+  const uint16_t* q_idx;
+  const float* w;
+  int n_q;
+  int64_t ctx;
+  int ratio;
+  float* scores;
+  int64_t n_rows;
+};
+cudaError_t launch_prefill_partial(const PartialArgs& a, cudaStream_t s);
+
+// Tensor map of a row-major 2-D array [rows][row_bytes] of elem_bytes-sized
+// elements (inner extent `inner` elements), 128-byte swizzle, box
+// {box_inner, box_rows}.
+cudaError_t encode_tma_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                          uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                          uint32_t box_rows);
 
 // Top-k by (score desc, index asc) among candidates with score > -inf; ids
 // are written ascending, padded with -1.

@@ -3,172 +3,287 @@
 // score = sum_h w_h * ReLU(q_h . k) is the one this library fixes).
 //
 // Per query the scores are one skinny contraction: keys [rows x 128] times
-// q_idx^T [128 x 16 heads]. Tiles of 128 key rows are the M side of a
-// tcgen05.mma (M = 128, N = 16, fp32 accumulators in tensor memory), so the
-// key stream stays HBM-bound instead of CUDA-core-bound (4096 flop per key).
+// q_idx^T [128 x 16 heads], 4096 flop per key. Tiles of 128 key rows are the
+// M side of a tcgen05.mma (M = 128, N = 16, fp32 accumulators in tensor
+// memory), which keeps the key stream HBM-bound: CUDA-core FMA could not keep
+// up with HBM at 31 flop per byte.
 //
-//  * bf16 keys are copied into 128-byte-swizzled shared tiles by cp.async and
-//    used directly as the bf16 A operand.
-//  * MXFP8 keys (e4m3 codes + one UE8M0 scale per 32 values) are converted
-//    code by code to f16 (exact: every e4m3 value is an f16 normal) and each
-//    32-wide group gets its own accumulator (4 x 16 TMEM columns), so the
-//    power-of-two group scales are applied exactly in the epilogue. The index
-//    query is taken to f16 with a power-of-two scale per head that puts its
-//    largest element in [2^14, 2^15); a bf16 value is then exact in f16 unless
-//    it is below 2^-31 of its head's largest element.
-// The epilogue thread of TMEM lane r reads the 16 head dot products of row r
-// and writes score = sum_h w_h * max(0, dot_h), summed in head order.
-#include <algorithm>
-
+// A persistent CTA per SM runs a warp-specialised pipeline over its share of
+// (query, tile) pairs, with four tiles in flight in tensor memory. Tiles
+// alternate between two halves of the CTA (tile i belongs to half i % 2), and
+// each half has its own producer warp and load ring: small gathered boxes
+// stream at about twice the rate with two independent producers per SM.
+//   warps 0-1  producers: TMA tiled loads (128-byte swizzle) of the tile's
+//              key rows: one box of 128 rows for block keys or a plain latent
+//              range, one box of 8 rows per candidate block otherwise; MXFP8
+//              scales arrive by 4-byte cp.async on the same mbarrier;
+//   warp 2     MMA issuer: 8 MMAs (K = 128) per tile;
+//   warps 3-10 two math sets of four warps, set k for half k.
+//              Thread = TMEM lane = key row of the tile.
+// bf16 keys: the swizzled raw tile is the MMA's A operand as loaded.
+// MXFP8 keys (e4m3 codes + one UE8M0 scale per 32 values): each math thread
+// converts its own row code by code to f16 (exact: every e4m3 value is an
+// f16 normal) and writes it into tensor memory, where the MMA reads A; each
+// 32-wide group gets its own accumulator (4 x 16 TMEM columns), so the
+// power-of-two scales are applied exactly in the epilogue. The index query is
+// taken to f16 with a power-of-two scale per head that puts its largest
+// element in [2^14, 2^15), which keeps every bf16 element exact unless it is
+// below 2^-31 of its head's largest.
+// The epilogue of tile i - 4 runs before tile i is prepared and writes
+// score = sum_h w_h * max(0, dot_h), summed in head order.
 #include "kernels.h"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kTile = 128;   // key rows per MMA (M)
+constexpr int kTile = 128;          // key rows per tile (MMA M)
+constexpr int kThreads = 352;       // 2 producers, MMA, 2 x 4 math warps
+constexpr int kMmaWarp = 2;
+constexpr int kMathWarp0 = 3;
+constexpr int kMathThreads = 128;   // per math set
+constexpr int kSlots = 4;           // tiles in flight (TMEM slots)
+constexpr int kQRing = 3;           // index-query slots per math set
+
 template <int FMT>
 struct Plan;
-
-// Shared-memory plan (offsets from a 1024-aligned base); kStages is the
-// depth of the cp.async ring (kStages - 1 tiles in flight).
 template <>
 struct Plan<DSA_FMT_BF16> {
-  static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kTile * 256;            // 2 K-atoms x 128 rows x 128 B
-  static constexpr int kRing = 0;
-  static constexpr int kQ = kRing + kStages * kStageBytes;  // 2 atoms x 16 rows x 128 B
-  static constexpr int kMisc = kQ + 4096;
-  static constexpr int kBytes = kMisc + 1024;
-  static constexpr int kTmemCols = 32;
+  static constexpr int kRowBytes = 256;
+  static constexpr int kStages = 3;                // per half
+  static constexpr int kStageBytes = kTile * 256;  // 2 K-atoms x 128 rows x 128 B
+  static constexpr int kAccCols = 16;
+  static constexpr int kSlotCols = 16;             // accumulator only
+  static constexpr int kTmemCols = 64;
 };
 template <>
 struct Plan<DSA_FMT_MXFP8> {
-  static constexpr int kStages = 6;
-  static constexpr int kStageBytes = kTile * 128;            // raw codes, swizzled
-  static constexpr int kRing = 0;
-  static constexpr int kScales = kRing + kStages * kStageBytes;  // kStages x 128 rows x 4 B
-  static constexpr int kOp = kScales + kStages * kTile * 4;       // 2 x f16 operand tiles
-  static constexpr int kOpBytes = kTile * 256;
-  static constexpr int kQ = kOp + 2 * kOpBytes;
-  static constexpr int kMisc = kQ + 4096;
-  static constexpr int kBytes = kMisc + 1024;
-  static constexpr int kTmemCols = 64;
+  static constexpr int kRowBytes = 128;
+  static constexpr int kStages = 5;  // per half
+  static constexpr int kStageBytes = kTile * 128 + kTile * 4;  // codes (swizzled), scales
+  static constexpr int kAccCols = 64;    // 4 groups x 16 heads
+  static constexpr int kSlotCols = 128;  // A operand (64 columns of f16 pairs) + accumulator
+  static constexpr int kTmemCols = 512;
 };
 
-struct Misc {
-  uint64_t bar;
-  uint32_t tmem_base;
+struct TileMeta {
+  uint32_t valid[4];  // row r holds a key
+};
+
+struct QSlot {
   float w[kIdxHeads];
-  float qinv[kIdxHeads];  // 2^-s_h (f16 path) or 1
+  float qinv[kIdxHeads];
+};
+
+struct Shared {
+  uint64_t raw_full[2][5], raw_empty[2][5];
+  uint64_t op_full[kSlots], op_empty[kSlots], acc_full[kSlots], acc_empty[kSlots];
+  uint32_t tmem_base;
+  int abort;
+  TileMeta meta[2][5];
+  QSlot qs[2][kQRing];
+};
+
+template <int FMT>
+struct Layout {
+  using P = Plan<FMT>;
+  static constexpr int kRawStride = (P::kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kRaw = 0;                                // [half][stage]
+  static constexpr int kQ = kRaw + 2 * P::kStages * kRawStride;  // [set][ring] x 4 KB B operands
+  static constexpr int kShared = kQ + 2 * kQRing * 4096;
+  static constexpr int kBytes = kShared + static_cast<int>(sizeof(Shared));
+};
+
+struct Maps {
+  CUtensorMap keys;  // bf16: {128 elems, rows}, box {64, R}; MXFP8: {128 B, rows}, box {128, R}
 };
 
 __device__ __forceinline__ int visible_latents(const ScanArgs& a, int b) {
-  if (a.prefill) return static_cast<int>((a.ctx + b + 1) / a.ratio);
-  return a.n_latents[b];
+  int n = a.prefill ? static_cast<int>((a.ctx + b + 1) / a.ratio) : a.n_latents[b];
+  if (n > a.max_latents) n = static_cast<int>(a.max_latents);
+  return n < 0 ? 0 : n;
 }
 
-// Key row of output row r of query b, or -1 if the row holds no key.
-__device__ __forceinline__ int64_t key_row(const ScanArgs& a, int b, int n_vis, int64_t r) {
-  if (r >= a.n_rows) return -1;
+// Key rows of query b in the contiguous modes. Prefill block rows stop at the
+// last complete block; a partially visible block is scored by its own kernel.
+__device__ __forceinline__ int64_t contiguous_rows(const ScanArgs& a, int n_vis) {
+  int64_t n;
   if (a.mode == ROWS_BLOCKS) {
-    const int64_t nb = (n_vis + 7) / 8;
-    return r < nb ? r : -1;
-  }
-  if (a.mode == ROWS_LATENTS) return r < n_vis ? r : -1;
-  const int64_t bi = r >> 3;
-  if (bi >= a.k_blocks) return -1;
-  const int blk = a.block_ids[static_cast<int64_t>(b) * a.k_blocks + bi];
-  if (blk < 0) return -1;
-  const int64_t t = static_cast<int64_t>(blk) * 8 + (r & 7);
-  return t < n_vis ? t : -1;
-}
-
-// Prefill block rows: the last block of a query that sees it only in part is
-// read from the per-query partial-block buffer instead of the pooled cache.
-__device__ __forceinline__ bool is_partial(const ScanArgs& a, int n_vis, int64_t kr) {
-  return a.prefill && a.mode == ROWS_BLOCKS && (n_vis & 7) != 0 && kr == (n_vis >> 3);
-}
-__device__ __forceinline__ const uint8_t* row_src(const ScanArgs& a, int b, int n_vis, int64_t kr,
-                                                  int64_t seq, const uint8_t* kd, int row_bytes) {
-  if (is_partial(a, n_vis, kr)) {
-    return static_cast<const uint8_t*>(a.partial_data) + static_cast<int64_t>(b) * row_bytes;
-  }
-  return kd + (seq + kr) * row_bytes;
-}
-
-template <int FMT>
-__device__ __forceinline__ void issue_tile_load(const ScanArgs& a, uint32_t sbase, int stage,
-                                                int64_t tile, int64_t tpq) {
-  using P = Plan<FMT>;
-  const int tid = threadIdx.x;
-  const int b = static_cast<int>(tile / tpq);
-  const int64_t r0 = (tile % tpq) * kTile;
-  int n_vis = visible_latents(a, b);
-  if (n_vis > a.max_latents) n_vis = static_cast<int>(a.max_latents);
-  const int64_t seq = static_cast<int64_t>(b) * a.key_stride;
-  if constexpr (FMT == DSA_FMT_BF16) {
-    const uint8_t* kd = static_cast<const uint8_t*>(a.key_data);
-    const uint32_t st = sbase + P::kRing + stage * P::kStageBytes;
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-      const int c = tid + kThreads * j;
-      const int row = c >> 4, cr = c & 15;
-      const int64_t kr = key_row(a, b, n_vis, r0 + row);
-      const uint32_t dst = st + (cr >> 3) * (kTile * 128) + sw128_off(row, cr & 7);
-      if (kr >= 0) {
-        cp_async_16(dst, row_src(a, b, n_vis, kr, seq, kd, 256) + cr * 16);
-      } else {
-        st_shared_v4(dst, make_uint4(0, 0, 0, 0));
-      }
-    }
+    n = a.prefill ? n_vis / 8 : (n_vis + 7) / 8;
   } else {
-    const uint8_t* kd = static_cast<const uint8_t*>(a.key_data);
-    const uint32_t st = sbase + P::kRing + stage * P::kStageBytes;
-#pragma unroll 4
-    for (int j = 0; j < 8; ++j) {
-      const int c = tid + kThreads * j;
-      const int row = c >> 3, cr = c & 7;
-      const int64_t kr = key_row(a, b, n_vis, r0 + row);
-      const uint32_t dst = st + sw128_off(row, cr);
-      if (kr >= 0) {
-        cp_async_16(dst, row_src(a, b, n_vis, kr, seq, kd, 128) + cr * 16);
-      } else {
-        st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+    n = n_vis;
+  }
+  return n < a.n_rows ? n : a.n_rows;
+}
+
+template <int FMT>
+__device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32_t sbase,
+                         int64_t t_begin, int64_t n_tiles, int64_t tpq, int half) {
+  using P = Plan<FMT>;
+  using Lo = Layout<FMT>;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) tma_prefetch_map(&maps.keys);
+  // Gathered mode: lane j < 16 holds the j-th block id of a tile; the ids of
+  // the half's next tile are loaded one iteration ahead.
+  auto fetch_block = [&](int64_t i) -> int {
+    if (a.mode != ROWS_GATHER || lane >= kTile / kBlock || i >= n_tiles) return -1;
+    const int64_t tile = t_begin + i;
+    const int64_t bi = (((tile % tpq) * kTile) >> 3) + lane;
+    if (bi >= a.k_blocks) return -1;
+    return a.block_ids[(tile / tpq) * a.k_blocks + bi];
+  };
+  int blk_next = fetch_block(half);
+  for (int64_t i = half; i < n_tiles; i += 2) {
+    const int blk = blk_next;
+    blk_next = fetch_block(i + 2);
+    const int64_t j = i >> 1;  // the half's own tile counter
+    const int s = static_cast<int>(j % P::kStages);
+    if (j >= P::kStages &&
+        !mbar_wait_abortable(&sh.raw_empty[half][s],
+                             static_cast<uint32_t>((j / P::kStages - 1) & 1), &sh.abort,
+                             a.status, SITE_SCAN)) {
+      return;
+    }
+    const int64_t tile = t_begin + i;
+    const int b = static_cast<int>(tile / tpq);
+    const int64_t r0 = (tile % tpq) * kTile;
+    const int n_vis = visible_latents(a, b);
+    const int64_t seq = static_cast<int64_t>(b) * a.key_stride;
+    const uint32_t raw = sbase + Lo::kRaw + (half * P::kStages + s) * Lo::kRawStride;
+
+    // This lane's run of valid rows [row0, row0 + nrows) of the tile, loaded
+    // as one box of `box_rows` key rows starting at key row y.
+    int row0 = 0, nrows = 0, box_rows = 0;
+    int64_t y = 0;
+    if (a.mode == ROWS_GATHER) {
+      if (blk >= 0) {
+        const int64_t t0 = static_cast<int64_t>(blk) * kBlock;
+        const int64_t v = n_vis - t0;
+        if (v > 0) {
+          row0 = lane * kBlock;
+          nrows = static_cast<int>(v < kBlock ? v : kBlock);
+          box_rows = kBlock;
+          y = seq + t0;
+        }
+      }
+    } else if (lane == 0) {
+      int64_t v = contiguous_rows(a, n_vis) - r0;
+      v = v < 0 ? 0 : (v > kTile ? kTile : v);
+      if (v > 0) {
+        nrows = static_cast<int>(v);
+        box_rows = kTile;
+        y = seq + r0;
       }
     }
-    const int64_t kr = key_row(a, b, n_vis, r0 + tid);
-    const uint32_t sdst = sbase + P::kScales + (stage * kTile + tid) * 4;
-    if (kr >= 0) {
-      const bool part = is_partial(a, n_vis, kr);
-      cp_async_4(sdst, part ? a.partial_scales + static_cast<int64_t>(b) * 4
-                            : a.key_scales + (seq + kr) * 4);
+    uint32_t bytes = static_cast<uint32_t>(box_rows) * P::kRowBytes;
+    uint32_t vm[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) vm[k] = range_bits(k, row0, row0 + nrows);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, o);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vm[k] |= __shfl_xor_sync(0xFFFFFFFFu, vm[k], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = vm[k];
+      mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
+    }
+    __syncwarp();
+    if (nrows > 0) {
+      if constexpr (FMT == DSA_FMT_BF16) {
+        // two K halves (64 elements = 128 bytes each) into the two K-atoms
+        tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
+        tma_load_2d(raw + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y),
+                    &sh.raw_full[half][s]);
+      } else {
+        tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
+      }
+    }
+    if constexpr (FMT == DSA_FMT_MXFP8) {
+      // Scales: lane l copies rows l, l + 32, l + 64, l + 96 (4 bytes each).
+      const uint32_t sc_dst = raw + kTile * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = lane + 32 * k;
+        const int bl = __shfl_sync(0xFFFFFFFFu, blk, r >> 3);  // every lane takes part
+        if ((vm[r >> 5] >> (r & 31)) & 1u) {
+          const int64_t key = (a.mode == ROWS_GATHER)
+                                  ? seq + static_cast<int64_t>(bl) * kBlock + (r & 7)
+                                  : seq + r0 + r;
+          cp_async_4(sc_dst + r * 4, a.key_scales + key * 4);
+        }
+      }
+    }
+    cp_async_mbar_arrive_noinc(&sh.raw_full[half][s]);
+  }
+}
+
+template <int FMT>
+__device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t n_tiles) {
+  using P = Plan<FMT>;
+  using Lo = Layout<FMT>;
+  constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, FMT == DSA_FMT_BF16, false, false);
+  const uint32_t tmem = sh.tmem_base;
+  for (int64_t i = 0; i < n_tiles; ++i) {
+    const int q = static_cast<int>(i % kSlots);
+    const uint32_t u = static_cast<uint32_t>(i / kSlots);
+    if (!mbar_wait_abortable(&sh.op_full[q], u & 1, &sh.abort, a.status, SITE_SCAN)) return;
+    if (i >= kSlots &&
+        !mbar_wait_abortable(&sh.acc_empty[q], (u - 1) & 1, &sh.abort, a.status, SITE_SCAN)) {
+      return;
+    }
+    tc_fence_after();
+    const int set = static_cast<int>(i & 1);
+    const int ring = static_cast<int>((i >> 1) % kQRing);
+    const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
+    const uint32_t slot = tmem + q * P::kSlotCols;
+    if constexpr (FMT == DSA_FMT_BF16) {
+      const int s = static_cast<int>((i >> 1) % P::kStages);
+      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {  // K = 128 in steps of 16
+        const uint64_t ad = sw128_desc(raw + (k >> 2) * (kTile * 128) + (k & 3) * 32, 16, 1024);
+        const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+        mma_f16(slot, ad, bd, idesc, k > 0 ? 1u : 0u);
+      }
+      mma_commit(&sh.acc_full[q]);
+      mma_commit(&sh.raw_empty[set][s]);
     } else {
-      asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(sdst), "r"(127u * 0x01010101u) : "memory");
+      // A in tensor memory: columns [slot, slot + 64) hold the row's 128 f16
+      // values in pairs; group g = k / 2 accumulates into columns 64 + 16 g.
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+        mma_f16_tmem_a(slot + 64 + (k >> 1) * 16, slot + k * 8, bd, idesc, (k & 1) ? 1u : 0u);
+      }
+      mma_commit(&sh.acc_full[q]);
+      mma_commit(&sh.op_empty[q]);
     }
   }
 }
 
-// Index query of query b -> B operand (16 rows x 128, K-major, swizzled).
+// Index query of query b -> ring slot [set][ring] (one math set, 128 threads).
 template <int FMT>
-__device__ __forceinline__ void load_query(const ScanArgs& a, uint32_t sbase, Misc* misc, int b) {
-  using P = Plan<FMT>;
-  const int tid = threadIdx.x;
+__device__ void build_query(const ScanArgs& a, Shared& sh, uint32_t sbase, int b, int mt,
+                            int set, int ring) {
+  using Lo = Layout<FMT>;
   const uint16_t* q = a.q_idx + static_cast<int64_t>(b) * kIdxHeads * kIdxDim;
-  if (tid < kIdxHeads) misc->w[tid] = a.w[static_cast<int64_t>(b) * kIdxHeads + tid];
+  const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
+  QSlot& slot = sh.qs[set][ring];
+  if (mt < kIdxHeads) slot.w[mt] = a.w[static_cast<int64_t>(b) * kIdxHeads + mt];
   if constexpr (FMT == DSA_FMT_BF16) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int c = tid + kThreads * j;
+      const int c = mt + kMathThreads * j;
       const int h = c >> 4, cr = c & 15;
       const uint4 v = *reinterpret_cast<const uint4*>(q + h * kIdxDim + cr * 8);
-      st_shared_v4(sbase + P::kQ + (cr >> 3) * 2048 + sw128_off(h, cr & 7), v);
+      st_shared_v4(qb + (cr >> 3) * 2048 + sw128_off(h, cr & 7), v);
     }
-    if (tid < kIdxHeads) misc->qinv[tid] = 1.0f;
+    if (mt < kIdxHeads) slot.qinv[mt] = 1.0f;
   } else {
-    // 8 threads per head, 16 elements each.
-    const int h = tid >> 3, part = tid & 7;
+    const int h = mt >> 3, part = mt & 7;  // 8 threads per head, 16 elements each
     const uint4 v0 = *reinterpret_cast<const uint4*>(q + h * kIdxDim + part * 16);
     const uint4 v1 = *reinterpret_cast<const uint4*>(q + h * kIdxDim + part * 16 + 8);
     const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -194,188 +309,238 @@ __device__ __forceinline__ void load_query(const ScanArgs& a, uint32_t sbase, Mi
       const __half2 hv = __floats2half2_rn(x[2 * i] * up, x[2 * i + 1] * up);
       hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
     }
-    const uint32_t qb = sbase + P::kQ;
-    const int c0 = 2 * part;  // f16 chunks c0, c0 + 1 (16 B each) of row h
-    st_shared_v4(qb + (c0 >> 3) * 2048 + sw128_off(h, c0 & 7), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    const int c0 = 2 * part;  // f16 chunks c0, c0 + 1 of row h
+    st_shared_v4(qb + (c0 >> 3) * 2048 + sw128_off(h, c0 & 7),
+                 make_uint4(hw[0], hw[1], hw[2], hw[3]));
     st_shared_v4(qb + ((c0 + 1) >> 3) * 2048 + sw128_off(h, (c0 + 1) & 7),
                  make_uint4(hw[4], hw[5], hw[6], hw[7]));
-    if (part == 0) misc->qinv[h] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    if (part == 0) slot.qinv[h] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   }
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) scan_kernel(ScanArgs a, int64_t tpq, int64_t total) {
+__device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_begin,
+                     int64_t n_tiles, int64_t tpq) {
   using P = Plan<FMT>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (sbase - raw);
-  Misc* misc = reinterpret_cast<Misc*>(gbase + P::kMisc);
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
+  using Lo = Layout<FMT>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int set = (warp - kMathWarp0) >> 2;               // tiles i with i % 2 == set
+  const int mt = threadIdx.x - 32 * kMathWarp0 - kMathThreads * set;  // 0..127 within the set
+  const int row = 32 * (warp & 3) + lane;  // TMEM lane = key row of this thread
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const uint32_t tmem = sh.tmem_base;
+  int ring_b0 = -1, ring_b1 = -1, ring_b2 = -1;  // query held by each ring slot
+  // per-thread state of this set's two tiles waiting for their epilogue
+  uint32_t pend_sc0 = 0, pend_sc1 = 0;
+  bool pend_valid0 = false, pend_valid1 = false;
 
-  // Contiguous share of the flattened (query, tile) space.
-  const int64_t per = total / gridDim.x, rem = total % gridDim.x;
-  const int64_t bx = blockIdx.x;
-  const int64_t t_begin = bx * per + (bx < rem ? bx : rem);
-  const int64_t t_end = t_begin + per + (bx < rem ? 1 : 0);
-
-  if (tid == 0) {
-    mbar_init(&misc->bar, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&misc->tmem_base, P::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = misc->tmem_base;
-
-  constexpr int kStages = P::kStages;
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (t_begin + s < t_end) issue_tile_load<FMT>(a, sbase, s, t_begin + s, tpq);
-    cp_async_commit();
-  }
-
-  uint32_t phase = 0;
-  bool ok = true;
-  int cur_b = -1;  // query whose index query sits in shared memory
-  for (int64_t tile = t_begin; tile < t_end && ok; ++tile) {
-    const int64_t it = tile - t_begin;
-    const int64_t nxt = tile + kStages - 1;
-    if (nxt < t_end) issue_tile_load<FMT>(a, sbase, static_cast<int>(nxt - t_begin) % kStages, nxt, tpq);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    const int stage = static_cast<int>(it % kStages);
+  auto epilogue = [&](int64_t e) -> bool {
+    const int q = static_cast<int>(e % kSlots);
+    const int pe = static_cast<int>((e >> 1) & 1);
+    const int64_t tile = t_begin + e;
     const int b = static_cast<int>(tile / tpq);
-    const int64_t r0 = (tile % tpq) * kTile;
-
-    // Every thread has finished the previous epilogue (which reads the query
-    // data) and every thread's copies of this tile have landed.
-    __syncthreads();
-    if (b != cur_b) {
-      load_query<FMT>(a, sbase, misc, b);
-      cur_b = b;
+    const int64_t r = (tile % tpq) * kTile + row;
+    if (!mbar_wait_abortable(&sh.acc_full[q], static_cast<uint32_t>((e / kSlots) & 1), &sh.abort,
+                             a.status, SITE_SCAN)) {
+      return false;
     }
-
-    uint32_t my_scales = 0;
-    uint32_t a_base;
-    if constexpr (FMT == DSA_FMT_BF16) {
-      a_base = sbase + P::kRing + stage * P::kStageBytes;
-    } else {
-      const uint32_t rawt = sbase + P::kRing + stage * P::kStageBytes;
-      const uint32_t op = sbase + P::kOp + static_cast<uint32_t>(it & 1) * P::kOpBytes;
-      const int row = tid;
-      asm volatile("ld.shared.u32 %0, [%1];\n"
-                   : "=r"(my_scales)
-                   : "r"(sbase + P::kScales + (stage * kTile + row) * 4));
-#pragma unroll
-      for (int cr = 0; cr < 8; ++cr) {
-        const uint4 v = ld_shared_v4(rawt + sw128_off(row, cr));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-              static_cast<__nv_fp8x2_storage_t>(wv[i] & 0xFFFF), __NV_E4M3);
-          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-              static_cast<__nv_fp8x2_storage_t>(wv[i] >> 16), __NV_E4M3);
-          h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-          h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-        }
-        const int c0 = 2 * cr;
-        st_shared_v4(op + (c0 >> 3) * (kTile * 128) + sw128_off(row, c0 & 7),
-                     make_uint4(h[0], h[1], h[2], h[3]));
-        st_shared_v4(op + ((c0 + 1) >> 3) * (kTile * 128) + sw128_off(row, (c0 + 1) & 7),
-                     make_uint4(h[4], h[5], h[6], h[7]));
-      }
-      a_base = op;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t qb = sbase + P::kQ;
-      if constexpr (FMT == DSA_FMT_BF16) {
-        constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, true, false, false);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = sw128_desc(a_base + (k >> 2) * (kTile * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
-          mma_f16(tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
-        }
-      } else {
-        constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, false, false, false);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // group g = k / 2 -> accumulator columns 16 g
-          const uint64_t ad = sw128_desc(a_base + (k >> 2) * (kTile * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
-          mma_f16(tmem + (k >> 1) * 16, ad, bd, idesc, (k & 1) ? 1u : 0u);
-        }
-      }
-      mma_commit(&misc->bar);
-    }
-    ok = mbar_wait(&misc->bar, phase, a.status, SITE_SCAN);
-    ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA
-    phase ^= 1u;
     tc_fence_after();
-    if (!ok) break;
-
-    // Epilogue: thread tid owns TMEM lane tid = row r0 + tid.
-    const uint32_t lane_addr = tmem_addr(tmem, static_cast<uint32_t>(warp * 32), 0);
+    const uint32_t acc = tmem + lane_base + q * P::kSlotCols + (P::kSlotCols - P::kAccCols);
     float dot[kIdxHeads];
     if constexpr (FMT == DSA_FMT_BF16) {
-      tmem_ld16(lane_addr, dot);
+      tmem_ld16(acc, dot);
     } else {
-      float acc[16];
+      float v[64];
+      tmem_ld64(acc, v);
 #pragma unroll
       for (int h = 0; h < kIdxHeads; ++h) dot[h] = 0.f;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        tmem_ld16(lane_addr + g * 16, acc);
-        const uint32_t sc = (my_scales >> (8 * g)) & 0xFF;
+        const uint32_t sc = ((pe ? pend_sc1 : pend_sc0) >> (8 * g)) & 0xFF;
         const float f = __uint_as_float(sc == 0 ? 0x00400000u : sc << 23);
 #pragma unroll
-        for (int h = 0; h < kIdxHeads; ++h) dot[h] = fmaf(acc[h], f, dot[h]);
+        for (int h = 0; h < kIdxHeads; ++h) dot[h] = fmaf(v[16 * g + h], f, dot[h]);
       }
-#pragma unroll
-      for (int h = 0; h < kIdxHeads; ++h) dot[h] *= misc->qinv[h];
     }
     tc_fence_before();
-    const int64_t r = r0 + tid;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.acc_empty[q]);
+    const QSlot& slot = sh.qs[set][(e >> 1) % kQRing];
     if (r < a.n_rows) {
-      int n_vis = visible_latents(a, b);
-      if (n_vis > a.max_latents) n_vis = static_cast<int>(a.max_latents);
       float s = -INFINITY;
-      if (key_row(a, b, n_vis, r) >= 0) {
+      if (pe ? pend_valid1 : pend_valid0) {
         s = 0.f;
 #pragma unroll
-        for (int h = 0; h < kIdxHeads; ++h) s = fmaf(misc->w[h], fmaxf(dot[h], 0.f), s);
+        for (int h = 0; h < kIdxHeads; ++h) {
+          s = fmaf(slot.w[h], fmaxf(dot[h] * slot.qinv[h], 0.f), s);
+        }
       }
       a.scores[static_cast<int64_t>(b) * a.n_rows + r] = s;
     }
+    return true;
+  };
+
+  // Own tiles i = set, set + 2, ...: the epilogue of tile i - 4 (which shares
+  // tile i's pending entry and TMEM slot), then the preparation of tile i.
+  for (int64_t i = set; i < n_tiles + 4; i += 2) {
+    const int pi = static_cast<int>((i >> 1) & 1);
+    if (i >= 4 && i - 4 < n_tiles) {
+      if (!epilogue(i - 4)) return;
+    }
+    if (i >= n_tiles) continue;
+    const int s = static_cast<int>((i >> 1) % P::kStages);
+    const int q = static_cast<int>(i % kSlots);
+    const int64_t tile = t_begin + i;
+    const int b = static_cast<int>(tile / tpq);
+    const int ring = static_cast<int>((i >> 1) % kQRing);
+    const int held = ring == 0 ? ring_b0 : (ring == 1 ? ring_b1 : ring_b2);
+    if (held != b) {
+      // The ring slot last served tile i - 6, whose epilogue every thread of
+      // the set has finished once all of them reach this barrier.
+      named_sync(1 + set, kMathThreads);
+      build_query<FMT>(a, sh, sbase, b, mt, set, ring);
+      fence_proxy_async_smem();
+      named_sync(1 + set, kMathThreads);
+      if (ring == 0) ring_b0 = b; else if (ring == 1) ring_b1 = b; else ring_b2 = b;
+    }
+    if (!mbar_wait_abortable(&sh.raw_full[set][s],
+                             static_cast<uint32_t>(((i >> 1) / P::kStages) & 1), &sh.abort,
+                             a.status, SITE_SCAN)) {
+      return;
+    }
+    const TileMeta& m = sh.meta[set][s];
+    const bool valid_i = (m.valid[row >> 5] >> (row & 31)) & 1u;
+    if (pi) pend_valid1 = valid_i; else pend_valid0 = valid_i;
+    if constexpr (FMT == DSA_FMT_MXFP8) {
+      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
+      // The A slot of tile i was last read by the MMA of tile i - 4, which the
+      // epilogue above has already seen complete.
+      if (i >= kSlots &&
+          !mbar_wait_abortable(&sh.op_empty[q], static_cast<uint32_t>((i / kSlots - 1) & 1),
+                               &sh.abort, a.status, SITE_SCAN)) {
+        return;
+      }
+      tc_fence_after();
+      // own row: 8 chunks of 16 codes at their swizzled positions
+      uint32_t f[64];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = ld_shared_v4(raw + sw128_off(row, c));
+        asm("{\n .reg .b16 a, b, c, d, e, f, g, h;\n"
+            " mov.b32 {a, b}, %8;\n mov.b32 {c, d}, %9;\n"
+            " mov.b32 {e, f}, %10;\n mov.b32 {g, h}, %11;\n"
+            " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
+            " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n"
+            " cvt.rn.f16x2.e4m3x2 %4, e;\n cvt.rn.f16x2.e4m3x2 %5, f;\n"
+            " cvt.rn.f16x2.e4m3x2 %6, g;\n cvt.rn.f16x2.e4m3x2 %7, h;\n}\n"
+            : "=r"(f[8 * c + 0]), "=r"(f[8 * c + 1]), "=r"(f[8 * c + 2]), "=r"(f[8 * c + 3]),
+              "=r"(f[8 * c + 4]), "=r"(f[8 * c + 5]), "=r"(f[8 * c + 6]), "=r"(f[8 * c + 7])
+            : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+      }
+      uint32_t sc_i;
+      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sc_i) : "r"(raw + kTile * 128 + row * 4));
+      if (pi) pend_sc1 = sc_i; else pend_sc0 = sc_i;
+      tmem_st64(tmem + lane_base + q * P::kSlotCols, f);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.raw_empty[set][s]);
+        mbar_arrive(&sh.op_full[q]);
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.op_full[q]);
+    }
   }
-  cp_async_wait<0>();
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_kernel(ScanArgs a, const __grid_constant__ Maps maps, int64_t tpq, int64_t total) {
+  using P = Plan<FMT>;
+  using Lo = Layout<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw + (sbase - raw) + Lo::kShared);
+  const int warp = threadIdx.x >> 5;
+
+  const int64_t per = total / gridDim.x, rem = total % gridDim.x;
+  const int64_t bx = blockIdx.x;
+  const int64_t t_begin = bx * per + (bx < rem ? bx : rem);
+  const int64_t n_tiles = per + (bx < rem ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int h = 0; h < 2; ++h) {
+      for (int s = 0; s < P::kStages; ++s) {
+        // raw_full: the producer's expect_tx arrival + one cp.async arrival per lane
+        mbar_init(&sh.raw_full[h][s], 1 + 32);
+        mbar_init(&sh.raw_empty[h][s], FMT == DSA_FMT_BF16 ? 1 : 4);
+      }
+    }
+    for (int q = 0; q < kSlots; ++q) {
+      mbar_init(&sh.op_full[q], 4);
+      mbar_init(&sh.op_empty[q], 1);
+      mbar_init(&sh.acc_full[q], 1);
+      mbar_init(&sh.acc_empty[q], 4);
+    }
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, P::kTmemCols);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  tc_fence_after();
+
+  if (warp < kMmaWarp) {
+    producer<FMT>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
+  } else if (warp == kMmaWarp) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<FMT>(a, sh, sbase, n_tiles);
+    __syncwarp();
+  } else {
+    math<FMT>(a, sh, sbase, t_begin, n_tiles, tpq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, P::kTmemCols);
+    tmem_dealloc(sh.tmem_base, P::kTmemCols);
   }
 }
 
 template <int FMT>
 cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
-  using P = Plan<FMT>;
+  using Lo = Layout<FMT>;
   const int64_t tpq = (a.n_rows + kTile - 1) / kTile;
   const int64_t total = tpq * a.B;
   if (total == 0) return cudaSuccess;
-  const int smem = P::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(scan_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // Rows the tensor map covers: every sequence's stride, and only the last
+  // sequence's own rows (a box reaching past them reads zeros).
+  int64_t last_rows;
+  if (a.mode == ROWS_BLOCKS) {
+    last_rows = a.prefill ? a.max_latents / 8 : (a.max_latents + 7) / 8;
+  } else {
+    last_rows = a.max_latents;
+  }
+  const int64_t rows = (a.prefill ? 0 : (a.B - 1) * a.key_stride) + last_rows;
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  const int box_rows = (a.mode == ROWS_GATHER) ? kBlock : kTile;
+  cudaError_t e = cudaSuccess;
+  if (rows > 0) {
+    if (FMT == DSA_FMT_BF16) {
+      e = encode_tma_2d(&maps.keys, a.key_data, /*elem_bytes=*/2, /*inner=*/128, rows,
+                        /*row_bytes=*/256, /*box_inner=*/64, box_rows);
+    } else {
+      e = encode_tma_2d(&maps.keys, a.key_data, 1, 128, rows, 128, 128, box_rows);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  const int smem = Lo::kBytes + 1024;
+  e = cudaFuncSetAttribute(scan_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int per_sm = (FMT == DSA_FMT_BF16) ? 1 : 2;
-  const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(num_sms) * per_sm);
-  scan_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, tpq, total);
+  const int64_t grid = total < num_sms ? total : num_sms;
+  scan_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, maps, tpq, total);
   return cudaGetLastError();
 }
 
