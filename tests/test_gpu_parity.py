@@ -362,3 +362,25 @@ def test_scan_many_short_queries(fmt):
                                 np.zeros(((T[b] + 7) // 8, 128)), T[b])
         pos = {int(t): s for t, s in zip(single["cand"], single["token_scores"])}
         check_ids(tok[b], single["token_ids"], lambda i: pos[i], 24, f"tokens {b}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_select_all_scores_tied(fmt):
+    """Weights 0 make every score 0: both tiers must keep the lowest indices
+    (the tie rule), whatever path the selection takes for heavy ties."""
+    inp = synth.decode_inputs([40000, 30001], 1, fmt, seed=42)
+    inp.w[:] = 0.0
+    cfg = dsa.config(k_blocks=64, k_tokens=100)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    bids = torch.empty((inp.B, 64), dtype=torch.int32, device="cuda")
+    dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws)
+    tok = torch.empty((inp.B, 100), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, bids, d.n_lat, d.cap, tok, d.ws)
+    tok_all = torch.empty((inp.B, 100), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, None, d.n_lat, d.cap, tok_all, d.ws)
+    assert d.status()[0] == 0
+    for b in range(inp.B):
+        assert bids[b].tolist() == list(range(64))
+        assert tok[b].tolist() == list(range(100))
+        assert tok_all[b].tolist() == list(range(100))

@@ -3,12 +3,19 @@
 // recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse attention";
 // ties to the lower index, the rule this library fixes).
 //
-// One CTA per query. Scores map to order-preserving 32-bit keys; a 4-pass
-// radix select (8 bits per pass, most significant first) finds the key T of
-// the k-th best candidate and how many candidates equal to T still fit. A
-// compaction pass then takes, in index order, every key > T and the first
-// `remaining` keys == T, so the ids come out ascending and ties resolve to the
-// lower index with no sort. Keys are cached in shared memory when they fit.
+// One CTA per query. Scores map to order-preserving 32-bit keys (larger score,
+// larger key; -0 as +0). The selection then works on exact integers
+// t = key - kmin (kmin the smallest valid key of the query):
+//   1. a radix select on t with 12-bit digits taken from the top of t's range
+//      (so the first histogram already spans the keys' own spread) narrows,
+//      level by level, to the digit bin that holds the k-th best key and how
+//      many of its members are still needed; it stops once that bin holds at
+//      most 256 candidates or all its members share one key;
+//   2. a small bin is ranked exactly by (key desc, index asc) and its best
+//      members are marked; in a bin of equal keys the first ones in index
+//      order are taken;
+//   3. one compaction pass in index order writes every key above the bin and
+//      the chosen bin members, so ids come out ascending with no sort.
 #include "kernels.h"
 
 namespace dsa {
@@ -17,21 +24,20 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int64_t kCacheMax = 49152;  // keys cached in shared memory (192 KB)
+constexpr int kBins = 4096;            // 12-bit digits
+constexpr int kBinMax = 256;           // bin size that is ranked exactly
+constexpr int64_t kCacheMax = 40960;   // keys cached in shared memory (160 KB)
+
+enum Mode { TAKE_ALL = 0, BY_BIN = 1 };
 
 struct SelShared {
-  uint32_t hist[256];
-  uint32_t warp_sum[kWarps];
-  uint32_t warp_a[kWarps];
-  uint32_t warp_b[kWarps];
-  uint32_t prefix, mask, remaining, n_valid, digit_found;
+  uint32_t hist[kBins];
+  uint32_t bin_idx[kBinMax];
+  uint32_t bin_key[kBinMax];
+  uint32_t warp_a[kWarps], warp_b[kWarps], warp_c[kWarps];
+  uint32_t kmin, kmax, n_valid, bstar, need, count, total, mode, take_eq;
 };
 
-__device__ __forceinline__ uint32_t load_key(const float* sc, const uint32_t* cache, int64_t i) {
-  return cache ? cache[i] : score_key(sc[i]);
-}
-
-// Inclusive scan of v over the warp.
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -42,117 +48,235 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
-__global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a, int use_cache) {
+struct KeySrc {
+  const float* sc;
+  const uint32_t* cache;
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const {
+    return cache ? cache[i] : score_key(sc[i]);
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a, int use_cache) {
   extern __shared__ uint32_t cache_mem[];
   __shared__ SelShared sh;
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = a.n;
+  const uint32_t k = static_cast<uint32_t>(a.k);
   const float* sc = a.scores + static_cast<int64_t>(b) * n;
-  const uint32_t* cache = nullptr;
-  if (use_cache) {
-    for (int64_t i = tid; i < n; i += kThreads) cache_mem[i] = score_key(sc[i]);
-    cache = cache_mem;
-  }
+
+  // Block ids of the token stage, kept in shared memory for the compaction.
+  int32_t* bids = reinterpret_cast<int32_t*>(cache_mem + (use_cache ? n : 0));
   if (a.block_ids) {
     // The candidate list must be ascending block ids with -1 padding at the
-    // end (as the block stage writes it): the lower-index tie rule and the
-    // ascending output rely on it.
+    // end: the lower-index tie rule and the ascending output rely on it.
     const int32_t* bl = a.block_ids + static_cast<int64_t>(b) * a.k_blocks;
-    for (int i = tid; i + 1 < a.k_blocks; i += kThreads) {
-      const int x = bl[i], y = bl[i + 1];
-      if ((y >= 0 && (x < 0 || y <= x))) {
-        record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
+    for (int i = tid; i < a.k_blocks; i += kThreads) {
+      const int x = bl[i];
+      bids[i] = x;
+      if (i + 1 < a.k_blocks) {
+        const int y = bl[i + 1];
+        if (y >= 0 && (x < 0 || y <= x)) {
+          record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
+        }
       }
     }
   }
-  if (tid == 0) {
-    sh.prefix = 0;
-    sh.mask = 0;
-    sh.remaining = static_cast<uint32_t>(a.k);
-    sh.digit_found = 0;
-  }
-  bool take_all = false;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kThreads) sh.hist[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = sh.prefix, mask = sh.mask, rem = sh.remaining;
-    uint32_t valid_cnt = 0;
-    for (int64_t base = 0; base < n; base += kThreads) {
-      const int64_t i = base + tid;
-      bool part = false;
-      uint32_t digit = 0;
-      if (i < n) {
-        const uint32_t key = load_key(sc, cache, i);
-        const bool valid = key > kInvalidKey;
-        valid_cnt += valid ? 1u : 0u;
-        part = valid && ((key & mask) == prefix);
-        digit = (key >> shift) & 0xFFu;
-      }
-      const uint32_t act = __ballot_sync(0xFFFFFFFFu, part);
-      if (part) {
-        const uint32_t peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], __popc(peers));
+
+  // 1. keys (cached when they fit), valid count, smallest and largest valid
+  // key; loads go out eight at a time so their latencies overlap.
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
+  constexpr int kBatch = 8;
+  for (int64_t base = 0; base < n; base += static_cast<int64_t>(kThreads) * kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t i = base + tid + static_cast<int64_t>(j) * kThreads;
+      v[j] = i < n ? sc[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t i = base + tid + static_cast<int64_t>(j) * kThreads;
+      const uint32_t key = score_key(v[j]);
+      if (use_cache && i < n) cache_mem[i] = key;
+      if (key > kInvalidKey) {
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+        ++cnt;
       }
     }
-    if (pass == 0) {
-      valid_cnt = __reduce_add_sync(0xFFFFFFFFu, valid_cnt);
-      if (lane == 0) sh.warp_sum[warp] = valid_cnt;
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  if (lane == 0) {
+    sh.warp_a[warp] = kmin;
+    sh.warp_b[warp] = kmax;
+    sh.warp_c[warp] = cnt;
+  }
+  for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
+  if (tid == 0) sh.count = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t mn = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
+    const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, sh.warp_c[lane]);
+    if (lane == 0) {
+      sh.kmin = mn;
+      sh.kmax = mx;
+      sh.n_valid = c;
+      sh.mode = (c <= k) ? TAKE_ALL : BY_BIN;
+    }
+  }
+  __syncthreads();
+  const KeySrc key_at{sc, use_cache ? cache_mem : nullptr};
+  kmin = sh.kmin;
+  const uint32_t span = sh.kmax - kmin;
+  // Level state: candidates are valid keys with (t >> hs) == P (hs = 32: all);
+  // the final bin is {t : t >> s == P}.
+  uint32_t P = 0, s_cur = 32;
+  bool ties = false;  // the final bin holds one key value
+  if (sh.mode == BY_BIN) {
+    uint32_t need = k;
+    // first digit: the smallest shift that fits t's range into 12 bits
+    uint32_t s_next = span < kBins ? 0u : static_cast<uint32_t>(32 - __clz(span)) - 12u;
+    for (int level = 0; level < 4; ++level) {
+      const uint32_t hs = s_cur, s_lv = s_next;
+      const uint32_t width = hs - s_lv;                // 1..12 bits
+      const uint32_t dmask = width >= 32 ? 0xFFFFFFFFu : (1u << width) - 1u;
+      for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
       __syncthreads();
-      if (tid == 0) {
-        uint32_t t = 0;
-        for (int w = 0; w < kWarps; ++w) t += sh.warp_sum[w];
-        sh.n_valid = t;
+      for (int64_t i = tid; i < n; i += kThreads) {
+        const uint32_t key = key_at(i);
+        if (key <= kInvalidKey) continue;
+        const uint32_t t = key - kmin;
+        if (hs < 32 && (t >> hs) != P) continue;
+        atomicAdd(&sh.hist[(t >> s_lv) & dmask], 1u);
       }
-    }
-    __syncthreads();
-    if (pass == 0 && sh.n_valid <= static_cast<uint32_t>(a.k)) {
-      take_all = true;
-      break;
-    }
-    // Suffix sums over digits, digit 255 first: thread t < 256 holds digit 255 - t.
-    uint32_t v = 0, inc = 0;
-    if (tid < 256) {
-      v = sh.hist[255 - tid];
-      inc = warp_incl_scan(v);
-      if (lane == 31) sh.warp_a[warp] = inc;
-    }
-    __syncthreads();
-    if (tid < 256) {
-      for (int w = 0; w < warp; ++w) inc += sh.warp_a[w];
-      // The k-th best lands in digit d when suffix(d) >= rem > suffix(d + 1).
-      if (inc >= rem && inc - v < rem) {
-        const uint32_t d = 255u - static_cast<uint32_t>(tid);
-        sh.prefix = prefix | (d << shift);
-        sh.mask = mask | (0xFFu << shift);
-        sh.remaining = rem - (inc - v);
-        sh.digit_found = static_cast<uint32_t>(pass + 1);
+      __syncthreads();
+      // suffix sums from the top digit down: thread t owns digits 4095 - 4t - j
+      uint32_t h[4], local = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[j] = sh.hist[kBins - 1 - (4 * tid + j)];
+        local += h[j];
       }
+      const uint32_t incl = warp_incl_scan(local);
+      if (lane == 31) sh.warp_a[warp] = incl;
+      __syncthreads();
+      uint32_t run = incl - local;
+      for (int w = 0; w < warp; ++w) run += sh.warp_a[w];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (run < need && run + h[j] >= need) {
+          sh.bstar = static_cast<uint32_t>(kBins - 1 - (4 * tid + j));
+          sh.need = need - run;
+          sh.count = h[j];
+        }
+        run += h[j];
+      }
+      __syncthreads();
+      P = (hs < 32 ? (P << width) : 0u) | sh.bstar;
+      need = sh.need;
+      s_cur = s_lv;
+      const uint32_t c = sh.count;
+      __syncthreads();
+      if (s_lv == 0) {
+        ties = true;  // every member of the bin has the same t
+        break;
+      }
+      if (c <= kBinMax) break;
+      s_next = s_lv > 12 ? s_lv - 12 : 0;
+    }
+    if (!ties) {
+      // collect the final bin, rank its members exactly, mark the best `need`
+      if (tid == 0) sh.count = 0;
+      __syncthreads();
+      for (int64_t i = tid; i < n; i += kThreads) {
+        const uint32_t key = key_at(i);
+        if (key > kInvalidKey && ((key - kmin) >> s_cur) == P) {
+          const uint32_t slot = atomicAdd(&sh.count, 1u);
+          sh.bin_idx[slot] = static_cast<uint32_t>(i);
+          sh.bin_key[slot] = key;
+        }
+      }
+      __syncthreads();
+      const uint32_t c = sh.count;
+      bool take = false;
+      if (tid < c) {
+        const uint32_t ke = sh.bin_key[tid], ie = sh.bin_idx[tid];
+        uint32_t rank = 0;
+        for (uint32_t o = 0; o < c; ++o) {
+          const uint32_t ko = sh.bin_key[o];
+          rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
+        }
+        take = rank < need;
+      }
+      __syncthreads();  // every rank is computed before any index word is marked
+      if (take) sh.bin_idx[tid] |= 0x80000000u;
+    } else if (tid == 0) {
+      sh.take_eq = need;
     }
     __syncthreads();
-    if (sh.digit_found != static_cast<uint32_t>(pass + 1)) {
-      // Cannot happen when more than k keys are valid; keep the result defined.
-      if (tid == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, pass);
-      take_all = true;
-      break;
-    }
   }
 
-  // Threshold T and how many keys equal to T to take.
-  const uint32_t T = take_all ? kInvalidKey : sh.prefix;
-  const uint32_t take_eq_total = take_all ? 0u : sh.remaining;
-
-  // Compaction in index order: each warp owns a contiguous segment.
+  // 3. compaction in index order: each warp owns a contiguous segment
+  const uint32_t mode = sh.mode;
+  const uint32_t c = ties ? 0u : sh.count;
+  // marked members of the final bin are looked up in a bitmap (hist reused)
+  uint32_t* marked = sh.hist;
+  const bool bitmap = (mode == BY_BIN) && !ties && ((n + 31) / 32 <= kBins);
+  if (mode == BY_BIN && !ties) {
+    for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
+    __syncthreads();
+    if (bitmap) {
+      for (uint32_t e = tid; e < c; e += kThreads) {
+        const uint32_t w = sh.bin_idx[e];
+        if (w & 0x80000000u) {
+          const uint32_t i = w & 0x7FFFFFFFu;
+          atomicOr(&marked[i >> 5], 1u << (i & 31));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  auto is_marked = [&](int64_t i) -> bool {
+    if (bitmap) return (marked[i >> 5] >> (i & 31)) & 1u;
+    for (uint32_t e = 0; e < c; ++e) {
+      if (sh.bin_idx[e] == (static_cast<uint32_t>(i) | 0x80000000u)) return true;
+    }
+    return false;
+  };
+  auto flags = [&](int64_t i, bool& gt, bool& eq) {
+    gt = false;
+    eq = false;
+    const uint32_t key = key_at(i);
+    if (key <= kInvalidKey) return;
+    if (mode == TAKE_ALL) {
+      gt = true;
+      return;
+    }
+    const uint32_t hi = (key - kmin) >> s_cur;
+    if (hi > P) {
+      gt = true;
+    } else if (hi == P) {
+      if (ties) {
+        eq = true;
+      } else {
+        gt = is_marked(i);
+      }
+    }
+  };
   const int64_t seg = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
   const int64_t s0 = static_cast<int64_t>(warp) * seg;
   const int64_t s1 = min(n, s0 + seg);
   uint32_t gt_cnt = 0, eq_cnt = 0;
   for (int64_t base = s0; base < s1; base += 32) {
     const int64_t i = base + lane;
-    const uint32_t key = (i < s1) ? load_key(sc, cache, i) : 0u;
-    gt_cnt += __popc(__ballot_sync(0xFFFFFFFFu, (i < s1) && key > T));
-    eq_cnt += __popc(__ballot_sync(0xFFFFFFFFu, (i < s1) && !take_all && key == T));
+    bool gt = false, eq = false;
+    if (i < s1) flags(i, gt, eq);
+    gt_cnt += __popc(__ballot_sync(0xFFFFFFFFu, gt));
+    eq_cnt += __popc(__ballot_sync(0xFFFFFFFFu, eq));
   }
   __syncthreads();
   if (lane == 0) {
@@ -161,6 +285,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a, int use_
   }
   __syncthreads();
   if (warp == 0) {
+    const uint32_t take_eq_total = (mode == BY_BIN && ties) ? sh.take_eq : 0u;
     const uint32_t eq = sh.warp_b[lane], gt = sh.warp_a[lane];
     const uint32_t eq_incl = warp_incl_scan(eq);
     const uint32_t eq_before = eq_incl - eq;
@@ -169,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a, int use_
     const uint32_t sel_incl = warp_incl_scan(sel);
     sh.warp_a[lane] = sel_incl - sel;  // output offset of this warp
     sh.warp_b[lane] = take_eq;
-    if (lane == 31) sh.n_valid = sel_incl;  // total selected
+    if (lane == 31) sh.total = sel_incl;
   }
   __syncthreads();
   int32_t* out = a.out_ids + static_cast<int64_t>(b) * a.k;
@@ -179,35 +304,290 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a, int use_
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int64_t base = s0; base < s1; base += 32) {
     const int64_t i = base + lane;
-    const uint32_t key = (i < s1) ? load_key(sc, cache, i) : 0u;
-    const bool gt = (i < s1) && key > T;
-    const bool eq = (i < s1) && !take_all && key == T;
+    bool gt = false, eq = false;
+    if (i < s1) flags(i, gt, eq);
     const uint32_t eq_b = __ballot_sync(0xFFFFFFFFu, eq);
     const bool take = gt || (eq && eq_seen + __popc(eq_b & lt_mask) < take_eq);
     const uint32_t tb = __ballot_sync(0xFFFFFFFFu, take);
     if (take) {
       int32_t id = static_cast<int32_t>(i);
-      if (a.block_ids) {
-        const int blk = a.block_ids[static_cast<int64_t>(b) * a.k_blocks + (i >> 3)];
-        id = blk * 8 + static_cast<int32_t>(i & 7);
-      }
+      if (a.block_ids) id = bids[i >> 3] * 8 + static_cast<int32_t>(i & 7);
       out[pos + __popc(tb & lt_mask)] = id;
     }
     pos += __popc(tb);
     eq_seen += __popc(eq_b);
   }
-  const uint32_t total = sh.n_valid;
+  const uint32_t total = sh.total;
+  for (int64_t j = total + tid; j < a.k; j += kThreads) out[j] = -1;
+}
+
+// Register-resident variant for n <= KPT * 1024: warp w owns the contiguous
+// candidates [32 KPT w, 32 KPT (w + 1)), lane l holding 32 j + l of them at
+// slot j, so every pass runs on registers and each warp lays out its own part
+// of the output; only the warps' totals need a block-wide scan.
+constexpr int kRankMax = 64;  // final bins at most this large are ranked exactly
+
+struct RegShared {
+  uint32_t hist[kBins];
+  uint32_t bin_key[kRankMax];
+  uint32_t bin_idx[kRankMax];
+  uint32_t bin_take[kRankMax];
+  uint32_t warp_a[kWarps], warp_b[kWarps], warp_c[kWarps];
+  uint32_t kmin, kmax, n_valid, bstar, need, count, total;
+};
+
+template <int KPT>
+__global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
+  __shared__ RegShared sh;
+  extern __shared__ int32_t bids[];  // token stage: the query's block ids
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = a.n;
+  const uint32_t k = static_cast<uint32_t>(a.k);
+  const float* sc = a.scores + static_cast<int64_t>(b) * n;
+
+  if (a.block_ids) {
+    // Ascending block ids with -1 padding at the end are required: the tie
+    // rule and the ascending output rely on it.
+    const int32_t* bl = a.block_ids + static_cast<int64_t>(b) * a.k_blocks;
+    for (int i = tid; i < a.k_blocks; i += kThreads) {
+      const int x = bl[i];
+      bids[i] = x;
+      if (i + 1 < a.k_blocks) {
+        const int y = bl[i + 1];
+        if (y >= 0 && (x < 0 || y <= x)) {
+          record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
+        }
+      }
+    }
+  }
+  uint32_t key[KPT];
+  float v[KPT];
+  const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int64_t i = wbase + 32 * j;
+    v[j] = i < n ? sc[i] : -INFINITY;
+  }
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    key[j] = score_key(v[j]);
+    if (key[j] > kInvalidKey) {
+      kmin = min(kmin, key[j]);
+      kmax = max(kmax, key[j]);
+      ++cnt;
+    }
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  if (lane == 0) {
+    sh.warp_a[warp] = kmin;
+    sh.warp_b[warp] = kmax;
+    sh.warp_c[warp] = cnt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t mn = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
+    const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, sh.warp_c[lane]);
+    if (lane == 0) {
+      sh.kmin = mn;
+      sh.kmax = mx;
+      sh.n_valid = c;
+    }
+  }
+  __syncthreads();
+  kmin = sh.kmin;
+  const bool take_all = sh.n_valid <= k;
+  const uint32_t span = sh.kmax - kmin;
+  uint32_t P = 0, s_cur = 32, need = k;
+  bool ties = false;
+  if (!take_all) {
+    uint32_t s_next = span < kBins ? 0u : static_cast<uint32_t>(32 - __clz(span)) - 12u;
+    for (int level = 0; level < 4; ++level) {
+      const uint32_t hs = s_cur, s_lv = s_next;
+      const uint32_t width = hs - s_lv;
+      const uint32_t dmask = width >= 32 ? 0xFFFFFFFFu : (1u << width) - 1u;
+      for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        if (key[j] > kInvalidKey) {
+          const uint32_t t = key[j] - kmin;
+          if (hs >= 32 || (t >> hs) == P) atomicAdd(&sh.hist[(t >> s_lv) & dmask], 1u);
+        }
+      }
+      __syncthreads();
+      uint32_t h[4], local = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[j] = sh.hist[kBins - 1 - (4 * tid + j)];
+        local += h[j];
+      }
+      const uint32_t incl = warp_incl_scan(local);
+      if (lane == 31) sh.warp_a[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t x = sh.warp_a[lane];
+        sh.warp_b[lane] = warp_incl_scan(x) - x;
+      }
+      __syncthreads();
+      uint32_t run = incl - local + sh.warp_b[warp];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (run < need && run + h[j] >= need) {
+          sh.bstar = static_cast<uint32_t>(kBins - 1 - (4 * tid + j));
+          sh.need = need - run;
+          sh.count = h[j];
+        }
+        run += h[j];
+      }
+      __syncthreads();
+      P = (hs < 32 ? (P << width) : 0u) | sh.bstar;
+      need = sh.need;
+      s_cur = s_lv;
+      const uint32_t c = sh.count;
+      if (s_lv == 0) {
+        ties = true;  // the bin holds one key value
+        break;
+      }
+      if (c <= kRankMax) break;
+      s_next = s_lv > 12 ? s_lv - 12 : 0;
+      __syncthreads();
+    }
+  }
+  // Final bin: rank its members exactly (unless they all tie).
+  uint32_t marked = 0;  // bit j: candidate j of this thread is a chosen bin member
+  if (!take_all && !ties) {
+    __syncthreads();  // every thread has read the last level's bin count
+    if (tid == 0) sh.count = 0;
+    __syncthreads();
+    uint32_t slot[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      slot[j] = 0xFFFFFFFFu;
+      if (key[j] > kInvalidKey && ((key[j] - kmin) >> s_cur) == P) {
+        slot[j] = atomicAdd(&sh.count, 1u);
+        sh.bin_key[slot[j]] = key[j];
+        sh.bin_idx[slot[j]] = static_cast<uint32_t>(wbase + 32 * j);
+      }
+    }
+    __syncthreads();
+    const uint32_t c = sh.count;
+    if (tid < c) {
+      const uint32_t ke = sh.bin_key[tid], ie = sh.bin_idx[tid];
+      uint32_t rank = 0;
+      for (uint32_t o = 0; o < c; ++o) {
+        const uint32_t ko = sh.bin_key[o];
+        rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
+      }
+      sh.bin_take[tid] = rank < need ? 1u : 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (slot[j] != 0xFFFFFFFFu && sh.bin_take[slot[j]]) marked |= 1u << j;
+    }
+  }
+  // Flags once per candidate; counts per (slot, warp) run.
+  uint32_t gt_mask[KPT], eq_mask[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    bool gt = false, eq = false;
+    if (key[j] > kInvalidKey) {
+      if (take_all) {
+        gt = true;
+      } else {
+        const uint32_t hi = (key[j] - kmin) >> s_cur;
+        if (hi > P) gt = true;
+        else if (hi == P) {
+          if (ties) eq = true;
+          else gt = (marked >> j) & 1u;
+        }
+      }
+    }
+    gt_mask[j] = __ballot_sync(0xFFFFFFFFu, gt);
+    eq_mask[j] = __ballot_sync(0xFFFFFFFFu, eq);
+  }
+  // Warp totals -> block scan (in warp order = index order) -> each warp's
+  // output offset and its share of the ties taken at the threshold.
+  uint32_t g_w = 0, e_w = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    g_w += __popc(gt_mask[j]);
+    e_w += __popc(eq_mask[j]);
+  }
+  if (lane == 0) {
+    sh.warp_a[warp] = g_w;
+    sh.warp_b[warp] = e_w;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t take_eq_total = ties ? need : 0u;
+    const uint32_t e = sh.warp_b[lane], g = sh.warp_a[lane];
+    const uint32_t e_incl = warp_incl_scan(e);
+    const uint32_t e_before = e_incl - e;
+    const uint32_t te = take_eq_total > e_before ? min(e, take_eq_total - e_before) : 0u;
+    const uint32_t sel = g + te;
+    const uint32_t sel_incl = warp_incl_scan(sel);
+    sh.warp_a[lane] = sel_incl - sel;  // output offset of the warp
+    sh.warp_b[lane] = te;              // ties the warp takes
+    if (lane == 31) sh.total = sel_incl;
+  }
+  __syncthreads();
+  int32_t* out = a.out_ids + static_cast<int64_t>(b) * a.k;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t pos = sh.warp_a[warp];
+  const uint32_t te_w = sh.warp_b[warp];
+  uint32_t eq_seen = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    // ties taken in this run: the first (te_w - eq_seen) tied lanes, if any left
+    const uint32_t left = te_w > eq_seen ? te_w - eq_seen : 0u;
+    const uint32_t eq_rank = __popc(eq_mask[j] & lt);
+    const bool is_gt = (gt_mask[j] >> lane) & 1u;
+    const bool is_eq = ((eq_mask[j] >> lane) & 1u) && eq_rank < left;
+    if (is_gt || is_eq) {
+      const int64_t i = wbase + 32 * j;
+      int32_t id = static_cast<int32_t>(i);
+      if (a.block_ids) id = bids[i >> 3] * 8 + static_cast<int32_t>(i & 7);
+      out[pos + __popc(gt_mask[j] & lt) + min(eq_rank, left)] = id;
+    }
+    const uint32_t taken_eq = min(static_cast<uint32_t>(__popc(eq_mask[j])), left);
+    pos += __popc(gt_mask[j]) + taken_eq;
+    eq_seen += __popc(eq_mask[j]);
+  }
+  const uint32_t total = sh.total;
   for (int64_t j = total + tid; j < a.k; j += kThreads) out[j] = -1;
 }
 
 }  // namespace
 
+template <int KPT>
+cudaError_t launch_reg(const SelectArgs& a, cudaStream_t s) {
+  const size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
+  cudaError_t e = cudaFuncSetAttribute(select_reg_kernel<KPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kMaxKBlocks * 4));
+  if (e != cudaSuccess) return e;
+  select_reg_kernel<KPT><<<a.B, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
+  if (a.n <= 2 * kThreads) return launch_reg<2>(a, s);
+  if (a.n <= 4 * kThreads) return launch_reg<4>(a, s);
+  if (a.n <= 8 * kThreads) return launch_reg<8>(a, s);
+  if (a.n <= 16 * kThreads) return launch_reg<16>(a, s);
+  if (a.n <= 32 * kThreads) return launch_reg<32>(a, s);
   const int use_cache = a.n <= kCacheMax ? 1 : 0;
-  const size_t smem = use_cache ? static_cast<size_t>(a.n) * 4 : 0;
+  const size_t smem = (use_cache ? static_cast<size_t>(a.n) * 4 : 0) +
+                      (a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kCacheMax * 4));
+                                       static_cast<int>(kCacheMax * 4 + kMaxKBlocks * 4));
   if (e != cudaSuccess) return e;
   select_kernel<<<a.B, kThreads, smem, s>>>(a, use_cache);
   return cudaGetLastError();
