@@ -323,6 +323,22 @@ def run_ours(args):
         except Exception:
             traffic = None
 
+    # Per-kernel breakdown (a separate untimed pass, so the timed steps above
+    # carry only the scan's events): mean device time per step of each kind.
+    kinds = {"pool": 1, "scan": launches_per_step, "select": launches_per_step, "attn": 1}
+    kev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n * K)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(n * K)])
+           for k, n in kinds.items()}
+    for k, (a_, b_) in kev.items():
+        dsa.profile_events(k, a_, b_)
+    for i in range(K):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for k in kinds:
+        dsa.profile_events(k, [], [])
+    kernel_ms = {k: float(sum(s.elapsed_time(e) for s, e in zip(*kev[k])) / K) for k in kinds}
+
     # End to end through the C ABI with host buffers.
     q_h = q.cpu().pin_memory()
     qi_h = q_idx.cpu().pin_memory()
@@ -396,6 +412,7 @@ def run_ours(args):
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
+        "kernel_ms_per_step": kernel_ms,
         "gpu_launches": int(sum(counts.values())),
         "gpu_launches_by_kind": counts,
         "clocks": clocks.summary(),

@@ -296,7 +296,11 @@ dsa_status_t dsa_launch_counts(uint64_t* counts, int reset);
 /*
  * Waits for `stream`, then reads and clears the status word in `workspace`:
  * DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (the earliest recorded).
- * If info is not NULL it receives the recorded detail word (0 if none).
+ * If info is not NULL it receives the recorded detail word (0 if none): bits
+ * 24..31 name the kernel (1 block-key pooling, 2 indexer scan, 3 top-k
+ * selection, 4 attention, 5 prefill partial block), bits 0..23 a detail (for
+ * DSA_ERR_TIMEOUT the shared-memory address of the barrier waited on; for
+ * DSA_ERR_DEVICE_CHECK the offending sequence index or id).
  */
 dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* info);
 

@@ -90,6 +90,14 @@ T* at(void* ws, size_t off) {
 
 dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
+// Split-KV setup of an attention launch over n queries: CTA pairs while the
+// pairs fit the SMs in one wave, else one CTA per query.
+void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
+  const int rows = c.k_tokens + c.window;
+  a.splits = 2 * n <= device_sm_count() ? kAttnSplits : 1;
+  a.split_rows = ((rows + a.splits - 1) / a.splits + 31) / 32 * 32;
+}
+
 #define DSA_TRY(expr)                  \
   do {                                 \
     dsa_status_t _s = (expr);          \
@@ -440,6 +448,7 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = at<DeviceStatus>(workspace, L.status);
+  set_splits(a, *cfg, B);
   DSA_CUDA(launch(DSA_KERNEL_ATTN, static_cast<cudaStream_t>(stream), [&] { return launch_attn(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
 }
@@ -518,6 +527,7 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = st;
+  set_splits(a, *cfg, B);
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
   return DSA_OK;
 }
@@ -572,6 +582,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   a.ctx = ctx_len;
   a.ratio = cfg->ratio;
   a.status = st;
+  set_splits(a, *cfg, n_q);
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
   return DSA_OK;
 }

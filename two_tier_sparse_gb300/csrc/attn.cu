@@ -4,44 +4,85 @@
 // recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse attention":
 // the 128-token window plus the selected latents).
 //
-// One CTA per query. Rows (selected latents, then window rows) stream through
-// shared memory in tiles of 64 by cp.async into 128-byte-swizzled tiles. For
-// each tile two tcgen05 MMAs run with fp32 accumulators in tensor memory:
-//   S   = Q . KV^T  (M = 128 with the 64 heads in lanes 0..63, N = 64 rows, K = 512)
+// A query's rows (selected latents in id order, then its window rows) stream
+// through shared memory in tiles of 32 rows; two tcgen05 MMAs per tile run
+// with fp32 accumulators in tensor memory:
+//   S   = Q . KV^T    (M = 128 with the 64 heads in lanes 0..63, N = 32 rows, K = 512)
 //   O^T += KV^T . P^T (four M = 128 slices of the 512 latent dims, N = 64 heads,
-//                      K = 64 rows; the KV tile is read as an MN-major operand)
-// The softmax runs in registers, one head per thread, online across tiles with
-// the running maximum only moved when it grows by more than 2^8 (the stale
-// maximum keeps every P value <= 256, exact enough in bf16 and fp32).
+//                      K = 32 rows; the KV tile is read as an MN-major operand)
+// Warp roles: warps 0-3 math (softmax for the 64 heads by warps 0-1, one head
+// per thread; O rescaling and the epilogue by all four, thread = TMEM lane),
+// warps 4-7 loaders (warp 4 + w owns ring slot w: cp.async gathers of random
+// 1 KB rows, waited by the warp and announced on the slot's mbarrier; each
+// also loads a quarter of Q), warp 8 MMA. Random rows reach shared memory
+// fastest through several slots with independent completion, hence four
+// 32 KB slots. S is double-buffered in tensor memory so QK^T of tile t + 1
+// runs while the softmax of tile t does. The running maximum only moves when
+// it grows by more than 2^8 (the stale maximum keeps every P value <= 256,
+// exact enough in bf16 and fp32), so rescaling O is rare.
+//
+// Split-KV: for small batches a query's rows are cut into two ranges handled
+// by the two CTAs of a cluster. Each CTA sends the partner, over distributed
+// shared memory in one bulk copy, its unnormalised O for the latent dims the
+// partner finishes plus its (max, sum); each then merges and writes one half
+// of the output dims.
 #include "kernels.h"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kRows = 64;  // KV rows per tile
+constexpr int kRows = 32;           // KV rows per tile
+constexpr int kSlots = 4;           // ring slots
+constexpr int kLoadWarp0 = 4;
+constexpr int kMmaWarp = kLoadWarp0 + kSlots;  // 8
+constexpr int kThreads = 32 * (kMmaWarp + 1);  // 288
+constexpr int kMathBar = 1;         // named barrier of the 128 math threads
 
-// Shared-memory plan (offsets from a 1024-aligned base).
-constexpr int kQ = 0;                        // 8 atoms x 64 heads x 128 B, + 8 KB read past the end
-constexpr int kQBytes = 8 * kHeads * 128 + 8192;
-constexpr int kKV = kQ + kQBytes;            // 2 buffers x 8 atoms x 64 rows x 128 B
-constexpr int kKVBytes = 8 * kRows * 128;
-constexpr int kP = kKV + 2 * kKVBytes;       // P: 64 heads x 64 rows bf16 (one atom)
-constexpr int kIds = kP + kHeads * 128;      // compacted latent ids
+// Shared-memory plan (offsets from a 1024-aligned base). The QK^T MMA reads
+// 64 rows past each Q atom (they only feed unused accumulator lanes); past
+// the last atom they land in the P buffers, which is harmless.
+constexpr int kQ = 0;                              // 8 atoms x 64 heads x 128 B; output staging
+constexpr int kP = kQ + 8 * kHeads * 128;          // 2 x (64 heads x 128 B; 32 rows bf16 used)
+constexpr int kPBytes = kHeads * 128;
+constexpr int kKV = kP + 2 * kPBytes;              // 4 slots x 8 atoms x 32 rows x 128 B
+constexpr int kAtomBytes = kRows * 128;            // 4 KB: one slot's rows of one 64-dim atom
+constexpr int kSlotBytes = 8 * kAtomBytes;         // 32 KB
+constexpr int kIds = kKV + kSlots * kSlotBytes;    // compacted latent ids
 constexpr int kMisc = kIds + kMaxKTokens * 4;
-constexpr int kSmemBytes = kMisc + 1024 + 1024;
-constexpr int kTmemCols = 512;               // S: cols [0, 64); O^T slice m: cols [64 + 64 m, 128 + 64 m)
+constexpr int kMiscBytes = 2048;
+constexpr int kSmemBytes = kMisc + kMiscBytes + 1024;  // + alignment slack of the base
+constexpr int kTmemCols = 512;  // S[b]: cols [64 b, 64 b + 32); O^T slice m: [128 + 64 m, ...)
+constexpr uint32_t kOutBytes = kHeads * kLatent * 2;  // one query's bf16 output, [64 h][512]
+static_assert(kP - kQ == static_cast<int>(kOutBytes), "the Q region stages the output");
+// Split-KV exchange payload: O of two 128-dim slices as float4 groups
+// [2 mm][16 g][128 d] (heads 4 g .. 4 g + 3 at dim d), then (max, sum) per head.
+constexpr uint32_t kXchgO = 2 * 16 * 128 * 16;                // 64 KB
+constexpr uint32_t kXchgBytes = kXchgO + kHeads * 2 * 4;       // + 512 B
+constexpr int kRecv = kKV;                                     // incoming payload
+constexpr int kSend = kKV + 65 * 1024;                         // outgoing payload
+static_assert(kRecv + static_cast<int>(kXchgBytes) <= kSend, "payloads apart");
+static_assert(kSend + static_cast<int>(kXchgBytes) <= kIds + kMaxKTokens * 4,
+              "the outgoing payload ends inside the (then unused) id list");
+static_assert(kAttnSplits == 2, "split-KV pairs the two CTAs of a cluster");
 
 struct Misc {
-  uint64_t bar;
+  uint64_t kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
+  uint64_t q_done, peer_ready, peer_data;  // peer_*: split-KV exchange
   uint32_t tmem_base;
+  int abort;
   int n_sel;
-  int rescale;
-  int warp_cnt[kThreads / 32];
+  int warp_cnt[4];
   float alpha[kHeads];
   float inv_l[kHeads];
+  float wgt[2][kHeads];
 };
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m,
+                                         DeviceStatus* st) {
+  return mbar_wait_abortable(bar, parity, &m->abort, st, SITE_ATTN);
+}
 
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -52,18 +93,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   int32_t* ids = reinterpret_cast<int32_t*>(gbase + kIds);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
+  const int split = blockIdx.y;
+  const bool paired = a.splits == 2;
 
   if (tid == 0) {
-    mbar_init(&misc->bar, 1);
-    misc->rescale = 0;
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&misc->kv_full[i], 32);  // arrivals of the slot's loader warp
+      mbar_init(&misc->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&misc->s_full[i], 1);
+      mbar_init(&misc->s_free[i], 2);
+      mbar_init(&misc->p_full[i], 2);
+      mbar_init(&misc->p_empty[i], 1);
+    }
+    mbar_init(&misc->q_done, 128);  // every loader thread, once its quarter of Q landed
+    mbar_init(&misc->peer_ready, 1);
+    mbar_init(&misc->peer_data, 1);  // the receiver's expect-tx arrival + the bulk copy
+    misc->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&misc->tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&misc->tmem_base, kTmemCols);
 
-  // Visible latents and this query's window rows.
-  int n_vis;
+  // This query's visible latents and window rows.
+  int n_vis, n_sw;
   const uint16_t* win;
-  int n_sw;
   if (a.prefill) {
     const int64_t P = a.ctx + b;
     n_vis = static_cast<int>((P + 1) / a.ratio);
@@ -75,17 +129,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     n_vis = a.n_latents[b];
     n_sw = a.swa_len[b];
     if (n_sw < 0 || n_sw > a.window) {
-      if (tid == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
+      if (tid == 0 && split == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
       n_sw = n_sw < 0 ? 0 : a.window;
     }
     win = a.swa + static_cast<int64_t>(b) * a.window * kLatent;
   }
   if (n_vis > a.lat_stride) n_vis = static_cast<int>(a.lat_stride);
+  const uint16_t* lat =
+      a.latents + (a.prefill ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
 
-  // Compact the valid token ids (>= 0 and < n_vis) in order.
-  {
+  const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
+  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
+    // Q does not depend on the ids: its copies start at once (64 heads x 64
+    // chunks of 16 B, a quarter per loader warp); each loader thread reports
+    // its part on q_done once it landed.
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int c = lane + 32 * (32 * (warp - kLoadWarp0) + j);
+      const int h = c >> 6, cr = c & 63;
+      cp_async_16(sbase + kQ + (cr >> 3) * (kHeads * 128) + sw128_off(h, cr & 7),
+                  qsrc + h * kLatent + cr * 8);
+    }
+    cp_async_commit();
+  }
+
+  // Compact the valid token ids (>= 0 and < n_vis) in order (math threads).
+  if (tid < 128) {
     const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
-    constexpr int kPer = kMaxKTokens / kThreads;  // 4
+    constexpr int kPer = kMaxKTokens / 128;  // 4
     int my[kPer];
     int cnt = 0;
 #pragma unroll
@@ -95,7 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       if (i < a.k_tokens) {
         id = tk[i];
         if (id >= n_vis) {
-          record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+          if (split == 0) {
+            record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+          }
           id = -1;
         }
       }
@@ -109,195 +182,402 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       if (lane >= o) incl += t;
     }
     if (lane == 31) misc->warp_cnt[warp] = incl;
-    __syncthreads();
+    named_sync(kMathBar, 128);
     int before = incl - cnt;
     for (int w = 0; w < warp; ++w) before += misc->warp_cnt[w];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       if (my[j] >= 0) ids[before++] = my[j];
     }
-    if (tid == kThreads - 1) misc->n_sel = before;
+    if (tid == 127) misc->n_sel = before;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The partner's barriers are initialised before any remote arrival: every
+  // thread arrives here and waits before its first cluster access.
+  if (paired) cluster_arrive_relaxed();
   const uint32_t tmem = misc->tmem_base;
   const int n_sel = misc->n_sel;
   const int n_rows = n_sel + n_sw;
-  const int n_tiles = (n_rows + kRows - 1) / kRows;
+  const int r_begin = split * a.split_rows;
+  const int r_end = min(n_rows, r_begin + a.split_rows);
+  const int n_tiles = r_end > r_begin ? (r_end - r_begin + kRows - 1) / kRows : 0;
 
-  const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
-  const uint16_t* lat = a.latents + (a.prefill ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
-  uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
-
-  if (n_tiles == 0) {
-    for (int i = tid; i < kHeads * kLatent / 8; i += kThreads) {
-      reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
-    }
-    if (a.lse && tid < kHeads) a.lse[static_cast<int64_t>(b) * kHeads + tid] = -INFINITY;
-  } else {
-    // Q: 64 rows x 64 chunks of 16 B.
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      const int c = tid + kThreads * j;
-      const int h = c >> 6, cr = c & 63;
-      cp_async_16(sbase + kQ + (cr >> 3) * (kHeads * 128) + sw128_off(h, cr & 7),
-                  qsrc + h * kLatent + cr * 8);
-    }
-    auto load_tile = [&](int t, int buf) {
-      const uint32_t dstb = sbase + kKV + buf * kKVBytes;
-#pragma unroll 4
-      for (int j = 0; j < 32; ++j) {
-        const int c = tid + kThreads * j;
+  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
+    // ---------------- loaders ----------------
+    // Warp 4 + w fills slot w with tiles w, w + 4, ...: it waits for its own
+    // copies of a tile, fences them into the async proxy (the tensor core's
+    // view) and then arrives, while the other slots' tiles are in flight.
+    const int w = warp - kLoadWarp0;
+    bool ok = true, q_reported = false;
+    for (int t = w; t < n_tiles && ok; t += kSlots) {
+      if (t >= kSlots &&
+          !wait_bar(&misc->kv_empty[w], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
+                    a.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t dstb = sbase + kKV + w * kSlotBytes;
+      const int g0 = r_begin + t * kRows;
+#pragma unroll 8
+      for (int j = 0; j < kRows * 64 / 32; ++j) {
+        const int c = lane + 32 * j;
         const int row = c >> 6, cr = c & 63;
-        const int g = t * kRows + row;
-        const uint32_t dst = dstb + (cr >> 3) * (kRows * 128) + sw128_off(row, cr & 7);
-        if (g < n_sel) {
-          cp_async_16(dst, lat + static_cast<int64_t>(ids[g]) * kLatent + cr * 8);
-        } else if (g < n_rows) {
-          cp_async_16(dst, win + static_cast<int64_t>(g - n_sel) * kLatent + cr * 8);
+        const int g = g0 + row;
+        const uint32_t dst = dstb + (cr >> 3) * kAtomBytes + sw128_off(row, cr & 7);
+        if (g < r_end) {
+          const uint16_t* src = (g < n_sel) ? lat + static_cast<int64_t>(ids[g]) * kLatent
+                                            : win + static_cast<int64_t>(g - n_sel) * kLatent;
+          cp_async_16(dst, src + cr * 8);
         } else {
           st_shared_v4(dst, make_uint4(0, 0, 0, 0));
         }
       }
-    };
-    load_tile(0, 0);
-    cp_async_commit();
-
-    float m_run = -INFINITY, l_run = 0.f;  // threads 0..63: head tid
-    uint32_t phase = 0;
-    bool ok = true;
-    constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
-    constexpr uint32_t idesc_o = mma_idesc(128, kHeads, true, true, false);
-    for (int t = 0; t < n_tiles && ok; ++t) {
-      const int buf = t & 1;
-      if (t + 1 < n_tiles) load_tile(t + 1, buf ^ 1);
       cp_async_commit();
-      cp_async_wait<1>();
-      if (tid == 0) misc->rescale = 0;
+      if (!q_reported) {  // the Q group is the older one
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&misc->q_done);
+        q_reported = true;
+      }
+      cp_async_wait<0>();
       fence_proxy_async_smem();
-      __syncthreads();
-      const uint32_t kvb = sbase + kKV + buf * kKVBytes;
-      if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kLatent / 16; ++ks) {
-          const uint64_t ad = sw128_desc(sbase + kQ + (ks >> 2) * (kHeads * 128) + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(kvb + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
-          mma_f16(tmem, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(&misc->bar);
-      }
-      ok = __syncthreads_and(mbar_wait(&misc->bar, phase, a.status, SITE_ATTN)) != 0;
-      phase ^= 1u;
-      tc_fence_after();
-      if (!ok) break;
-
-      if (tid < kHeads) {
-        const int valid = min(kRows, n_rows - t * kRows);
-        float z[kRows];
-#pragma unroll
-        for (int c = 0; c < kRows / 16; ++c) {
-          float v[16];
-          tmem_ld16(tmem_addr(tmem, static_cast<uint32_t>(warp * 32), c * 16), v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) z[c * 16 + i] = (c * 16 + i < valid) ? v[i] * a.scale_log2 : -INFINITY;
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) mt = fmaxf(mt, z[i]);
-        float alpha = 1.f;
-        if (t == 0) {
-          m_run = mt;
-        } else if (mt > m_run + 8.f) {
-          alpha = exp2f(m_run - mt);
-          m_run = mt;
-          misc->rescale = 1;
-        }
-        float sum = 0.f;
-        uint32_t pk[kRows / 2];
-#pragma unroll
-        for (int i = 0; i < kRows; i += 2) {
-          const float p0 = exp2f(z[i] - m_run), p1 = exp2f(z[i + 1] - m_run);
-          sum += p0 + p1;  // the denominator sums the fp32 probabilities
-          const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
-          pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
-        }
-        l_run = l_run * alpha + sum;
-        misc->alpha[tid] = alpha;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          st_shared_v4(sbase + kP + sw128_off(tid, c),
-                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-        }
-      }
-      tc_fence_before();
+      mbar_arrive(&misc->kv_full[w]);
+    }
+    if (!q_reported) {
+      cp_async_wait<0>();
       fence_proxy_async_smem();
-      __syncthreads();
-      if (misc->rescale) {
-        tc_fence_after();
-        const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(warp * 32), 0);
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[16];
-            const uint32_t addr = la + 64 + 64 * m + 16 * c;
-            tmem_ld16(addr, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] *= misc->alpha[16 * c + i];
-            tmem_st16(addr, v);
-          }
+      mbar_arrive(&misc->q_done);
+    }
+    if (paired) cluster_wait();
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
+      constexpr uint32_t idesc_o = mma_idesc(128, kHeads, true, true, false);
+      auto issue_pv = [&](int t) -> bool {
+        const int sb = t & 1;
+        if (!wait_bar(&misc->p_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status)) {
+          return false;
         }
-        tc_fence_before();
-        __syncthreads();
-      }
-      if (tid == 0) {
         tc_fence_after();
+        fence_proxy_async_smem();
+        const uint32_t kvb = sbase + kKV + (t % kSlots) * kSlotBytes;
+        const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
           for (int ks = 0; ks < kRows / 16; ++ks) {
-            const uint64_t ad = sw128_desc(kvb + m * 2 * (kRows * 128) + ks * 16 * 128, kRows * 128, 1024);
-            const uint64_t bd = sw128_desc(sbase + kP + ks * 32, 16, 1024);
-            mma_f16(tmem + 64 + 64 * m, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+            const uint64_t ad =
+                sw128_desc(kvb + m * 2 * kAtomBytes + ks * 16 * 128, kAtomBytes, 1024);
+            const uint64_t bd = sw128_desc(pb + ks * 32, 16, 1024);
+            mma_f16(tmem + 128 + 64 * m, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
           }
         }
-        mma_commit(&misc->bar);
+        mma_commit(&misc->kv_empty[t % kSlots]);
+        mma_commit(&misc->p_empty[sb]);
+        return true;
+      };
+      bool ok = n_tiles == 0 || wait_bar(&misc->q_done, 0u, misc, a.status);
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int slot = t % kSlots, sb = t & 1;
+        if (!wait_bar(&misc->kv_full[slot], static_cast<uint32_t>((t / kSlots) & 1), misc,
+                      a.status)) {
+          ok = false;
+          break;
+        }
+        if (t >= 2 && !wait_bar(&misc->s_free[sb], static_cast<uint32_t>(((t >> 1) - 1) & 1),
+                                misc, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        fence_proxy_async_smem();
+        const uint32_t kvb = sbase + kKV + slot * kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < kLatent / 16; ++ks) {
+          const uint64_t ad =
+              sw128_desc(sbase + kQ + (ks >> 2) * (kHeads * 128) + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(kvb + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
+          mma_f16(tmem + 64 * sb, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&misc->s_full[sb]);
+        if (t >= 1) ok = issue_pv(t - 1);
       }
-      ok = __syncthreads_and(mbar_wait(&misc->bar, phase, a.status, SITE_ATTN)) != 0;
-      phase ^= 1u;
-      tc_fence_after();
+      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+    }
+    __syncwarp();
+    if (paired) cluster_wait();
+  } else {
+    // ---------------- math: softmax, rescale, epilogue ----------------
+    // A failed (timed-out) wait makes `ok` false for good; the thread then
+    // skips the work but still reaches every named barrier, so the math warps
+    // never part ways at a barrier.
+    float m_run = -INFINITY, l_run = 0.f;  // threads 0..63: head tid
+    const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
+    bool ok = true;
+    // PV(j) is known complete through p_empty[j & 1], whose phases a thread
+    // consumes in order (at most one phase ahead of its last wait), so a
+    // parity wait is never more than one phase off; waiting on PV(j) early (to
+    // rescale) and again later (to reuse the buffer) both read the right phase.
+    auto wait_pv = [&](int j) {
+      if (ok) {
+        ok = wait_bar(&misc->p_empty[j & 1], static_cast<uint32_t>((j >> 1) & 1), misc, a.status);
+      }
+    };
+    for (int t = 0; t < n_tiles; ++t) {
+      const int sb = t & 1;
+      const int valid = min(kRows, r_end - (r_begin + t * kRows));
+      float z[kRows];
+      float alpha = 1.f;
+      bool resc = false;
+      if (warp < 2) {
+        if (ok) ok = wait_bar(&misc->s_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status);
+        tc_fence_after();
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < kRows / 16; ++c) {
+            float v[16];
+            tmem_ld16(la + 64 * sb + c * 16, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              z[c * 16 + i] = (c * 16 + i < valid) ? v[i] * a.scale_log2 : -INFINITY;
+            }
+          }
+          float mt = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) mt = fmaxf(mt, z[i]);
+          if (t == 0) {
+            m_run = mt;
+          } else if (mt > m_run + 8.f) {
+            alpha = exp2f(m_run - mt);
+            m_run = mt;
+            resc = true;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&misc->s_free[sb]);
+        misc->alpha[tid] = alpha;
+      }
+      // O^T holds PV(0..t-1); if any head's maximum moved, scale every head's
+      // column by its alpha (alpha = 1 for heads whose maximum stayed).
+      const bool any_resc = named_sync_or(kMathBar, 128, resc);
+      if (any_resc) {
+        if (t > 0) wait_pv(t - 1);
+        tc_fence_after();
+        if (ok && t > 0) {
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float v[16];
+              const uint32_t addr = la + 128 + 64 * m + 16 * c;
+              tmem_ld16(addr, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] *= misc->alpha[16 * c + i];
+              tmem_st16(addr, v);
+            }
+          }
+        }
+        tc_fence_before();
+        named_sync(kMathBar, 128);  // alpha is read by all before the next tile rewrites it
+      }
+      if (warp < 2) {
+        // P[sb] was last read by PV(t - 2)
+        if (t >= 2) wait_pv(t - 2);
+        if (ok) {
+          float sum = 0.f;
+          uint32_t pk[kRows / 2];
+#pragma unroll
+          for (int i = 0; i < kRows; i += 2) {
+            const float p0 = exp2f(z[i] - m_run), p1 = exp2f(z[i + 1] - m_run);
+            sum += p0 + p1;  // the denominator sums the fp32 probabilities
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
+            pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+          }
+          l_run = l_run * alpha + sum;
+          const uint32_t pb = sbase + kP + sb * kPBytes;
+#pragma unroll
+          for (int c = 0; c < kRows / 8; ++c) {
+            st_shared_v4(pb + sw128_off(tid, c),
+                         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&misc->p_full[sb]);
+      }
     }
 
-    if (tid < kHeads) {
-      misc->inv_l[tid] = 1.f / l_run;
-      if (a.lse) a.lse[static_cast<int64_t>(b) * kHeads + tid] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    // ---------------- epilogue ----------------
+    // Once the last PV has completed every MMA has: Q, P and the ring are free.
+    // (Warps 2-3 have waited on no p_empty phase unless they rescaled: their
+    // own waits run in order up to the last PV here.)
+    if (n_tiles > 0) {
+      if (warp >= 2 && n_tiles >= 2) wait_pv(n_tiles - 2);
+      wait_pv(n_tiles - 1);
+    } else if (ok) {
+      // no tiles: nothing ordered the Q copies before the staging writes below
+      ok = wait_bar(&misc->q_done, 0u, misc, a.status);
     }
-    __syncthreads();
-    if (ok) {
-      const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(warp * 32), 0);
+    tc_fence_after();
+    const bool have_o = ok && n_tiles > 0;
+    uint16_t* stage_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][512]
+    uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
+    // O^T slice m, heads 16 c .. 16 c + 15 at dim m * 128 + tid (zeros without rows)
+    auto load_o = [&](int m, int c, float (&v)[16]) {
+      if (have_o) {
+        tmem_ld16(la + 128 + 64 * m + 16 * c, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+    };
+    auto put_out = [&](int m, int c, const float (&v)[16]) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        stage_o[(16 * c + i) * kLatent + m * 128 + tid] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+      }
+    };
+    auto store_out = [&]() {
+      fence_proxy_async_smem();
+      named_sync(kMathBar, 128);
+      if (tid == 0) {
+        bulk_s2g(out, sbase + kQ, kOutBytes);
+        bulk_commit();
+        bulk_wait_read();
+      }
+    };
+    if (!paired) {
+      if (warp < 2) {
+        misc->inv_l[tid] = l_run > 0.f ? 1.f / l_run : 0.f;
+        if (a.lse) {
+          a.lse[static_cast<int64_t>(b) * kHeads + tid] =
+              l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+      named_sync(kMathBar, 128);
+#pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-        const int d = m * 128 + tid;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[16];
-          tmem_ld16(la + 64 + 64 * m + 16 * c, v);
+          load_o(m, c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int h = 16 * c + i;
-            out[h * kLatent + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * misc->inv_l[h]));
+          for (int i = 0; i < 16; ++i) v[i] *= misc->inv_l[16 * c + i];
+          put_out(m, c, v);
+        }
+      }
+      store_out();
+    } else {
+      // CTA `split` finishes latent dims [256 split, 256 split + 256) (slices
+      // 2 split, 2 split + 1) and sends its partner the other two slices.
+      const int peer = 1 - split;
+      cluster_wait();  // both CTAs' barriers are initialised
+      if (tid == 0) {
+        // The ring is free (every MMA completed): the partner may write it.
+        mbar_arrive_expect_tx(&misc->peer_data, kXchgBytes);
+        mbar_arrive_cluster(mapa_shared(smem_u32(&misc->peer_ready), peer));
+      }
+      // Outgoing payload: O of the partner's slices, then (max, sum).
+      float4* send = reinterpret_cast<float4*>(gbase + kSend);
+#pragma unroll 1
+      for (int mm = 0; mm < 2; ++mm) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[16];
+          load_o(2 * peer + mm, c, v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            send[(mm * 16 + 4 * c + j) * 128 + tid] =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           }
         }
       }
+      if (warp < 2) {
+        float* ml = reinterpret_cast<float*>(gbase + kSend + kXchgO);
+        ml[2 * tid] = have_o ? m_run : -INFINITY;
+        ml[2 * tid + 1] = have_o ? l_run : 0.f;
+      }
+      fence_proxy_async_smem();
+      named_sync(kMathBar, 128);
+      if (tid == 0) {
+        if (ok) ok = mbar_wait_cluster(&misc->peer_ready, 0u, &misc->abort, a.status, SITE_ATTN);
+        if (ok) {
+          bulk_s2cluster(mapa_shared(sbase + kRecv, peer), sbase + kSend, kXchgBytes,
+                         mapa_shared(smem_u32(&misc->peer_data), peer));
+        }
+      }
+      if (ok) ok = mbar_wait_cluster(&misc->peer_data, 0u, &misc->abort, a.status, SITE_ATTN);
+      // out = w_own O_own + w_peer O_peer with w_s = 2^(m_s - M) / L,
+      // M = max_s m_s, L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0).
+      if (warp < 2) {
+        const float* pml = reinterpret_cast<const float*>(gbase + kRecv + kXchgO);
+        const float m0 = have_o ? m_run : -INFINITY, l0 = have_o ? l_run : 0.f;
+        const float m1 = ok ? pml[2 * tid] : -INFINITY;
+        const float l1 = ok ? pml[2 * tid + 1] : 0.f;
+        float M = -INFINITY;
+        if (l0 > 0.f) M = m0;
+        if (l1 > 0.f) M = fmaxf(M, m1);
+        const float e0 = l0 > 0.f ? exp2f(m0 - M) : 0.f;
+        const float e1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
+        const float L = e0 * l0 + e1 * l1;
+        const float inv_L = L > 0.f ? 1.f / L : 0.f;
+        misc->wgt[0][tid] = e0 * inv_L;
+        misc->wgt[1][tid] = e1 * inv_L;
+        if (a.lse && split == 0) {
+          a.lse[static_cast<int64_t>(b) * kHeads + tid] =
+              L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+      named_sync(kMathBar, 128);
+      const float4* recv = reinterpret_cast<const float4*>(gbase + kRecv);
+      uint16_t* half_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][256]
+#pragma unroll 1
+      for (int mm = 0; mm < 2; ++mm) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[16];
+          load_o(2 * split + mm, c, v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok) q = recv[(mm * 16 + 4 * c + j) * 128 + tid];
+            const float pv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int hh = 16 * c + 4 * j + e;
+              const float o = fmaf(misc->wgt[1][hh], pv[e], v[4 * j + e] * misc->wgt[0][hh]);
+              half_o[hh * 256 + mm * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+          }
+        }
+      }
+      named_sync(kMathBar, 128);
+      // 64 rows of 512 B: a warp stores one row per instruction
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int e = tid + 128 * i;
+        const int hh = e >> 5, ch = e & 31;
+        const uint4 v = *reinterpret_cast<const uint4*>(gbase + kQ + hh * 512 + ch * 16);
+        *reinterpret_cast<uint4*>(out + hh * kLatent + 256 * split + ch * 8) = v;
+      }
     }
   }
-  cp_async_wait<0>();
+
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // No CTA of a pair leaves while its partner may still touch its shared memory.
+  if (paired) {
+    cluster_arrive();
+    cluster_wait();
   }
 }
 
@@ -305,10 +585,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (a.splits != 1 && a.splits != 2) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_kernel<<<a.B, kThreads, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B, a.splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_kernel, a);
 }
 
 }  // namespace dsa

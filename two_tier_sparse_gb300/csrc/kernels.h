@@ -131,9 +131,15 @@ struct AttnArgs {
   int prefill;
   int64_t ctx;
   int ratio;
+  // Split-KV: with splits = 2 each query's rows are cut into two ranges of
+  // `split_rows` rows handled by the two CTAs of a cluster (merged on chip).
+  int splits;
+  int split_rows;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+// Split-KV runs query pairs of CTAs while 2 x queries fits the SMs in one wave.
+constexpr int kAttnSplits = 2;
 
 // block_ids[b] = 0, 1, ..., ceil(n_latents[b] / 8) - 1, then -1.
 cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks,
