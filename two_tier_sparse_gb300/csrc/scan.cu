@@ -17,7 +17,9 @@
 //              key rows: one box of 128 rows for block keys or a plain latent
 //              range, one box of 8 rows per candidate block otherwise; MXFP8
 //              scales arrive by 4-byte cp.async on the same mbarrier;
-//   warp 2     MMA issuer: 8 MMAs (K = 128) per tile;
+//   warps 2, 11 MMA issuers, one per half: 8 MMAs (K = 128) per tile (a
+//              barrier wait costs a single thread a few hundred cycles, so
+//              two issuers overlap their waits);
 //   warps 3-10 two math sets of four warps, set k for half k.
 //              Thread = TMEM lane = key row of the tile.
 // bf16 keys: the swizzled raw tile is the MMA's A operand as loaded.
@@ -38,8 +40,9 @@ namespace dsa {
 namespace {
 
 constexpr int kTile = 128;          // key rows per tile (MMA M)
-constexpr int kThreads = 352;       // 2 producers, MMA, 2 x 4 math warps
-constexpr int kMmaWarp = 2;
+constexpr int kThreads = 384;       // 2 producers, MMA, 2 x 4 math warps, MMA
+constexpr int kMmaWarp = 2;         // issues the MMAs of even tiles
+constexpr int kMmaWarp2 = 11;       // issues the MMAs of odd tiles
 constexpr int kMathWarp0 = 3;
 constexpr int kMathThreads = 128;   // per math set
 constexpr int kSlots = 4;           // tiles in flight (TMEM slots)
@@ -77,7 +80,7 @@ struct QSlot {
 
 struct Shared {
   uint64_t raw_full[2][5], raw_empty[2][5];
-  uint64_t op_full[kSlots], op_empty[kSlots], acc_full[kSlots], acc_empty[kSlots];
+  uint64_t op_full[kSlots], acc_full[kSlots];
   uint32_t tmem_base;
   int abort;
   TileMeta meta[2][5];
@@ -116,6 +119,25 @@ __device__ __forceinline__ int64_t contiguous_rows(const ScanArgs& a, int n_vis)
   return n < a.n_rows ? n : a.n_rows;
 }
 
+// Position of a CTA's tile: query b and first row r0 of that query's rows.
+// Tiles advance by a fixed step without divisions (the step is at most two
+// tiles, so at most two queries are crossed).
+struct TilePos {
+  int b;
+  int64_t r0;
+  __device__ void init(int64_t tile, int64_t tpq) {
+    b = static_cast<int>(tile / tpq);
+    r0 = (tile % tpq) * kTile;
+  }
+  __device__ void advance(int step, int64_t q_rows) {
+    r0 += static_cast<int64_t>(step) * kTile;
+    while (r0 >= q_rows) {
+      r0 -= q_rows;
+      ++b;
+    }
+  }
+};
+
 template <int FMT>
 __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32_t sbase,
                          int64_t t_begin, int64_t n_tiles, int64_t tpq, int half) {
@@ -123,144 +145,179 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
   using Lo = Layout<FMT>;
   const int lane = threadIdx.x & 31;
   if (lane == 0) tma_prefetch_map(&maps.keys);
+  if (half >= n_tiles) return;
+  const int64_t q_rows = tpq * kTile;
+  const bool gather = a.mode == ROWS_GATHER;
+  // MXFP8 scales of 8 (gathered block) or 128 (contiguous tile) consecutive
+  // rows are 32 or 512 contiguous bytes: one bulk copy when 16-byte aligned.
+  const bool scale_bulk =
+      ((reinterpret_cast<uintptr_t>(a.key_scales) | static_cast<uintptr_t>(a.key_stride * 4)) &
+       15u) == 0;
+  TilePos pos, nxt;
+  pos.init(t_begin + half, tpq);
+  nxt = pos;
   // Gathered mode: lane j < 16 holds the j-th block id of a tile; the ids of
   // the half's next tile are loaded one iteration ahead.
-  auto fetch_block = [&](int64_t i) -> int {
-    if (a.mode != ROWS_GATHER || lane >= kTile / kBlock || i >= n_tiles) return -1;
-    const int64_t tile = t_begin + i;
-    const int64_t bi = (((tile % tpq) * kTile) >> 3) + lane;
+  auto fetch_block = [&](const TilePos& tp, bool exists) -> int {
+    if (!gather || lane >= kTile / kBlock || !exists) return -1;
+    const int64_t bi = (tp.r0 >> 3) + lane;
     if (bi >= a.k_blocks) return -1;
-    return a.block_ids[(tile / tpq) * a.k_blocks + bi];
+    return a.block_ids[static_cast<int64_t>(tp.b) * a.k_blocks + bi];
   };
-  int blk_next = fetch_block(half);
-  for (int64_t i = half; i < n_tiles; i += 2) {
+  int blk_next = fetch_block(pos, true);
+  int nv_b = -1, n_vis = 0;
+  int s = 0;           // stage of this iteration
+  uint32_t kpar = 0;   // parity of the stage's use count
+  for (int64_t i = half, j = 0; i < n_tiles; i += 2, ++j) {
     const int blk = blk_next;
-    blk_next = fetch_block(i + 2);
-    const int64_t j = i >> 1;  // the half's own tile counter
-    const int s = static_cast<int>(j % P::kStages);
+    nxt.advance(2, q_rows);
+    blk_next = fetch_block(nxt, i + 2 < n_tiles);
     if (j >= P::kStages &&
-        !mbar_wait_abortable(&sh.raw_empty[half][s],
-                             static_cast<uint32_t>((j / P::kStages - 1) & 1), &sh.abort,
-                             a.status, SITE_SCAN)) {
+        !mbar_wait_abortable(&sh.raw_empty[half][s], kpar ^ 1u, &sh.abort, a.status, SITE_SCAN)) {
       return;
     }
-    const int64_t tile = t_begin + i;
-    const int b = static_cast<int>(tile / tpq);
-    const int64_t r0 = (tile % tpq) * kTile;
-    const int n_vis = visible_latents(a, b);
+    const int b = pos.b;
+    const int64_t r0 = pos.r0;
+    if (b != nv_b) {
+      n_vis = visible_latents(a, b);
+      nv_b = b;
+    }
     const int64_t seq = static_cast<int64_t>(b) * a.key_stride;
     const uint32_t raw = sbase + Lo::kRaw + (half * P::kStages + s) * Lo::kRawStride;
-
-    // This lane's run of valid rows [row0, row0 + nrows) of the tile, loaded
-    // as one box of `box_rows` key rows starting at key row y.
-    int row0 = 0, nrows = 0, box_rows = 0;
-    int64_t y = 0;
-    if (a.mode == ROWS_GATHER) {
+    uint32_t vm[4];
+    uint32_t bytes;
+    if (gather) {
+      // This lane's block: rows [8 lane, 8 lane + nrows) of the tile.
+      int nrows = 0;
+      int64_t y = 0;
       if (blk >= 0) {
         const int64_t t0 = static_cast<int64_t>(blk) * kBlock;
         const int64_t v = n_vis - t0;
         if (v > 0) {
-          row0 = lane * kBlock;
           nrows = static_cast<int>(v < kBlock ? v : kBlock);
-          box_rows = kBlock;
           y = seq + t0;
         }
       }
-    } else if (lane == 0) {
+      const int row0 = lane * kBlock;
+      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_bulk && nrows == kBlock;
+      bytes = (nrows > 0 ? kBlock * P::kRowBytes : 0) + (bulk_sc ? kBlock * 4 : 0);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vm[k] = range_bits(k, row0, row0 + nrows);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, o);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vm[k] |= __shfl_xor_sync(0xFFFFFFFFu, vm[k], o);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = vm[k];
+        mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
+      }
+      __syncwarp();
+      if (nrows > 0) {
+        if constexpr (FMT == DSA_FMT_BF16) {
+          // two K halves (64 elements = 128 bytes each) into the two K-atoms
+          tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
+          tma_load_2d(raw + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y),
+                      &sh.raw_full[half][s]);
+        } else {
+          tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
+          const uint32_t sc_dst = raw + kTile * 128 + row0 * 4;
+          if (bulk_sc) {
+            bulk_g2s(sc_dst, a.key_scales + y * 4, kBlock * 4, &sh.raw_full[half][s]);
+          } else {
+            for (int r = 0; r < nrows; ++r) cp_async_4(sc_dst + r * 4, a.key_scales + (y + r) * 4);
+          }
+        }
+      }
+    } else {
+      // Contiguous rows: uniform across the warp, lane 0 issues.
       int64_t v = contiguous_rows(a, n_vis) - r0;
       v = v < 0 ? 0 : (v > kTile ? kTile : v);
-      if (v > 0) {
-        nrows = static_cast<int>(v);
-        box_rows = kTile;
-        y = seq + r0;
+      const int nrows = static_cast<int>(v);
+      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_bulk && nrows == kTile;
+      bytes = (nrows > 0 ? kTile * P::kRowBytes : 0) + (bulk_sc ? kTile * 4 : 0);
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = range_bits(k, 0, nrows);
+        mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
+        if (nrows > 0) {
+          const int yy = static_cast<int>(seq + r0);
+          if constexpr (FMT == DSA_FMT_BF16) {
+            tma_load_2d(raw, &maps.keys, 0, yy, &sh.raw_full[half][s]);
+            tma_load_2d(raw + kTile * 128, &maps.keys, 64, yy, &sh.raw_full[half][s]);
+          } else {
+            tma_load_2d(raw, &maps.keys, 0, yy, &sh.raw_full[half][s]);
+            if (bulk_sc) {
+              bulk_g2s(raw + kTile * 128, a.key_scales + (seq + r0) * 4, kTile * 4,
+                       &sh.raw_full[half][s]);
+            }
+          }
+        }
       }
-    }
-    uint32_t bytes = static_cast<uint32_t>(box_rows) * P::kRowBytes;
-    uint32_t vm[4];
+      if constexpr (FMT == DSA_FMT_MXFP8) {
+        if (!bulk_sc) {
+          // lane l copies the scales of rows l, l + 32, l + 64, l + 96
 #pragma unroll
-    for (int k = 0; k < 4; ++k) vm[k] = range_bits(k, row0, row0 + nrows);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, o);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) vm[k] |= __shfl_xor_sync(0xFFFFFFFFu, vm[k], o);
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = vm[k];
-      mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
-    }
-    __syncwarp();
-    if (nrows > 0) {
-      if constexpr (FMT == DSA_FMT_BF16) {
-        // two K halves (64 elements = 128 bytes each) into the two K-atoms
-        tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
-        tma_load_2d(raw + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y),
-                    &sh.raw_full[half][s]);
-      } else {
-        tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
-      }
-    }
-    if constexpr (FMT == DSA_FMT_MXFP8) {
-      // Scales: lane l copies rows l, l + 32, l + 64, l + 96 (4 bytes each).
-      const uint32_t sc_dst = raw + kTile * 128;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int r = lane + 32 * k;
-        const int bl = __shfl_sync(0xFFFFFFFFu, blk, r >> 3);  // every lane takes part
-        if ((vm[r >> 5] >> (r & 31)) & 1u) {
-          const int64_t key = (a.mode == ROWS_GATHER)
-                                  ? seq + static_cast<int64_t>(bl) * kBlock + (r & 7)
-                                  : seq + r0 + r;
-          cp_async_4(sc_dst + r * 4, a.key_scales + key * 4);
+          for (int k = 0; k < 4; ++k) {
+            const int r = lane + 32 * k;
+            if (r < nrows) cp_async_4(raw + kTile * 128 + r * 4, a.key_scales + (seq + r0 + r) * 4);
+          }
         }
       }
     }
     cp_async_mbar_arrive_noinc(&sh.raw_full[half][s]);
+    pos = nxt;
+    if (++s == P::kStages) {
+      s = 0;
+      kpar ^= 1u;
+    }
   }
 }
 
 template <int FMT>
-__device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t n_tiles) {
+__device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_tiles, int set) {
   using P = Plan<FMT>;
   using Lo = Layout<FMT>;
   constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, FMT == DSA_FMT_BF16, false, false);
   const uint32_t tmem = sh.tmem_base;
-  for (int64_t i = 0; i < n_tiles; ++i) {
-    const int q = static_cast<int>(i % kSlots);
-    const uint32_t u = static_cast<uint32_t>(i / kSlots);
+  int ring = 0;   // index-query ring slot of the set's tile i (advances per own tile)
+  int stage = 0;  // bf16: raw stage of the half of tile i (advances per own tile)
+  for (int i = set; i < n_tiles; i += 2) {
+    const int q = i & (kSlots - 1);
+    const uint32_t u = static_cast<uint32_t>(i >> 2);
+    // op_full(i) also means the slot's accumulator is free: the set that
+    // prepares tile i read tile i - 4's accumulator before (program order,
+    // with the tcgen05 fence before its arrival).
     if (!mbar_wait_abortable(&sh.op_full[q], u & 1, &sh.abort, a.status, SITE_SCAN)) return;
-    if (i >= kSlots &&
-        !mbar_wait_abortable(&sh.acc_empty[q], (u - 1) & 1, &sh.abort, a.status, SITE_SCAN)) {
-      return;
-    }
     tc_fence_after();
-    const int set = static_cast<int>(i & 1);
-    const int ring = static_cast<int>((i >> 1) % kQRing);
     const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
+    const uint64_t bd0 = sw128_desc(qb, 16, 1024);
     const uint32_t slot = tmem + q * P::kSlotCols;
     if constexpr (FMT == DSA_FMT_BF16) {
-      const int s = static_cast<int>((i >> 1) % P::kStages);
-      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
+      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + stage) * Lo::kRawStride;
+      const uint64_t ad0 = sw128_desc(raw, 16, 1024);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {  // K = 128 in steps of 16
-        const uint64_t ad = sw128_desc(raw + (k >> 2) * (kTile * 128) + (k & 3) * 32, 16, 1024);
-        const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+        const uint64_t ad = ad0 + (((k >> 2) * (kTile * 128) + (k & 3) * 32) >> 4);
+        const uint64_t bd = bd0 + (((k >> 2) * 2048 + (k & 3) * 32) >> 4);
         mma_f16(slot, ad, bd, idesc, k > 0 ? 1u : 0u);
       }
       mma_commit(&sh.acc_full[q]);
-      mma_commit(&sh.raw_empty[set][s]);
+      mma_commit(&sh.raw_empty[set][stage]);
     } else {
       // A in tensor memory: columns [slot, slot + 64) hold the row's 128 f16
       // values in pairs; group g = k / 2 accumulates into columns 64 + 16 g.
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint64_t bd = sw128_desc(qb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+        const uint64_t bd = bd0 + (((k >> 2) * 2048 + (k & 3) * 32) >> 4);
         mma_f16_tmem_a(slot + 64 + (k >> 1) * 16, slot + k * 8, bd, idesc, (k & 1) ? 1u : 0u);
       }
       mma_commit(&sh.acc_full[q]);
-      mma_commit(&sh.op_empty[q]);
     }
+    if (++ring == kQRing) ring = 0;
+    if (++stage == P::kStages) stage = 0;
   }
 }
 
@@ -320,7 +377,7 @@ __device__ void build_query(const ScanArgs& a, Shared& sh, uint32_t sbase, int b
 
 template <int FMT>
 __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_begin,
-                     int64_t n_tiles, int64_t tpq) {
+                     int n_tiles, int64_t tpq) {
   using P = Plan<FMT>;
   using Lo = Layout<FMT>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,18 +386,23 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
   const int row = 32 * (warp & 3) + lane;  // TMEM lane = key row of this thread
   const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   const uint32_t tmem = sh.tmem_base;
+  const int64_t q_rows = tpq * kTile;
   int ring_b0 = -1, ring_b1 = -1, ring_b2 = -1;  // query held by each ring slot
   // per-thread state of this set's two tiles waiting for their epilogue
   uint32_t pend_sc0 = 0, pend_sc1 = 0;
   bool pend_valid0 = false, pend_valid1 = false;
+  TilePos prep, epi;  // positions of this set's next prepared and next finished tile
+  prep.init(t_begin + set, tpq);
+  epi = prep;
+  int ring = 0, stage = 0;       // of the tile being prepared (advance per own tile)
+  int ring_e = 0;                // of the tile being finished
 
-  auto epilogue = [&](int64_t e) -> bool {
-    const int q = static_cast<int>(e % kSlots);
-    const int pe = static_cast<int>((e >> 1) & 1);
-    const int64_t tile = t_begin + e;
-    const int b = static_cast<int>(tile / tpq);
-    const int64_t r = (tile % tpq) * kTile + row;
-    if (!mbar_wait_abortable(&sh.acc_full[q], static_cast<uint32_t>((e / kSlots) & 1), &sh.abort,
+  auto epilogue = [&](int e) -> bool {
+    const int q = e & (kSlots - 1);
+    const int pe = (e >> 1) & 1;
+    const int b = epi.b;
+    const int64_t r = epi.r0 + row;
+    if (!mbar_wait_abortable(&sh.acc_full[q], static_cast<uint32_t>((e >> 2) & 1), &sh.abort,
                              a.status, SITE_SCAN)) {
       return false;
     }
@@ -363,9 +425,7 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       }
     }
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.acc_empty[q]);
-    const QSlot& slot = sh.qs[set][(e >> 1) % kQRing];
+    const QSlot& slot = sh.qs[set][ring_e];
     if (r < a.n_rows) {
       float s = -INFINITY;
       if (pe ? pend_valid1 : pend_valid0) {
@@ -377,22 +437,22 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       }
       a.scores[static_cast<int64_t>(b) * a.n_rows + r] = s;
     }
+    epi.advance(2, q_rows);
+    if (++ring_e == kQRing) ring_e = 0;
     return true;
   };
 
   // Own tiles i = set, set + 2, ...: the epilogue of tile i - 4 (which shares
   // tile i's pending entry and TMEM slot), then the preparation of tile i.
-  for (int64_t i = set; i < n_tiles + 4; i += 2) {
-    const int pi = static_cast<int>((i >> 1) & 1);
+  for (int i = set; i < n_tiles + 4; i += 2) {
+    const int pi = (i >> 1) & 1;
     if (i >= 4 && i - 4 < n_tiles) {
       if (!epilogue(i - 4)) return;
     }
     if (i >= n_tiles) continue;
-    const int s = static_cast<int>((i >> 1) % P::kStages);
-    const int q = static_cast<int>(i % kSlots);
-    const int64_t tile = t_begin + i;
-    const int b = static_cast<int>(tile / tpq);
-    const int ring = static_cast<int>((i >> 1) % kQRing);
+    const int s = stage;
+    const int q = i & (kSlots - 1);
+    const int b = prep.b;
     const int held = ring == 0 ? ring_b0 : (ring == 1 ? ring_b1 : ring_b2);
     if (held != b) {
       // The ring slot last served tile i - 6, whose epilogue every thread of
@@ -414,13 +474,7 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     if constexpr (FMT == DSA_FMT_MXFP8) {
       const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
       // The A slot of tile i was last read by the MMA of tile i - 4, which the
-      // epilogue above has already seen complete.
-      if (i >= kSlots &&
-          !mbar_wait_abortable(&sh.op_empty[q], static_cast<uint32_t>((i / kSlots - 1) & 1),
-                               &sh.abort, a.status, SITE_SCAN)) {
-        return;
-      }
-      tc_fence_after();
+      // epilogue above has already seen complete (its acc_full commit).
       // own row: 8 chunks of 16 codes at their swizzled positions
       uint32_t f[64];
 #pragma unroll
@@ -451,6 +505,9 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.op_full[q]);
     }
+    prep.advance(2, q_rows);
+    if (++ring == kQRing) ring = 0;
+    if (++stage == P::kStages) stage = 0;
   }
 }
 
@@ -468,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t per = total / gridDim.x, rem = total % gridDim.x;
   const int64_t bx = blockIdx.x;
   const int64_t t_begin = bx * per + (bx < rem ? bx : rem);
-  const int64_t n_tiles = per + (bx < rem ? 1 : 0);
+  const int n_tiles = static_cast<int>(per + (bx < rem ? 1 : 0));
 
   if (threadIdx.x == 0) {
     for (int h = 0; h < 2; ++h) {
@@ -480,9 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < kSlots; ++q) {
       mbar_init(&sh.op_full[q], 4);
-      mbar_init(&sh.op_empty[q], 1);
       mbar_init(&sh.acc_full[q], 1);
-      mbar_init(&sh.acc_empty[q], 4);
     }
     sh.abort = 0;
     fence_mbar_init();
@@ -494,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kMmaWarp) {
     producer<FMT>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
-  } else if (warp == kMmaWarp) {
-    if ((threadIdx.x & 31) == 0) mma_issuer<FMT>(a, sh, sbase, n_tiles);
+  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<FMT>(a, sh, sbase, n_tiles, warp == kMmaWarp ? 0 : 1);
     __syncwarp();
   } else {
     math<FMT>(a, sh, sbase, t_begin, n_tiles, tpq);
