@@ -274,6 +274,8 @@ int device_sm_count() {
 namespace {
 
 __global__ void identity_blocks_kernel(const int32_t* n_latents, int k_blocks, int32_t* out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int b = blockIdx.x;
   const int nb = (n_latents[b] + 7) / 8;
   for (int i = threadIdx.x; i < k_blocks; i += blockDim.x) {
@@ -286,7 +288,9 @@ __global__ void identity_blocks_kernel(const int32_t* n_latents, int k_blocks, i
 cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks,
                                    int32_t* block_ids, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  identity_blocks_kernel<<<B, 256, 0, s>>>(n_latents, k_blocks, block_ids);
+  cudaError_t e = launch_pdl(identity_blocks_kernel, dim3(B), dim3(256), 0, s, 1, n_latents, k_blocks,
+                             block_ids);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&misc->tmem_base, kTmemCols);
+  griddep_launch_dependents();
+  griddep_wait();  // token ids and the window come from the previous kernels
 
   // This query's visible latents and window rows.
   int n_vis, n_sw;
@@ -586,22 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
   if (a.splits != 1 && a.splits != 2) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B, a.splits);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = a.splits;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_kernel, a);
+  return launch_pdl(attn_kernel, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s, a.splits, a);
 }
 
 }  // namespace dsa

@@ -202,6 +202,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel lets the next kernel of the stream
+// start its launch (griddep_launch_dependents) and waits for the previous
+// kernel's grid to finish and flush its memory (griddep_wait) before touching
+// global memory. Both are no-ops when the launch did not ask for it.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Thread-block clusters and distributed shared memory
 // ---------------------------------------------------------------------------
 

@@ -147,4 +147,45 @@ cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks
 
 int device_sm_count();
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device): `cache` is the caller's per-kernel array.
+inline cudaError_t ensure_smem(const void* kernel, int bytes, int (&cache)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = bytes;
+  return e;
+}
+
+// Launches `kernel` on `s` with programmatic dependent launch allowed (the
+// kernel starts while the previous one drains and waits for it with
+// griddep_wait before touching global memory), optionally as clusters of
+// (1, cluster_y, 1) CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, int cluster_y, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_y > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = static_cast<unsigned>(cluster_y);
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace dsa

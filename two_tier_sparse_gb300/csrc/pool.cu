@@ -109,6 +109,8 @@ __device__ __forceinline__ Stored round_to_format(int fmt, const float (&v)[4], 
 
 // One warp per (sequence, block).
 __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y;
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
 
 // One warp per prefill query: pool its partially visible last block and score it.
 __global__ void __launch_bounds__(256) prefill_partial_kernel(PartialArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= a.n_q) return;
@@ -178,16 +182,14 @@ cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s) {
   const int threads = a.tail_only ? 32 : 256;
   const int wpb = threads / 32;
   dim3 grid((warps + wpb - 1) / wpb, a.B);
-  pool_kernel<<<grid, threads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(pool_kernel, grid, dim3(threads), 0, s, 1, a);
 }
 
 cudaError_t launch_prefill_partial(const PartialArgs& a, cudaStream_t s) {
   if (a.n_q == 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (a.n_q + warps_per_block - 1) / warps_per_block;
-  prefill_partial_kernel<<<grid, 32 * warps_per_block, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(prefill_partial_kernel, dim3(grid), dim3(32 * warps_per_block), 0, s, 1, a);
 }
 
 }  // namespace dsa

@@ -521,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw + (sbase - raw) + Lo::kShared);
   const int warp = threadIdx.x >> 5;
+  griddep_launch_dependents();
 
   const int64_t per = total / gridDim.x, rem = total % gridDim.x;
   const int64_t bx = blockIdx.x;
@@ -546,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();  // the previous kernel's outputs (scores, ids, pooled keys) are final
 
   if (warp < kMmaWarp) {
     producer<FMT>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
@@ -592,11 +594,12 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const int smem = Lo::kBytes + 1024;
-  e = cudaFuncSetAttribute(scan_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static int smem_set[64] = {0};
+  e = ensure_smem(reinterpret_cast<const void*>(scan_kernel<FMT>), smem, smem_set);
   if (e != cudaSuccess) return e;
   const int64_t grid = total < num_sms ? total : num_sms;
-  scan_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, maps, tpq, total);
-  return cudaGetLastError();
+  return launch_pdl(scan_kernel<FMT>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1,
+                    a, maps, tpq, total);
 }
 
 }  // namespace

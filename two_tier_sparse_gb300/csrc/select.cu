@@ -57,6 +57,8 @@ struct KeySrc {
 };
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a, int use_cache) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ uint32_t cache_mem[];
   __shared__ SelShared sh;
   const int b = blockIdx.x;
@@ -340,6 +342,8 @@ template <int KPT>
 __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   __shared__ RegShared sh;
   extern __shared__ int32_t bids[];  // token stage: the query's block ids
+  griddep_launch_dependents();
+  griddep_wait();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = a.n;
@@ -568,12 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
 template <int KPT>
 cudaError_t launch_reg(const SelectArgs& a, cudaStream_t s) {
   const size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
-  cudaError_t e = cudaFuncSetAttribute(select_reg_kernel<KPT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kMaxKBlocks * 4));
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
+                              static_cast<int>(kMaxKBlocks * 4), smem_set);
   if (e != cudaSuccess) return e;
-  select_reg_kernel<KPT><<<a.B, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(select_reg_kernel<KPT>, dim3(a.B), dim3(kThreads), smem, s, 1, a);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
@@ -586,11 +589,11 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
   const int use_cache = a.n <= kCacheMax ? 1 : 0;
   const size_t smem = (use_cache ? static_cast<size_t>(a.n) * 4 : 0) +
                       (a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kCacheMax * 4 + kMaxKBlocks * 4));
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_kernel),
+                              static_cast<int>(kCacheMax * 4 + kMaxKBlocks * 4), smem_set);
   if (e != cudaSuccess) return e;
-  select_kernel<<<a.B, kThreads, smem, s>>>(a, use_cache);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(a.B), dim3(kThreads), smem, s, 1, a, use_cache);
 }
 
 }  // namespace dsa
