@@ -16,7 +16,8 @@
 //   warps 0-1  producers: TMA tiled loads (128-byte swizzle) of the tile's
 //              key rows: one box of 128 rows for block keys or a plain latent
 //              range, one box of 8 rows per candidate block otherwise; MXFP8
-//              scales arrive by 4-byte cp.async on the same mbarrier;
+//              scales (4 bytes a row) come with the tile: one bulk copy for a
+//              contiguous tile, two 16-byte cp.async per gathered block;
 //   warps 2, 11 MMA issuers, one per half: 8 MMAs (K = 128) per tile (a
 //              barrier wait costs a single thread a few hundred cycles, so
 //              two issuers overlap their waits);
@@ -33,6 +34,8 @@
 // below 2^-31 of its head's largest.
 // The epilogue of tile i - 4 runs before tile i is prepared and writes
 // score = sum_h w_h * max(0, dot_h), summed in head order.
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace dsa {
@@ -79,11 +82,11 @@ struct QSlot {
 };
 
 struct Shared {
-  uint64_t raw_full[2][5], raw_empty[2][5];
+  uint64_t raw_full[2][6], raw_empty[2][6];
   uint64_t op_full[kSlots], acc_full[kSlots];
   uint32_t tmem_base;
   int abort;
-  TileMeta meta[2][5];
+  TileMeta meta[2][6];
   QSlot qs[2][kQRing];
 };
 
@@ -149,8 +152,8 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
   const int64_t q_rows = tpq * kTile;
   const bool gather = a.mode == ROWS_GATHER;
   // MXFP8 scales of 8 (gathered block) or 128 (contiguous tile) consecutive
-  // rows are 32 or 512 contiguous bytes: one bulk copy when 16-byte aligned.
-  const bool scale_bulk =
+  // rows are 32 or 512 contiguous bytes, copied whole when 16-byte aligned.
+  const bool scale_vec =
       ((reinterpret_cast<uintptr_t>(a.key_scales) | static_cast<uintptr_t>(a.key_stride * 4)) &
        15u) == 0;
   TilePos pos, nxt;
@@ -199,8 +202,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         }
       }
       const int row0 = lane * kBlock;
-      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_bulk && nrows == kBlock;
-      bytes = (nrows > 0 ? kBlock * P::kRowBytes : 0) + (bulk_sc ? kBlock * 4 : 0);
+      bytes = nrows > 0 ? kBlock * P::kRowBytes : 0;
 #pragma unroll
       for (int k = 0; k < 4; ++k) vm[k] = range_bits(k, row0, row0 + nrows);
 #pragma unroll
@@ -224,10 +226,12 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         } else {
           tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
           const uint32_t sc_dst = raw + kTile * 128 + row0 * 4;
-          if (bulk_sc) {
-            bulk_g2s(sc_dst, a.key_scales + y * 4, kBlock * 4, &sh.raw_full[half][s]);
+          const uint8_t* sc_src = a.key_scales + y * 4;
+          if (scale_vec && nrows == kBlock) {
+            cp_async_16(sc_dst, sc_src);
+            cp_async_16(sc_dst + 16, sc_src + 16);
           } else {
-            for (int r = 0; r < nrows; ++r) cp_async_4(sc_dst + r * 4, a.key_scales + (y + r) * 4);
+            for (int r = 0; r < nrows; ++r) cp_async_4(sc_dst + r * 4, sc_src + r * 4);
           }
         }
       }
@@ -236,7 +240,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
       int64_t v = contiguous_rows(a, n_vis) - r0;
       v = v < 0 ? 0 : (v > kTile ? kTile : v);
       const int nrows = static_cast<int>(v);
-      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_bulk && nrows == kTile;
+      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_vec && nrows == kTile;
       bytes = (nrows > 0 ? kTile * P::kRowBytes : 0) + (bulk_sc ? kTile * 4 : 0);
       if (lane == 0) {
 #pragma unroll
@@ -444,12 +448,15 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
 
   // Own tiles i = set, set + 2, ...: the epilogue of tile i - 4 (which shares
   // tile i's pending entry and TMEM slot), then the preparation of tile i.
-  for (int i = set; i < n_tiles + 4; i += 2) {
-    const int pi = (i >> 1) & 1;
+  // The loop is unrolled by two own tiles so that the two pending entries
+  // (parity pi) are distinct registers: the MXFP8 scale load issued here is
+  // first used two own tiles later and its latency stays hidden.
+  auto own_tile = [&](int i, auto pic) -> bool {
+    constexpr int pi = decltype(pic)::value;
     if (i >= 4 && i - 4 < n_tiles) {
-      if (!epilogue(i - 4)) return;
+      if (!epilogue(i - 4)) return false;
     }
-    if (i >= n_tiles) continue;
+    if (i >= n_tiles) return true;
     const int s = stage;
     const int q = i & (kSlots - 1);
     const int b = prep.b;
@@ -466,11 +473,11 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     if (!mbar_wait_abortable(&sh.raw_full[set][s],
                              static_cast<uint32_t>(((i >> 1) / P::kStages) & 1), &sh.abort,
                              a.status, SITE_SCAN)) {
-      return;
+      return false;
     }
     const TileMeta& m = sh.meta[set][s];
     const bool valid_i = (m.valid[row >> 5] >> (row & 31)) & 1u;
-    if (pi) pend_valid1 = valid_i; else pend_valid0 = valid_i;
+    if constexpr (pi) pend_valid1 = valid_i; else pend_valid0 = valid_i;
     if constexpr (FMT == DSA_FMT_MXFP8) {
       const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
       // The A slot of tile i was last read by the MMA of tile i - 4, which the
@@ -491,9 +498,10 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
               "=r"(f[8 * c + 4]), "=r"(f[8 * c + 5]), "=r"(f[8 * c + 6]), "=r"(f[8 * c + 7])
             : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
       }
-      uint32_t sc_i;
+      // The row's four group scales (one 32-bit word): loaded now, used by the
+      // epilogue two own tiles later, so the global load's latency is hidden.
+      uint32_t& sc_i = pi ? pend_sc1 : pend_sc0;
       asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sc_i) : "r"(raw + kTile * 128 + row * 4));
-      if (pi) pend_sc1 = sc_i; else pend_sc0 = sc_i;
       tmem_st64(tmem + lane_base + q * P::kSlotCols, f);
       tc_fence_before();
       __syncwarp();
@@ -508,6 +516,12 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     prep.advance(2, q_rows);
     if (++ring == kQRing) ring = 0;
     if (++stage == P::kStages) stage = 0;
+    return true;
+  };
+  // Own tiles i = set, set + 2, ... taken two at a time (parities 0, 1).
+  for (int i = set; i < n_tiles + 4; i += 4) {
+    if (!own_tile(i, std::integral_constant<int, 0>{})) return;
+    if (!own_tile(i + 2, std::integral_constant<int, 1>{})) return;
   }
 }
 
