@@ -14,7 +14,9 @@
 // per thread; O rescaling and the epilogue by all four, thread = TMEM lane),
 // warps 4-7 loaders (warp 4 + w owns ring slot w: cp.async gathers of random
 // 1 KB rows, waited by the warp and announced on the slot's mbarrier; each
-// also loads a quarter of Q), warp 8 MMA. Random rows reach shared memory
+// also loads a quarter of Q), warp 8 issues the QK^T MMAs and warp 9 the PV
+// MMAs (a barrier wait costs a single thread a few hundred cycles; two issuers
+// overlap their waits). Random rows reach shared memory
 // fastest through several slots with independent completion, hence four
 // 32 KB slots. S is double-buffered in tensor memory so QK^T of tile t + 1
 // runs while the softmax of tile t does. The running maximum only moves when
@@ -35,8 +37,9 @@ namespace {
 constexpr int kRows = 32;           // KV rows per tile
 constexpr int kSlots = 4;           // ring slots
 constexpr int kLoadWarp0 = 4;
-constexpr int kMmaWarp = kLoadWarp0 + kSlots;  // 8
-constexpr int kThreads = 32 * (kMmaWarp + 1);  // 288
+constexpr int kMmaWarp = kLoadWarp0 + kSlots;  // 8: QK^T issuer (and TMEM owner)
+constexpr int kPvWarp = kMmaWarp + 1;          // 9: PV issuer
+constexpr int kThreads = 32 * (kPvWarp + 1);   // 320
 constexpr int kMathBar = 1;         // named barrier of the 128 math threads
 
 // Shared-memory plan (offsets from a 1024-aligned base). The QK^T MMA reads
@@ -253,15 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       mbar_arrive(&misc->q_done);
     }
     if (paired) cluster_wait();
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ---------------- MMA issuers ----------------
+    // PV(t) is issued only after the softmax of tile t, hence after QK^T(t)
+    // completed: its commit alone frees the tile's slot, and the PV issuer's
+    // last commit means every MMA of the CTA has completed.
+    if (lane == 0 && warp == kPvWarp) {
       constexpr uint32_t idesc_o = mma_idesc(128, kHeads, true, true, false);
-      auto issue_pv = [&](int t) -> bool {
+      for (int t = 0; t < n_tiles; ++t) {
         const int sb = t & 1;
         if (!wait_bar(&misc->p_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status)) {
-          return false;
+          break;
         }
         tc_fence_after();
         fence_proxy_async_smem();
@@ -279,8 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
         mma_commit(&misc->kv_empty[t % kSlots]);
         mma_commit(&misc->p_empty[sb]);
-        return true;
-      };
+      }
+    }
+    if (lane == 0 && warp == kMmaWarp) {
+      constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
       bool ok = n_tiles == 0 || wait_bar(&misc->q_done, 0u, misc, a.status);
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int slot = t % kSlots, sb = t & 1;
@@ -305,9 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
           mma_f16(tmem + 64 * sb, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
         mma_commit(&misc->s_full[sb]);
-        if (t >= 1) ok = issue_pv(t - 1);
       }
-      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
     }
     __syncwarp();
     if (paired) cluster_wait();
@@ -428,20 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     const bool have_o = ok && n_tiles > 0;
     uint16_t* stage_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][512]
     uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
-    // O^T slice m, heads 16 c .. 16 c + 15 at dim m * 128 + tid (zeros without rows)
-    auto load_o = [&](int m, int c, float (&v)[16]) {
+    // O^T slice m: the 64 heads at dim m * 128 + tid (zeros without rows),
+    // one tensor-memory load of 64 columns.
+    auto load_o = [&](int m, float (&v)[64]) {
       if (have_o) {
-        tmem_ld16(la + 128 + 64 * m + 16 * c, v);
+        tmem_ld64(la + 128 + 64 * m, v);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        for (int i = 0; i < 64; ++i) v[i] = 0.f;
       }
     };
-    auto put_out = [&](int m, int c, const float (&v)[16]) {
+    auto put_out = [&](int m, const float (&v)[64]) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        stage_o[(16 * c + i) * kLatent + m * 128 + tid] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+      for (int h = 0; h < kHeads; ++h) {
+        stage_o[h * kLatent + m * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
       }
     };
     auto store_out = [&]() {
@@ -464,14 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       named_sync(kMathBar, 128);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
+        float v[64];
+        load_o(m, v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          load_o(m, c, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= misc->inv_l[16 * c + i];
-          put_out(m, c, v);
-        }
+        for (int h = 0; h < kHeads; ++h) v[h] *= misc->inv_l[h];
+        put_out(m, v);
       }
       store_out();
     } else {
@@ -488,15 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       float4* send = reinterpret_cast<float4*>(gbase + kSend);
 #pragma unroll 1
       for (int mm = 0; mm < 2; ++mm) {
+        float v[64];
+        load_o(2 * peer + mm, v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          load_o(2 * peer + mm, c, v);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            send[(mm * 16 + 4 * c + j) * 128 + tid] =
-                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
+        for (int g = 0; g < 16; ++g) {
+          send[(mm * 16 + g) * 128 + tid] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
       }
       if (warp < 2) {
@@ -540,21 +538,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       uint16_t* half_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][256]
 #pragma unroll 1
       for (int mm = 0; mm < 2; ++mm) {
+        float v[64];
+        load_o(2 * split + mm, v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          load_o(2 * split + mm, c, v);
+        for (int g = 0; g < 16; ++g) {
+          float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ok) q = recv[(mm * 16 + g) * 128 + tid];
+          const float pv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ok) q = recv[(mm * 16 + 4 * c + j) * 128 + tid];
-            const float pv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int hh = 16 * c + 4 * j + e;
-              const float o = fmaf(misc->wgt[1][hh], pv[e], v[4 * j + e] * misc->wgt[0][hh]);
-              half_o[hh * 256 + mm * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int hh = 4 * g + e;
+            const float o = fmaf(misc->wgt[1][hh], pv[e], v[hh] * misc->wgt[0][hh]);
+            half_o[hh * 256 + mm * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
           }
         }
       }

@@ -329,11 +329,22 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a, int u
 // of the output; only the warps' totals need a block-wide scan.
 constexpr int kRankMax = 64;  // final bins at most this large are ranked exactly
 
+// The score a valid order-preserving key stands for (inverse of score_key).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+// Value-space histogram bin: non-decreasing in v for v >= vmin.
+__device__ __forceinline__ uint32_t value_bin(float v, float vmin, float vscale) {
+  const float t = (v - vmin) * vscale;
+  return t >= static_cast<float>(kBins - 1) ? static_cast<uint32_t>(kBins - 1)
+                                             : static_cast<uint32_t>(t);
+}
+
 struct RegShared {
   uint32_t hist[kBins];
   uint32_t bin_key[kRankMax];
   uint32_t bin_idx[kRankMax];
-  uint32_t bin_take[kRankMax];
+  uint32_t taken[kThreads];  // bit i: candidate i of the final bin is selected (n <= 32 x 1024)
   uint32_t warp_a[kWarps], warp_b[kWarps], warp_c[kWarps];
   uint32_t kmin, kmax, n_valid, bstar, need, count, total;
 };
@@ -365,18 +376,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       }
     }
   }
+  sh.taken[tid] = 0u;
   uint32_t key[KPT];
-  float v[KPT];
   const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const int64_t i = wbase + 32 * j;
-    v[j] = i < n ? sc[i] : -INFINITY;
+    key[j] = score_key(i < n ? sc[i] : -INFINITY);
   }
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
-    key[j] = score_key(v[j]);
     if (key[j] > kInvalidKey) {
       kmin = min(kmin, key[j]);
       kmax = max(kmax, key[j]);
@@ -408,7 +418,73 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   const uint32_t span = sh.kmax - kmin;
   uint32_t P = 0, s_cur = 32, need = k;
   bool ties = false;
+  // Threshold search over a histogram in sh.hist: the bin holding the
+  // need-th largest key, counted from the top bin down.
+  auto find_threshold = [&](uint32_t nd) {
+    uint32_t h[4], local = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[j] = sh.hist[kBins - 1 - (4 * tid + j)];
+      local += h[j];
+    }
+    const uint32_t incl = warp_incl_scan(local);
+    if (lane == 31) sh.warp_a[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t x = sh.warp_a[lane];
+      sh.warp_b[lane] = warp_incl_scan(x) - x;
+    }
+    __syncthreads();
+    uint32_t run = incl - local + sh.warp_b[warp];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (run < nd && run + h[j] >= nd) {
+        sh.bstar = static_cast<uint32_t>(kBins - 1 - (4 * tid + j));
+        sh.need = nd - run;
+        sh.count = h[j];
+      }
+      run += h[j];
+    }
+    __syncthreads();
+  };
+  // Value-space level: bin = floor((v - vmin) * 4096 / (vmax - vmin)) is
+  // non-decreasing in v, so every key in a higher bin is strictly larger than
+  // every key in a lower one and equal keys share a bin; for smooth score
+  // distributions the threshold bin holds a handful of keys, which are then
+  // ranked exactly. Otherwise the radix levels below run from the start.
+  // Each candidate's bin is kept, two 16-bit bins per register.
+  bool vspace = false;
+  uint32_t vbin = 0;
+  uint32_t binp[(KPT + 1) / 2];
+#pragma unroll
+  for (int j = 0; j < (KPT + 1) / 2; ++j) binp[j] = 0;
   if (!take_all) {
+    const float vmin = key_value(kmin);
+    const float vspan = key_value(sh.kmax) - vmin;
+    const float vscale = static_cast<float>(kBins) / vspan;
+    if (vspan > 0.f && isfinite(vspan) && isfinite(vscale)) {
+      for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        if (key[j] > kInvalidKey) {
+          const uint32_t bj = value_bin(key_value(key[j]), vmin, vscale);
+          binp[j >> 1] |= bj << (16 * (j & 1));
+          atomicAdd(&sh.hist[bj], 1u);
+        }
+      }
+      __syncthreads();
+      find_threshold(need);
+      if (sh.count <= kRankMax) {
+        vspace = true;
+        vbin = sh.bstar;
+        need = sh.need;
+      }
+      __syncthreads();
+    }
+  }
+  auto bin_of = [&](int j) -> uint32_t { return (binp[j >> 1] >> (16 * (j & 1))) & 0xFFFFu; };
+  if (!take_all && !vspace) {
     uint32_t s_next = span < kBins ? 0u : static_cast<uint32_t>(32 - __clz(span)) - 12u;
     for (int level = 0; level < 4; ++level) {
       const uint32_t hs = s_cur, s_lv = s_next;
@@ -424,31 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         }
       }
       __syncthreads();
-      uint32_t h[4], local = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        h[j] = sh.hist[kBins - 1 - (4 * tid + j)];
-        local += h[j];
-      }
-      const uint32_t incl = warp_incl_scan(local);
-      if (lane == 31) sh.warp_a[warp] = incl;
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t x = sh.warp_a[lane];
-        sh.warp_b[lane] = warp_incl_scan(x) - x;
-      }
-      __syncthreads();
-      uint32_t run = incl - local + sh.warp_b[warp];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (run < need && run + h[j] >= need) {
-          sh.bstar = static_cast<uint32_t>(kBins - 1 - (4 * tid + j));
-          sh.need = need - run;
-          sh.count = h[j];
-        }
-        run += h[j];
-      }
-      __syncthreads();
+      find_threshold(need);
       P = (hs < 32 ? (P << width) : 0u) | sh.bstar;
       need = sh.need;
       s_cur = s_lv;
@@ -462,41 +514,49 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       __syncthreads();
     }
   }
-  // Final bin: rank its members exactly (unless they all tie).
-  uint32_t marked = 0;  // bit j: candidate j of this thread is a chosen bin member
+  // Candidate j's position relative to the threshold bin: 1 above, 0 in it, -1 below.
+  auto side = [&](int j) -> int {
+    if (vspace) {
+      const uint32_t bj = bin_of(j);
+      return bj > vbin ? 1 : (bj == vbin ? 0 : -1);
+    }
+    const uint32_t hi = (key[j] - kmin) >> s_cur;
+    return hi > P ? 1 : (hi == P ? 0 : -1);
+  };
+  // Final bin: rank its members exactly (unless they all tie), 16 threads per
+  // member, and mark the taken ones in sh.taken by candidate index.
   if (!take_all && !ties) {
     __syncthreads();  // every thread has read the last level's bin count
     if (tid == 0) sh.count = 0;
     __syncthreads();
-    uint32_t slot[KPT];
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      slot[j] = 0xFFFFFFFFu;
-      if (key[j] > kInvalidKey && ((key[j] - kmin) >> s_cur) == P) {
-        slot[j] = atomicAdd(&sh.count, 1u);
-        sh.bin_key[slot[j]] = key[j];
-        sh.bin_idx[slot[j]] = static_cast<uint32_t>(wbase + 32 * j);
+      if (key[j] > kInvalidKey && side(j) == 0) {
+        const uint32_t slot = atomicAdd(&sh.count, 1u);
+        sh.bin_key[slot] = key[j];
+        sh.bin_idx[slot] = static_cast<uint32_t>(wbase + 32 * j);
       }
     }
     __syncthreads();
     const uint32_t c = sh.count;
-    if (tid < c) {
-      const uint32_t ke = sh.bin_key[tid], ie = sh.bin_idx[tid];
-      uint32_t rank = 0;
-      for (uint32_t o = 0; o < c; ++o) {
+    const uint32_t mi = static_cast<uint32_t>(tid >> 4), part = static_cast<uint32_t>(tid & 15);
+    uint32_t rank = 0, ke = 0, ie = 0;
+    if (mi < c) {
+      ke = sh.bin_key[mi];
+      ie = sh.bin_idx[mi];
+      for (uint32_t o = part; o < c; o += 16) {
         const uint32_t ko = sh.bin_key[o];
         rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
       }
-      sh.bin_take[tid] = rank < need ? 1u : 0u;
     }
-    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      if (slot[j] != 0xFFFFFFFFu && sh.bin_take[slot[j]]) marked |= 1u << j;
-    }
+    for (int o = 8; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    if (part == 0 && mi < c && rank < need) atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
+    __syncthreads();
   }
-  // Flags once per candidate; counts per (slot, warp) run.
+  // Selection masks per slot run, then the warps' totals -> output offsets.
   uint32_t gt_mask[KPT], eq_mask[KPT];
+  uint32_t g_w = 0, e_w = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     bool gt = false, eq = false;
@@ -504,25 +564,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       if (take_all) {
         gt = true;
       } else {
-        const uint32_t hi = (key[j] - kmin) >> s_cur;
-        if (hi > P) gt = true;
-        else if (hi == P) {
-          if (ties) eq = true;
-          else gt = (marked >> j) & 1u;
+        const int sd = side(j);
+        if (sd > 0) {
+          gt = true;
+        } else if (sd == 0) {
+          if (ties) {
+            eq = true;
+          } else {
+            const uint32_t i = static_cast<uint32_t>(wbase + 32 * j);
+            gt = (sh.taken[i >> 5] >> (i & 31)) & 1u;
+          }
         }
       }
     }
     gt_mask[j] = __ballot_sync(0xFFFFFFFFu, gt);
-    eq_mask[j] = __ballot_sync(0xFFFFFFFFu, eq);
-  }
-  // Warp totals -> block scan (in warp order = index order) -> each warp's
-  // output offset and its share of the ties taken at the threshold.
-  uint32_t g_w = 0, e_w = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
+    eq_mask[j] = ties ? __ballot_sync(0xFFFFFFFFu, eq) : 0u;
     g_w += __popc(gt_mask[j]);
     e_w += __popc(eq_mask[j]);
   }
+  // Warp totals -> block scan (in warp order = index order) -> each warp's
+  // output offset and its share of the ties taken at the threshold.
   if (lane == 0) {
     sh.warp_a[warp] = g_w;
     sh.warp_b[warp] = e_w;
@@ -544,24 +605,31 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   int32_t* out = a.out_ids + static_cast<int64_t>(b) * a.k;
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t pos = sh.warp_a[warp];
-  const uint32_t te_w = sh.warp_b[warp];
-  uint32_t eq_seen = 0;
+  auto out_id = [&](int j) -> int32_t {
+    const int64_t i = wbase + 32 * j;
+    return a.block_ids ? bids[i >> 3] * 8 + static_cast<int32_t>(i & 7) : static_cast<int32_t>(i);
+  };
+  if (!ties) {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    // ties taken in this run: the first (te_w - eq_seen) tied lanes, if any left
-    const uint32_t left = te_w > eq_seen ? te_w - eq_seen : 0u;
-    const uint32_t eq_rank = __popc(eq_mask[j] & lt);
-    const bool is_gt = (gt_mask[j] >> lane) & 1u;
-    const bool is_eq = ((eq_mask[j] >> lane) & 1u) && eq_rank < left;
-    if (is_gt || is_eq) {
-      const int64_t i = wbase + 32 * j;
-      int32_t id = static_cast<int32_t>(i);
-      if (a.block_ids) id = bids[i >> 3] * 8 + static_cast<int32_t>(i & 7);
-      out[pos + __popc(gt_mask[j] & lt) + min(eq_rank, left)] = id;
+    for (int j = 0; j < KPT; ++j) {
+      if ((gt_mask[j] >> lane) & 1u) out[pos + __popc(gt_mask[j] & lt)] = out_id(j);
+      pos += __popc(gt_mask[j]);
     }
-    const uint32_t taken_eq = min(static_cast<uint32_t>(__popc(eq_mask[j])), left);
-    pos += __popc(gt_mask[j]) + taken_eq;
-    eq_seen += __popc(eq_mask[j]);
+  } else {
+    const uint32_t te_w = sh.warp_b[warp];
+    uint32_t eq_seen = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      // ties taken in this run: the first (te_w - eq_seen) tied lanes, if any left
+      const uint32_t left = te_w > eq_seen ? te_w - eq_seen : 0u;
+      const uint32_t eq_rank = __popc(eq_mask[j] & lt);
+      const bool is_gt = (gt_mask[j] >> lane) & 1u;
+      const bool is_eq = ((eq_mask[j] >> lane) & 1u) && eq_rank < left;
+      if (is_gt || is_eq) out[pos + __popc(gt_mask[j] & lt) + min(eq_rank, left)] = out_id(j);
+      const uint32_t taken_eq = min(static_cast<uint32_t>(__popc(eq_mask[j])), left);
+      pos += __popc(gt_mask[j]) + taken_eq;
+      eq_seen += __popc(eq_mask[j]);
+    }
   }
   const uint32_t total = sh.total;
   for (int64_t j = total + tid; j < a.k; j += kThreads) out[j] = -1;
