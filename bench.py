@@ -205,8 +205,8 @@ def run_ours(args):
     import two_tier_sparse_gb300 as dsa
 
     spec = dict(synth.WORKLOADS[args.workload])
-    if spec["kind"] != "decode":
-        raise SystemExit("bench.py times the decode step; prefill is measured by bench_prefill")
+    if spec["kind"] == "prefill":
+        return run_prefill(args, spec, dsa, synth, dev, rank, world)
     B, T, ratio, fmt = spec["B"], spec["T"], spec["ratio"], spec["key_fmt"]
     if args.batch:
         B = args.batch
@@ -419,6 +419,130 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# Algorithmic flops per prefill query (multiply-adds x 2): the block scan over
+# the visible blocks, the token scan over the kept tokens, QK^T and PV.
+def prefill_flops(n_q: int, ctx: int, ratio: int, k_blocks: int = 2048, k_tokens: int = 512,
+                  window: int = 128) -> float:
+    total = 0.0
+    for i in range(n_q):
+        p = ctx + i
+        n_vis = (p + 1) // ratio
+        nb = (n_vis + 7) // 8
+        kept = min(nb, k_blocks)
+        tokens = min(n_vis, kept * 8)
+        rows = min(tokens, k_tokens) + min(window, p + 1)
+        total += 2.0 * 16 * 128 * (nb + tokens) + 2.0 * 2 * 64 * 512 * rows
+    return total
+
+
+def run_prefill(args, spec, dsa, synth, dev, rank, world):
+    """A prefill chunk per step: n_q causal queries appended to ctx tokens of
+    one sequence (cache build, i.e. the pooled keys, outside the step)."""
+    import torch
+    n_q, ctx, ratio, fmt = spec["n_q"], spec["ctx"], spec["ratio"], spec["key_fmt"]
+    t0 = time.time()
+    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, spec["seed"] + 1000 * rank)
+    gen_s = time.time() - t0
+    cfg = dsa.config(ratio=ratio)
+    n_lat = (ctx + n_q) // ratio
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, q_idx, w, latents, swa = d(pf.q), d(pf.q_idx), d(pf.w), d(pf.latents), d(pf.swa)
+    keys = dsa.Keys(fmt, d(pf.keys.data), None if pf.keys.scales is None else d(pf.keys.scales))
+    del pf
+    nbf = n_lat // 8
+    if fmt == "bf16":
+        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.int16, device=dev))
+    else:
+        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.uint8, device=dev),
+                          torch.zeros((1, max(nbf, 1), 4), dtype=torch.uint8, device=dev))
+    ws = dsa.workspace(cfg, n_q, n_lat, dev)
+    keys1 = dsa.Keys(fmt, keys.data[None], None if keys.scales is None else keys.scales[None])
+    dsa.pool_index_keys(cfg, keys1, torch.tensor([nbf * 8], dtype=torch.int32, device=dev),
+                        nbf * 8, pooled, ws)
+    pooled2 = dsa.Keys(fmt, pooled.data[0], None if pooled.scales is None else pooled.scales[0])
+    out = torch.empty((n_q, 64, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((n_q, 64), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        dsa.sparse_attn_prefill(cfg, ctx, q, q_idx, w, latents, keys, pooled2, swa, out, ws, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    dsa.launch_counts(reset=True)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clocks:
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
+        dsa.launch_counts(reset=True)
+        for i in range(K):
+            flush.zero_()
+            ev_s[i].record()
+            step()
+            ev_e[i].record()
+        torch.cuda.synchronize()
+    counts = dsa.launch_counts(reset=True)
+    step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
+    ms = float(np.mean(step_ms))
+    # per-kernel breakdown (second pass with events around each launch)
+    kinds = {"pool": 1, "scan": 2, "select": 2, "attn": 1, "other": 1}
+    kev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n * K)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(n * K)])
+           for k, n in kinds.items()}
+    for k, (a_, b_) in kev.items():
+        dsa.profile_events(k, a_, b_)
+    for i in range(K):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for k in kinds:
+        dsa.profile_events(k, [], [])
+    n_launch = dsa.launch_counts(reset=True)
+    kernel_ms = {k: float(sum(s_.elapsed_time(e_) for s_, e_ in list(zip(*kev[k]))[:n_launch[k]]) / K)
+                 for k in kinds}
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+    flops = prefill_flops(n_q, ctx, ratio)
+    _, tf_peak, peak_kind = measured_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": "sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
+                      "TFLOP/s vs roofline",
+            "value": n_q / (ms * 1e-3), "unit": "queries/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "n_q": n_q, "ctx": ctx, "ratio": ratio,
+                       "key_fmt": fmt, "latents": n_lat,
+                       "l2": "flushed before every timed step (512 MiB write)",
+                       "input_gen_s": round(gen_s, 1)},
+            "roofline": {"kernel": "whole prefill step (tensor-core contractions)", "bound": "tensor",
+                         "achieved": tflops, "peak": tf_peak, "peak_kind": peak_kind,
+                         "unit": "TFLOP/s", "frac": tflops / tf_peak,
+                         "algorithmic_flops_per_step": flops},
+            "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q_)) for q_ in (10, 50, 90)],
+            "kernel_ms_per_step": kernel_ms,
+            "gpu_launches": int(sum(counts.values())),
+            "gpu_launches_by_kind": counts,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
 
 
 def main():
