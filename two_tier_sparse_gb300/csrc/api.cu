@@ -93,9 +93,8 @@ dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA
 // Split-KV setup of an attention launch over n queries: CTA pairs while the
 // pairs fit the SMs in one wave, else one CTA per query.
 void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
-  const int rows = c.k_tokens + c.window;
+  (void)c;
   a.splits = 2 * n <= device_sm_count() ? kAttnSplits : 1;
-  a.split_rows = ((rows + a.splits - 1) / a.splits + 31) / 32 * 32;
 }
 
 #define DSA_TRY(expr)                  \

@@ -4,8 +4,8 @@
 // recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse attention":
 // the 128-token window plus the selected latents).
 //
-// A query's rows (selected latents in id order, then its window rows) stream
-// through shared memory in tiles of 32 rows; two tcgen05 MMAs per tile run
+// A CTA's rows (its share of the window rows, then its share of the selected
+// latents in id order) stream through shared memory in tiles of 32 rows; two tcgen05 MMAs per tile run
 // with fp32 accumulators in tensor memory:
 //   S   = Q . KV^T    (M = 128 with the 64 heads in lanes 0..63, N = 32 rows, K = 512)
 //   O^T += KV^T . P^T (four M = 128 slices of the 512 latent dims, N = 64 heads,
@@ -23,8 +23,13 @@
 // it grows by more than 2^8 (the stale maximum keeps every P value <= 256,
 // exact enough in bf16 and fp32), so rescaling O is rare.
 //
-// Split-KV: for small batches a query's rows are cut into two ranges handled
-// by the two CTAs of a cluster. Each CTA sends the partner, over distributed
+// The window rows are inputs of the step: they stream while the previous
+// kernel (the token selection) still runs, and only the tiles holding
+// selected latents wait for its ids (programmatic dependent launch).
+//
+// Split-KV: for small batches the window rows and the selected latents of a
+// query are each cut in two halves handled by the two CTAs of a cluster. Each
+// CTA sends the partner, over distributed
 // shared memory in one bulk copy, its unnormalised O for the latent dims the
 // partner finishes plus its (max, sum); each then merges and writes one half
 // of the output dims.
@@ -71,7 +76,7 @@ static_assert(kAttnSplits == 2, "split-KV pairs the two CTAs of a cluster");
 
 struct Misc {
   uint64_t kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
-  uint64_t q_done, peer_ready, peer_data;  // peer_*: split-KV exchange
+  uint64_t q_done, ids_ready, peer_ready, peer_data;  // peer_*: split-KV exchange
   uint32_t tmem_base;
   int abort;
   int n_sel;
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       mbar_init(&misc->p_empty[i], 1);
     }
     mbar_init(&misc->q_done, 128);  // every loader thread, once its quarter of Q landed
+    mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
     mbar_init(&misc->peer_ready, 1);
     mbar_init(&misc->peer_data, 1);  // the receiver's expect-tx arrival + the bulk copy
     misc->abort = 0;
@@ -118,7 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   }
   if (warp == kMmaWarp) tmem_alloc(&misc->tmem_base, kTmemCols);
   griddep_launch_dependents();
-  griddep_wait();  // token ids and the window come from the previous kernels
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
+  // The partner's barriers are initialised before any remote arrival: every
+  // thread arrives here and waits before its first cluster access.
+  if (paired) cluster_arrive_relaxed();
 
   // This query's visible latents and window rows.
   int n_vis, n_sw;
@@ -142,6 +153,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   if (n_vis > a.lat_stride) n_vis = static_cast<int>(a.lat_stride);
   const uint16_t* lat =
       a.latents + (a.prefill ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
+  // This CTA's rows: its half of the window rows first (they are inputs of the
+  // step, so they stream while the previous kernel still selects the tokens),
+  // then its half of the selected latents (known once the ids are compacted).
+  const int w_half = (n_sw + 1) >> 1;
+  const int w_begin = paired ? min(n_sw, split * w_half) : 0;
+  const int w_cnt = paired ? min(n_sw, w_begin + w_half) - w_begin : n_sw;
+  auto sel_range = [&](int n_sel, int& s_begin, int& s_cnt) {
+    const int h = (n_sel + 1) >> 1;
+    s_begin = paired ? min(n_sel, split * h) : 0;
+    s_cnt = paired ? min(n_sel, s_begin + h) - s_begin : n_sel;
+  };
+  const uint32_t tmem = misc->tmem_base;
 
   const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
@@ -158,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     cp_async_commit();
   }
 
-  // Compact the valid token ids (>= 0 and < n_vis) in order (math threads).
+  // Compact the valid token ids (>= 0 and < n_vis) in order (math threads,
+  // once the previous kernel's ids are final).
   if (tid < 128) {
+    griddep_wait();
     const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
     constexpr int kPer = kMaxKTokens / 128;  // 4
     int my[kPer];
@@ -195,28 +220,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       if (my[j] >= 0) ids[before++] = my[j];
     }
     if (tid == 127) misc->n_sel = before;
+    named_sync(kMathBar, 128);
+    if (tid == 0) mbar_arrive(&misc->ids_ready);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  // The partner's barriers are initialised before any remote arrival: every
-  // thread arrives here and waits before its first cluster access.
-  if (paired) cluster_arrive_relaxed();
-  const uint32_t tmem = misc->tmem_base;
-  const int n_sel = misc->n_sel;
-  const int n_rows = n_sel + n_sw;
-  const int r_begin = split * a.split_rows;
-  const int r_end = min(n_rows, r_begin + a.split_rows);
-  const int n_tiles = r_end > r_begin ? (r_end - r_begin + kRows - 1) / kRows : 0;
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
     // ---------------- loaders ----------------
     // Warp 4 + w fills slot w with tiles w, w + 4, ...: it waits for its own
     // copies of a tile, fences them into the async proxy (the tensor core's
     // view) and then arrives, while the other slots' tiles are in flight.
+    // Tiles made only of window rows need no ids.
     const int w = warp - kLoadWarp0;
-    bool ok = true, q_reported = false;
-    for (int t = w; t < n_tiles && ok; t += kSlots) {
+    bool ok = true, q_reported = false, have_ids = false;
+    int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
+    for (int t = w;; t += kSlots) {
+      const int g0 = t * kRows;
+      if (!have_ids && g0 + kRows > w_cnt) {
+        if (!wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
+          ok = false;
+          break;
+        }
+        int s_cnt;
+        sel_range(misc->n_sel, s_begin, s_cnt);
+        n_rows_cta = w_cnt + s_cnt;
+        n_tiles = (n_rows_cta + kRows - 1) / kRows;
+        have_ids = true;
+      }
+      if (have_ids && t >= n_tiles) break;
       if (t >= kSlots &&
           !wait_bar(&misc->kv_empty[w], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
@@ -224,16 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         break;
       }
       const uint32_t dstb = sbase + kKV + w * kSlotBytes;
-      const int g0 = r_begin + t * kRows;
 #pragma unroll 8
       for (int j = 0; j < kRows * 64 / 32; ++j) {
         const int c = lane + 32 * j;
         const int row = c >> 6, cr = c & 63;
         const int g = g0 + row;
         const uint32_t dst = dstb + (cr >> 3) * kAtomBytes + sw128_off(row, cr & 7);
-        if (g < r_end) {
-          const uint16_t* src = (g < n_sel) ? lat + static_cast<int64_t>(ids[g]) * kLatent
-                                            : win + static_cast<int64_t>(g - n_sel) * kLatent;
+        if (g < n_rows_cta) {
+          const uint16_t* src = (g < w_cnt)
+                                    ? win + static_cast<int64_t>(w_begin + g) * kLatent
+                                    : lat + static_cast<int64_t>(ids[s_begin + g - w_cnt]) * kLatent;
           cp_async_16(dst, src + cr * 8);
         } else {
           st_shared_v4(dst, make_uint4(0, 0, 0, 0));
@@ -258,6 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     if (paired) cluster_wait();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ---------------- MMA issuers ----------------
+    int n_tiles = 0;
+    if (lane == 0 && wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
+      int s_begin, s_cnt;
+      sel_range(misc->n_sel, s_begin, s_cnt);
+      n_tiles = (w_cnt + s_cnt + kRows - 1) / kRows;
+    }
     // PV(t) is issued only after the softmax of tile t, hence after QK^T(t)
     // completed: its commit alone frees the tile's slot, and the PV issuer's
     // last commit means every MMA of the CTA has completed.
@@ -318,6 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     if (paired) cluster_wait();
   } else {
     // ---------------- math: softmax, rescale, epilogue ----------------
+    int s_begin, s_cnt;
+    sel_range(misc->n_sel, s_begin, s_cnt);
+    const int n_rows_cta = w_cnt + s_cnt;
+    const int n_tiles = (n_rows_cta + kRows - 1) / kRows;
     // A failed (timed-out) wait makes `ok` false for good; the thread then
     // skips the work but still reaches every named barrier, so the math warps
     // never part ways at a barrier.
@@ -335,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     };
     for (int t = 0; t < n_tiles; ++t) {
       const int sb = t & 1;
-      const int valid = min(kRows, r_end - (r_begin + t * kRows));
+      const int valid = min(kRows, n_rows_cta - t * kRows);
       float z[kRows];
       float alpha = 1.f;
       bool resc = false;

@@ -131,10 +131,10 @@ struct AttnArgs {
   int prefill;
   int64_t ctx;
   int ratio;
-  // Split-KV: with splits = 2 each query's rows are cut into two ranges of
-  // `split_rows` rows handled by the two CTAs of a cluster (merged on chip).
+  // Split-KV: with splits = 2 each query's window rows and selected latents
+  // are each cut in two halves handled by the two CTAs of a cluster (merged
+  // on chip).
   int splits;
-  int split_rows;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
