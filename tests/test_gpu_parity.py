@@ -364,16 +364,18 @@ def test_scan_many_short_queries(fmt):
         check_ids(tok[b], single["token_ids"], lambda i: pos[i], 24, f"tokens {b}")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
-def test_select_all_scores_tied(fmt):
+@pytest.mark.parametrize("fmt,k_blocks", [("bf16", 64), ("mxfp8", 64), ("bf16", 4096)])
+def test_select_all_scores_tied(fmt, k_blocks):
     """Weights 0 make every score 0: both tiers must keep the lowest indices
-    (the tie rule), whatever path the selection takes for heavy ties."""
+    (the tie rule), whatever path the selection takes for heavy ties. With
+    4096 of 5000 blocks most candidates are kept and the shorter sequence
+    keeps all of its blocks, padded with -1."""
     inp = synth.decode_inputs([40000, 30001], 1, fmt, seed=42)
     inp.w[:] = 0.0
-    cfg = dsa.config(k_blocks=64, k_tokens=100)
+    cfg = dsa.config(k_blocks=k_blocks, k_tokens=100)
     d = DecodeOnDevice(inp, cfg)
     d.pool()
-    bids = torch.empty((inp.B, 64), dtype=torch.int32, device="cuda")
+    bids = torch.empty((inp.B, k_blocks), dtype=torch.int32, device="cuda")
     dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws)
     tok = torch.empty((inp.B, 100), dtype=torch.int32, device="cuda")
     dsa.topk(cfg, d.q_idx, d.w, d.keys, bids, d.n_lat, d.cap, tok, d.ws)
@@ -381,6 +383,70 @@ def test_select_all_scores_tied(fmt):
     dsa.topk(cfg, d.q_idx, d.w, d.keys, None, d.n_lat, d.cap, tok_all, d.ws)
     assert d.status()[0] == 0
     for b in range(inp.B):
-        assert bids[b].tolist() == list(range(64))
+        nb = (int(inp.n_latents[b]) + 7) // 8
+        m = min(k_blocks, nb)
+        assert bids[b].tolist() == list(range(m)) + [-1] * (k_blocks - m)
         assert tok[b].tolist() == list(range(100))
         assert tok_all[b].tolist() == list(range(100))
+
+
+def top_k_of(scores, k):
+    """Ids of the k best finite scores (score desc, index asc), ascending, -1 padded."""
+    scores = np.asarray(scores)
+    idx = np.flatnonzero(np.isfinite(scores))
+    order = np.lexsort((idx, -scores[idx].astype(np.float64)))
+    sel = np.sort(idx[order[:k]])
+    return np.concatenate([sel, np.full(k - len(sel), -1)]).astype(np.int64)
+
+
+def scale_key_row(inp, b, t, log2_factor):
+    """Multiply index key t of sequence b by 2**log2_factor, exactly."""
+    if inp.keys.fmt == "bf16":
+        row = inp.keys.data[b, t]
+        nz = (row & 0x7FFF) != 0
+        row[nz] = row[nz] + np.uint16(log2_factor << 7)
+    else:
+        inp.keys.scales[b, t] += np.uint8(log2_factor)
+
+
+@pytest.mark.parametrize("fmt,k_blocks,outliers", [("bf16", 2048, False), ("mxfp8", 4096, False),
+                                                   ("bf16", 2048, True), ("mxfp8", 600, True)])
+def test_select_thousands_of_candidates(fmt, k_blocks, outliers):
+    """Block sets of 2500-7500 and token sets of 4800-32768 candidates. With outliers a
+    few keys are 4096x larger, so nearly every other score falls in the lowest
+    few of the value-space bins and the selection must refine by key bits.
+    The ids are checked against the oracle and, exactly, against the scores the
+    GPU returned (top-k of those by score desc, index asc)."""
+    T = [60000, 33000, 20000]
+    inp = synth.decode_inputs(T, 1, fmt, seed=26)
+    if outliers:
+        for t in (803, 32001, 56000):
+            scale_key_row(inp, 0, t, 12)
+        scale_key_row(inp, 1, 9, 12)
+    cfg = dsa.config(k_blocks=k_blocks, k_tokens=512, ratio=1)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    nbc = d.cap // 8
+    bids = torch.empty((inp.B, k_blocks), dtype=torch.int32, device="cuda")
+    bsc = torch.empty((inp.B, nbc), dtype=torch.float32, device="cuda")
+    dsa.index_blocks(cfg, d.q_idx, d.w, d.pooled, d.n_lat, d.cap, bids, d.ws, block_scores=bsc)
+    tok = torch.empty((inp.B, 512), dtype=torch.int32, device="cuda")
+    tsc = torch.empty((inp.B, k_blocks * 8), dtype=torch.float32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, bids, d.n_lat, d.cap, tok, d.ws, token_scores=tsc)
+    assert d.status()[0] == 0
+    bids_h, bsc_h = bids.cpu().numpy(), bsc.cpu().numpy()
+    tok_h, tsc_h = tok.cpu().numpy(), tsc.cpu().numpy()
+    oc = oracle_cfg(cfg)
+    for b in range(inp.B):
+        assert np.array_equal(bids_h[b], top_k_of(bsc_h[b], k_blocks)), f"blocks {b} vs own scores"
+        cand = top_k_of(tsc_h[b], 512)
+        want = np.where(cand >= 0, 8 * bids_h[b][np.maximum(cand, 0) // 8] + cand % 8, -1)
+        assert np.array_equal(tok_h[b], want), f"tokens {b} vs own scores"
+        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        nb = len(r["block_scores"])
+        check_scores(bsc_h[b, :nb], r["block_scores"], f"block scores {b}")
+        check_ids(bids_h[b], r["block_ids"], lambda i: r["block_scores"][i], k_blocks,
+                  f"blocks {b}")
+        r = O.decode_sequence(oc, inp, b, with_attention=False, block_ids=bids_h[b])
+        pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
+        check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
