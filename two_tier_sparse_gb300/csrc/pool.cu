@@ -39,17 +39,24 @@ __device__ __forceinline__ void load4(int fmt, const void* key_data, const uint8
   }
 }
 
-// Mean of rows [row0, row0 + c): fp32 sum in member order, then / c in fp32.
+// Mean of rows [row0, row0 + c), c in 1..8: fp32 sum in member order, then
+// / c in fp32. The c loads are all issued before the first add, so the block
+// costs one memory round trip rather than c.
 __device__ __forceinline__ void block_mean(int fmt, const void* key_data, const uint8_t* key_scales,
                                            int64_t row0, int c, int lane, float (&acc)[4]) {
-  float x[4];
-  load4(fmt, key_data, key_scales, row0, lane, x);
+  float x[8][4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) acc[e] = x[e];
-  for (int j = 1; j < c; ++j) {
-    load4(fmt, key_data, key_scales, row0 + j, lane, x);
+  for (int j = 0; j < 8; ++j) {
+    if (j < c) load4(fmt, key_data, key_scales, row0 + j, lane, x[j]);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+  for (int e = 0; e < 4; ++e) acc[e] = x[0][e];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) {
+    if (j < c) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], x[j][e]);
+    }
   }
   const float cf = static_cast<float>(c);
 #pragma unroll
