@@ -130,9 +130,10 @@ def test_topk_over_gpu_blocks(fmt, ratio):
         check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
-def test_topk_all_blocks(fmt):
-    T = [4096, 1000, 513, 30]
+@pytest.mark.parametrize("fmt,T", [("bf16", [4096, 1000, 513, 30]),
+                                   ("mxfp8", [4096, 1000, 513, 30]),
+                                   ("bf16", [90000, 70001, 3])])  # > 32768 latents: two passes
+def test_topk_all_blocks(fmt, T):
     inp = synth.decode_inputs(T, 2, fmt, seed=25)
     cfg = dsa.config(k_tokens=512, ratio=2)
     d = DecodeOnDevice(inp, cfg)
@@ -142,7 +143,10 @@ def test_topk_all_blocks(fmt):
     tok_h = tok.cpu().numpy()
     oc = oracle_cfg(cfg)
     for b in range(inp.B):
-        r = O.decode_sequence(oc, inp, b, with_attention=False)
+        # without block ids every visible latent is a candidate: the oracle's
+        # token stage over all blocks
+        nb = (int(inp.n_latents[b]) + 7) // 8
+        r = O.decode_sequence(oc, inp, b, with_attention=False, block_ids=np.arange(nb))
         pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
         check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
 
@@ -409,15 +413,22 @@ def scale_key_row(inp, b, t, log2_factor):
         inp.keys.scales[b, t] += np.uint8(log2_factor)
 
 
-@pytest.mark.parametrize("fmt,k_blocks,outliers", [("bf16", 2048, False), ("mxfp8", 4096, False),
-                                                   ("bf16", 2048, True), ("mxfp8", 600, True)])
-def test_select_thousands_of_candidates(fmt, k_blocks, outliers):
-    """Block sets of 2500-7500 and token sets of 4800-32768 candidates. With outliers a
+@pytest.mark.parametrize("T,fmt,k_blocks,outliers", [
+    ([60000, 33000, 20000], "bf16", 2048, False),
+    ([60000, 33000, 20000], "mxfp8", 4096, False),
+    ([60000, 33000, 20000], "bf16", 2048, True),
+    ([60000, 33000, 20000], "mxfp8", 600, True),
+    ([300000, 270001, 5000], "mxfp8", 2048, False),  # 37500 blocks: two-pass selection
+    ([300000, 270001, 5000], "bf16", 64, True),
+])
+def test_select_thousands_of_candidates(T, fmt, k_blocks, outliers):
+    """Block sets of 600-37500 and token sets of 4800-32768 candidates (above
+    32768 a query's block selection runs in two passes, chunk by chunk, then
+    over the chunks' winners). With outliers a
     few keys are 4096x larger, so nearly every other score falls in the lowest
     few of the value-space bins and the selection must refine by key bits.
     The ids are checked against the oracle and, exactly, against the scores the
     GPU returned (top-k of those by score desc, index asc)."""
-    T = [60000, 33000, 20000]
     inp = synth.decode_inputs(T, 1, fmt, seed=26)
     if outliers:
         for t in (803, 32001, 56000):

@@ -20,9 +20,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace regions for n queries over sequences of at most max_latents latents.
 struct Layout {
-  size_t status, block_scores, token_scores, block_ids, token_ids, total;
+  size_t status, block_scores, token_scores, block_ids, token_ids, select_tmp, total;
   int64_t nb_max, n_cand;
+  bool has_select_tmp;
 };
+
+// Candidates per query above which the selection runs in two passes through
+// a scratch of 32768 ids per query.
+constexpr int64_t kSelectOnePass = 32768;
 
 Layout layout(const dsa_config_t& c, int n, int64_t max_latents) {
   Layout L{};
@@ -41,6 +46,9 @@ Layout layout(const dsa_config_t& c, int n, int64_t max_latents) {
   off = align_up(off + static_cast<size_t>(n) * c.k_blocks * 4);
   L.token_ids = off;
   off = align_up(off + static_cast<size_t>(n) * c.k_tokens * 4);
+  L.select_tmp = off;
+  L.has_select_tmp = std::max(L.nb_max, L.n_cand) > kSelectOnePass;
+  if (L.has_select_tmp) off = align_up(off + static_cast<size_t>(n) * kSelectOnePass * 4);
   L.total = off;
   return L;
 }
@@ -125,9 +133,10 @@ cudaError_t launch(int kind, cudaStream_t s, F&& f) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(p.starts[slot]), s);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = f();
+  int n_launched = 1;
+  cudaError_t e = f(&n_launched);
   if (e != cudaSuccess) return e;
-  ++g_launches[kind];
+  g_launches[kind] += static_cast<uint64_t>(n_launched);
   if (timed) {
     ++p.next;
     return cudaEventRecord(static_cast<cudaEvent_t>(p.ends[slot]), s);
@@ -135,12 +144,20 @@ cudaError_t launch(int kind, cudaStream_t s, F&& f) {
   return cudaSuccess;
 }
 
-// Launch sequences shared by the public calls.
+// The workspace's selection scratch, or null when no query can have more than
+// kSelectOnePass candidates.
+int32_t* select_tmp(void* workspace, const Layout& L) {
+  return L.has_select_tmp ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.select_tmp)
+                          : nullptr;
+}
+
+// Launch sequences shared by the public calls. `sel_tmp`: scratch of
+// 32768 ids per query for two-pass selections (may be null).
 dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
                              const dsa_keys_t& pooled, const int32_t* n_lat, int B,
                              int64_t max_latents, int32_t* block_ids, float* scores,
-                             DeviceStatus* st, cudaStream_t s, int prefill, int64_t ctx,
-                             const dsa_keys_t* partial_keys) {
+                             DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s, int prefill,
+                             int64_t ctx, const dsa_keys_t* partial_keys) {
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
   ScanArgs sa{};
   sa.fmt = pooled.fmt;
@@ -159,7 +176,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
   sa.ctx = ctx;
   sa.ratio = c.ratio;
   sa.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&] { return launch_scan(sa, device_sm_count(), s); }));
+  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
   if (prefill) {
     PartialArgs pa{};
     pa.fmt = pooled.fmt;
@@ -172,7 +189,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     pa.ratio = c.ratio;
     pa.scores = scores;
     pa.n_rows = nb_max;
-    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_prefill_partial(pa, s); }));
+    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_prefill_partial(pa, s); }));
   }
   SelectArgs se{};
   se.scores = scores;
@@ -181,15 +198,16 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
   se.B = B;
   se.out_ids = block_ids;
   se.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&] { return launch_select(se, s); }));
+  se.tmp = sel_tmp;
+  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&](int* nl) { return launch_select(se, s, nl); }));
   return DSA_OK;
 }
 
 dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
                              const dsa_keys_t& keys, const int32_t* block_ids,
                              const int32_t* n_lat, int B, int64_t max_latents, int32_t* token_ids,
-                             float* scores, DeviceStatus* st, cudaStream_t s, int prefill,
-                             int64_t ctx) {
+                             float* scores, DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s,
+                             int prefill, int64_t ctx) {
   ScanArgs sa{};
   sa.fmt = keys.fmt;
   sa.key_data = keys.data;
@@ -214,7 +232,7 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
   sa.ctx = ctx;
   sa.ratio = c.ratio;
   sa.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&] { return launch_scan(sa, device_sm_count(), s); }));
+  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
   SelectArgs se{};
   se.scores = scores;
   se.n = sa.n_rows;
@@ -224,7 +242,8 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
   se.k_blocks = c.k_blocks;
   se.out_ids = token_ids;
   se.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&] { return launch_select(se, s); }));
+  se.tmp = sel_tmp;
+  DSA_CUDA(launch(DSA_KERNEL_SELECT, s, [&](int* nl) { return launch_select(se, s, nl); }));
   return DSA_OK;
 }
 
@@ -365,7 +384,7 @@ dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys
   a.out_scales = pooled->scales;
   a.out_stride = pooled->seq_stride_rows;
   a.status = at<DeviceStatus>(workspace, L.status);
-  DSA_CUDA(launch(DSA_KERNEL_POOL, static_cast<cudaStream_t>(stream), [&] { return launch_pool(a, static_cast<cudaStream_t>(stream)); }));
+  DSA_CUDA(launch(DSA_KERNEL_POOL, static_cast<cudaStream_t>(stream), [&](int*) { return launch_pool(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
 }
 
@@ -389,7 +408,8 @@ dsa_status_t dsa_index_blocks(const dsa_config_t* cfg, const void* q_idx, const 
   float* scores = block_scores ? block_scores : at<float>(workspace, L.block_scores);
   return run_block_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *pooled, n_latents, B,
                          max_latents, block_ids, scores, at<DeviceStatus>(workspace, L.status),
-                         static_cast<cudaStream_t>(stream), 0, 0, nullptr);
+                         select_tmp(workspace, L), static_cast<cudaStream_t>(stream), 0, 0,
+                         nullptr);
 }
 
 dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w,
@@ -413,8 +433,8 @@ dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w
   float* scores = token_scores ? token_scores : at<float>(workspace, L.token_scores);
   return run_token_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *keys, block_ids,
                          n_latents, B, max_latents, token_ids, scores,
-                         at<DeviceStatus>(workspace, L.status), static_cast<cudaStream_t>(stream),
-                         0, 0);
+                         at<DeviceStatus>(workspace, L.status), select_tmp(workspace, L),
+                         static_cast<cudaStream_t>(stream), 0, 0);
 }
 
 dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, const void* latents,
@@ -452,7 +472,7 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
   a.lse = lse;
   a.status = at<DeviceStatus>(workspace, L.status);
   set_splits(a, *cfg, B);
-  DSA_CUDA(launch(DSA_KERNEL_ATTN, static_cast<cudaStream_t>(stream), [&] { return launch_attn(a, static_cast<cudaStream_t>(stream)); }));
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, static_cast<cudaStream_t>(stream), [&](int*) { return launch_attn(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
 }
 
@@ -500,21 +520,23 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
     a.out_scales = pooled->scales;
     a.out_stride = pooled->seq_stride_rows;
     a.status = st;
-    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&] { return launch_pool(a, s); }));
+    DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_pool(a, s); }));
   }
   const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
   int32_t* bids = block_ids ? block_ids : at<int32_t>(workspace, L.block_ids);
   const int32_t* gather_ids = nullptr;
   if (L.nb_max > cfg->k_blocks) {
     DSA_TRY(run_block_stage(*cfg, qi, w, pk, n_latents, B, max_latents, bids,
-                            at<float>(workspace, L.block_scores), st, s, 0, 0, nullptr));
+                            at<float>(workspace, L.block_scores), st, select_tmp(workspace, L), s,
+                            0, 0, nullptr));
     gather_ids = bids;
   } else if (block_ids) {
-    DSA_CUDA(launch(DSA_KERNEL_OTHER, s, [&] { return launch_identity_blocks(n_latents, B, cfg->k_blocks, block_ids, s); }));
+    DSA_CUDA(launch(DSA_KERNEL_OTHER, s, [&](int*) { return launch_identity_blocks(n_latents, B, cfg->k_blocks, block_ids, s); }));
   }
   int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
   DSA_TRY(run_token_stage(*cfg, qi, w, *keys, gather_ids, n_latents, B, max_latents, tids,
-                          at<float>(workspace, L.token_scores), st, s, 0, 0));
+                          at<float>(workspace, L.token_scores), st, select_tmp(workspace, L), s, 0,
+                          0));
   AttnArgs a{};
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
@@ -531,7 +553,7 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   a.lse = lse;
   a.status = st;
   set_splits(a, *cfg, B);
-  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }
 
@@ -565,10 +587,12 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
   int32_t* bids = at<int32_t>(workspace, L.block_ids);
   DSA_TRY(run_block_stage(*cfg, qi, w, *pooled, nullptr, n_q, n_lat, bids,
-                          at<float>(workspace, L.block_scores), st, s, 1, ctx_len, keys));
+                          at<float>(workspace, L.block_scores), st, select_tmp(workspace, L), s, 1,
+                          ctx_len, keys));
   int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
   DSA_TRY(run_token_stage(*cfg, qi, w, *keys, bids, nullptr, n_q, n_lat, tids,
-                          at<float>(workspace, L.token_scores), st, s, 1, ctx_len));
+                          at<float>(workspace, L.token_scores), st, select_tmp(workspace, L), s, 1,
+                          ctx_len));
   AttnArgs a{};
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
@@ -586,7 +610,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   a.ratio = cfg->ratio;
   a.status = st;
   set_splits(a, *cfg, n_q);
-  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&] { return launch_attn(a, s); }));
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }
 
@@ -686,6 +710,6 @@ extern "C" dsa_status_t dsa_topk_noalloc(const dsa_config_t* cfg, const void* q_
   float* scores = nullptr;
   DSA_TRY(topk_scratch(&scores));
   return run_token_stage(*cfg, static_cast<const uint16_t*>(q_idx), w, *keys, block_ids,
-                         n_latents, B, max_latents, token_ids, scores, nullptr,
+                         n_latents, B, max_latents, token_ids, scores, nullptr, nullptr,
                          static_cast<cudaStream_t>(stream), 0, 0);
 }

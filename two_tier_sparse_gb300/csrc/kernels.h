@@ -109,8 +109,19 @@ struct SelectArgs {
   int k_blocks;
   int32_t* out_ids;  // [B, k]
   DeviceStatus* status;
+  // Scratch of B * 32768 ids (may be null) that lets a query with more than
+  // 32768 candidates be selected in two passes: the best k of each of C
+  // chunks of its candidates, then the best k of those C * k (C * k <= 32768).
+  int32_t* tmp;
+  // Set by launch_select for the two passes (zero for a plain selection):
+  int chunks;              // pass 1: CTA b * chunks + c takes chunk c of query b
+  int64_t chunk;           //         candidates [c * chunk, (c + 1) * chunk)
+  const int32_t* in_ids;   // pass 2: candidate i of query b is id in_ids[b * n_in + i]
+  int64_t n_in;
 };
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+// Returns the number of kernels launched in `launches` (1, or 2 for a
+// two-pass selection).
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches = nullptr);
 
 struct AttnArgs {
   const uint16_t* q;        // bf16 [B, 64, 512]

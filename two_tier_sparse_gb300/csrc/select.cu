@@ -16,6 +16,8 @@
 //      order are taken;
 //   3. one compaction pass in index order writes every key above the bin and
 //      the chosen bin members, so ids come out ascending with no sort.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace dsa {
@@ -355,11 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   extern __shared__ int32_t bids[];  // token stage: the query's block ids
   griddep_launch_dependents();
   griddep_wait();
-  const int b = blockIdx.x;
+  // The CTA's candidates: all of query b's (plain), chunk c of them (first
+  // pass of a two-pass selection), or the ids the first pass kept (second).
+  const int b = a.chunks ? static_cast<int>(blockIdx.x / a.chunks) : static_cast<int>(blockIdx.x);
+  const int64_t base = a.chunks ? static_cast<int64_t>(blockIdx.x % a.chunks) * a.chunk : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t n = a.n;
+  const int64_t n = a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n);
   const uint32_t k = static_cast<uint32_t>(a.k);
-  const float* sc = a.scores + static_cast<int64_t>(b) * n;
+  const float* sc = a.scores + static_cast<int64_t>(b) * a.n;
+  const int32_t* ids_in = a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in : nullptr;
 
   if (a.block_ids) {
     // Ascending block ids with -1 padding at the end are required: the tie
@@ -379,10 +385,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   sh.taken[tid] = 0u;
   uint32_t key[KPT];
   const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
+  if (ids_in) {
+    // Second pass: the kept ids ascend along the list (chunks in order, each
+    // ascending, -1 padded), so list order is id order for the tie rule.
+    // (The key registers hold the ids first: no second array.)
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int64_t i = wbase + 32 * j;
-    key[j] = score_key(i < n ? sc[i] : -INFINITY);
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t i = wbase + 32 * j;
+      key[j] = static_cast<uint32_t>(i < n ? ids_in[i] : -1);
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int32_t id = static_cast<int32_t>(key[j]);
+      key[j] = score_key(id >= 0 ? sc[id] : -INFINITY);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t i = wbase + 32 * j;
+      key[j] = score_key(i < n ? sc[base + i] : -INFINITY);
+    }
   }
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
 #pragma unroll
@@ -602,12 +624,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     if (lane == 31) sh.total = sel_incl;
   }
   __syncthreads();
-  int32_t* out = a.out_ids + static_cast<int64_t>(b) * a.k;
+  // First pass: row b * chunks + c of the scratch, i.e. row blockIdx.x.
+  int32_t* out = a.out_ids + static_cast<int64_t>(blockIdx.x) * a.k;
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t pos = sh.warp_a[warp];
   auto out_id = [&](int j) -> int32_t {
     const int64_t i = wbase + 32 * j;
-    return a.block_ids ? bids[i >> 3] * 8 + static_cast<int32_t>(i & 7) : static_cast<int32_t>(i);
+    if (ids_in) return ids_in[i];
+    return a.block_ids ? bids[i >> 3] * 8 + static_cast<int32_t>(i & 7)
+                       : static_cast<int32_t>(base + i);
   };
   if (!ties) {
 #pragma unroll
@@ -638,22 +663,52 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
 }  // namespace
 
 template <int KPT>
-cudaError_t launch_reg(const SelectArgs& a, cudaStream_t s) {
+cudaError_t launch_reg(const SelectArgs& a, unsigned grid, cudaStream_t s) {
   const size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
   static int smem_set[64] = {0};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
                               static_cast<int>(kMaxKBlocks * 4), smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_reg_kernel<KPT>, dim3(a.B), dim3(kThreads), smem, s, 1, a);
+  return launch_pdl(select_reg_kernel<KPT>, dim3(grid), dim3(kThreads), smem, s, 1, a);
 }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
+// Register-resident selection of m <= 32 * kThreads candidates per CTA.
+cudaError_t launch_reg_for(const SelectArgs& a, int64_t m, unsigned grid, cudaStream_t s) {
+  if (m <= 2 * kThreads) return launch_reg<2>(a, grid, s);
+  if (m <= 4 * kThreads) return launch_reg<4>(a, grid, s);
+  if (m <= 8 * kThreads) return launch_reg<8>(a, grid, s);
+  if (m <= 16 * kThreads) return launch_reg<16>(a, grid, s);
+  return launch_reg<32>(a, grid, s);
+}
+
+constexpr int64_t kRegMax = 32 * kThreads;  // candidates a register-resident CTA holds
+constexpr int kMaxChunks = 64;
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
+  if (launches) *launches = 0;
   if (a.B == 0) return cudaSuccess;
-  if (a.n <= 2 * kThreads) return launch_reg<2>(a, s);
-  if (a.n <= 4 * kThreads) return launch_reg<4>(a, s);
-  if (a.n <= 8 * kThreads) return launch_reg<8>(a, s);
-  if (a.n <= 16 * kThreads) return launch_reg<16>(a, s);
-  if (a.n <= 32 * kThreads) return launch_reg<32>(a, s);
+  if (launches) *launches = 1;
+  if (a.n <= kRegMax) return launch_reg_for(a, a.n, a.B, s);
+  // Two passes over C chunks: every query's best k lies within the best k of
+  // its own chunk (same order, same ids), so the second pass over the C * k
+  // kept ids finds exactly the plain selection.
+  if (a.tmp && !a.block_ids && a.k > 0) {
+    const int64_t C = std::min<int64_t>(kRegMax / a.k, kMaxChunks);
+    const int64_t chunk = (a.n + C - 1) / C;
+    if (C >= 2 && chunk <= kRegMax && chunk > a.k) {
+      SelectArgs p1 = a;
+      p1.chunks = static_cast<int>(C);
+      p1.chunk = chunk;
+      p1.out_ids = a.tmp;
+      cudaError_t e = launch_reg_for(p1, chunk, static_cast<unsigned>(a.B * C), s);
+      if (e != cudaSuccess) return e;
+      SelectArgs p2 = a;
+      p2.in_ids = a.tmp;
+      p2.n_in = C * a.k;
+      if (launches) *launches = 2;
+      return launch_reg_for(p2, p2.n_in, a.B, s);
+    }
+  }
   const int use_cache = a.n <= kCacheMax ? 1 : 0;
   const size_t smem = (use_cache ? static_cast<size_t>(a.n) * 4 : 0) +
                       (a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0);
