@@ -693,7 +693,11 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
   // its own chunk (same order, same ids), so the second pass over the C * k
   // kept ids finds exactly the plain selection.
   if (a.tmp && !a.block_ids && a.k > 0) {
-    const int64_t C = std::min<int64_t>(kRegMax / a.k, kMaxChunks);
+    // As many chunks as keep the second pass at 16 candidates a thread (the
+    // 32-a-thread kernel spills), but enough for each chunk to fit a CTA.
+    const int64_t c_fit = (a.n + kRegMax - 1) / kRegMax;
+    const int64_t c_pref = std::min<int64_t>(kRegMax / 2 / a.k, kMaxChunks);
+    const int64_t C = std::min<int64_t>(std::max(c_fit, c_pref), kRegMax / a.k);
     const int64_t chunk = (a.n + C - 1) / C;
     if (C >= 2 && chunk <= kRegMax && chunk > a.k) {
       SelectArgs p1 = a;
