@@ -98,11 +98,18 @@ T* at(void* ws, size_t off) {
 
 dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
-// Split-KV setup of an attention launch over n queries: CTA pairs while the
-// pairs fit the SMs in one wave, else one CTA per query.
+// Split-KV setup of an attention launch over n queries: the most CTAs per
+// query (8, 4 or 2) that still fit the SMs in one wave, else one.
 void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
   (void)c;
-  a.splits = 2 * n <= device_sm_count() ? kAttnSplits : 1;
+  const int sms = device_sm_count();
+  a.splits = 1;
+  for (int sp = kMaxAttnSplits; sp >= 2; sp /= 2) {
+    if (static_cast<int64_t>(sp) * n <= sms) {
+      a.splits = sp;
+      break;
+    }
+  }
 }
 
 #define DSA_TRY(expr)                  \

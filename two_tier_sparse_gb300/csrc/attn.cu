@@ -27,12 +27,12 @@
 // kernel (the token selection) still runs, and only the tiles holding
 // selected latents wait for its ids (programmatic dependent launch).
 //
-// Split-KV: for small batches the window rows and the selected latents of a
-// query are each cut in two halves handled by the two CTAs of a cluster. Each
-// CTA sends the partner, over distributed
-// shared memory in one bulk copy, its unnormalised O for the latent dims the
-// partner finishes plus its (max, sum); each then merges and writes one half
-// of the output dims.
+// Split-KV: while S x queries CTAs fit the SMs (S = 8, 4 or 2), the window
+// rows and the selected latents of a query are each cut in S parts handled by
+// the S CTAs of a cluster. CTA r finishes the latent dims [r D, r D + D),
+// D = 512 / S: every CTA stores, into each peer's then idle ring (distributed
+// shared memory), its unnormalised O for that peer's dims and its (max, sum);
+// after a cluster barrier each merges its dims and writes them.
 #include "kernels.h"
 
 namespace dsa {
@@ -63,27 +63,25 @@ constexpr int kSmemBytes = kMisc + kMiscBytes + 1024;  // + alignment slack of t
 constexpr int kTmemCols = 512;  // S[b]: cols [64 b, 64 b + 32); O^T slice m: [128 + 64 m, ...)
 constexpr uint32_t kOutBytes = kHeads * kLatent * 2;  // one query's bf16 output, [64 h][512]
 static_assert(kP - kQ == static_cast<int>(kOutBytes), "the Q region stages the output");
-// Split-KV exchange payload: O of two 128-dim slices as float4 groups
-// [2 mm][16 g][128 d] (heads 4 g .. 4 g + 3 at dim d), then (max, sum) per head.
-constexpr uint32_t kXchgO = 2 * 16 * 128 * 16;                // 64 KB
-constexpr uint32_t kXchgBytes = kXchgO + kHeads * 2 * 4;       // + 512 B
-constexpr int kRecv = kKV;                                     // incoming payload
-constexpr int kSend = kKV + 65 * 1024;                         // outgoing payload
-static_assert(kRecv + static_cast<int>(kXchgBytes) <= kSend, "payloads apart");
-static_assert(kSend + static_cast<int>(kXchgBytes) <= kIds + kMaxKTokens * 4,
-              "the outgoing payload ends inside the (then unused) id list");
-static_assert(kAttnSplits == 2, "split-KV pairs the two CTAs of a cluster");
+// Split-KV exchange, received into the ring: from sender s, O of the
+// receiver's D dims as float4 groups [16 g][D d] (heads 4 g .. 4 g + 3 at dim
+// d), at kRecv + s * D * 256 (S slots of D * 256 bytes: 128 KB whatever S).
+// The (max, sum) of every sender and the merge weights go to the P buffers.
+constexpr int kRecv = kKV;
+static_assert(kSlots * kSlotBytes == kLatent * kHeads * 4, "S receive slots fill the ring");
+constexpr int kMl = kP;                          // [S][64 h][2] (max, sum)
+constexpr int kWgt = kMl + kMaxAttnSplits * kHeads * 2 * 4;  // [S][64 h] merge weights
+static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge tables fit the P buffers");
 
 struct Misc {
   uint64_t kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
-  uint64_t q_done, ids_ready, peer_ready, peer_data;  // peer_*: split-KV exchange
+  uint64_t q_done, ids_ready;
   uint32_t tmem_base;
   int abort;
   int n_sel;
   int warp_cnt[4];
   float alpha[kHeads];
   float inv_l[kHeads];
-  float wgt[2][kHeads];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 
@@ -101,8 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   int32_t* ids = reinterpret_cast<int32_t*>(gbase + kIds);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
-  const int split = blockIdx.y;
-  const bool paired = a.splits == 2;
+  const int split = blockIdx.y;  // rank in the cluster
+  const int S = a.splits;
+  const bool paired = S > 1;
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -117,8 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     }
     mbar_init(&misc->q_done, 128);  // every loader thread, once its quarter of Q landed
     mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
-    mbar_init(&misc->peer_ready, 1);
-    mbar_init(&misc->peer_data, 1);  // the receiver's expect-tx arrival + the bulk copy
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -153,18 +150,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   if (n_vis > a.lat_stride) n_vis = static_cast<int>(a.lat_stride);
   const uint16_t* lat =
       a.latents + (a.prefill ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
-  // This CTA's rows: its half of the window rows first (they are inputs of the
+  // This CTA's rows: its part of the window rows first (they are inputs of the
   // step, so they stream while the previous kernel still selects the tokens),
-  // then its half of the selected latents (known once the ids are compacted).
-  const int w_half = (n_sw + 1) >> 1;
-  const int w_begin = paired ? min(n_sw, split * w_half) : 0;
-  const int w_cnt = paired ? min(n_sw, w_begin + w_half) - w_begin : n_sw;
+  // then its part of the selected latents (known once the ids are compacted).
+  const int w_part = (n_sw + S - 1) / S;
+  const int w_begin = min(n_sw, split * w_part);
+  const int w_cnt = min(n_sw, w_begin + w_part) - w_begin;
   auto sel_range = [&](int n_sel, int& s_begin, int& s_cnt) {
-    const int h = (n_sel + 1) >> 1;
-    s_begin = paired ? min(n_sel, split * h) : 0;
-    s_cnt = paired ? min(n_sel, s_begin + h) - s_begin : n_sel;
+    const int h = (n_sel + S - 1) / S;
+    s_begin = min(n_sel, split * h);
+    s_cnt = min(n_sel, s_begin + h) - s_begin;
   };
   const uint32_t tmem = misc->tmem_base;
+  // Cluster barrier phases of a split-KV CTA, for the warps that do not take
+  // part in the exchange: every thread of the cluster arrives at each.
+  //   0 (arrived at start-up): every CTA's barriers are initialised;
+  //   1: every CTA's MMAs are done, so its ring and P buffers may be written;
+  //   2: every exchange store has landed.
+  auto exchange_phases = [&]() {
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+  };
 
   const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
@@ -231,13 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     // view) and then arrives, while the other slots' tiles are in flight.
     // Tiles made only of window rows need no ids.
     const int w = warp - kLoadWarp0;
-    bool ok = true, q_reported = false, have_ids = false;
+    bool q_reported = false, have_ids = false;
     int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
     for (int t = w;; t += kSlots) {
       const int g0 = t * kRows;
       if (!have_ids && g0 + kRows > w_cnt) {
         if (!wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
-          ok = false;
           break;
         }
         int s_cnt;
@@ -250,7 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       if (t >= kSlots &&
           !wait_bar(&misc->kv_empty[w], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
-        ok = false;
         break;
       }
       const uint32_t dstb = sbase + kKV + w * kSlotBytes;
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       fence_proxy_async_smem();
       mbar_arrive(&misc->q_done);
     }
-    if (paired) cluster_wait();
+    if (paired) exchange_phases();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ---------------- MMA issuers ----------------
     int n_tiles = 0;
@@ -306,15 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
         tc_fence_after();
         fence_proxy_async_smem();
-        const uint32_t kvb = sbase + kKV + (t % kSlots) * kSlotBytes;
-        const uint32_t pb = sbase + kP + sb * kPBytes;
+        // Descriptors are built once and stepped by their start-address field
+        // (16-byte units; every operand lies below 256 KB, so no carry).
+        const uint64_t ad0 =
+            sw128_desc(sbase + kKV + (t % kSlots) * kSlotBytes, kAtomBytes, 1024);
+        const uint64_t bd0 = sw128_desc(sbase + kP + sb * kPBytes, 16, 1024);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
           for (int ks = 0; ks < kRows / 16; ++ks) {
-            const uint64_t ad =
-                sw128_desc(kvb + m * 2 * kAtomBytes + ks * 16 * 128, kAtomBytes, 1024);
-            const uint64_t bd = sw128_desc(pb + ks * 32, 16, 1024);
+            const uint64_t ad = ad0 + ((m * 2 * kAtomBytes + ks * 16 * 128) >> 4);
+            const uint64_t bd = bd0 + ((ks * 32) >> 4);
             mma_f16(tmem + 128 + 64 * m, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
           }
         }
@@ -339,19 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
         tc_fence_after();
         fence_proxy_async_smem();
-        const uint32_t kvb = sbase + kKV + slot * kSlotBytes;
+        const uint64_t ad0 = sw128_desc(sbase + kQ, 16, 1024);
+        const uint64_t bd0 = sw128_desc(sbase + kKV + slot * kSlotBytes, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < kLatent / 16; ++ks) {
-          const uint64_t ad =
-              sw128_desc(sbase + kQ + (ks >> 2) * (kHeads * 128) + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(kvb + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
+          const uint64_t ad = ad0 + (((ks >> 2) * (kHeads * 128) + (ks & 3) * 32) >> 4);
+          const uint64_t bd = bd0 + (((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
           mma_f16(tmem + 64 * sb, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
         mma_commit(&misc->s_full[sb]);
       }
     }
     __syncwarp();
-    if (paired) cluster_wait();
+    if (paired) exchange_phases();
   } else {
     // ---------------- math: softmax, rescale, epilogue ----------------
     int s_begin, s_cnt;
@@ -517,90 +526,104 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       }
       store_out();
     } else {
-      // CTA `split` finishes latent dims [256 split, 256 split + 256) (slices
-      // 2 split, 2 split + 1) and sends its partner the other two slices.
-      const int peer = 1 - split;
-      cluster_wait();  // both CTAs' barriers are initialised
-      if (tid == 0) {
-        // The ring is free (every MMA completed): the partner may write it.
-        mbar_arrive_expect_tx(&misc->peer_data, kXchgBytes);
-        mbar_arrive_cluster(mapa_shared(smem_u32(&misc->peer_ready), peer));
-      }
-      // Outgoing payload: O of the partner's slices, then (max, sum).
-      float4* send = reinterpret_cast<float4*>(gbase + kSend);
+      // CTA `split` finishes latent dims [split D, split D + D). O^T slice m
+      // holds dim 128 m + tid in this thread's lane, so the thread's four dims
+      // go to CTAs (128 m + tid) / D (a warp's 32 dims always go to one CTA).
+      const int D = kLatent / S;
+      const uint32_t pay = static_cast<uint32_t>(D) * kHeads * 4;  // bytes from one sender
+      float* ml = reinterpret_cast<float*>(gbase + kMl);            // [S][64][2]
+      float* wgt = reinterpret_cast<float*>(gbase + kWgt);          // [S][64]
+      const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
+      cluster_wait();     // phase 0
+      cluster_arrive();   // phase 1: this CTA's MMAs are done (waited above)
+      cluster_wait();
 #pragma unroll 1
-      for (int mm = 0; mm < 2; ++mm) {
+      for (int m = 0; m < 4; ++m) {
+        const int d = 128 * m + tid;
+        const int p = d / D;
+        if (p == split) continue;
         float v[64];
-        load_o(2 * peer + mm, v);
+        load_o(m, v);
+        const uint32_t dst = mapa_shared(sbase + kRecv + split * pay, static_cast<uint32_t>(p)) +
+                             static_cast<uint32_t>(d - p * D) * 16;
 #pragma unroll
         for (int g = 0; g < 16; ++g) {
-          send[(mm * 16 + g) * 128 + tid] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          st_cluster_v4(dst + static_cast<uint32_t>(g * D) * 16, v[4 * g], v[4 * g + 1],
+                        v[4 * g + 2], v[4 * g + 3]);
         }
       }
       if (warp < 2) {
-        float* ml = reinterpret_cast<float*>(gbase + kSend + kXchgO);
-        ml[2 * tid] = have_o ? m_run : -INFINITY;
-        ml[2 * tid + 1] = have_o ? l_run : 0.f;
-      }
-      fence_proxy_async_smem();
-      named_sync(kMathBar, 128);
-      if (tid == 0) {
-        if (ok) ok = mbar_wait_cluster(&misc->peer_ready, 0u, &misc->abort, a.status, SITE_ATTN);
-        if (ok) {
-          bulk_s2cluster(mapa_shared(sbase + kRecv, peer), sbase + kSend, kXchgBytes,
-                         mapa_shared(smem_u32(&misc->peer_data), peer));
+        const uint32_t off = static_cast<uint32_t>((split * kHeads + tid) * 2) * 4;
+        for (int p = 0; p < S; ++p) {
+          if (p == split) {
+            ml[(split * kHeads + tid) * 2] = m_own;
+            ml[(split * kHeads + tid) * 2 + 1] = l_own;
+          } else {
+            const uint32_t dst = mapa_shared(sbase + kMl + off, static_cast<uint32_t>(p));
+            st_cluster_f32(dst, m_own);
+            st_cluster_f32(dst + 4, l_own);
+          }
         }
       }
-      if (ok) ok = mbar_wait_cluster(&misc->peer_data, 0u, &misc->abort, a.status, SITE_ATTN);
-      // out = w_own O_own + w_peer O_peer with w_s = 2^(m_s - M) / L,
-      // M = max_s m_s, L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0).
+      cluster_arrive();   // phase 2: this CTA's stores are out (release)
+      cluster_wait();     // ... and every peer's have landed here (acquire)
+      // out = sum_s w_s O_s with w_s = 2^(m_s - M) / L, M = max_s m_s,
+      // L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0).
       if (warp < 2) {
-        const float* pml = reinterpret_cast<const float*>(gbase + kRecv + kXchgO);
-        const float m0 = have_o ? m_run : -INFINITY, l0 = have_o ? l_run : 0.f;
-        const float m1 = ok ? pml[2 * tid] : -INFINITY;
-        const float l1 = ok ? pml[2 * tid + 1] : 0.f;
         float M = -INFINITY;
-        if (l0 > 0.f) M = m0;
-        if (l1 > 0.f) M = fmaxf(M, m1);
-        const float e0 = l0 > 0.f ? exp2f(m0 - M) : 0.f;
-        const float e1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
-        const float L = e0 * l0 + e1 * l1;
+        for (int q = 0; q < S; ++q) {
+          if (ml[(q * kHeads + tid) * 2 + 1] > 0.f) M = fmaxf(M, ml[(q * kHeads + tid) * 2]);
+        }
+        float L = 0.f;
+        for (int q = 0; q < S; ++q) {
+          const float lq = ml[(q * kHeads + tid) * 2 + 1];
+          const float eq = lq > 0.f ? exp2f(ml[(q * kHeads + tid) * 2] - M) : 0.f;
+          wgt[q * kHeads + tid] = eq;
+          L = fmaf(eq, lq, L);
+        }
         const float inv_L = L > 0.f ? 1.f / L : 0.f;
-        misc->wgt[0][tid] = e0 * inv_L;
-        misc->wgt[1][tid] = e1 * inv_L;
+        for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
         if (a.lse && split == 0) {
           a.lse[static_cast<int64_t>(b) * kHeads + tid] =
               L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
         }
       }
       named_sync(kMathBar, 128);
-      const float4* recv = reinterpret_cast<const float4*>(gbase + kRecv);
-      uint16_t* half_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][256]
+      uint16_t* part_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][D]
 #pragma unroll 1
-      for (int mm = 0; mm < 2; ++mm) {
+      for (int m = 0; m < 4; ++m) {
+        const int d = 128 * m + tid;
+        if (d / D != split) continue;
+        const int dd = d - split * D;
         float v[64];
-        load_o(2 * split + mm, v);
+        load_o(m, v);
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (ok) q = recv[(mm * 16 + g) * 128 + tid];
-          const float pv[4] = {q.x, q.y, q.z, q.w};
+        for (int h = 0; h < kHeads; ++h) v[h] *= wgt[split * kHeads + h];
+        for (int q = 0; q < S; ++q) {
+          if (q == split) continue;
+          const float4* rq =
+              reinterpret_cast<const float4*>(gbase + kRecv + static_cast<uint32_t>(q) * pay);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int hh = 4 * g + e;
-            const float o = fmaf(misc->wgt[1][hh], pv[e], v[hh] * misc->wgt[0][hh]);
-            half_o[hh * 256 + mm * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          for (int g = 0; g < 16; ++g) {
+            const float4 x = rq[g * D + dd];
+            v[4 * g] = fmaf(wgt[q * kHeads + 4 * g], x.x, v[4 * g]);
+            v[4 * g + 1] = fmaf(wgt[q * kHeads + 4 * g + 1], x.y, v[4 * g + 1]);
+            v[4 * g + 2] = fmaf(wgt[q * kHeads + 4 * g + 2], x.z, v[4 * g + 2]);
+            v[4 * g + 3] = fmaf(wgt[q * kHeads + 4 * g + 3], x.w, v[4 * g + 3]);
           }
+        }
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) {
+          part_o[h * D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
         }
       }
       named_sync(kMathBar, 128);
-      // 64 rows of 512 B: a warp stores one row per instruction
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int e = tid + 128 * i;
-        const int hh = e >> 5, ch = e & 31;
-        const uint4 v = *reinterpret_cast<const uint4*>(gbase + kQ + hh * 512 + ch * 16);
-        *reinterpret_cast<uint4*>(out + hh * kLatent + 256 * split + ch * 8) = v;
+      // 64 rows of 2 D bytes, 16 bytes a store
+      const int per_row = D / 8;
+      for (int i = tid; i < kHeads * per_row; i += 128) {
+        const int hh = i / per_row, ch = i - hh * per_row;
+        const uint4 v = *reinterpret_cast<const uint4*>(gbase + kQ + hh * 2 * D + ch * 16);
+        *reinterpret_cast<uint4*>(out + hh * kLatent + D * split + ch * 8) = v;
       }
     }
   }
@@ -611,18 +634,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // No CTA of a pair leaves while its partner may still touch its shared memory.
-  if (paired) {
-    cluster_arrive();
-    cluster_wait();
-  }
+  // (No remote access follows phase 2 of the exchange, so a CTA may leave
+  // while its peers still merge.)
 }
 
 }  // namespace
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
-  if (a.splits != 1 && a.splits != 2) return cudaErrorInvalidValue;
+  if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) {
+    return cudaErrorInvalidValue;
+  }
   static int smem_set[64] = {0};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;

@@ -142,15 +142,16 @@ struct AttnArgs {
   int prefill;
   int64_t ctx;
   int ratio;
-  // Split-KV: with splits = 2 each query's window rows and selected latents
-  // are each cut in two halves handled by the two CTAs of a cluster (merged
-  // on chip).
+  // Split-KV: with splits = S in {2, 4, 8} each query's window rows and
+  // selected latents are each cut in S parts handled by the S CTAs of a
+  // cluster (merged on chip); 1: one CTA per query.
   int splits;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
-// Split-KV runs query pairs of CTAs while 2 x queries fits the SMs in one wave.
-constexpr int kAttnSplits = 2;
+// Split-KV runs S CTAs per query, the largest S in {8, 4, 2} for which S x
+// queries fits the SMs in one wave.
+constexpr int kMaxAttnSplits = 8;
 
 // block_ids[b] = 0, 1, ..., ceil(n_latents[b] / 8) - 1, then -1.
 cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks,
