@@ -63,19 +63,21 @@ constexpr int kSmemBytes = kMisc + kMiscBytes + 1024;  // + alignment slack of t
 constexpr int kTmemCols = 512;  // S[b]: cols [64 b, 64 b + 32); O^T slice m: [128 + 64 m, ...)
 constexpr uint32_t kOutBytes = kHeads * kLatent * 2;  // one query's bf16 output, [64 h][512]
 static_assert(kP - kQ == static_cast<int>(kOutBytes), "the Q region stages the output");
-// Split-KV exchange, received into the ring: from sender s, O of the
-// receiver's D dims as float4 groups [16 g][D d] (heads 4 g .. 4 g + 3 at dim
-// d), at kRecv + s * D * 256 (S slots of D * 256 bytes: 128 KB whatever S).
-// The (max, sum) of every sender and the merge weights go to the P buffers.
-constexpr int kRecv = kKV;
-static_assert(kSlots * kSlotBytes == kLatent * kHeads * 4, "S receive slots fill the ring");
-constexpr int kMl = kP;                          // [S][64 h][2] (max, sum)
-constexpr int kWgt = kMl + kMaxAttnSplits * kHeads * 2 * 4;  // [S][64 h] merge weights
-static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge tables fit the P buffers");
+// Split-KV exchange payload from a sender to the CTA finishing dims
+// [p D, p D + D): the sender's O for those dims divided by its own sum, bf16,
+// one 128-byte row of 64 heads per dim (16-byte chunk c of row dd stored at
+// chunk c ^ (dd & 7)), then the sender's (max, sum) per head.
+__host__ __device__ constexpr int xchg_bytes(int S) { return (kLatent / S) * 128 + kHeads * 8; }
+constexpr int kSend = kQ;    // outgoing payloads, S - 1 of them, in the Q region
+constexpr int kRecv = kKV;   // incoming payloads: slot s from sender s, in the ring
+static_assert((kMaxAttnSplits - 1) * xchg_bytes(kMaxAttnSplits) <= kP - kQ, "send staging");
+static_assert(xchg_bytes(2) <= kP - kQ, "send staging");
+constexpr int kWgt = kP;     // [S][64 h] merge weights, in the P buffers
+static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge weights fit the P buffers");
 
 struct Misc {
   uint64_t kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
-  uint64_t q_done, ids_ready;
+  uint64_t q_done, ids_ready, xchg;  // xchg: the split-KV payloads received
   uint32_t tmem_base;
   int abort;
   int n_sel;
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     }
     mbar_init(&misc->q_done, 128);  // every loader thread, once its quarter of Q landed
     mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
+    mbar_init(&misc->xchg, 1);       // the receiver's expect-tx arrival + the S - 1 copies
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -162,17 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     s_cnt = min(n_sel, s_begin + h) - s_begin;
   };
   const uint32_t tmem = misc->tmem_base;
-  // Cluster barrier phases of a split-KV CTA, for the warps that do not take
-  // part in the exchange: every thread of the cluster arrives at each.
+  // Cluster barrier phases of a split-KV CTA (every thread of the cluster
+  // arrives at each):
   //   0 (arrived at start-up): every CTA's barriers are initialised;
-  //   1: every CTA's MMAs are done, so its ring and P buffers may be written;
-  //   2: every exchange store has landed.
+  //   1: every CTA's MMAs are done and its payloads are staged, so rings may
+  //      be written and payloads read;
+  //   2: every CTA has received its payloads, so no copy reads or writes a
+  //      CTA's memory any more (waited at exit).
+  // The warps outside the exchange arrive at phase 2 at once.
   auto exchange_phases = [&]() {
     cluster_wait();
     cluster_arrive();
     cluster_wait();
     cluster_arrive();
-    cluster_wait();
   };
 
   const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
@@ -530,13 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       // holds dim 128 m + tid in this thread's lane, so the thread's four dims
       // go to CTAs (128 m + tid) / D (a warp's 32 dims always go to one CTA).
       const int D = kLatent / S;
-      const uint32_t pay = static_cast<uint32_t>(D) * kHeads * 4;  // bytes from one sender
-      float* ml = reinterpret_cast<float*>(gbase + kMl);            // [S][64][2]
-      float* wgt = reinterpret_cast<float*>(gbase + kWgt);          // [S][64]
+      const uint32_t pay = static_cast<uint32_t>(xchg_bytes(S));
       const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
-      cluster_wait();     // phase 0
-      cluster_arrive();   // phase 1: this CTA's MMAs are done (waited above)
-      cluster_wait();
+      auto send_slot = [&](int p) -> uint32_t {  // staging of the payload for CTA p
+        return sbase + kSend + static_cast<uint32_t>(p < split ? p : p - 1) * pay;
+      };
+      cluster_wait();  // phase 0
+      if (warp < 2) misc->inv_l[tid] = l_own > 0.f ? 1.f / l_own : 0.f;
+      named_sync(kMathBar, 128);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         const int d = 128 * m + tid;
@@ -544,42 +550,75 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         if (p == split) continue;
         float v[64];
         load_o(m, v);
-        const uint32_t dst = mapa_shared(sbase + kRecv + split * pay, static_cast<uint32_t>(p)) +
-                             static_cast<uint32_t>(d - p * D) * 16;
+        const int dd = d - p * D;
+        const uint32_t row = send_slot(p) + static_cast<uint32_t>(dd) * 128;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          st_cluster_v4(dst + static_cast<uint32_t>(g * D) * 16, v[4 * g], v[4 * g + 1],
-                        v[4 * g + 2], v[4 * g + 3]);
-        }
-      }
-      if (warp < 2) {
-        const uint32_t off = static_cast<uint32_t>((split * kHeads + tid) * 2) * 4;
-        for (int p = 0; p < S; ++p) {
-          if (p == split) {
-            ml[(split * kHeads + tid) * 2] = m_own;
-            ml[(split * kHeads + tid) * 2 + 1] = l_own;
-          } else {
-            const uint32_t dst = mapa_shared(sbase + kMl + off, static_cast<uint32_t>(p));
-            st_cluster_f32(dst, m_own);
-            st_cluster_f32(dst + 4, l_own);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = 8 * c + 2 * e;
+            const __nv_bfloat162 x =
+                __floats2bfloat162_rn(v[h] * misc->inv_l[h], v[h + 1] * misc->inv_l[h + 1]);
+            w4[e] = *reinterpret_cast<const uint32_t*>(&x);
           }
+          st_shared_v4(row + static_cast<uint32_t>(c ^ (dd & 7)) * 16,
+                       make_uint4(w4[0], w4[1], w4[2], w4[3]));
         }
       }
-      cluster_arrive();   // phase 2: this CTA's stores are out (release)
-      cluster_wait();     // ... and every peer's have landed here (acquire)
-      // out = sum_s w_s O_s with w_s = 2^(m_s - M) / L, M = max_s m_s,
-      // L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0).
       if (warp < 2) {
+        for (int p = 0; p < S; ++p) {
+          if (p == split) continue;
+          float* t = reinterpret_cast<float*>(gbase + (send_slot(p) - sbase) + D * 128);
+          t[2 * tid] = m_own;
+          t[2 * tid + 1] = l_own;
+        }
+      }
+      fence_proxy_async_smem();  // the staged payloads, for the copy engine
+      if (tid == 0) mbar_arrive_expect_tx(&misc->xchg, static_cast<uint32_t>(S - 1) * pay);
+      named_sync(kMathBar, 128);
+      cluster_arrive();  // phase 1
+      cluster_wait();
+      if (tid == 0) {
+        for (int p = 0; p < S; ++p) {
+          if (p == split) continue;
+          bulk_s2cluster(mapa_shared(sbase + kRecv + static_cast<uint32_t>(split) * pay,
+                                     static_cast<uint32_t>(p)),
+                         send_slot(p), pay,
+                         mapa_shared(smem_u32(&misc->xchg), static_cast<uint32_t>(p)));
+        }
+      }
+      if (ok) ok = wait_bar(&misc->xchg, 0u, misc, a.status);
+      cluster_arrive();  // phase 2: this CTA's payloads have all landed
+      // out = sum_s w_s O_s with w_s = 2^(m_s - M) / L, M = max_s m_s,
+      // L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0); a
+      // received O_s comes divided by l_s, so its weight takes l_s back.
+      float* wgt = reinterpret_cast<float*>(gbase + kWgt);  // [S][64]
+      if (warp < 2) {
+        auto ml_of = [&](int q, float& mq, float& lq) {
+          if (q == split) {
+            mq = m_own;
+            lq = l_own;
+          } else {
+            const float* t = reinterpret_cast<const float*>(
+                gbase + kRecv + static_cast<uint32_t>(q) * pay + D * 128);
+            mq = ok ? t[2 * tid] : -INFINITY;
+            lq = ok ? t[2 * tid + 1] : 0.f;
+          }
+        };
         float M = -INFINITY;
         for (int q = 0; q < S; ++q) {
-          if (ml[(q * kHeads + tid) * 2 + 1] > 0.f) M = fmaxf(M, ml[(q * kHeads + tid) * 2]);
+          float mq, lq;
+          ml_of(q, mq, lq);
+          if (lq > 0.f) M = fmaxf(M, mq);
         }
         float L = 0.f;
         for (int q = 0; q < S; ++q) {
-          const float lq = ml[(q * kHeads + tid) * 2 + 1];
-          const float eq = lq > 0.f ? exp2f(ml[(q * kHeads + tid) * 2] - M) : 0.f;
-          wgt[q * kHeads + tid] = eq;
+          float mq, lq;
+          ml_of(q, mq, lq);
+          const float eq = lq > 0.f ? exp2f(mq - M) : 0.f;
           L = fmaf(eq, lq, L);
+          wgt[q * kHeads + tid] = q == split ? eq : eq * lq;
         }
         const float inv_L = L > 0.f ? 1.f / L : 0.f;
         for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
@@ -589,7 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
       }
       named_sync(kMathBar, 128);
-      uint16_t* part_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][D]
+      // bf16 [64 h][D] in the ring past the receive slots (the staged
+      // payloads may still be read by the partners' copies until phase 2).
+      const uint32_t part_off = kRecv + static_cast<uint32_t>(S) * pay;
+      uint16_t* part_o = reinterpret_cast<uint16_t*>(gbase + part_off);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         const int d = 128 * m + tid;
@@ -600,16 +642,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 #pragma unroll
         for (int h = 0; h < kHeads; ++h) v[h] *= wgt[split * kHeads + h];
         for (int q = 0; q < S; ++q) {
-          if (q == split) continue;
-          const float4* rq =
-              reinterpret_cast<const float4*>(gbase + kRecv + static_cast<uint32_t>(q) * pay);
+          if (q == split || !ok) continue;
+          const uint32_t row = sbase + kRecv + static_cast<uint32_t>(q) * pay +
+                               static_cast<uint32_t>(dd) * 128;
 #pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            const float4 x = rq[g * D + dd];
-            v[4 * g] = fmaf(wgt[q * kHeads + 4 * g], x.x, v[4 * g]);
-            v[4 * g + 1] = fmaf(wgt[q * kHeads + 4 * g + 1], x.y, v[4 * g + 1]);
-            v[4 * g + 2] = fmaf(wgt[q * kHeads + 4 * g + 2], x.z, v[4 * g + 2]);
-            v[4 * g + 3] = fmaf(wgt[q * kHeads + 4 * g + 3], x.w, v[4 * g + 3]);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = ld_shared_v4(row + static_cast<uint32_t>(c ^ (dd & 7)) * 16);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = 8 * c + 2 * e;
+              v[h] = fmaf(wgt[q * kHeads + h], bf16_bits_to_float(xs[e] & 0xFFFF), v[h]);
+              v[h + 1] = fmaf(wgt[q * kHeads + h + 1], bf16_bits_to_float(xs[e] >> 16), v[h + 1]);
+            }
           }
         }
 #pragma unroll
@@ -622,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       const int per_row = D / 8;
       for (int i = tid; i < kHeads * per_row; i += 128) {
         const int hh = i / per_row, ch = i - hh * per_row;
-        const uint4 v = *reinterpret_cast<const uint4*>(gbase + kQ + hh * 2 * D + ch * 16);
+        const uint4 v = *reinterpret_cast<const uint4*>(gbase + part_off + hh * 2 * D + ch * 16);
         *reinterpret_cast<uint4*>(out + hh * kLatent + D * split + ch * 8) = v;
       }
     }
@@ -634,8 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // (No remote access follows phase 2 of the exchange, so a CTA may leave
-  // while its peers still merge.)
+  if (paired) cluster_wait();  // phase 2: no copy touches this CTA any more
 }
 
 }  // namespace
