@@ -158,6 +158,12 @@ int32_t* select_tmp(void* workspace, const Layout& L) {
                           : nullptr;
 }
 
+// Prefill with bf16 keys runs its indexer stages batched over queries (one
+// shared key array, sixteen queries per MMA) when the array has rows.
+bool prefill_batched(const dsa_keys_t& k, int prefill, int64_t rows) {
+  return prefill && k.fmt == DSA_FMT_BF16 && rows > 0;
+}
+
 // Launch sequences shared by the public calls. `sel_tmp`: scratch of
 // 32768 ids per query for two-pass selections (may be null).
 dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
@@ -166,24 +172,40 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s, int prefill,
                              int64_t ctx, const dsa_keys_t* partial_keys) {
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
-  ScanArgs sa{};
-  sa.fmt = pooled.fmt;
-  sa.key_data = pooled.data;
-  sa.key_scales = pooled.scales;
-  sa.key_stride = prefill ? 0 : pooled.seq_stride_rows;
-  sa.q_idx = q_idx;
-  sa.w = w;
-  sa.n_latents = n_lat;
-  sa.max_latents = max_latents;
-  sa.mode = ROWS_BLOCKS;
-  sa.n_rows = nb_max;
-  sa.scores = scores;
-  sa.B = B;
-  sa.prefill = prefill;
-  sa.ctx = ctx;
-  sa.ratio = c.ratio;
-  sa.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
+  if (prefill_batched(pooled, prefill, max_latents / kBlock)) {
+    BatchedScanArgs ba{};
+    ba.key_data = static_cast<const uint16_t*>(pooled.data);
+    ba.key_rows = max_latents / kBlock;  // complete blocks
+    ba.q_idx = q_idx;
+    ba.w = w;
+    ba.n_q = B;
+    ba.ctx = ctx;
+    ba.ratio = c.ratio;
+    ba.mode = ROWS_BLOCKS;
+    ba.scores = scores;
+    ba.n_cols = nb_max;
+    ba.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan_batched(ba, device_sm_count(), s); }));
+  } else {
+    ScanArgs sa{};
+    sa.fmt = pooled.fmt;
+    sa.key_data = pooled.data;
+    sa.key_scales = pooled.scales;
+    sa.key_stride = prefill ? 0 : pooled.seq_stride_rows;
+    sa.q_idx = q_idx;
+    sa.w = w;
+    sa.n_latents = n_lat;
+    sa.max_latents = max_latents;
+    sa.mode = ROWS_BLOCKS;
+    sa.n_rows = nb_max;
+    sa.scores = scores;
+    sa.B = B;
+    sa.prefill = prefill;
+    sa.ctx = ctx;
+    sa.ratio = c.ratio;
+    sa.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
+  }
   if (prefill) {
     PartialArgs pa{};
     pa.fmt = pooled.fmt;
@@ -215,34 +237,55 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              const int32_t* n_lat, int B, int64_t max_latents, int32_t* token_ids,
                              float* scores, DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s,
                              int prefill, int64_t ctx) {
-  ScanArgs sa{};
-  sa.fmt = keys.fmt;
-  sa.key_data = keys.data;
-  sa.key_scales = keys.scales;
-  sa.key_stride = prefill ? 0 : keys.seq_stride_rows;
-  sa.q_idx = q_idx;
-  sa.w = w;
-  sa.n_latents = n_lat;
-  sa.max_latents = max_latents;
-  if (block_ids) {
-    sa.mode = ROWS_GATHER;
-    sa.block_ids = block_ids;
-    sa.k_blocks = c.k_blocks;
-    sa.n_rows = static_cast<int64_t>(c.k_blocks) * kBlock;
-  } else {
-    sa.mode = ROWS_LATENTS;
-    sa.n_rows = (max_latents + 7) / 8 * 8;
-  }
-  sa.scores = scores;
-  sa.B = B;
-  sa.prefill = prefill;
-  sa.ctx = ctx;
-  sa.ratio = c.ratio;
-  sa.status = st;
-  DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
   SelectArgs se{};
-  se.scores = scores;
-  se.n = sa.n_rows;
+  if (block_ids && prefill_batched(keys, prefill, max_latents)) {
+    // Dense token scores over every latent, read by the selection through
+    // the block ids.
+    BatchedScanArgs ba{};
+    ba.key_data = static_cast<const uint16_t*>(keys.data);
+    ba.key_rows = max_latents;
+    ba.q_idx = q_idx;
+    ba.w = w;
+    ba.n_q = B;
+    ba.ctx = ctx;
+    ba.ratio = c.ratio;
+    ba.mode = ROWS_LATENTS;
+    ba.scores = scores;
+    ba.n_cols = (max_latents + 7) / 8 * 8;
+    ba.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan_batched(ba, device_sm_count(), s); }));
+    se.scores = scores;
+    se.n = static_cast<int64_t>(c.k_blocks) * kBlock;
+    se.dense_stride = ba.n_cols;
+  } else {
+    ScanArgs sa{};
+    sa.fmt = keys.fmt;
+    sa.key_data = keys.data;
+    sa.key_scales = keys.scales;
+    sa.key_stride = prefill ? 0 : keys.seq_stride_rows;
+    sa.q_idx = q_idx;
+    sa.w = w;
+    sa.n_latents = n_lat;
+    sa.max_latents = max_latents;
+    if (block_ids) {
+      sa.mode = ROWS_GATHER;
+      sa.block_ids = block_ids;
+      sa.k_blocks = c.k_blocks;
+      sa.n_rows = static_cast<int64_t>(c.k_blocks) * kBlock;
+    } else {
+      sa.mode = ROWS_LATENTS;
+      sa.n_rows = (max_latents + 7) / 8 * 8;
+    }
+    sa.scores = scores;
+    sa.B = B;
+    sa.prefill = prefill;
+    sa.ctx = ctx;
+    sa.ratio = c.ratio;
+    sa.status = st;
+    DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
+    se.scores = scores;
+    se.n = sa.n_rows;
+  }
   se.k = c.k_tokens;
   se.B = B;
   se.block_ids = block_ids;

@@ -73,6 +73,28 @@ struct ScanArgs {
 // partially visible last block is left at -inf for launch_prefill_partial.
 cudaError_t launch_scan(const ScanArgs& a, int num_sms, cudaStream_t s);
 
+// Prefill indexer scores of n_q queries (positions ctx .. ctx + n_q - 1) over
+// one shared bf16 key array, sixteen queries per MMA. mode ROWS_BLOCKS: rows
+// are complete pooled blocks, query q sees ((ctx + q + 1) / ratio) / 8 of
+// them, and every column of its score row is written (-inf where unseen).
+// mode ROWS_LATENTS: rows are latents, query q sees (ctx + q + 1) / ratio,
+// and columns are written up to the end of the last block any query of its
+// group of sixteen can see.
+struct BatchedScanArgs {
+  const uint16_t* key_data;  // bf16 [key_rows][128]
+  int64_t key_rows;
+  const uint16_t* q_idx;     // bf16 [n_q][16][128]
+  const float* w;            // [n_q][16]
+  int64_t n_q;
+  int64_t ctx;
+  int ratio;
+  int mode;
+  float* scores;             // [n_q][n_cols]
+  int64_t n_cols;
+  DeviceStatus* status;
+};
+cudaError_t launch_scan_batched(const BatchedScanArgs& a, int num_sms, cudaStream_t s);
+
 // Prefill: for each query whose last visible block is incomplete, pool that
 // block over its visible members (fp32 sum in order, / count, rounded to the
 // key format), score it against the query's index heads and store the score
@@ -118,6 +140,9 @@ struct SelectArgs {
   int64_t chunk;           //         candidates [c * chunk, (c + 1) * chunk)
   const int32_t* in_ids;   // pass 2: candidate i of query b is id in_ids[b * n_in + i]
   int64_t n_in;
+  // Non-zero (with block_ids): scores are dense rows over every token,
+  // scores[b * dense_stride + t]; candidate i is token 8 * block_ids[i / 8] + i % 8.
+  int64_t dense_stride;
 };
 // Returns the number of kernels launched in `launches` (1, or 2 for a
 // two-pass selection).

@@ -381,11 +381,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         }
       }
     }
+    if (a.dense_stride) __syncthreads();  // the keys below are read through the block ids
   }
   sh.taken[tid] = 0u;
   uint32_t key[KPT];
   const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
-  if (ids_in) {
+  if (a.dense_stride && a.block_ids) {
+    const float* row = a.scores + static_cast<int64_t>(b) * a.dense_stride;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t i = wbase + 32 * j;
+      const int blk = i < n ? bids[i >> 3] : -1;
+      key[j] = score_key(blk >= 0 ? row[static_cast<int64_t>(blk) * 8 + (i & 7)] : -INFINITY);
+    }
+  } else if (ids_in) {
     // Second pass: the kept ids ascend along the list (chunks in order, each
     // ascending, -1 padded), so list order is id order for the tie rule.
     // (The key registers hold the ids first: no second array.)
@@ -689,6 +698,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
   if (a.B == 0) return cudaSuccess;
   if (launches) *launches = 1;
   if (a.n <= kRegMax) return launch_reg_for(a, a.n, a.B, s);
+  if (a.dense_stride) return cudaErrorInvalidValue;  // dense rows: register-resident kernel only
   // Two passes over C chunks: every query's best k lies within the best k of
   // its own chunk (same order, same ids), so the second pass over the C * k
   // kept ids finds exactly the plain selection.
