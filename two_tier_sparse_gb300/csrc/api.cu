@@ -98,10 +98,12 @@ T* at(void* ws, size_t off) {
 
 dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
-// Split-KV setup of an attention launch over n queries: the most CTAs per
-// query (8, 4 or 2) that still fit the SMs in one wave, else one.
+// Launch shape of an attention call over n queries: split-KV over the most
+// CTAs per query (8, 4 or 2) that still fit the SMs in one wave, else one;
+// 64-row tiles for prefill chunks, 32-row tiles for decode.
 void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
   (void)c;
+  a.tile_rows = a.prefill ? 64 : 32;
   const int sms = device_sm_count();
   a.splits = 1;
   for (int sp = kMaxAttnSplits; sp >= 2; sp /= 2) {

@@ -39,10 +39,10 @@ namespace dsa {
 
 namespace {
 
-constexpr int kRows = 32;           // KV rows per tile
-constexpr int kSlots = 4;           // ring slots
 constexpr int kLoadWarp0 = 4;
-constexpr int kMmaWarp = kLoadWarp0 + kSlots;  // 8: QK^T issuer (and TMEM owner)
+constexpr int kLoadWarps = 4;
+constexpr int kMaxSlots = 4;
+constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;  // 8: QK^T issuer (and TMEM owner)
 constexpr int kPvWarp = kMmaWarp + 1;          // 9: PV issuer
 constexpr int kThreads = 32 * (kPvWarp + 1);   // 320
 constexpr int kMathBar = 1;         // named barrier of the 128 math threads
@@ -51,12 +51,22 @@ constexpr int kMathBar = 1;         // named barrier of the 128 math threads
 // 64 rows past each Q atom (they only feed unused accumulator lanes); past
 // the last atom they land in the P buffers, which is harmless.
 constexpr int kQ = 0;                              // 8 atoms x 64 heads x 128 B; output staging
-constexpr int kP = kQ + 8 * kHeads * 128;          // 2 x (64 heads x 128 B; 32 rows bf16 used)
+constexpr int kP = kQ + 8 * kHeads * 128;          // 2 x (64 heads x 128 B: up to 64 rows bf16)
 constexpr int kPBytes = kHeads * 128;
-constexpr int kKV = kP + 2 * kPBytes;              // 4 slots x 8 atoms x 32 rows x 128 B
-constexpr int kAtomBytes = kRows * 128;            // 4 KB: one slot's rows of one 64-dim atom
-constexpr int kSlotBytes = 8 * kAtomBytes;         // 32 KB
-constexpr int kIds = kKV + kSlots * kSlotBytes;    // compacted latent ids
+constexpr int kKV = kP + 2 * kPBytes;              // the ring: 128 KB of tiles
+constexpr int kKVBytes = 128 * 1024;
+constexpr int kIds = kKV + kKVBytes;               // compacted latent ids
+
+// Tiles of ROWS rows (32 or 64): 128 / ROWS ring slots of 8 atoms (64 dims x
+// ROWS rows x 128 B each); each loader warp fills 32 rows of its slot's tiles.
+template <int ROWS>
+struct TileShape {
+  static_assert(ROWS == 32 || ROWS == 64, "tile rows");
+  static constexpr int kSlots = kKVBytes / (ROWS * 1024);
+  static constexpr int kAtomBytes = ROWS * 128;
+  static constexpr int kSlotBytes = 8 * kAtomBytes;
+  static constexpr int kWarpsPerSlot = kLoadWarps / kSlots;
+};
 constexpr int kMisc = kIds + kMaxKTokens * 4;
 constexpr int kMiscBytes = 2048;
 constexpr int kSmemBytes = kMisc + kMiscBytes + 1024;  // + alignment slack of the base
@@ -76,7 +86,7 @@ constexpr int kWgt = kP;     // [S][64 h] merge weights, in the P buffers
 static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge weights fit the P buffers");
 
 struct Misc {
-  uint64_t kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
+  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
   uint64_t q_done, ids_ready, xchg;  // xchg: the split-KV payloads received
   uint32_t tmem_base;
   int abort;
@@ -92,7 +102,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
   return mbar_wait_abortable(bar, parity, &m->abort, st, SITE_ATTN);
 }
 
+template <int ROWS>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
+  using TS = TileShape<ROWS>;
+  constexpr int kRows = ROWS;
+  constexpr int kSlots = TS::kSlots;
+  constexpr int kAtomBytes = TS::kAtomBytes;
+  constexpr int kSlotBytes = TS::kSlotBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -107,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&misc->kv_full[i], 32);  // arrivals of the slot's loader warp
+      mbar_init(&misc->kv_full[i], 32 * TS::kWarpsPerSlot);  // the slot's loader threads
       mbar_init(&misc->kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -240,14 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
     // ---------------- loaders ----------------
-    // Warp 4 + w fills slot w with tiles w, w + 4, ...: it waits for its own
-    // copies of a tile, fences them into the async proxy (the tensor core's
-    // view) and then arrives, while the other slots' tiles are in flight.
-    // Tiles made only of window rows need no ids.
+    // Warp 4 + w fills 32 rows (part w / kSlots) of slot w % kSlots's tiles
+    // (tiles sl, sl + kSlots, ...): it waits for its own copies of a tile,
+    // fences them into the async proxy (the tensor core's view) and then
+    // arrives, while the other slots' tiles are in flight. Tiles made only of
+    // window rows need no ids.
     const int w = warp - kLoadWarp0;
+    const int sl = w % kSlots, part = w / kSlots;
     bool q_reported = false, have_ids = false;
     int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
-    for (int t = w;; t += kSlots) {
+    for (int t = sl;; t += kSlots) {
       const int g0 = t * kRows;
       if (!have_ids && g0 + kRows > w_cnt) {
         if (!wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
@@ -261,15 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       }
       if (have_ids && t >= n_tiles) break;
       if (t >= kSlots &&
-          !wait_bar(&misc->kv_empty[w], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
+          !wait_bar(&misc->kv_empty[sl], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
         break;
       }
-      const uint32_t dstb = sbase + kKV + w * kSlotBytes;
+      const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
 #pragma unroll 8
-      for (int j = 0; j < kRows * 64 / 32; ++j) {
+      for (int j = 0; j < 64; ++j) {  // 32 rows x 64 chunks of 16 B
         const int c = lane + 32 * j;
-        const int row = c >> 6, cr = c & 63;
+        const int row = 32 * part + (c >> 6), cr = c & 63;
         const int g = g0 + row;
         const uint32_t dst = dstb + (cr >> 3) * kAtomBytes + sw128_off(row, cr & 7);
         if (g < n_rows_cta) {
@@ -290,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       }
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      mbar_arrive(&misc->kv_full[w]);
+      mbar_arrive(&misc->kv_full[sl]);
     }
     if (!q_reported) {
       cp_async_wait<0>();
@@ -689,10 +707,19 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) {
     return cudaErrorInvalidValue;
   }
+  if (a.tile_rows == 64) {
+    static int smem_set[64] = {0};
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
+                      a.splits, a);
+  }
+  if (a.tile_rows != 32) return cudaErrorInvalidValue;
   static int smem_set[64] = {0};
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel), kSmemBytes, smem_set);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_kernel, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s, a.splits, a);
+  return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
+                    a.splits, a);
 }
 
 }  // namespace dsa

@@ -171,6 +171,9 @@ struct AttnArgs {
   // selected latents are each cut in S parts handled by the S CTAs of a
   // cluster (merged on chip); 1: one CTA per query.
   int splits;
+  // KV rows per tile: 32 (four ring slots) or 64 (two ring slots; half the
+  // QK^T instructions per row).
+  int tile_rows;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
