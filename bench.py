@@ -462,6 +462,8 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
     one sequence (cache build, i.e. the pooled keys, outside the step)."""
     import torch
     n_q, ctx, ratio, fmt = spec["n_q"], spec["ctx"], spec["ratio"], spec["key_fmt"]
+    if args.batch:
+        n_q = args.batch  # a smaller chunk (profiling); the line then names it in config
     t0 = time.time()
     pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, spec["seed"] + 1000 * rank)
     gen_s = time.time() - t0
