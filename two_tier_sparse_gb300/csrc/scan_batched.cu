@@ -232,19 +232,34 @@ __device__ void epilogue(const BatchedScanArgs& a, Shared& sh, int64_t i0, int64
     const int r = it.t * kTile + row;
     const bool in_cols = r < a.n_cols;
     float* out = a.scores + (static_cast<int64_t>(it.g) * kGroup + 8 * half) * a.n_cols + r;
+    // Two tensor-memory loads of four queries' 64 columns each (one wait per
+    // load), then the ReLU-weighted head sums in head order.
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int qj = 8 * half + j;  // query within the group
-      float v[16];
-      tmem_ld16(tmem + lane_base + static_cast<uint32_t>(slot * kN + 16 * qj), v);
-      if (vis[j] >= 0 && in_cols) {
-        float sc = -INFINITY;
-        if (r < vis[j]) {
-          sc = 0.f;
+    for (int jj = 0; jj < 2; ++jj) {
+      float v[64];
+      tmem_ld64(tmem + lane_base + static_cast<uint32_t>(slot * kN + 16 * (8 * half + 4 * jj)), v);
 #pragma unroll
-          for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(sh.w[qj * kIdxHeads + h], fmaxf(v[h], 0.f), sc);
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * jj + k;
+        const int qj = 8 * half + j;  // query within the group
+        if (vis[j] >= 0 && in_cols) {
+          float sc = -INFINITY;
+          if (r < vis[j]) {
+            sc = 0.f;
+            const float4* w4 = reinterpret_cast<const float4*>(sh.w + qj * kIdxHeads);
+#pragma unroll
+            for (int h4 = 0; h4 < kIdxHeads / 4; ++h4) {
+              const float4 ww = w4[h4];
+              sc = fmaf(ww.x, fmaxf(v[16 * k + 4 * h4], 0.f), sc);
+              sc = fmaf(ww.y, fmaxf(v[16 * k + 4 * h4 + 1], 0.f), sc);
+              sc = fmaf(ww.z, fmaxf(v[16 * k + 4 * h4 + 2], 0.f), sc);
+              sc = fmaf(ww.w, fmaxf(v[16 * k + 4 * h4 + 3], 0.f), sc);
+            }
+          }
+          // Streaming store (evict first): the score rows must not push the
+          // shared key array, re-read by every group, out of L2.
+          __stcs(out + j * a.n_cols, sc);
         }
-        out[j * a.n_cols] = sc;
       }
     }
     tc_fence_before();
