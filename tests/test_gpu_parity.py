@@ -252,17 +252,26 @@ def test_decode_step(T, ratio, fmt, k_blocks, q_scale, sm):
     check_step(inp, cfg, outs, range(inp.B))
 
 
-def test_decode_step_is_deterministic_and_updates_the_pool():
-    inp = synth.decode_inputs([30000, 17], 1, "mxfp8", seed=29)
-    cfg = dsa.config(k_blocks=256)
+@pytest.mark.parametrize("fmt,k_blocks", [("mxfp8", 256), ("bf16", 256), ("mxfp8", 4096)])
+def test_decode_step_is_deterministic_and_updates_the_pool(fmt, k_blocks):
+    """The step's pooling of each sequence's newest block restores it bit for
+    bit (codes and MXFP8 scales), with a block stage (k_blocks 256) and
+    without one (k_blocks 4096)."""
+    inp = synth.decode_inputs([30000, 17], 1, fmt, seed=29)
+    cfg = dsa.config(k_blocks=k_blocks)
     d = DecodeOnDevice(inp, cfg)
     d.pool()
     ref_pool = d.pooled.data.clone()
+    ref_scales = None if d.pooled.scales is None else d.pooled.scales.clone()
     # clobber each sequence's newest block, then let the step rebuild it
     for b, n in enumerate(inp.n_latents):
         d.pooled.data[b, (int(n) - 1) // 8] = 0
+        if d.pooled.scales is not None:
+            d.pooled.scales[b, (int(n) - 1) // 8] = 0
     a = run_step(d, cfg, update_pool=True)
     assert torch.equal(d.pooled.data, ref_pool)
+    if ref_scales is not None:
+        assert torch.equal(d.pooled.scales, ref_scales)
     b_ = run_step(d, cfg, update_pool=True)
     for x, y in zip(a, b_):
         assert torch.equal(x, y)
