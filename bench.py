@@ -79,6 +79,30 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank runs its own batch (weak scaling, no collective on the data
+    path): its inputs come from its own seed."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(values, device):
+    """Element-wise maximum of per-rank values over all ranks (the slowest
+    rank's time sets the job's); the values unchanged for a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's units per step over the slowest
+    rank's step time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -233,7 +257,7 @@ def run_ours(args):
         B = args.batch
     # Every rank decodes its own batch: seeds differ per rank.
     t0 = time.time()
-    inp = synth.decode_inputs([T] * B, ratio, fmt, spec["seed"] + 1000 * rank)
+    inp = synth.decode_inputs([T] * B, ratio, fmt, shard_seed(spec["seed"], rank))
     gen_s = time.time() - t0
     cfg = dsa.config(ratio=ratio)
     cap = inp.cap
@@ -303,12 +327,9 @@ def run_ours(args):
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
     total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max([total_ms], dev)[0]
     ms_per_step = total_ms / K
-    value = world * B / (ms_per_step * 1e-3)
+    value = job_rate(B, world, ms_per_step)
 
     # Second timed pass, same steps, with CUDA events around every launch of the
     # library on the launching stream: the per-kernel breakdown and the scan's
@@ -451,10 +472,7 @@ def run_ours(args):
 
     run_pipelined(3)
     e2e_pipe_ms = run_pipelined(K)
-    if world > 1:
-        t = torch.tensor([e2e_ms, e2e_pipe_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms, e2e_pipe_ms = float(t[0].item()), float(t[1].item())
+    e2e_ms, e2e_pipe_ms = reduce_max([e2e_ms, e2e_pipe_ms], dev)
     h2d = in_n   # bytes of the one input copy (q, q_idx, w, each padded to 256 B)
     d2h = out_n  # bytes of the one result copy (out, lse)
     code, info = dsa.read_device_status(ws)
@@ -492,13 +510,13 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": scan_avg_ms, "launches_per_step": launches_per_step},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * B / (e2e_pipe_ms * 1e-3), "unit": "queries/s",
+        "e2e": {"value": job_rate(B, world, e2e_pipe_ms), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_pipe_ms,
                 "mode": "pipelined: each step's input copy and result copy overlap the "
                         "neighbouring steps' compute; one timed region over the steps, "
                         "no L2 flush inside it",
-                "serial": {"value": world * B / (e2e_ms * 1e-3), "ms_per_step": e2e_ms,
+                "serial": {"value": job_rate(B, world, e2e_ms), "ms_per_step": e2e_ms,
                            "mode": "copy in, step, copy out; L2 flushed before each step"}},
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
         "kernel_ms_per_step": kernel_ms,
@@ -535,7 +553,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
     if args.batch:
         n_q = args.batch  # a smaller chunk (profiling); the line then names it in config
     t0 = time.time()
-    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, spec["seed"] + 1000 * rank)
+    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, shard_seed(spec["seed"], rank))
     gen_s = time.time() - t0
     cfg = dsa.config(ratio=ratio)
     n_lat = (ctx + n_q) // ratio
@@ -589,8 +607,10 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
             ev_e[i].record()
         torch.cuda.synchronize()
     counts = dsa.launch_counts(reset=True)
+    if world > 1:
+        torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(ev_s, ev_e)]
-    ms = float(np.mean(step_ms))
+    ms = reduce_max([float(np.mean(step_ms))], dev)[0]
     # per-kernel breakdown (second pass with events around each launch)
     kinds = {"pool": 1, "scan": 2, "select": 2, "attn": 1, "other": 1}
     kev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n * K)],
@@ -617,7 +637,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
         line = {
             "metric": "sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
                       "TFLOP/s vs roofline",
-            "value": n_q / (ms * 1e-3), "unit": "queries/s", "n_gpus": world, "steps": K,
+            "value": job_rate(n_q, world, ms), "unit": "queries/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "n_q": n_q, "ctx": ctx, "ratio": ratio,
@@ -635,6 +655,8 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
 
 def main():
