@@ -298,11 +298,22 @@ dsa_status_t dsa_launch_counts(uint64_t* counts, int reset);
  * DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (the earliest recorded).
  * If info is not NULL it receives the recorded detail word (0 if none): bits
  * 24..31 name the kernel (1 block-key pooling, 2 indexer scan, 3 top-k
- * selection, 4 attention, 5 prefill partial block), bits 0..23 a detail (for
+ * selection, 4 attention, 5 prefill partial block, 6 the self-test below),
+ * bits 0..23 a detail (for
  * DSA_ERR_TIMEOUT the shared-memory address of the barrier waited on; for
  * DSA_ERR_DEVICE_CHECK the offending sequence index or id).
  */
 dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* info);
+
+/*
+ * Self-test of the device failure report (no counterpart on the pages): a
+ * kernel waits on a barrier that nothing arrives at, under the bounded-wait
+ * scheme the step's kernels use but with a limit of about one millisecond,
+ * gives up and records DSA_ERR_TIMEOUT in `workspace`'s status word. A
+ * following dsa_read_device_status returns DSA_ERR_TIMEOUT with site 6; the
+ * device stays usable. Returns DSA_ERR_INVALID_ARG without a workspace.
+ */
+dsa_status_t dsa_selftest_timeout(void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 
 #ifdef __cplusplus
 }

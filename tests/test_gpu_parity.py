@@ -470,3 +470,28 @@ def test_select_thousands_of_candidates(T, fmt, k_blocks, outliers):
         r = O.decode_sequence(oc, inp, b, with_attention=False, block_ids=bids_h[b])
         pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
         check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
+
+
+# ---------------------------------------------------------------------------
+# Failure report: a bounded device wait that runs out
+# ---------------------------------------------------------------------------
+
+
+def test_bounded_wait_reports_a_timeout_and_the_device_stays_usable():
+    """A wait that nothing satisfies gives up after its limit (~1 ms here) and
+    records DSA_ERR_TIMEOUT (site 6); the status is read and cleared on the
+    host and the next step runs normally."""
+    inp = synth.decode_inputs([300, 40], 1, "bf16", seed=31)
+    cfg = dsa.config(k_blocks=16, k_tokens=64)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    dsa.selftest_timeout(d.ws)
+    code, info = d.status()
+    assert code == 7, (code, hex(info))
+    assert info >> 24 == 6
+    assert d.status()[0] == 0  # read and cleared
+    outs = run_step(d, cfg, update_pool=True)
+    assert d.status()[0] == 0
+    assert np.isfinite(outs[1].cpu().numpy()).all()
+    check_step(inp, cfg, outs, [0, 1])
+

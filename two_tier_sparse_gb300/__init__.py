@@ -31,7 +31,8 @@ STATUS = {
 EXPORTS = ("dsa_default_config", "dsa_status_string", "dsa_workspace_size",
            "dsa_pool_index_keys", "dsa_index_blocks", "dsa_topk", "dsa_sparse_attn_decode",
            "dsa_decode_step", "dsa_sparse_attn_prefill", "dsa_read_device_status",
-           "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc")
+           "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc",
+           "dsa_selftest_timeout")
 
 TOPK_NOALLOC_MAX_SCORES = 1 << 21
 
@@ -90,6 +91,7 @@ def load() -> ctypes.CDLL:
         lib.dsa_profile_events.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32]
         lib.dsa_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
         lib.dsa_topk_noalloc.argtypes = [cp, vp, vp, kp, vp, vp, i32, i64, vp, vp]
+        lib.dsa_selftest_timeout.argtypes = [vp, sz, vp]
         for f in EXPORTS:
             if f not in ("dsa_default_config", "dsa_status_string"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -220,6 +222,14 @@ def read_device_status(ws, stream=None):
     info = ctypes.c_uint32(0)
     code = load().dsa_read_device_status(_p(ws), _stream(stream), ctypes.byref(info))
     return int(code), int(info.value)
+
+
+def selftest_timeout(ws, stream=None) -> None:
+    """Launches the failure-report self-test: a wait that nothing satisfies
+    runs out (about 1 ms) and records DSA_ERR_TIMEOUT in ws's status word (read
+    it with read_device_status)."""
+    _check(load().dsa_selftest_timeout(_p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "dsa_selftest_timeout")
 
 
 def profile_events(kind: str, starts, ends) -> None:

@@ -686,6 +686,17 @@ dsa_status_t dsa_launch_counts(uint64_t* counts, int reset) {
   return DSA_OK;
 }
 
+dsa_status_t dsa_selftest_timeout(void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  if (workspace == nullptr || workspace_bytes < sizeof(DeviceStatus)) return DSA_ERR_INVALID_ARG;
+  // about 1 ms at the GB300's 2.07 GHz maximum SM clock
+  constexpr long long kLimitCycles = 2000000;
+  DSA_CUDA(launch(DSA_KERNEL_OTHER, static_cast<cudaStream_t>(stream), [&](int*) {
+    return launch_timeout_selftest(static_cast<DeviceStatus*>(workspace), kLimitCycles,
+                                   static_cast<cudaStream_t>(stream));
+  }));
+  return DSA_OK;
+}
+
 dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* info) {
   if (workspace == nullptr) return DSA_ERR_INVALID_ARG;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -31,6 +31,7 @@ enum : uint32_t {
   SITE_SELECT = 3,
   SITE_ATTN = 4,
   SITE_PREFILL = 5,
+  SITE_SELFTEST = 6,
 };
 
 __device__ __forceinline__ void record_status(DeviceStatus* st, uint32_t code, uint32_t site,

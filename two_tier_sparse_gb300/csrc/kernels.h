@@ -187,6 +187,10 @@ cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks
 
 int device_sm_count();
 
+// One CTA waits, bounded by limit_cycles, on a barrier that nothing arrives
+// at, and records DSA_ERR_TIMEOUT (site SITE_SELFTEST) in `st`.
+cudaError_t launch_timeout_selftest(DeviceStatus* st, long long limit_cycles, cudaStream_t s);
+
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device): `cache` is the caller's per-kernel array.
 inline cudaError_t ensure_smem(const void* kernel, int bytes, int (&cache)[64]) {
