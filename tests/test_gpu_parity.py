@@ -278,6 +278,59 @@ def test_decode_step_is_deterministic_and_updates_the_pool(fmt, k_blocks):
     assert d.status()[0] == 0
 
 
+@pytest.mark.parametrize("fmt,k_blocks", [("mxfp8", 256), ("bf16", 2048)])
+def test_decode_step_replays_from_a_cuda_graph(fmt, k_blocks):
+    """The whole step captured once in a CUDA graph, programmatic launch edges
+    included, replays to the same bits as direct launches. A replay after new
+    queries are copied into the same buffers follows them, and it agrees with
+    the oracle."""
+    import dataclasses
+    inp = synth.decode_inputs([30000, 9001, 17], 1, fmt, seed=33)
+    cfg = dsa.config(k_blocks=k_blocks)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    B = inp.B
+    outs = (torch.empty((B, 64, 512), dtype=torch.int16, device="cuda"),
+            torch.empty((B, 64), dtype=torch.float32, device="cuda"),
+            torch.empty((B, cfg.k_blocks), dtype=torch.int32, device="cuda"),
+            torch.empty((B, cfg.k_tokens), dtype=torch.int32, device="cuda"))
+
+    def step():
+        dsa.decode_step(cfg, d.q, d.q_idx, d.w, d.keys, d.pooled, d.latents, d.n_lat, d.cap,
+                        d.swa, d.swa_len, outs[0], d.ws, lse=outs[1], block_ids=outs[2],
+                        token_ids=outs[3], update_pool=True)
+
+    step()  # first use sets the kernels' shared-memory attributes, outside the capture
+    torch.cuda.synchronize()
+    direct = [x.clone() for x in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for x in outs:
+        x.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert d.status()[0] == 0
+    for x, y in zip(outs, direct):
+        assert torch.equal(x, y)
+    # new queries in the same buffers: the replay reads them
+    inp2 = synth.decode_inputs([30000, 9001, 17], 1, fmt, seed=34)
+    d.q.copy_(dev(inp2.q))
+    d.q_idx.copy_(dev(inp2.q_idx))
+    d.w.copy_(dev(inp2.w))
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = [x.clone() for x in outs]
+    assert not torch.equal(replayed[0], direct[0])
+    step()
+    torch.cuda.synchronize()
+    for x, y in zip(outs, replayed):
+        assert torch.equal(x, y)
+    assert d.status()[0] == 0
+    check_step(dataclasses.replace(inp, q=inp2.q, q_idx=inp2.q_idx, w=inp2.w), cfg, replayed,
+               [0, 2])
+
+
 def test_decode_32_sequences_of_32768_tokens():
     """Decode, batch 32, 32768 tokens at ratio 2 (16384 latents, 2048 blocks, all kept)."""
     inp = synth.workload_inputs("decode_b32_t32768_r2_bf16")
