@@ -115,6 +115,16 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def sustained_bf16_peak():
+    """The bf16 GEMM rate measured over seconds under the power cap (for a
+    kernel timed inside a long step), or None when it was not measured."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------------------
 # Clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -587,6 +597,35 @@ def prefill_flops(n_q: int, ctx: int, ratio: int, k_blocks: int = 2048, k_tokens
     return total
 
 
+def prefill_executed_flops(n_q: int, ctx: int, ratio: int, k_blocks: int = 2048,
+                           k_tokens: int = 512, window: int = 128) -> float:
+    """Flops the tensor cores execute for a prefill chunk, padding included.
+
+    The batched scans run one M=128 x N=256 x K=128 MMA per 128-row tile for
+    each group of 16 queries. The block stage covers every complete block of
+    the chunk's context; the token stage covers the visible latents of the
+    group's last query, rounded up to whole blocks. Attention runs 64-row
+    tiles: QK^T at M=128 (64 heads in half the rows, N=64 rows, K=512) and PV
+    as four M=128 latent slices (N=64 heads, K=64 rows).
+    """
+    n_lat = (ctx + n_q) // ratio
+    lat_cols = -(-n_lat // 8) * 8
+    blk_tiles = -(-(n_lat // 8) // 128)
+    per_tile = 2.0 * 128 * 256 * 128
+    total = 0.0
+    for g0 in range(0, n_q, 16):
+        vis = (ctx + min(g0 + 16, n_q)) // ratio  # the group's last query, at ctx + min(...) - 1
+        cover = min(-(-vis // 8) * 8, lat_cols)
+        total += (blk_tiles + -(-cover // 128)) * per_tile
+    for i in range(n_q):
+        p = ctx + i
+        n_vis = (p + 1) // ratio
+        tokens = min(n_vis, min((n_vis + 7) // 8, k_blocks) * 8)
+        rows = min(tokens, k_tokens) + min(window, p + 1)
+        total += (-(-rows // 64) * 64) * (2.0 * 128 * 512 + 2.0 * 512 * 64)
+    return total
+
+
 def run_prefill(args, spec, dsa, synth, dev, rank, world):
     """A prefill chunk per step: n_q causal queries appended to ctx tokens of
     one sequence (cache build, i.e. the pooled keys, outside the step)."""
@@ -673,8 +712,11 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
     if code != 0:
         raise SystemExit(f"device status {code} info {info:#x}")
     flops = prefill_flops(n_q, ctx, ratio)
+    exec_flops = prefill_executed_flops(n_q, ctx, ratio)
     _, tf_peak, peak_kind = measured_peaks()
+    tf_sus = sustained_bf16_peak()
     tflops = flops / (ms * 1e-3) / 1e12
+    exec_tflops = exec_flops / (ms * 1e-3) / 1e12
     if rank == 0:
         line = {
             "metric": "sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
@@ -689,7 +731,12 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
             "roofline": {"kernel": "whole prefill step (tensor-core contractions)", "bound": "tensor",
                          "achieved": tflops, "peak": tf_peak, "peak_kind": peak_kind,
                          "unit": "TFLOP/s", "frac": tflops / tf_peak,
-                         "algorithmic_flops_per_step": flops},
+                         "algorithmic_flops_per_step": flops,
+                         "frac_of_sustained": tflops / tf_sus if tf_sus else None,
+                         "sustained_peak": tf_sus,
+                         "executed_flops_per_step": exec_flops,
+                         "executed_tflops": exec_tflops,
+                         "executed_frac": exec_tflops / tf_peak},
             "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q_)) for q_ in (10, 50, 90)],
             "kernel_ms_per_step": kernel_ms,
             "gpu_launches": int(sum(counts.values())),

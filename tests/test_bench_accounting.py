@@ -1,0 +1,34 @@
+"""The bench's flop accounting for a prefill chunk, against counts made by hand."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_algorithmic_prefill_flops_small_chunk():
+    # 3 queries at positions 20, 21, 22, ratio 1: 21..23 visible latents in 3 blocks;
+    # k_blocks 2 keeps 2 blocks = 16 tokens; k_tokens 4, window 5 -> 9 attention rows.
+    # Per query: scores 2*16*128 flop per key over 3 blocks + 16 tokens, and
+    # QK^T + PV 2*2*64*512 flop per row.
+    per_query = 2 * 16 * 128 * (3 + 16) + 2 * 2 * 64 * 512 * 9
+    assert bench.prefill_flops(3, 20, 1, k_blocks=2, k_tokens=4, window=5) == 3 * per_query
+
+
+def test_executed_prefill_flops_small_chunk():
+    # 23 latents: 2 complete blocks (one 128-row block tile) and 24 latent columns
+    # (one token tile) for the single group of 16 queries; each MMA tile is
+    # 2*128*256*128 flop. Attention rows 42, 44, 46 round up to one 64-row
+    # tile each, at 2*128*512 (QK^T, M=128) + 2*512*64 (PV) flop per row.
+    scans = 2 * (2 * 128 * 256 * 128)
+    attn = 3 * 64 * (2 * 128 * 512 + 2 * 512 * 64)
+    assert bench.prefill_executed_flops(3, 20, 1) == scans + attn
+
+
+def test_executed_covers_algorithmic_at_the_prefill_workload():
+    a = bench.prefill_flops(4096, 65536, 2)
+    e = bench.prefill_executed_flops(4096, 65536, 2)
+    assert 689e9 < a < 690e9
+    assert a < e < 2 * a
