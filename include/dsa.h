@@ -25,6 +25,9 @@
  *   - Streams: calls enqueue work on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and return without synchronising, except
  *     dsa_read_device_status.
+ *   - Threads: calls may come from several host threads at once, each with
+ *     its own workspace; the library's host-side caches and launch counters
+ *     are atomic. The profiling hook dsa_profile_events is the exception.
  *   - Layout: row-major, innermost dimension last. bf16 tensors are passed as
  *     raw 16-bit patterns. Every base pointer must be 16-byte aligned.
  *   - Dimensions: the kernels are built for 64 query heads, latent width 512,

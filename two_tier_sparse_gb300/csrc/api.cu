@@ -131,7 +131,7 @@ struct Profile {
   uint64_t next = 0;
 };
 Profile g_profile[DSA_KERNEL_KINDS];
-uint64_t g_launches[DSA_KERNEL_KINDS] = {0};
+std::atomic<uint64_t> g_launches[DSA_KERNEL_KINDS]{};
 
 template <typename F>
 cudaError_t launch(int kind, cudaStream_t s, F&& f) {
@@ -145,7 +145,7 @@ cudaError_t launch(int kind, cudaStream_t s, F&& f) {
   int n_launched = 1;
   cudaError_t e = f(&n_launched);
   if (e != cudaSuccess) return e;
-  g_launches[kind] += static_cast<uint64_t>(n_launched);
+  g_launches[kind].fetch_add(static_cast<uint64_t>(n_launched), std::memory_order_relaxed);
   if (timed) {
     ++p.next;
     return cudaEventRecord(static_cast<cudaEvent_t>(p.ends[slot]), s);
@@ -304,17 +304,18 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
 cudaError_t encode_tma_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
                           uint32_t box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encode == nullptr) {
+  // Looked up once, under the thread-safe initialisation of a local static.
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = []() {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr) {
-      return cudaErrorNotSupported;
+        q != cudaDriverEntryPointSuccess) {
+      fn = nullptr;
     }
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (encode == nullptr) return cudaErrorNotSupported;
   const CUtensorMapDataType dt =
       elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   const cuuint64_t dims[2] = {inner, rows};
@@ -328,17 +329,17 @@ cudaError_t encode_tma_2d(CUtensorMap* map, const void* base, int elem_bytes, ui
 }
 
 int device_sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64]{};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-      n = 148;
+      n = 152;
     }
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 namespace {
@@ -680,8 +681,8 @@ dsa_status_t dsa_profile_events(int kind, void* const* starts, void* const* ends
 dsa_status_t dsa_launch_counts(uint64_t* counts, int reset) {
   if (counts == nullptr) return DSA_ERR_INVALID_ARG;
   for (int k = 0; k < DSA_KERNEL_KINDS; ++k) {
-    counts[k] = g_launches[k];
-    if (reset) g_launches[k] = 0;
+    counts[k] = reset ? g_launches[k].exchange(0, std::memory_order_relaxed)
+                      : g_launches[k].load(std::memory_order_relaxed);
   }
   return DSA_OK;
 }

@@ -708,14 +708,14 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   if (a.tile_rows == 64) {
-    static int smem_set[64] = {0};
+    static std::atomic<int> smem_set[64]{};
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
                       a.splits, a);
   }
   if (a.tile_rows != 32) return cudaErrorInvalidValue;
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64]{};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,

@@ -4,6 +4,8 @@
 
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -193,13 +195,17 @@ cudaError_t launch_timeout_selftest(DeviceStatus* st, long long limit_cycles, cu
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device): `cache` is the caller's per-kernel array.
-inline cudaError_t ensure_smem(const void* kernel, int bytes, int (&cache)[64]) {
+// Host threads may race here; the attribute call is idempotent and the cache
+// is atomic.
+inline cudaError_t ensure_smem(const void* kernel, int bytes, std::atomic<int> (&cache)[64]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && cache[dev] >= bytes) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && cache[dev].load(std::memory_order_acquire) >= bytes) {
+    return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = bytes;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev].store(bytes, std::memory_order_release);
   return e;
 }
 

@@ -608,7 +608,7 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const int smem = Lo::kBytes + 1024;
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64]{};
   e = ensure_smem(reinterpret_cast<const void*>(scan_kernel<FMT>), smem, smem_set);
   if (e != cudaSuccess) return e;
   const int64_t grid = total < num_sms ? total : num_sms;

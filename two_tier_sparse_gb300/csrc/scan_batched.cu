@@ -338,7 +338,7 @@ cudaError_t launch_scan_batched(const BatchedScanArgs& a, int num_sms, cudaStrea
   e = encode_tma_2d(&maps.q, a.q_idx, 2, kIdxDim, static_cast<uint64_t>(a.n_q) * kIdxHeads,
                     kIdxDim * 2, 64, kN);
   if (e != cudaSuccess) return e;
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64]{};
   e = ensure_smem(reinterpret_cast<const void*>(batched_scan_kernel), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const int64_t grid = total < num_sms ? total : num_sms;

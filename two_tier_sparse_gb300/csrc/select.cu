@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
 template <int KPT>
 cudaError_t launch_reg(const SelectArgs& a, unsigned grid, cudaStream_t s) {
   const size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64]{};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
                               static_cast<int>(kMaxKBlocks * 4), smem_set);
   if (e != cudaSuccess) return e;
@@ -726,7 +726,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
   const int use_cache = a.n <= kCacheMax ? 1 : 0;
   const size_t smem = (use_cache ? static_cast<size_t>(a.n) * 4 : 0) +
                       (a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0);
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64]{};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_kernel),
                               static_cast<int>(kCacheMax * 4 + kMaxKBlocks * 4), smem_set);
   if (e != cudaSuccess) return e;
