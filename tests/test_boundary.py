@@ -97,3 +97,157 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(dsa, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         dsa.load()
+
+
+# The cases below pass fake device addresses (A is 256-byte aligned, A + 2 is
+# not). None is dereferenced: each case stops in the host-side checks, and the
+# zero-size calls return before any launch.
+A = 1 << 12
+
+
+def _k(fmt=0, data=A, scales=None, stride=100):
+    return dsa._Keys(fmt, data, scales, stride)
+
+
+def _ref(x):
+    return ctypes.byref(x) if x is not None else None
+
+
+def test_index_blocks_argument_errors(lib):
+    cfg = dsa.config()
+
+    def call(q=A, w=A, pooled=_k(stride=13), n=A, B=2, L=100, ids=A, sc=None, ws=A,
+             wsb=1 << 30, c=cfg):
+        return lib.dsa_index_blocks(ctypes.byref(c), q, w, _ref(pooled), n, B, L, ids, sc, ws,
+                                    wsb, None)
+    assert call(q=None) == 1
+    assert call(ids=None) == 1
+    assert call(n=None) == 1
+    assert call(w=A + 4) == 2
+    assert call(sc=A + 8) == 2
+    assert call(pooled=None) == 1
+    assert call(pooled=_k(stride=12)) == 1             # fewer rows than ceil(100 / 8) blocks
+    assert call(pooled=_k(data=A + 2, stride=13)) == 2
+    assert call(pooled=_k(fmt=1, scales=A + 2, stride=13)) == 2  # scales need 4-byte alignment
+    assert call(ws=None) == 4
+    assert call(wsb=16) == 4
+    assert call(ws=A + 16) == 2                        # workspace not 256-byte aligned
+    assert call(B=-1) == 1
+    assert call(L=-1) == 1
+    assert call(L=(1 << 30) + 1) == 1
+    assert call(B=0) == 0                              # nothing to do, nothing launched
+
+
+def test_attention_argument_errors(lib):
+    cfg = dsa.config()
+
+    def call(q=A, lat=A, stride=100, n=A, tok=A, swa=A, swl=A, B=2, out=A, lse=None, ws=A,
+             wsb=1 << 30, c=cfg):
+        return lib.dsa_sparse_attn_decode(ctypes.byref(c), q, lat, stride, n, tok, swa, swl, B,
+                                          out, lse, ws, wsb, None)
+    for bad in ("q", "lat", "n", "tok", "swa", "swl", "out"):
+        assert call(**{bad: None}) == 1, bad
+    assert call(stride=-1) == 1
+    assert call(B=-1) == 1
+    assert call(out=A + 2) == 2
+    assert call(lse=A + 4) == 2
+    assert call(ws=None) == 4
+    assert call(ws=A + 16) == 2
+    assert call(c=dsa.config(window=129)) == 1
+    assert call(c=dsa.config(sm_scale=float("nan"))) == 1
+    assert call(c=dsa.config(sm_scale=float("inf"))) == 1
+    bad = dsa.config()
+    bad.latent_dim = 256
+    assert call(c=bad) == 3
+    assert call(B=0) == 0
+
+
+def test_decode_step_argument_errors(lib):
+    cfg = dsa.config()
+
+    def call(q=A, qi=A, w=A, keys=_k(), pooled=_k(stride=13), lat=A, stride=100, n=A, L=100,
+             swa=A, swl=A, B=2, bids=None, tok=None, out=A, lse=None, ws=A, wsb=1 << 30, c=cfg):
+        return lib.dsa_decode_step(ctypes.byref(c), q, qi, w, _ref(keys), _ref(pooled), 1, lat,
+                                   stride, n, L, swa, swl, B, bids, tok, out, lse, ws, wsb, None)
+    assert call(pooled=None) == 1
+    assert call(keys=None) == 1
+    assert call(stride=99) == 1                        # latent rows per sequence < max_latents
+    assert call(keys=_k(stride=99)) == 1               # key rows per sequence < max_latents
+    assert call(pooled=_k(stride=12)) == 1
+    assert call(keys=_k(fmt=1, scales=A), pooled=_k(stride=13)) == 1  # formats differ
+    assert call(qi=None) == 1
+    assert call(qi=A + 2) == 2
+    assert call(tok=A + 8) == 2
+    assert call(bids=A + 8) == 2
+    assert call(ws=None) == 4
+    assert call(wsb=1024) == 4
+    assert call(B=-1) == 1
+    assert call(B=0) == 0
+
+
+def test_prefill_argument_errors(lib):
+    cfg = dsa.config(ratio=2)
+
+    def call(nq=16, ctx=100, q=A, qi=A, w=A, lat=A, keys=_k(), pooled=_k(), swa=A, out=A,
+             lse=None, tok=None, ws=A, wsb=1 << 30, c=cfg):
+        return lib.dsa_sparse_attn_prefill(ctypes.byref(c), nq, ctx, q, qi, w, lat, _ref(keys),
+                                           _ref(pooled), swa, out, lse, tok, ws, wsb, None)
+    assert call(nq=-1) == 1
+    assert call(ctx=-1) == 1
+    assert call(ctx=1 << 32) == 1                      # more latents than the library supports
+    for bad in ("q", "qi", "w", "lat", "swa", "out"):
+        assert call(**{bad: None}) == 1, bad
+    assert call(out=A + 2) == 2
+    assert call(tok=A + 4) == 2
+    assert call(keys=None) == 1
+    assert call(pooled=_k(fmt=1, scales=A)) == 1       # formats differ
+    assert call(ws=None) == 4
+    assert call(wsb=4096) == 4
+    assert call(nq=0) == 0
+
+
+def test_pool_argument_errors(lib):
+    cfg = dsa.config()
+
+    def call(keys=_k(), n=A, B=2, L=100, pooled=_k(stride=13), ws=A, wsb=1 << 30, c=cfg):
+        return lib.dsa_pool_index_keys(ctypes.byref(c), _ref(keys), n, B, L, 0, _ref(pooled), ws,
+                                       wsb, None)
+    assert call(pooled=None) == 1
+    assert call(keys=_k(fmt=1, scales=None)) == 1      # MXFP8 without scales
+    assert call(pooled=_k(stride=12)) == 1
+    assert call(n=None) == 1
+    assert call(keys=_k(fmt=1, scales=A), pooled=_k(stride=13)) == 1
+    assert call(ws=None) == 4
+    assert call(B=-1) == 1
+    assert call(B=0) == 0
+
+
+def test_topk_noalloc_capacity_and_errors(lib):
+    cfg = dsa.config()
+
+    def call(q=A, w=A, keys=_k(stride=1 << 20), bids=A, n=A, B=2, L=1 << 20, tok=A, c=cfg):
+        return lib.dsa_topk_noalloc(ctypes.byref(c), q, w, _ref(keys), bids, n, B, L, tok, None)
+    # 2^21 fp32 candidate scores: 128 queries of 2048 x 8 candidates fit, 129 do not
+    assert call(B=129) == 4
+    assert call(bids=None, B=3) == 4                   # 3 x 2^20 latents without a block stage
+    assert call(tok=None) == 1
+    assert call(bids=A + 4) == 2
+    assert call(keys=_k(stride=10)) == 1
+    assert call(B=0) == 0
+
+
+def test_hooks_and_self_test_argument_errors(lib):
+    n_kinds = len(dsa.KERNEL_KINDS)
+    assert lib.dsa_profile_events(-1, None, None, 0) == 1
+    assert lib.dsa_profile_events(n_kinds, None, None, 0) == 1
+    assert lib.dsa_profile_events(0, None, None, -1) == 1
+    assert lib.dsa_profile_events(0, None, None, 2) == 1  # events needed when n > 0
+    assert lib.dsa_profile_events(0, None, None, 0) == 0  # switched off
+    assert lib.dsa_launch_counts(None, 0) == 1
+    counts = (ctypes.c_uint64 * n_kinds)()
+    assert lib.dsa_launch_counts(counts, 1) == 0
+    assert lib.dsa_selftest_timeout(None, 1 << 20, None) == 1
+    assert lib.dsa_selftest_timeout(A, 8, None) == 1     # smaller than the status word
+    size = ctypes.c_size_t(0)
+    assert lib.dsa_workspace_size(ctypes.byref(dsa.config()), 1, 10, None) == 1
+    assert lib.dsa_workspace_size(None, 1, 10, ctypes.byref(size)) == 1
