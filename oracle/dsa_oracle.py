@@ -4,7 +4,9 @@ This module is the plain, slow, obviously correct statement of what the step
 computes. Only the tests, the smoke check and the benchmark's CPU-baseline leg
 use it; the library never imports it and it imports nothing from the library.
 Floating point runs in float64 except where the method itself fixes a storage
-format (bf16, fp32, e4m3/UE8M0); library matmuls serve as plain dot products.
+format (bf16, fp32, e4m3/UE8M0, e2m1/UE8M0); library matmuls serve as plain dot
+products. The MXFP4 index-key format (e2m1 codes) is stated here ahead of the
+library, which does not take it yet.
 
 The method (DeepSeek-V4.1, two-tier sparse attention):
   * recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, bullet "Two-tier sparse
@@ -18,6 +20,8 @@ The method (DeepSeek-V4.1, two-tier sparse attention):
     top-512 candidate set per retrieving layer; a coarser candidate-block pass.
   * Same page, §1: fp8 weights use a 32-wide UE8M0 block scale; the vLLM page's
     Overview bullet "Mixed MXFP4/MXFP8 checkpoint" names MXFP8 with UE8M0 scales.
+  * The vLLM page's serving configurations set indexer_kv_dtype to mxfp4, and the
+    sglang page lists an FP4 indexer cache: MXFP4 per OCP MX v1.0.
   * The pages leave the indexer formula open; this build fixes it as
     score = sum_h w_h * ReLU(q_h . k), the block key as the mean of the block's
     8 index keys and ties as "lower index first".
@@ -165,12 +169,98 @@ def mxfp8_encode(v32: np.ndarray):
     return codes, (X + 127).astype(np.uint8)
 
 
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit e2m1 code (OCP MX v1.0, FP4 E2M1: 1 sign, 2 exponent
+    bits with bias 1, 1 mantissa bit; no infinities or NaN; largest normal 6,
+    subnormals m * 0.5)."""
+    s = -1.0 if code & 0x8 else 1.0
+    E = (code >> 1) & 0x3
+    m = code & 0x1
+    if E == 0:
+        return s * m * 0.5
+    return s * (1.0 + m / 2.0) * 2.0 ** (E - 1)
+
+
+E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], np.float64)
+
+
+def e2m1_encode(y: np.ndarray) -> np.ndarray:
+    """float64 values to e2m1 codes (0..15): round to nearest, ties to the even
+    mantissa, finite values beyond 6 saturating to +-6 (the element rounding of
+    the OCP MX conversion)."""
+    y = np.asarray(y, np.float64)
+    sign = np.where(np.signbit(y), 0x8, 0).astype(np.int64)
+    a = np.abs(y)
+    code = np.zeros(y.shape, np.int64)
+    sub = a < 1.0
+    code[sub] = np.rint(a[sub] * 2.0).astype(np.int64)             # 0, 1, or 2 (= 1.0)
+    nrm = ~sub
+    if np.any(nrm):
+        an = a[nrm]
+        _, e = np.frexp(an)
+        E = e.astype(np.int64) - 1                                  # 2^E <= a < 2^(E+1)
+        m = np.rint((an / np.ldexp(1.0, E) - 1.0) * 2.0).astype(np.int64)
+        carry = m == 2
+        E[carry] += 1
+        m[carry] = 0
+        c = ((E + 1) << 1) | m
+        code[nrm] = np.where(E > 2, 0x7, np.minimum(c, 0x7))
+    return (code | sign).astype(np.uint8)
+
+
+def mxfp4_pack(codes: np.ndarray) -> np.ndarray:
+    """e2m1 codes [..., d] to bytes [..., d/2]: element 2i in the low nibble,
+    element 2i + 1 in the high one (this library's storage order)."""
+    c = np.asarray(codes, np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def mxfp4_unpack(packed: np.ndarray) -> np.ndarray:
+    """Bytes [..., d/2] to e2m1 codes [..., d] (inverse of mxfp4_pack)."""
+    p = np.asarray(packed, np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def mxfp4_decode(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """MXFP4 rows (packed bytes [..., d/2], scales [..., d/32]) to float64,
+    exactly: v = e2m1(code) * 2^(scale - 127) (OCP MX v1.0, 32-element blocks).
+    The pages name the format for the indexer cache: recipes.vllm.ai
+    "DeepSeek-V4.1-Flash" sets indexer_kv_dtype to mxfp4; the sglang page lists
+    an FP4 indexer cache."""
+    v = E2M1_TABLE[mxfp4_unpack(packed)]
+    sc = ue8m0_scale(scales)
+    shp = v.shape
+    v = v.reshape(shp[:-1] + (shp[-1] // 32, 32)) * sc[..., None]
+    return v.reshape(shp)
+
+
+def mxfp4_encode(v32: np.ndarray):
+    """fp32 rows [..., d] to MXFP4 (OCP MX v1.0): per 32-element group
+    X = floor(log2(amax)) - 2 (2 = emax of e2m1), clamped to [-127, 127],
+    X = 0 for an all-zero group; codes = e2m1(v / 2^X), packed two a byte;
+    scale byte X + 127."""
+    v = np.asarray(v32, np.float32).astype(np.float64)
+    shp = v.shape
+    g = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    amax = np.max(np.abs(g), axis=-1)
+    _, e = np.frexp(amax)
+    X = np.where(amax > 0, e.astype(np.int64) - 1 - 2, 0)
+    X = np.clip(X, -127, 127)
+    codes = e2m1_encode(g * np.ldexp(1.0, -X)[..., None]).reshape(shp)
+    return mxfp4_pack(codes), (X + 127).astype(np.uint8)
+
+
 def decode_keys(fmt: str, data: np.ndarray, scales: Optional[np.ndarray] = None) -> np.ndarray:
     """Index keys (or pooled keys) in their storage format to float64."""
     if fmt == "bf16":
         return bf16_to_f64(data)
     if fmt == "mxfp8":
         return mxfp8_decode(data, scales)
+    if fmt == "mxfp4":
+        return mxfp4_decode(data, scales)
     if fmt == "fp32":
         return np.asarray(data, np.float32).astype(np.float64)
     raise ValueError(fmt)
@@ -219,6 +309,8 @@ def store_f32(v32: np.ndarray, fmt: str):
         return f32_to_bf16_rne(v32), None
     if fmt == "mxfp8":
         return mxfp8_encode(v32)
+    if fmt == "mxfp4":
+        return mxfp4_encode(v32)
     if fmt == "fp32":
         return np.asarray(v32, np.float32).copy(), None
     raise ValueError(fmt)

@@ -62,6 +62,7 @@ def _load():
         lib.synth_normal_f32.argtypes = [u64, u64, i64, i64, dbl, vp]
         lib.synth_uniform_f32.argtypes = [u64, u64, i64, i64, vp]
         lib.synth_normal_mxfp8.argtypes = [u64, u64, i64, i64, ctypes.c_int, dbl, vp, vp]
+        lib.synth_normal_mxfp4.argtypes = [u64, u64, i64, i64, ctypes.c_int, dbl, vp, vp]
         lib.synth_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -111,6 +112,20 @@ def normal_mxfp8(seed: int, tag: int, row_offset: int, rows: int, dim: int, scal
     return codes, scales
 
 
+def normal_mxfp4(seed: int, tag: int, row_offset: int, rows: int, dim: int, scale: float,
+                 packed=None, scales=None):
+    """MXFP4 rows of scale * N(0,1): (packed e2m1 codes uint8 [rows, dim/2], element 2i
+    in the low nibble; scales uint8 [rows, dim/32]). The values are those of
+    normal_mxfp8 with the same arguments."""
+    assert dim % 32 == 0
+    packed = np.empty((rows, dim // 2), np.uint8) if packed is None else packed
+    scales = np.empty((rows, dim // 32), np.uint8) if scales is None else scales
+    if rows:
+        _load().synth_normal_mxfp4(seed, tag, row_offset, rows, dim, scale, _ptr(packed),
+                                   _ptr(scales))
+    return packed, scales
+
+
 def _seq_offset(b: int) -> int:
     # Counter space of sequence b: elements (b << 40) + row * dim + j.
     return b << 40
@@ -122,6 +137,8 @@ class Keys:
 
     fmt "bf16": data uint16 [..., rows, 128], scales None.
     fmt "mxfp8": data uint8 e4m3 codes [..., rows, 128], scales uint8 UE8M0 [..., rows, 4].
+    fmt "mxfp4": data uint8 packed e2m1 codes [..., rows, 64] (element 2i in the low
+    nibble), scales uint8 UE8M0 [..., rows, 4].
     """
     fmt: str
     data: np.ndarray
@@ -167,7 +184,7 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
     (default: max latents rounded up to a multiple of 8). q_scale multiplies
     the N(0,1)/sqrt(512) query (the "sharpened" variants use 8).
     poison_tail fills rows past each sequence's end with +inf (bf16) or the
-    largest MXFP8 value, so a kernel that reads them gives a visibly wrong result.
+    largest MXFP8 or MXFP4 value, so a kernel that reads them gives a visibly wrong result.
     """
     T = np.asarray(T, np.int64).reshape(-1)
     B = int(T.shape[0])
@@ -189,6 +206,9 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
     elif key_fmt == "mxfp8":
         kdata = np.empty((B, cap, IDX_DIM), np.uint8)
         kscales = np.empty((B, cap, IDX_DIM // 32), np.uint8)
+    elif key_fmt == "mxfp4":
+        kdata = np.empty((B, cap, IDX_DIM // 2), np.uint8)
+        kscales = np.empty((B, cap, IDX_DIM // 32), np.uint8)
     else:
         raise ValueError(key_fmt)
     for b in range(B):
@@ -203,16 +223,22 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
                         out=swa[b, :n_sw].reshape(-1))
         if key_fmt == "bf16":
             normal_bf16(seed, TAG_KEYS, off, cap * IDX_DIM, s128, out=kdata[b].reshape(-1))
-        else:
+        elif key_fmt == "mxfp8":
             normal_mxfp8(seed, TAG_KEYS, b << 31, cap, IDX_DIM, s128, codes=kdata[b],
+                         scales=kscales[b])
+        else:
+            normal_mxfp4(seed, TAG_KEYS, b << 31, cap, IDX_DIM, s128, packed=kdata[b],
                          scales=kscales[b])
         if poison_tail:
             n = int(n_lat[b])
             lat[b, n:] = BF16_POS_INF
             if key_fmt == "bf16":
                 kdata[b, n:] = BF16_POS_INF
-            else:
+            elif key_fmt == "mxfp8":
                 kdata[b, n:] = 0x7E
+                kscales[b, n:] = 254
+            else:
+                kdata[b, n:] = 0x77  # 6, 6
                 kscales[b, n:] = 254
     return DecodeInputs(T=T, ratio=ratio, q=q, q_idx=q_idx, w=w, latents=lat,
                         keys=Keys(key_fmt, kdata, kscales), swa=swa, n_latents=n_lat,
@@ -260,6 +286,9 @@ def prefill_inputs(n_q: int, ctx: int, ratio: int, key_fmt: str, seed: int,
     elif key_fmt == "mxfp8":
         c, s = normal_mxfp8(seed, TAG_KEYS, 0, n_lat_cap, IDX_DIM, s128)
         keys = Keys("mxfp8", c, s)
+    elif key_fmt == "mxfp4":
+        c, s = normal_mxfp4(seed, TAG_KEYS, 0, n_lat_cap, IDX_DIM, s128)
+        keys = Keys("mxfp4", c, s)
     else:
         raise ValueError(key_fmt)
     return PrefillInputs(ctx=ctx, ratio=ratio,

@@ -3,8 +3,9 @@
  *
  * This file holds no arithmetic of the attention method. It only turns
  * (seed, tensor tag, element index) into numbers with the distributions the
- * workloads call for: N(0,1)/sqrt(d) values stored as bf16 or as MXFP8
- * (e4m3 codes plus one UE8M0 scale per 32 elements), and U(0,1) head weights.
+ * workloads call for: N(0,1)/sqrt(d) values stored as bf16, as MXFP8 (e4m3
+ * codes plus one UE8M0 scale per 32 elements) or as MXFP4 (e2m1 codes, two a
+ * byte, plus one UE8M0 scale per 32 elements), and U(0,1) head weights.
  * Both the CUDA path and the CPU oracle are fed the bytes this file writes.
  *
  * Generator: SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom
@@ -63,6 +64,26 @@ static uint8_t e4m3_code(double y) {
   }
   if (E > 8 || (E == 8 && m > 6.0)) return s | 0x7E;
   return s | (uint8_t)(((E + 7) << 3) | (int)m);
+}
+
+/* e2m1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; magnitudes 0,
+ * 0.5, 1, 1.5, 2, 3, 4, 6) code nearest to y, ties to the even mantissa,
+ * saturating at +-6. */
+static uint8_t e2m1_code(double y) {
+  uint8_t s = (y < 0) ? 0x8 : 0x0;
+  double a = fabs(y);
+  if (a >= 6.0) return s | 0x7;
+  if (a < 1.0) return s | (uint8_t)nearbyint(a * 2.0); /* 0, 1, or 2 (= 1.0) */
+  int e;
+  frexp(a, &e);
+  int E = e - 1; /* a in [2^E, 2^(E+1)), E in 0..2 */
+  double m = nearbyint((a / ldexp(1.0, E) - 1.0) * 2.0);
+  if (m >= 2.0) {
+    m = 0.0;
+    E += 1;
+  }
+  if (E > 2) return s | 0x7;
+  return s | (uint8_t)(((E + 1) << 1) | (int)m);
 }
 
 /* Both normals of pair j: element 2j takes the cosine, 2j + 1 the sine. */
@@ -157,6 +178,50 @@ void synth_normal_mxfp8(uint64_t seed, uint64_t tag, int64_t row_offset, int64_t
       scales[r * groups + g] = (uint8_t)(X + 127);
       for (int j = 0; j < 32; ++j) {
         codes[r * dim + g * 32 + j] = e4m3_code(ldexp((double)v[j], -X));
+      }
+    }
+  }
+}
+
+/*
+ * As synth_normal_mxfp8, stored as MXFP4: per group of 32, X = floor(log2(amax))
+ * - 2 clamped to [-127, 127] (X = 0 for an all-zero group), scale byte X + 127,
+ * codes = e2m1(v / 2^X), two a byte (element 2i in the low nibble). packed is
+ * [rows, dim / 2], scales is [rows, dim / 32].
+ */
+void synth_normal_mxfp4(uint64_t seed, uint64_t tag, int64_t row_offset, int64_t rows, int dim,
+                        double scale, uint8_t* packed, uint8_t* scales) {
+  uint64_t key = stream_key(seed, tag);
+  int groups = dim / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int g = 0; g < groups; ++g) {
+      float v[32];
+      float amax = 0.0f;
+      for (int j = 0; j < 32; j += 2) {
+        uint64_t c = (uint64_t)((row_offset + r) * dim + g * 32 + j); /* even */
+        double z0, z1;
+        normal_pair(key, c >> 1, &z0, &z1);
+        v[j] = (float)(scale * z0);
+        v[j + 1] = (float)(scale * z1);
+      }
+      for (int j = 0; j < 32; ++j) {
+        float a = fabsf(v[j]);
+        if (a > amax) amax = a;
+      }
+      int X = 0;
+      if (amax > 0.0f) {
+        int e;
+        frexpf(amax, &e);
+        X = (e - 1) - 2;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+      }
+      scales[r * groups + g] = (uint8_t)(X + 127);
+      for (int j = 0; j < 32; j += 2) {
+        uint8_t lo = e2m1_code(ldexp((double)v[j], -X));
+        uint8_t hi = e2m1_code(ldexp((double)v[j + 1], -X));
+        packed[r * (dim / 2) + g * 16 + j / 2] = (uint8_t)(lo | (hi << 4));
       }
     }
   }

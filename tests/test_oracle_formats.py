@@ -189,3 +189,111 @@ def test_pool_keys_brute_force_partial_blocks():
     dm, sm = O.pool_keys(kv, n, "mxfp8")
     c2, s2 = O.mxfp8_encode(d)
     assert np.array_equal(dm, c2) and np.array_equal(sm, s2)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 (OCP MX v1.0: e2m1 elements, 32-element groups, UE8M0 scale), the
+# indexer-cache format the pages name (recipes.vllm.ai "DeepSeek-V4.1-Flash":
+# indexer_kv_dtype mxfp4; sglang page: FP4 indexer cache). torch has no CPU
+# conversion for float4_e2m1fn_x2, so the pins are the format's closed forms
+# and a brute-force nearest-value search.
+# ---------------------------------------------------------------------------
+
+
+def test_e2m1_table_closed_forms():
+    # the eight magnitudes of E2M1: subnormal 0.5, normals 1..6, then negatives
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(O.E2M1_TABLE[:8]) == mags
+    assert list(O.E2M1_TABLE[8:]) == [-m for m in mags]
+    assert math.copysign(1.0, O.E2M1_TABLE[8]) < 0
+
+
+def _nearest_e2m1(y):
+    """Brute force: the code of the representable magnitude nearest min(|y|, 6);
+    on a tie the one with mantissa bit 0 (neighbouring codes differ in it)."""
+    mags = O.E2M1_TABLE[:8]
+    d = np.abs(mags - min(abs(y), 6.0))
+    best = np.flatnonzero(d == d.min())
+    c = int(best[0]) if len(best) == 1 else int([b for b in best if b % 2 == 0][0])
+    return c | (8 if np.signbit(y) else 0)
+
+
+def test_e2m1_encode_vs_brute_force():
+    rng = np.random.default_rng(40)
+    mags = O.E2M1_TABLE[:8]
+    mids = (mags[1:] + mags[:-1]) / 2  # exact ties: 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5
+    ys = np.concatenate([mags, mids, mids + 1e-9, mids - 1e-9, rng.uniform(0, 8, 3000),
+                         [6.5, 7.0, 7.5, 8.0, 100.0, 1e30]])
+    ys = np.concatenate([ys, -ys])
+    want = np.array([_nearest_e2m1(y) for y in ys], np.uint8)
+    assert np.array_equal(O.e2m1_encode(ys), want)
+    # the ties named: each goes to the even mantissa
+    assert list(O.E2M1_TABLE[O.e2m1_encode(mids)]) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+
+
+def test_mxfp4_pack_order_and_round_trip():
+    codes = (np.arange(64) % 16).astype(np.uint8).reshape(2, 32)
+    p = O.mxfp4_pack(codes)
+    assert p.shape == (2, 16)
+    assert p[0, 0] == codes[0, 0] | (codes[0, 1] << 4) and p[1, 15] == codes[1, 30] | (
+        codes[1, 31] << 4)
+    assert np.array_equal(O.mxfp4_unpack(p), codes)
+
+
+def test_mxfp4_encode_scale_rule():
+    # X = floor(log2(amax)) - 2: amax 1.0 -> -2; 0.75 -> -3; 6 -> 0; 7.9 -> 0; 8 -> 1;
+    # 1.5 * 2^-30 -> -32
+    for amax, X in [(1.0, -2), (0.75, -3), (6.0, 0), (7.9, 0), (8.0, 1),
+                    (1.5 * 2.0 ** -30, -32)]:
+        v = np.zeros((1, 32), np.float32)
+        v[0, 11] = amax
+        v[0, 2] = -amax / 3
+        _, s = O.mxfp4_encode(v)
+        assert int(s[0, 0]) - 127 == X, (amax, s)
+    d, s = O.mxfp4_encode(np.zeros((2, 64), np.float32))
+    assert (d == 0).all() and (s == 127).all()
+
+
+def test_mxfp4_round_trip_of_representable_groups():
+    rng = np.random.default_rng(41)
+    for X in (-20, -3, 0, 7):
+        codes = rng.integers(0, 16, (16, 32)).astype(np.uint8)
+        codes[:, 0] = rng.choice([6, 7, 14, 15], 16)  # |amax| in {4, 6}: scale stays X
+        v = O.E2M1_TABLE[codes] * 2.0 ** X
+        d, s = O.mxfp4_encode(v.astype(np.float32))
+        assert (s.astype(int) - 127 == X).all()
+        assert np.array_equal(O.mxfp4_decode(d, s), v)
+        assert np.array_equal(d, O.mxfp4_pack(codes))  # the same codes, -0 included
+
+
+def test_mxfp4_encode_error_bound():
+    rng = np.random.default_rng(42)
+    v = (rng.standard_normal((200, 128)) / np.sqrt(128)).astype(np.float32)
+    d, s = O.mxfp4_encode(v)
+    dec = O.mxfp4_decode(d, s)
+    X = np.repeat(s.astype(np.int64) - 127, 32, axis=-1)
+    scaled = np.abs(v.astype(np.float64)) * np.ldexp(1.0, -X)
+    assert scaled.max() < 8.0  # the group's largest element lands in [4, 8)
+    # half the local spacing of the grid (0.25 below 2, 0.5 below 4, 1 up to 6),
+    # and saturation above 6: |error| <= 2^X * max(0.25, |v / 2^X| / 4)
+    bound = np.ldexp(1.0, X) * np.maximum(0.25, scaled / 4)
+    assert (np.abs(dec - v) <= bound + 1e-300).all()
+    # no sign flips: a decoded value is zero or has the input's sign
+    assert ((dec == 0) | (np.sign(dec) == np.sign(v))).all()
+
+
+def test_pool_keys_in_mxfp4():
+    rng = np.random.default_rng(43)
+    k = rng.standard_normal((1, 128)).astype(np.float32)
+    d, s = O.mxfp4_encode(k)
+    km = O.mxfp4_decode(d, s)[0]
+    # identical members pool to the member's own codes and scales
+    pd, ps = O.pool_keys(np.tile(km, (8, 1)), 8, "mxfp4")
+    assert np.array_equal(pd[0], d[0]) and np.array_equal(ps[0], s[0])
+    # otherwise the pooled key is the fp32 mean, then the MXFP4 conversion
+    kv = O.bf16_to_f64(O.f32_to_bf16_rne(rng.standard_normal((21, 64)).astype(np.float32)))
+    mean, _ = O.pool_keys(kv, 21, "fp32")
+    dm, sm = O.pool_keys(kv, 21, "mxfp4")
+    c2, s2 = O.mxfp4_encode(mean)
+    assert np.array_equal(dm, c2) and np.array_equal(sm, s2)
+    assert np.array_equal(O.decode_keys("mxfp4", dm, sm), O.mxfp4_decode(c2, s2))

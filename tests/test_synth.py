@@ -45,3 +45,27 @@ def test_decode_inputs_layout():
     assert (inp.swa[1, 37:] == 0).all()
     lat = O.bf16_to_f64(inp.latents[0, :50])
     assert abs(lat.std() * np.sqrt(512) - 1) < 0.02
+
+
+def test_mxfp4_generator_is_the_ocp_conversion_of_its_normals():
+    packed, scales = synth.normal_mxfp4(1, 5, 0, 300, 128, 1 / np.sqrt(128))
+    assert packed.shape == (300, 64) and scales.shape == (300, 4)
+    ref = synth.normal_f32(1, 5, 0, 300 * 128, 1 / np.sqrt(128)).reshape(300, 128)
+    # two independent statements of the OCP MX conversion: the generator's C and
+    # the oracle's numpy
+    c2, s2 = O.mxfp4_encode(ref)
+    assert np.array_equal(packed, c2) and np.array_equal(scales, s2)
+    # the same values as the MXFP8 generator, so the two formats share one scale
+    # grid: X(fp4) = X(fp8) + 6
+    _, s8 = synth.normal_mxfp8(1, 5, 0, 300, 128, 1 / np.sqrt(128))
+    assert np.array_equal(scales.astype(int), s8.astype(int) + 6)
+
+
+def test_decode_inputs_with_mxfp4_keys():
+    inp = synth.decode_inputs([100, 37], 2, "mxfp4", seed=3)
+    assert inp.keys.data.shape == (2, 56, 64) and inp.keys.scales.shape == (2, 56, 4)
+    assert (inp.keys.data[1, 18:] == 0x77).all() and (inp.keys.scales[1, 18:] == 254).all()
+    k = O.decode_keys("mxfp4", inp.keys.data[0, :50], inp.keys.scales[0, :50])
+    assert abs(k.std() * np.sqrt(128) - 1) < 0.1
+    pf = synth.prefill_inputs(20, 100, 2, "mxfp4", seed=4)
+    assert pf.keys.data.shape == (64, 64) and pf.keys.fmt == "mxfp4"
