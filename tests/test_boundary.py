@@ -251,3 +251,41 @@ def test_hooks_and_self_test_argument_errors(lib):
     size = ctypes.c_size_t(0)
     assert lib.dsa_workspace_size(ctypes.byref(dsa.config()), 1, 10, None) == 1
     assert lib.dsa_workspace_size(None, 1, 10, ctypes.byref(size)) == 1
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dsa.h"
+int main(void) {
+  dsa_config_t c;
+  size_t bytes = 0;
+  dsa_default_config(&c);
+  if (c.n_heads != 64 || c.latent_dim != 512 || c.k_blocks != 2048 || c.k_tokens != 512) return 1;
+  if (dsa_workspace_size(&c, 4, 4096, &bytes) != DSA_OK || bytes == 0) return 2;
+  if (dsa_workspace_size(&c, -1, 4096, &bytes) != DSA_ERR_INVALID_ARG) return 3;
+  if (strcmp(dsa_status_string(DSA_ERR_TIMEOUT), "DSA_ERR_TIMEOUT") != 0) return 4;
+  printf("%zu\n", bytes);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 and a C program
+    links against the library and calls it (host-only calls, no GPU)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(dsa.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-ldsa",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    c = dsa.config()
+    assert int(out.stdout) == dsa.workspace_size(c, 4, 4096)
