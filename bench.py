@@ -38,6 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn decode queries/s at 128K ctx; achieved HBM GB/s vs roofline"
+PREFILL_METRIC = ("sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
+                  "TFLOP/s vs roofline")
+PREFILL_CPU_SAMPLE = 512  # oracle queries timed for a prefill chunk's CPU figure
 DEFAULT_WORKLOAD = "decode_b64_t131072_r1_mxfp8"
 L2_FLUSH_BYTES = 512 << 20
 L2_READ_BYTES = 256 << 20
@@ -73,7 +76,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0,
-                   help="sequences in the CPU-oracle sample (0: automatic)")
+                   help="sequences (decode) or queries (prefill) in the CPU-oracle sample (0: automatic)")
     return p.parse_args()
 
 
@@ -213,6 +216,35 @@ def cpu_oracle_rate(workload: str, n_seq: int, steps: int = 1):
     return n_seq / t, t, threads, sample
 
 
+def cpu_oracle_prefill_rate(workload: str, n_sample: int, steps: int = 1):
+    """Times the oracle, as it stands, on n_sample queries spread evenly over the
+    workload's prefill chunk. The complete-block keys are built once outside the
+    timed region, as the GPU step takes them from its cache; each query pools its
+    own partly visible block. Returns (queries/s, seconds per step, threads,
+    sample description)."""
+    import oracle as O
+    import synth
+    spec = dict(synth.WORKLOADS[workload])
+    assert spec.pop("kind") == "prefill"
+    n_q, ctx, ratio, fmt = spec["n_q"], spec["ctx"], spec["ratio"], spec["key_fmt"]
+    inp = synth.prefill_inputs(n_q, ctx, ratio, fmt, spec["seed"])
+    cfg = O.StepConfig(ratio=ratio)
+    kv, pooled, _ = O.prefill_caches(cfg, inp)
+    picks = np.unique(np.linspace(0, n_q - 1, max(1, min(n_sample, n_q))).round().astype(int))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for i in picks:
+            O.prefill_query(cfg, inp, int(i), kv, pooled)
+        times.append(time.perf_counter() - t0)
+    threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or os.cpu_count() or 1
+    sample = (f"{len(picks)} of the chunk's {n_q} queries, evenly spaced (context {ctx}, ratio "
+              f"{ratio}, {fmt} keys); the complete-block keys are built once, outside the "
+              "timed region")
+    t = float(np.median(times))
+    return len(picks) / t, t, threads, sample
+
+
 def auto_cpu_sample(workload: str) -> int:
     import synth
     T = synth.WORKLOADS[workload]["T"]
@@ -225,6 +257,26 @@ def run_reference(args):
         return
     import synth
     spec = synth.WORKLOADS[args.workload]
+    if spec["kind"] == "prefill":
+        n = args.cpu_sample or PREFILL_CPU_SAMPLE
+        for _ in range(args.warmup):
+            cpu_oracle_prefill_rate(args.workload, n)
+        qps, t, threads, sample = cpu_oracle_prefill_rate(args.workload, n,
+                                                          steps=max(1, args.steps))
+        line = {
+            "impl": "reference", "metric": PREFILL_METRIC, "value": qps, "unit": "queries/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "n_q": spec["n_q"], "ctx": spec["ctx"],
+                       "ratio": spec["ratio"], "key_fmt": spec["key_fmt"]},
+            "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     n = args.cpu_sample or auto_cpu_sample(args.workload)
     for _ in range(args.warmup):
         cpu_oracle_rate(args.workload, n)
@@ -718,9 +770,14 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
     tflops = flops / (ms * 1e-3) / 1e12
     exec_tflops = exec_flops / (ms * 1e-3) / 1e12
     if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            qps, _, threads, sample = cpu_oracle_prefill_rate(
+                args.workload, args.cpu_sample or PREFILL_CPU_SAMPLE)
+            cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
+                   "sample": sample}
         line = {
-            "metric": "sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
-                      "TFLOP/s vs roofline",
+            "metric": PREFILL_METRIC,
             "value": job_rate(n_q, world, ms), "unit": "queries/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -737,6 +794,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
                          "executed_flops_per_step": exec_flops,
                          "executed_tflops": exec_tflops,
                          "executed_frac": exec_tflops / tf_peak},
+            "cpu_baseline": cpu,
             "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q_)) for q_ in (10, 50, 90)],
             "kernel_ms_per_step": kernel_ms,
             "gpu_launches": int(sum(counts.values())),

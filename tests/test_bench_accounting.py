@@ -1,4 +1,4 @@
-"""The bench's flop accounting for a prefill chunk, against counts made by hand."""
+"""The bench's flop accounting for a prefill chunk, against counts made by hand, and its CPU legs."""
 import os
 import sys
 
@@ -32,3 +32,9 @@ def test_executed_covers_algorithmic_at_the_prefill_workload():
     e = bench.prefill_executed_flops(4096, 65536, 2)
     assert 689e9 < a < 690e9
     assert a < e < 2 * a
+
+
+def test_prefill_cpu_leg_runs_on_a_spread_sample():
+    qps, t, threads, sample = bench.cpu_oracle_prefill_rate("prefill_q4096_ctx65536_r2_bf16", 3)
+    assert qps > 0 and t > 0 and threads >= 1
+    assert sample.startswith("3 of the chunk's 4096 queries")
