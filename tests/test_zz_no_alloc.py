@@ -33,6 +33,11 @@ def _dev(a):
 @pytest.mark.parametrize("fmt,ratio,T,k_blocks,gathered", [
     ("mxfp8", 1, [20000, 9001, 777, 5], 96, True),
     ("bf16", 2, [4096, 1000, 30], 2048, False),
+    # more than 32768 candidates without a workspace: the selection without the
+    # two-pass scratch (keys cached in shared memory up to 40960, global passes
+    # beyond), against dsa_topk's two-pass selection
+    ("bf16", 1, [36000, 33001], 4096, False),
+    ("mxfp8", 1, [50000, 12345], 4096, False),
 ])
 def test_noalloc_topk_matches_topk(fmt, ratio, T, k_blocks, gathered):
     inp = synth.decode_inputs(T, ratio, fmt, seed=40)
