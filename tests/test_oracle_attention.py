@@ -124,6 +124,39 @@ def test_prefill_last_query_equals_decode(fmt, ratio):
     assert np.array_equal(rp["out"], rd["out"])
 
 
+@pytest.mark.parametrize("fmt,ratio", [("bf16", 2), ("mxfp8", 1)])
+def test_every_prefill_query_equals_decode_of_its_prefix(fmt, ratio):
+    """Query i of a chunk sits at position ctx + i: it must see exactly what a
+    one-query decode of the sequence's first ctx + i + 1 tokens sees (visible
+    latents, the partly visible last block, the window ending at itself).
+    The chunk crosses block boundaries and keeps the block stage active."""
+    ctx, n_q = 150, 12
+    cfg = _cfg(ratio=ratio, k_blocks=6, k_tokens=24)
+    pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, seed=13)
+    kv, pooled, _ = O.prefill_caches(cfg, pf)
+    seen_partial = set()
+    for i in range(n_q):
+        T = ctx + i + 1
+        L = T // ratio
+        dec = synth.decode_inputs([T], ratio, fmt, seed=14)
+        dec.q[0], dec.q_idx[0], dec.w[0] = pf.q[i], pf.q_idx[i], pf.w[i]
+        dec.latents[0, :L] = pf.latents[:L]
+        dec.keys.data[0, :L] = pf.keys.data[:L]
+        if fmt == "mxfp8":
+            dec.keys.scales[0, :L] = pf.keys.scales[:L]
+        lo, hi = O.prefill_window_rows(ctx, i, 128)
+        assert hi - lo == int(dec.swa_len[0]) == min(128, T)
+        dec.swa[0, : hi - lo] = pf.swa[lo:hi]
+        rp = O.prefill_query(cfg, pf, i, kv, pooled)
+        rd = O.decode_sequence(cfg, dec, 0)
+        assert int(dec.n_latents[0]) == O.prefill_visible(ctx, i, ratio) == L
+        assert np.array_equal(rp["block_ids"], rd["block_ids"]), i
+        assert np.array_equal(rp["token_ids"], rd["token_ids"]), i
+        assert np.array_equal(rp["out"], rd["out"]) and np.array_equal(rp["lse"], rd["lse"]), i
+        seen_partial.add(L % 8 != 0)
+    assert seen_partial == {True, False}  # both a complete and a partial last block occur
+
+
 def test_prefill_partial_block_is_mean_of_visible_members():
     ctx, n_q, ratio = 100, 12, 1
     cfg = _cfg(ratio=ratio, k_blocks=3, k_tokens=16)
