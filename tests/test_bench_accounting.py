@@ -38,3 +38,30 @@ def test_prefill_cpu_leg_runs_on_a_spread_sample():
     qps, t, threads, sample = bench.cpu_oracle_prefill_rate("prefill_q4096_ctx65536_r2_bf16", 3)
     assert qps > 0 and t > 0 and threads >= 1
     assert sample.startswith("3 of the chunk's 4096 queries")
+
+
+def test_profile_summaries_name_commands_the_bench_accepts():
+    """Every summary under profiles/ gives the command that made it; each bench
+    command there parses with the bench's own arguments and names a workload
+    that exists."""
+    import glob
+    import re
+    import shlex
+
+    import synth
+    cmds = set()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        found = re.findall(r"python bench\.py[^`|\n]*", text)
+        assert found or "ncu" not in text, f"{path} names no bench command"
+        cmds.update(c.strip() for c in found)
+    assert cmds
+    for c in cmds:
+        argv = shlex.split(c)[2:]
+        old = sys.argv
+        sys.argv = ["bench.py"] + argv
+        try:
+            args = bench.parse()
+        finally:
+            sys.argv = old
+        assert args.workload in synth.WORKLOADS, c
