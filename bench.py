@@ -42,6 +42,7 @@ PREFILL_METRIC = ("sparse-attn prefill queries/s (4096 queries on 64K context); 
                   "TFLOP/s vs roofline")
 PREFILL_CPU_SAMPLE = 512  # oracle queries timed for a prefill chunk's CPU figure
 DEFAULT_WORKLOAD = "decode_b64_t131072_r1_mxfp8"
+PREFILL_WORKLOAD = "prefill_q4096_ctx65536_r2_bf16"
 L2_FLUSH_BYTES = 512 << 20
 L2_READ_BYTES = 256 << 20
 
@@ -75,6 +76,9 @@ def parse():
                    help="override the workload's batch (smaller cases for profiling)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="skip the prefill chunk that the default decode run measures after "
+                        "its own steps (reported under extra.prefill)")
     p.add_argument("--cpu-sample", type=int, default=0,
                    help="sequences (decode) or queries (prefill) in the CPU-oracle sample (0: automatic)")
     return p.parse_args()
@@ -628,6 +632,14 @@ def run_ours(args):
         "gpu_launches_by_kind": counts,
         "clocks": clocks.summary(),
     }
+    if args.workload == DEFAULT_WORKLOAD and not args.no_prefill and world == 1 and not args.batch:
+        # The prefill chunk's line rides along under extra.prefill, measured in
+        # the same run (its own timing rules, clocks and CPU figure).
+        pspec = dict(synth.WORKLOADS[PREFILL_WORKLOAD])
+        pspec.pop("kind")
+        line["extra"] = {"prefill": run_prefill(args, pspec, dsa, synth, dev, rank, world,
+                                                workload=PREFILL_WORKLOAD,
+                                                steps=min(K, 10), emit=False)}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -678,12 +690,15 @@ def prefill_executed_flops(n_q: int, ctx: int, ratio: int, k_blocks: int = 2048,
     return total
 
 
-def run_prefill(args, spec, dsa, synth, dev, rank, world):
+def run_prefill(args, spec, dsa, synth, dev, rank, world, workload=None, steps=None,
+                emit=True):
     """A prefill chunk per step: n_q causal queries appended to ctx tokens of
-    one sequence (cache build, i.e. the pooled keys, outside the step)."""
+    one sequence (cache build, i.e. the pooled keys, outside the step).
+    Returns rank 0's JSON line (printed when `emit`)."""
     import torch
+    workload = workload or args.workload
     n_q, ctx, ratio, fmt = spec["n_q"], spec["ctx"], spec["ratio"], spec["key_fmt"]
-    if args.batch:
+    if args.batch and emit:
         n_q = args.batch  # a smaller chunk (profiling); the line then names it in config
     t0 = time.time()
     pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, shard_seed(spec["seed"], rank))
@@ -721,7 +736,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
     code, info = dsa.read_device_status(ws)
     if code != 0:
         raise SystemExit(f"device status {code} info {info:#x}")
-    K = args.steps
+    K = steps or args.steps
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     dsa.launch_counts(reset=True)
@@ -773,7 +788,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             qps, _, threads, sample = cpu_oracle_prefill_rate(
-                args.workload, args.cpu_sample or PREFILL_CPU_SAMPLE)
+                workload, (args.cpu_sample if emit else 0) or PREFILL_CPU_SAMPLE)
             cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
                    "sample": sample}
         line = {
@@ -781,7 +796,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
             "value": job_rate(n_q, world, ms), "unit": "queries/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "n_q": n_q, "ctx": ctx, "ratio": ratio,
+            "config": {"workload": workload, "n_q": n_q, "ctx": ctx, "ratio": ratio,
                        "key_fmt": fmt, "latents": n_lat,
                        "l2": L2Flush.DESCRIPTION,
                        "input_gen_s": round(gen_s, 1)},
@@ -801,9 +816,11 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world):
             "gpu_launches_by_kind": counts,
             "clocks": clocks.summary(),
         }
-        print(json.dumps(line), flush=True)
-    if world > 1:
+        if emit:
+            print(json.dumps(line), flush=True)
+    if world > 1 and emit:
         torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
 
 
 def main():

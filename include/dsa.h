@@ -259,9 +259,13 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
  *     the last call's contents (every score the kernels read is written first
  *     by the same call, so nothing needs clearing). Calls that may overlap on
  *     the GPU (different streams without ordering) race on it: serialise them.
- *   - Device-side input checks (ids outside a sequence, unordered block ids)
- *     have no status word to write here: the offending elements are skipped
- *     and nothing is reported. Use dsa_topk to have them reported.
+ *   - No status word: device-side input checks (ids outside a sequence,
+ *     unordered block ids) skip the offending elements and report nothing,
+ *     and a bounded device wait that runs out (DSA_ERR_TIMEOUT in the other
+ *     calls) is not reported either. After such a timeout the scan leaves
+ *     score slots unwritten, so the selection may rank scores left in the
+ *     scratch by an earlier call while the call still returns DSA_OK. Use
+ *     dsa_topk with a workspace where these conditions must be seen.
  */
 #define DSA_TOPK_NOALLOC_MAX_SCORES (1 << 21)
 dsa_status_t dsa_topk_noalloc(const dsa_config_t* cfg, const void* q_idx, const float* w,

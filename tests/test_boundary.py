@@ -225,7 +225,9 @@ def test_pool_argument_errors(lib):
 def test_topk_noalloc_capacity_and_errors(lib):
     cfg = dsa.config()
 
-    def call(q=A, w=A, keys=_k(stride=1 << 20), bids=A, n=A, B=2, L=1 << 20, tok=A, c=cfg):
+    # The default request (129 queries) is beyond the scratch: a case that got
+    # past the argument checks would stop at the capacity check, never launch.
+    def call(q=A, w=A, keys=_k(stride=1 << 20), bids=A, n=A, B=129, L=1 << 20, tok=A, c=cfg):
         return lib.dsa_topk_noalloc(ctypes.byref(c), q, w, _ref(keys), bids, n, B, L, tok, None)
     # 2^21 fp32 candidate scores: 128 queries of 2048 x 8 candidates fit, 129 do not
     assert call(B=129) == 4

@@ -158,7 +158,8 @@ def test_topk_all_blocks(fmt, T):
 
 @pytest.mark.parametrize("T,ratio,q_scale,sm_scale", [
     ([4096, 1000, 300, 100, 5], 2, 1.0, 0.0),     # default scale (near-uniform softmax)
-    ([4096, 1000, 300, 100, 5], 2, 8.0, 1.0),     # sharpened: logit std about 3
+    ([4096, 1000, 300, 100, 5], 2, 8.0, 1.0),     # sharpened: logit std about 0.35
+    ([4096, 1000, 300, 100, 5], 2, 8.0, 8.0),     # sharper: logit std about 2.8
     ([70000, 1], 1, 8.0, 1.0),                    # 512 selected of many; a 1-token sequence
     ([2], 2, 1.0, 0.0),                           # one latent, two window rows
 ])
@@ -331,15 +332,52 @@ def test_decode_step_replays_from_a_cuda_graph(fmt, k_blocks):
                [0, 2])
 
 
-def test_decode_32_sequences_of_32768_tokens():
-    """Decode, batch 32, 32768 tokens at ratio 2 (16384 latents, 2048 blocks, all kept)."""
-    inp = synth.workload_inputs("decode_b32_t32768_r2_bf16")
-    cfg = dsa.config(ratio=2)
+@pytest.mark.parametrize("q_scale,sm", [(1.0, 0.0), (8.0, 8.0)])
+def test_decode_32_sequences_of_32768_tokens(q_scale, sm):
+    """Decode, batch 32, 32768 tokens at ratio 2 (16384 latents, 2048 blocks, all
+    kept), at the default softmax scale and sharpened (q x 8, tau = 8: logit std
+    about 2.8, so each split's running maximum differs)."""
+    inp = synth.workload_inputs("decode_b32_t32768_r2_bf16", q_scale=q_scale)
+    cfg = dsa.config(ratio=2, sm_scale=sm)
     d = DecodeOnDevice(inp, cfg)
     d.pool()
     outs = run_step(d, cfg)
     assert d.status()[0] == 0
     check_step(inp, cfg, outs, range(inp.B))
+
+
+def plant_dominant_row(inp, b, s, strength):
+    """Make window row s of sequence b line up with head 0 of its query (row =
+    strength x the query row's direction, rounded to bf16), so that one row,
+    held by one CTA of a split, dominates that head's softmax."""
+    qh = O.bf16_to_f64(inp.q[b, 0])
+    v = qh / np.sqrt((qh ** 2).sum()) * strength
+    inp.swa[b, s] = O.f32_to_bf16_rne(v.astype(np.float32))
+
+
+@pytest.mark.parametrize("B", [19, 20, 32, 38, 39, 64, 76, 77, 128])
+def test_decode_step_split_paths_sharpened(B):
+    """The attention splits a query's rows over an S-CTA cluster while S x B
+    fits the SMs (152 on a GB300: S = 8 up to 19 queries, 4 up to 38, 2 up to
+    76) and runs one CTA a query beyond. With a sharpened softmax (q x 8,
+    tau = 8: logit std about 2.8) the CTAs of a cluster see different running
+    maxima, so a wrong max or sum rescale in the on-chip merge shows; in every
+    fourth sequence one window row is made to dominate head 0. Both selection
+    tiers run (k_blocks 96 of up to 500 blocks) on ragged sequences; every
+    sequence is checked against the oracle."""
+    rng = np.random.default_rng(1000 + B)
+    T = [int(t) for t in rng.integers(900, 4000, B)]
+    T[0], T[-1] = 4000, 70          # the longest, and one shorter than the window
+    fmt = "mxfp8" if B % 2 else "bf16"
+    inp = synth.decode_inputs(T, 1, fmt, seed=50 + B, q_scale=8.0)
+    for b in range(0, B, 4):
+        plant_dominant_row(inp, b, int(rng.integers(0, inp.swa_len[b])), 0.6)
+    cfg = dsa.config(k_blocks=96, ratio=1, sm_scale=8.0)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    outs = run_step(d, cfg)
+    assert d.status()[0] == 0
+    check_step(inp, cfg, outs, range(B))
 
 
 # ---------------------------------------------------------------------------

@@ -69,6 +69,47 @@ def test_noalloc_topk_matches_topk(fmt, ratio, T, k_blocks, gathered):
         assert torch.equal(got, ref)
 
 
+def _gathered_case(fmt, T, k_blocks, seed):
+    """Inputs, block ids and dsa_topk's token ids for a token stage over the
+    block stage's choice (both computed with a caller workspace)."""
+    inp = synth.decode_inputs(T, 1, fmt, seed=seed)
+    cfg = dsa.config(k_blocks=k_blocks)
+    B, cap = inp.B, inp.cap
+    keys = dsa.Keys(fmt, _dev(inp.keys.data),
+                    None if inp.keys.scales is None else _dev(inp.keys.scales))
+    q_idx, w, n_lat = _dev(inp.q_idx), _dev(inp.w), _dev(inp.n_latents)
+    ws = dsa.workspace(cfg, B, cap)
+    nbc = cap // 8
+    pdat = torch.zeros((B, nbc, 128), dtype=torch.int16 if fmt == "bf16" else torch.uint8,
+                       device="cuda")
+    psc = None if fmt == "bf16" else torch.zeros((B, nbc, 4), dtype=torch.uint8, device="cuda")
+    pooled = dsa.Keys(fmt, pdat, psc)
+    dsa.pool_index_keys(cfg, keys, n_lat, cap, pooled, ws)
+    bids = torch.empty((B, k_blocks), dtype=torch.int32, device="cuda")
+    dsa.index_blocks(cfg, q_idx, w, pooled, n_lat, cap, bids, ws)
+    ref = torch.empty((B, cfg.k_tokens), dtype=torch.int32, device="cuda")
+    dsa.topk(cfg, q_idx, w, keys, bids, n_lat, cap, ref, ws)
+    assert dsa.read_device_status(ws)[0] == 0
+    return dict(cfg=cfg, q_idx=q_idx, w=w, keys=keys, bids=bids, n_lat=n_lat, cap=cap, ref=ref)
+
+
+def test_noalloc_smaller_call_after_a_larger_one():
+    """The scratch keeps the previous call's scores. A large call (four long
+    sequences) followed by a smaller one with other inputs, whose short
+    sequences leave most of their block lists as -1 padding, must give exactly
+    dsa_topk's ids for the smaller inputs: nothing the second call reads may
+    come from the first."""
+    big = _gathered_case("mxfp8", [40000, 39001, 38000, 30000], 256, seed=61)
+    small = _gathered_case("mxfp8", [900, 333, 64], 256, seed=62)
+    for c in (big, small):
+        got = torch.full_like(c["ref"], -7)
+        dsa.topk_noalloc(c["cfg"], c["q_idx"], c["w"], c["keys"], c["bids"], c["n_lat"],
+                         c["cap"], got)
+        torch.cuda.synchronize()
+        assert torch.equal(got, c["ref"])
+    assert (small["bids"].cpu().numpy() == -1).sum() > 256  # most of the list is padding
+
+
 def test_noalloc_topk_rejects_requests_beyond_its_scratch():
     cfg = dsa.config(k_blocks=2048)
     lib = dsa.load()
