@@ -345,7 +345,9 @@ def run_ours(args):
     if fmt == "bf16":
         pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.int16, device=dev))
     else:
-        pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.uint8, device=dev),
+        nbc += nbc & 1 if fmt == "mxfp4" else 0  # MXFP4 rows are read in pairs
+        width = 64 if fmt == "mxfp4" else 128
+        pooled = dsa.Keys(fmt, torch.empty((B, nbc, width), dtype=torch.uint8, device=dev),
                           torch.empty((B, nbc, 4), dtype=torch.uint8, device=dev))
     ws = dsa.workspace(cfg, B, cap, dev)
     out = torch.empty((B, 64, 512), dtype=torch.int16, device=dev)
@@ -460,9 +462,9 @@ def run_ours(args):
 
     # Roofline of the dominant kernel: the indexer scan. Algorithmic bytes per
     # launch = rows scanned x bytes per key row (MXFP8: 128 codes + 4 scale
-    # bytes; bf16: 256); both launches of a step scan 2048 x 8 = 16384 rows per
+    # bytes; MXFP4: 64 + 4; bf16: 256); both launches of a step scan 2048 x 8 = 16384 rows per
     # query (16384 block keys, then 16384 candidate latents).
-    row_bytes = 132 if fmt == "mxfp8" else 256
+    row_bytes = {"mxfp8": 132, "mxfp4": 68}.get(fmt, 256)
     nb = -(-L // 8)
     blk_rows = nb if nb > cfg.k_blocks else 0
     tok_rows = 8 * cfg.k_blocks if nb > cfg.k_blocks else L

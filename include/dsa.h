@@ -66,11 +66,19 @@ typedef enum {
   DSA_ERR_TIMEOUT = 7       /* a bounded device wait ran out (dsa_read_device_status) */
 } dsa_status_t;
 
-/* Storage format of index keys and of block-pooled keys. */
+/* Storage format of index keys and of block-pooled keys (recipes.vllm.ai
+ * "DeepSeek-V4.1-Flash" names an MXFP8 and an MXFP4 indexer cache: the
+ * "Mixed MXFP4/MXFP8 checkpoint" bullet and indexer_kv_dtype mxfp4 in its
+ * serving configurations). */
 typedef enum {
   DSA_FMT_BF16 = 0,  /* data: bf16 [rows, 128]; scales: NULL */
-  DSA_FMT_MXFP8 = 1  /* data: e4m3 bytes [rows, 128]; scales: UE8M0 bytes [rows, 4]
+  DSA_FMT_MXFP8 = 1, /* data: e4m3 bytes [rows, 128]; scales: UE8M0 bytes [rows, 4]
                         (OCP MX v1.0: one power-of-two scale 2^(s-127) per 32 values) */
+  DSA_FMT_MXFP4 = 2  /* data: e2m1 codes two a byte [rows, 64], element 2i in the low
+                        nibble of byte i; scales: UE8M0 bytes [rows, 4] (OCP MX v1.0).
+                        The kernels read these arrays in pairs of rows: seq_stride_rows
+                        must be even, and a buffer whose last sequence's rows are odd in
+                        number must hold one row more (it is read, never used). */
 } dsa_fmt_t;
 
 typedef struct {
@@ -128,8 +136,9 @@ dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int n_queries, int64_t 
  * block holding latent n_latents[b] - 1 when tail_only != 0):
  *     pooled[b][j] = RN_fmt( fp32_sum_in_order(keys[b][8j .. 8j+c-1]) / c ),
  * c = min(8, n_latents[b] - 8j). RN_fmt is round-to-nearest-even to bf16, or
- * the OCP MX conversion (X = floor(log2 amax) - 8 per 32 values, elements
- * rounded to e4m3 with saturation). pooled->fmt must equal keys->fmt.
+ * the OCP MX conversion (X = floor(log2 amax) - emax per 32 values, emax 8
+ * for e4m3 and 2 for e2m1, elements rounded to nearest even with saturation).
+ * pooled->fmt must equal keys->fmt.
  *   n_latents: device int32 [B], each in [0, max_latents].
  */
 dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys,

@@ -299,7 +299,7 @@ def prefill_inputs(n_q: int, ctx: int, ratio: int, key_fmt: str, seed: int,
                          keys=keys, swa=swa.reshape(n_sw, LATENT_DIM), window=window)
 
 
-# The five workloads, named by what they are (tokens per sequence, batch,
+# The workloads, named by what they are (tokens per sequence, batch,
 # compression ratio, index-key format) with their seeds.
 WORKLOADS = {
     "decode_b1_t4096_r2_bf16": dict(kind="decode", B=1, T=4096, ratio=2, key_fmt="bf16", seed=0),
@@ -311,6 +311,10 @@ WORKLOADS = {
                                            key_fmt="bf16", seed=3),
     "decode_b8_t1048576_r1_mxfp8": dict(kind="decode", B=8, T=1048576, ratio=1,
                                         key_fmt="mxfp8", seed=4),
+    # The 64 x 131072 decode with the MXFP4 index cache the serving pages name
+    # (recipes.vllm.ai "DeepSeek-V4.1-Flash", indexer_kv_dtype mxfp4).
+    "decode_b64_t131072_r1_mxfp4": dict(kind="decode", B=64, T=131072, ratio=1,
+                                        key_fmt="mxfp4", seed=2),
 }
 
 

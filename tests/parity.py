@@ -33,6 +33,18 @@ def host_u16(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
+def pooled_buffer(fmt, B, blocks, device="cuda"):
+    """Zeroed block-key cache [B, blocks, ...] in `fmt`. MXFP4 caches are read in
+    pairs of rows, so their per-sequence row count is even."""
+    if fmt == "bf16":
+        return dsa.Keys(fmt, torch.zeros((B, blocks, 128), dtype=torch.int16, device=device))
+    if fmt == "mxfp4":
+        blocks += blocks & 1
+    width = 64 if fmt == "mxfp4" else 128
+    return dsa.Keys(fmt, torch.zeros((B, blocks, width), dtype=torch.uint8, device=device),
+                    torch.zeros((B, blocks, 4), dtype=torch.uint8, device=device))
+
+
 class DecodeOnDevice:
     """A DecodeInputs batch resident on the GPU, with its pooled-key buffers."""
 
@@ -51,14 +63,7 @@ class DecodeOnDevice:
         fmt = inp.keys.fmt
         self.keys = dsa.Keys(fmt, dev(inp.keys.data, device),
                              None if inp.keys.scales is None else dev(inp.keys.scales, device))
-        nbc = cap // 8
-        if fmt == "bf16":
-            self.pooled = dsa.Keys(fmt, torch.zeros((B, nbc, 128), dtype=torch.int16,
-                                                    device=device))
-        else:
-            self.pooled = dsa.Keys(fmt, torch.zeros((B, nbc, 128), dtype=torch.uint8,
-                                                    device=device),
-                                   torch.zeros((B, nbc, 4), dtype=torch.uint8, device=device))
+        self.pooled = pooled_buffer(fmt, B, cap // 8, device)
         self.ws = dsa.workspace(cfg, B, cap, device)
         self.device = device
 

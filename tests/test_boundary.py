@@ -77,6 +77,10 @@ def test_argument_errors_are_found_on_the_host(lib):
     assert _call_topk(lib, cfg, q=18) == 2                         # misaligned
     assert _call_topk(lib, cfg, keys=dsa._Keys(1, 16, None, 100)) == 1  # MXFP8 without scales
     assert _call_topk(lib, cfg, keys=dsa._Keys(7, 16, None, 100)) == 1  # bad format
+    assert _call_topk(lib, cfg, keys=dsa._Keys(3, 16, 16, 100)) == 1    # bad format
+    assert _call_topk(lib, cfg, keys=dsa._Keys(2, 16, None, 100)) == 1  # MXFP4 without scales
+    assert _call_topk(lib, cfg, keys=dsa._Keys(2, 16, 18, 100)) == 2    # scales misaligned
+    assert _call_topk(lib, cfg, keys=dsa._Keys(2, 16, 16, 101)) == 1    # MXFP4: odd row stride
     assert _call_topk(lib, cfg, keys=dsa._Keys(0, 16, None, 50)) == 1   # stride < max_latents
     assert _call_topk(lib, cfg, ws_bytes=10) == 4                  # workspace too small
     assert _call_topk(lib, cfg, ws=None) == 4

@@ -40,8 +40,9 @@ def check_all_sequences(inp, cfg, outs):
 
 @pytest.mark.parametrize("workload,sample", [
     ("decode_b1_t4096_r2_bf16", [0]),
-    ("decode_b64_t131072_r1_mxfp8", [0, 37, 63]),
-    ("decode_b8_t1048576_r1_mxfp8", [0, 7]),
+    ("decode_b64_t131072_r1_mxfp8", [0, 9, 18, 27, 37, 45, 54, 63]),
+    ("decode_b8_t1048576_r1_mxfp8", [0, 3, 5, 7]),
+    ("decode_b64_t131072_r1_mxfp4", [0, 21, 42, 63]),
 ])
 def test_decode_workload_full_size(workload, sample):
     spec = synth.WORKLOADS[workload]
@@ -75,7 +76,9 @@ def test_prefill_workload_full_size():
     # sampled queries against the oracle
     oc = oracle_cfg(cfg)
     kv, pooled, _ = O.prefill_caches(oc, pf)
-    for i in (0, 1, 1000, 2047, 4095):
+    # queries whose last block is complete (0, 2047, 4095) and partly visible
+    # (1, 3, 13, 1000, 2999, 4093: 1, 2, 7, 4, 4 and 7 of its 8 members)
+    for i in (0, 1, 3, 13, 1000, 2047, 2999, 4093, 4095):
         r = O.prefill_query(oc, pf, i, kv, pooled, with_attention=False)
         pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
         if not block_near_tie(r["block_scores"], cfg.k_blocks):

@@ -10,7 +10,8 @@ import torch
 import oracle as O
 import synth
 import two_tier_sparse_gb300 as dsa
-from parity import (DecodeOnDevice, check_ids, check_out, check_scores, dev, host_u16)
+from parity import (DecodeOnDevice, check_ids, check_out, check_scores, dev, host_u16,
+                    pooled_buffer)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +34,7 @@ def oracle_cfg(cfg):
 # ---------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "mxfp4"])
 def test_pool_bit_exact(fmt):
     inp = synth.decode_inputs([1003, 77, 8, 1, 2051], 1, fmt, seed=21)
     cfg = dsa.config(ratio=1)
@@ -50,20 +51,21 @@ def test_pool_bit_exact(fmt):
         nb = want.shape[0]
         got = pdat[b, :nb].view(np.uint16) if fmt == "bf16" else pdat[b, :nb]
         assert np.array_equal(got, want), f"seq {b}"
-        if fmt == "mxfp8":
+        if fmt != "bf16":
             assert np.array_equal(psc[b, :nb], want_s), f"seq {b} scales"
 
 
-def test_pool_tail_only_writes_the_last_block():
-    inp = synth.decode_inputs([1003, 64], 1, "mxfp8", seed=22)
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_pool_tail_only_writes_the_last_block(fmt):
+    inp = synth.decode_inputs([1003, 64], 1, fmt, seed=22)
     d = DecodeOnDevice(inp, dsa.config())
     d.pooled.data.fill_(0x55)
     d.pool(tail_only=True)
     got = d.pooled.data.cpu().numpy()
     for b, n in enumerate(inp.n_latents):
         last = (int(n) - 1) // 8
-        kv = O.decode_keys("mxfp8", inp.keys.data[b][:n], inp.keys.scales[b][:n])
-        want, _ = O.pool_keys(kv, int(n), "mxfp8")
+        kv = O.decode_keys(fmt, inp.keys.data[b][:n], inp.keys.scales[b][:n])
+        want, _ = O.pool_keys(kv, int(n), fmt)
         assert np.array_equal(got[b, last], want[last])
         assert (got[b, :last] == 0x55).all()
 
@@ -74,7 +76,7 @@ def test_pool_tail_only_writes_the_last_block():
 
 
 @pytest.mark.parametrize("fmt,k_blocks", [("bf16", 64), ("mxfp8", 64), ("mxfp8", 4096),
-                                          ("bf16", 1)])
+                                          ("bf16", 1), ("mxfp4", 64), ("mxfp4", 4096)])
 def test_index_blocks(fmt, k_blocks):
     T = [5000, 3001, 700, 9]
     inp = synth.decode_inputs(T, 1, fmt, seed=23)
@@ -101,7 +103,7 @@ def test_index_blocks(fmt, k_blocks):
 # ---------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("fmt,ratio", [("bf16", 2), ("mxfp8", 1)])
+@pytest.mark.parametrize("fmt,ratio", [("bf16", 2), ("mxfp8", 1), ("mxfp4", 1), ("mxfp4", 2)])
 def test_topk_over_gpu_blocks(fmt, ratio):
     T = [12000, 4099, 2000]
     inp = synth.decode_inputs(T, ratio, fmt, seed=24)
@@ -132,6 +134,7 @@ def test_topk_over_gpu_blocks(fmt, ratio):
 
 @pytest.mark.parametrize("fmt,T", [("bf16", [4096, 1000, 513, 30]),
                                    ("mxfp8", [4096, 1000, 513, 30]),
+                                   ("mxfp4", [4096, 1000, 513, 31]),
                                    ("bf16", [90000, 70001, 3])])  # > 32768 latents: two passes
 def test_topk_all_blocks(fmt, T):
     inp = synth.decode_inputs(T, 2, fmt, seed=25)
@@ -242,6 +245,8 @@ def check_step(inp, cfg, outs, seqs):
     ([4096], 2, "bf16", 2048, 1.0, 0.0),                       # decode, 4096 tokens, batch 1
     ([20000, 9001, 777, 64, 3], 1, "mxfp8", 128, 8.0, 1.0),     # both tiers, ragged, sharpened
     ([20000, 9001, 777], 2, "bf16", 200, 1.0, 0.0),
+    ([20000, 9001, 777, 64, 3], 1, "mxfp4", 128, 8.0, 8.0),     # MXFP4 keys, sharpened
+    ([30001, 5003], 2, "mxfp4", 300, 1.0, 0.0),
 ])
 def test_decode_step(T, ratio, fmt, k_blocks, q_scale, sm):
     inp = synth.decode_inputs(T, ratio, fmt, seed=28, q_scale=q_scale)
@@ -253,7 +258,8 @@ def test_decode_step(T, ratio, fmt, k_blocks, q_scale, sm):
     check_step(inp, cfg, outs, range(inp.B))
 
 
-@pytest.mark.parametrize("fmt,k_blocks", [("mxfp8", 256), ("bf16", 256), ("mxfp8", 4096)])
+@pytest.mark.parametrize("fmt,k_blocks", [("mxfp8", 256), ("bf16", 256), ("mxfp8", 4096),
+                                          ("mxfp4", 256)])
 def test_decode_step_is_deterministic_and_updates_the_pool(fmt, k_blocks):
     """The step's pooling of each sequence's newest block restores it bit for
     bit (codes and MXFP8 scales), with a block stage (k_blocks 256) and
@@ -400,11 +406,7 @@ def run_prefill(pf, cfg):
     keys = dsa.Keys(fmt, dev(pf.keys.data), None if pf.keys.scales is None else dev(pf.keys.scales))
     # pooled keys of complete blocks, built on the GPU (the pool call over one sequence)
     nbf = n_lat // 8
-    if fmt == "bf16":
-        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.int16, device="cuda"))
-    else:
-        pooled = dsa.Keys(fmt, torch.zeros((1, max(nbf, 1), 128), dtype=torch.uint8, device="cuda"),
-                          torch.zeros((1, max(nbf, 1), 4), dtype=torch.uint8, device="cuda"))
+    pooled = pooled_buffer(fmt, 1, max(nbf, 1))
     ws = dsa.workspace(cfg, n_q, n_lat)
     keys1 = dsa.Keys(fmt, keys.data[None], None if keys.scales is None else keys.scales[None])
     n1 = torch.tensor([nbf * 8], dtype=torch.int32, device="cuda")
@@ -421,7 +423,8 @@ def run_prefill(pf, cfg):
 
 
 @pytest.mark.parametrize("fmt,ratio,ctx,n_q", [("bf16", 2, 333, 50), ("mxfp8", 1, 1000, 37),
-                                               ("bf16", 1, 5, 130)])
+                                               ("bf16", 1, 5, 130), ("mxfp4", 2, 333, 50),
+                                               ("mxfp4", 1, 1001, 37)])
 def test_prefill(fmt, ratio, ctx, n_q):
     pf = synth.prefill_inputs(n_q, ctx, ratio, fmt, seed=30, q_scale=8.0)
     cfg = dsa.config(k_blocks=12, k_tokens=40, ratio=ratio, sm_scale=1.0)
@@ -437,7 +440,7 @@ def test_prefill(fmt, ratio, ctx, n_q):
         check_out(out[i], lse[i], r2["out"], r2["lse"], f"q{i}")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "mxfp4"])
 def test_scan_many_short_queries(fmt):
     """One or two tiles per query, so the scan pipeline switches query on
     almost every tile (the per-query operand slots are rebuilt constantly)."""
@@ -520,6 +523,7 @@ def scale_key_row(inp, b, t, log2_factor):
     ([60000, 33000, 20000], "mxfp8", 600, True),
     ([300000, 270001, 5000], "mxfp8", 2048, False),  # 37500 blocks: two-pass selection
     ([300000, 270001, 5000], "bf16", 64, True),
+    ([60000, 33000, 20000], "mxfp4", 2048, True),
 ])
 def test_select_thousands_of_candidates(T, fmt, k_blocks, outliers):
     """Block sets of 600-37500 and token sets of 4800-32768 candidates (above

@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 FMT_BF16 = 0
 FMT_MXFP8 = 1
-_FMT = {"bf16": FMT_BF16, "mxfp8": FMT_MXFP8}
+FMT_MXFP4 = 2
+_FMT = {"bf16": FMT_BF16, "mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4}
 
 STATUS = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_MISALIGNED", 3: "DSA_ERR_UNSUPPORTED",
@@ -126,7 +127,8 @@ def config(k_blocks=2048, k_tokens=512, window=128, ratio=1, sm_scale=0.0) -> Co
 @dataclass
 class Keys:
     """A key cache on the device: data [B, rows, 128] (bf16 as 16-bit words, or
-    uint8 e4m3 codes) and, for MXFP8, scales uint8 [B, rows, 4]."""
+    uint8 e4m3 codes) or [B, rows, 64] (uint8, two e2m1 codes a byte) and, for
+    MXFP8 and MXFP4, scales uint8 [B, rows, 4]."""
     fmt: str
     data: torch.Tensor
     scales: Optional[torch.Tensor] = None

@@ -73,13 +73,18 @@ float tau(const dsa_config_t& c) {
 
 dsa_status_t check_keys(const dsa_keys_t* k, int64_t min_stride, bool need_stride) {
   if (k == nullptr || k->data == nullptr) return DSA_ERR_INVALID_ARG;
-  if (k->fmt != DSA_FMT_BF16 && k->fmt != DSA_FMT_MXFP8) return DSA_ERR_INVALID_ARG;
-  if (k->fmt == DSA_FMT_MXFP8 && k->scales == nullptr) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(k->data)) return DSA_ERR_MISALIGNED;
-  if (k->fmt == DSA_FMT_MXFP8 && (reinterpret_cast<uintptr_t>(k->scales) & 3u)) {
-    return DSA_ERR_MISALIGNED;
+  if (k->fmt != DSA_FMT_BF16 && k->fmt != DSA_FMT_MXFP8 && k->fmt != DSA_FMT_MXFP4) {
+    return DSA_ERR_INVALID_ARG;
   }
+  const bool mx = k->fmt != DSA_FMT_BF16;
+  if (mx && k->scales == nullptr) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(k->data)) return DSA_ERR_MISALIGNED;
+  if (mx && (reinterpret_cast<uintptr_t>(k->scales) & 3u)) return DSA_ERR_MISALIGNED;
   if (need_stride && k->seq_stride_rows < min_stride) return DSA_ERR_INVALID_ARG;
+  // MXFP4 rows are read two at a time (128 bytes): sequences start on a pair.
+  if (k->fmt == DSA_FMT_MXFP4 && need_stride && (k->seq_stride_rows & 1)) {
+    return DSA_ERR_INVALID_ARG;
+  }
   return DSA_OK;
 }
 

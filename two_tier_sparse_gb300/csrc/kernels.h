@@ -2,6 +2,7 @@
 // kernels of the two-tier sparse-attention step.
 #pragma once
 
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include <atomic>

@@ -3,7 +3,7 @@
 // "Two-tier sparse attention": a candidate stage over "blocks of 8"; the mean
 // is the block-key rule this library fixes), summed in fp32 in member order,
 // divided by the member count in fp32 and stored in the keys' own format:
-// bf16 round-to-nearest-even, or MXFP8 by the OCP MX v1.0 conversion.
+// bf16 round-to-nearest-even, or MXFP8 / MXFP4 by the OCP MX v1.0 conversion.
 #include "kernels.h"
 
 namespace dsa {
@@ -20,6 +20,23 @@ __device__ __forceinline__ void load4(int fmt, const void* key_data, const uint8
     x[1] = bf16_bits_to_float(v.x >> 16);
     x[2] = bf16_bits_to_float(v.y & 0xFFFF);
     x[3] = bf16_bits_to_float(v.y >> 16);
+  } else if (fmt == DSA_FMT_MXFP4) {
+    // bytes 2 lane, 2 lane + 1 of the 64-byte row: elements 4 lane .. 4 lane + 3
+    const uint8_t* k = static_cast<const uint8_t*>(key_data);
+    const uint32_t codes = *reinterpret_cast<const uint16_t*>(k + row * 64 + lane * 2);
+    const int sc = key_scales[row * 4 + (lane >> 3)];
+    const float f = __uint_as_float(sc == 0 ? 0x00400000u : static_cast<uint32_t>(sc) << 23);
+    // e2m1 -> f16 -> f32 is exact, and so is the power-of-two scaling.
+    const __half2_raw h01 = __nv_cvt_fp4x2_to_halfraw2(
+        static_cast<__nv_fp4x2_storage_t>(codes & 0xFF), __NV_E2M1);
+    const __half2_raw h23 = __nv_cvt_fp4x2_to_halfraw2(
+        static_cast<__nv_fp4x2_storage_t>(codes >> 8), __NV_E2M1);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    x[0] = f01.x * f;
+    x[1] = f01.y * f;
+    x[2] = f23.x * f;
+    x[3] = f23.y * f;
   } else {
     const uint8_t* k = static_cast<const uint8_t*>(key_data);
     const uint32_t codes = *reinterpret_cast<const uint32_t*>(k + row * 128 + lane * 4);
@@ -64,8 +81,9 @@ __device__ __forceinline__ void block_mean(int fmt, const void* key_data, const 
 }
 
 // Rounds a warp's 128 fp32 values to the key format. Returns the packed
-// storage (bf16: 2 words; MXFP8: 1 word of codes + the group's scale byte)
-// and, in `dec`, the stored values decoded back to fp32 (exact).
+// storage (bf16: 2 words; MXFP8: 1 word of codes, MXFP4: 16 bits of codes,
+// + the group's scale byte) and, in `dec`, the stored values decoded back to
+// fp32 (exact).
 struct Stored {
   uint32_t w0, w1;
   uint8_t scale;
@@ -83,8 +101,9 @@ __device__ __forceinline__ Stored round_to_format(int fmt, const float (&v)[4], 
     st.w1 = h[2] | (static_cast<uint32_t>(h[3]) << 16);
     return st;
   }
-  // Group of 32 values = 8 lanes: X = floor(log2(amax)) - 8, clamped to
-  // [-127, 127]; an all-zero group takes X = 0.
+  // Group of 32 values = 8 lanes: X = floor(log2(amax)) - emax (8 for e4m3,
+  // 2 for e2m1), clamped to [-127, 127]; an all-zero group takes X = 0.
+  const int emax = fmt == DSA_FMT_MXFP4 ? 2 : 8;
   float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
   for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
@@ -93,13 +112,27 @@ __device__ __forceinline__ Stored round_to_format(int fmt, const float (&v)[4], 
     X = 0;
   } else {
     const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
-    X = (e == 0) ? -127 : max(-127, e - 127 - 8);
+    X = (e == 0) ? -127 : max(-127, e - 127 - emax);
   }
-  // v * 2^-X is exact (a power-of-two scaling); then e4m3, nearest-even,
-  // saturating to +-448.
-  const int ex = 127 - X;  // biased exponent of 2^-X, in [0, 254]
+  // v * 2^-X is exact (a power-of-two scaling); then the element format,
+  // nearest-even, saturating (e4m3 to +-448, e2m1 to +-6).
+  const int ex = 127 - X;  // biased exponent of 2^-X, in [2, 254]
   const float inv = __uint_as_float(ex == 0 ? 0x00400000u : static_cast<uint32_t>(ex) << 23);
   const float back = __uint_as_float(X + 127 == 0 ? 0x00400000u : static_cast<uint32_t>(X + 127) << 23);
+  st.scale = static_cast<uint8_t>(X + 127);
+  if (fmt == DSA_FMT_MXFP4) {
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const float2 pr = make_float2(v[e] * inv, v[e + 1] * inv);
+      const __nv_fp4x2_storage_t q = __nv_cvt_float2_to_fp4x2(pr, __NV_E2M1, cudaRoundNearest);
+      st.w0 |= static_cast<uint32_t>(q) << (8 * (e >> 1));
+      const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2(q, __NV_E2M1);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      dec[e] = f.x * back;
+      dec[e + 1] = f.y * back;
+    }
+    return st;
+  }
 #pragma unroll
   for (int e = 0; e < 4; e += 2) {
     const float2 pr = make_float2(v[e] * inv, v[e + 1] * inv);
@@ -110,7 +143,6 @@ __device__ __forceinline__ Stored round_to_format(int fmt, const float (&v)[4], 
     dec[e] = f.x * back;
     dec[e + 1] = f.y * back;
   }
-  st.scale = static_cast<uint8_t>(X + 127);
   return st;
 }
 
@@ -146,7 +178,11 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
     *reinterpret_cast<uint2*>(o + orow * 128 + lane * 4) = make_uint2(st.w0, st.w1);
   } else {
     uint8_t* o = static_cast<uint8_t*>(a.out_data);
-    *reinterpret_cast<uint32_t*>(o + orow * 128 + lane * 4) = st.w0;
+    if (a.fmt == DSA_FMT_MXFP4) {
+      *reinterpret_cast<uint16_t*>(o + orow * 64 + lane * 2) = static_cast<uint16_t>(st.w0);
+    } else {
+      *reinterpret_cast<uint32_t*>(o + orow * 128 + lane * 4) = st.w0;
+    }
     if ((lane & 7) == 0) a.out_scales[orow * 4 + (lane >> 3)] = st.scale;
   }
 }

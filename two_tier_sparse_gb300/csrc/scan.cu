@@ -12,11 +12,14 @@
 // (query, tile) pairs, with four tiles in flight in tensor memory. Tiles
 // alternate between two halves of the CTA (tile i belongs to half i % 2), and
 // each half has its own producer warp and load ring: small gathered boxes
-// stream at about twice the rate with two independent producers per SM.
-//   warps 0-1  producers: TMA tiled loads (128-byte swizzle) of the tile's
-//              key rows: one box of 128 rows for block keys or a plain latent
-//              range, one box of 8 rows per candidate block otherwise; MXFP8
-//              scales (4 bytes a row) come with the tile: one bulk copy for a
+// stream at about twice the rate with two independent producers per SM. A
+// ring stage holds TPS of its half's tiles behind one TMA barrier (1 for bf16
+// keys, whose tiles are 32 KB; 2 or 4 for the narrower MXFP8 and MXFP4 tiles)
+// because a TMA ring streams HBM fastest with about 32 KB per barrier.
+//   warps 0-1  producers: TMA tiled loads (128-byte swizzle) of the tiles' key
+//              rows: one box of 128 rows for block keys or a plain latent
+//              range, one box of 8 rows per candidate block otherwise; MX
+//              scales (4 bytes a row) come with the tiles: one bulk copy for a
 //              contiguous tile, two 16-byte cp.async per gathered block;
 //   warps 2, 11 MMA issuers, one per half: 8 MMAs (K = 128) per tile (a
 //              barrier wait costs a single thread a few hundred cycles, so
@@ -24,14 +27,18 @@
 //   warps 3-10 two math sets of four warps, set k for half k.
 //              Thread = TMEM lane = key row of the tile.
 // bf16 keys: the swizzled raw tile is the MMA's A operand as loaded.
-// MXFP8 keys (e4m3 codes + one UE8M0 scale per 32 values): each math thread
-// converts its own row code by code to f16 (exact: every e4m3 value is an
-// f16 normal) and writes it into tensor memory, where the MMA reads A; each
-// 32-wide group gets its own accumulator (4 x 16 TMEM columns), so the
-// power-of-two scales are applied exactly in the epilogue. The index query is
-// taken to f16 with a power-of-two scale per head that puts its largest
-// element in [2^14, 2^15), which keeps every bf16 element exact unless it is
-// below 2^-31 of its head's largest.
+// MXFP8 keys (e4m3 codes + one UE8M0 scale per 32 values) and MXFP4 keys
+// (e2m1 codes two a byte + one UE8M0 scale per 32 values): each math thread
+// converts its own row code by code to f16 (exact: every e4m3 and every e2m1
+// value is an f16 normal or zero) and writes it into tensor memory, where the
+// MMA reads A; each 32-wide group gets its own accumulator (4 x 16 TMEM
+// columns), so the power-of-two scales are applied exactly in the epilogue.
+// An MXFP4 row is 64 bytes: the TMA sees the key array as rows of 128 bytes
+// (two keys each), so a 128-key tile is a box of 64 such rows and a gathered
+// block of 8 keys a box of 4. The index query is taken to f16 with a
+// power-of-two scale per head that puts its largest element in [2^14, 2^15),
+// which keeps every bf16 element exact unless it is below 2^-31 of its head's
+// largest.
 // The epilogue of tile i - 4 runs before tile i is prepared and writes
 // score = sum_h w_h * max(0, dot_h), summed in head order.
 #include <type_traits>
@@ -56,8 +63,8 @@ struct Plan;
 template <>
 struct Plan<DSA_FMT_BF16> {
   static constexpr int kRowBytes = 256;
-  static constexpr int kStages = 3;                // per half
-  static constexpr int kStageBytes = kTile * 256;  // 2 K-atoms x 128 rows x 128 B
+  static constexpr int kCodeBytes = kTile * 256;  // 2 K-atoms x 128 rows x 128 B
+  static constexpr int kScaleBytes = 0;
   static constexpr int kAccCols = 16;
   static constexpr int kSlotCols = 16;             // accumulator only
   static constexpr int kTmemCols = 64;
@@ -65,12 +72,46 @@ struct Plan<DSA_FMT_BF16> {
 template <>
 struct Plan<DSA_FMT_MXFP8> {
   static constexpr int kRowBytes = 128;
-  static constexpr int kStages = 5;  // per half
-  static constexpr int kStageBytes = kTile * 128 + kTile * 4;  // codes (swizzled), scales
+  static constexpr int kCodeBytes = kTile * 128;  // codes, swizzled
+  static constexpr int kScaleBytes = kTile * 4;
   static constexpr int kAccCols = 64;    // 4 groups x 16 heads
   static constexpr int kSlotCols = 128;  // A operand (64 columns of f16 pairs) + accumulator
   static constexpr int kTmemCols = 512;
 };
+template <>
+struct Plan<DSA_FMT_MXFP4> {
+  static constexpr int kRowBytes = 64;
+  static constexpr int kCodeBytes = kTile * 64;   // 64 rows of two keys, swizzled
+  static constexpr int kScaleBytes = kTile * 4;
+  static constexpr int kAccCols = 64;
+  static constexpr int kSlotCols = 128;
+  static constexpr int kTmemCols = 512;
+};
+
+// Tiles per ring stage of a gathered (token-stage) scan over MX keys.
+#ifndef DSA_SCAN_GATHER_TPS
+#define DSA_SCAN_GATHER_TPS 2
+#endif
+
+// A ring stage: TPS tiles' codes (each 1024-byte aligned, as the 128-byte
+// swizzle wants), then their scales; stages per half as shared memory allows.
+template <int FMT, int TPS>
+struct Ring {
+  using P = Plan<FMT>;
+  static constexpr int kTPS = TPS;
+  static constexpr int kStageBytes = TPS * (P::kCodeBytes + P::kScaleBytes);
+  static constexpr int kRawStride = (kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = FMT == DSA_FMT_BF16 ? 3 : (TPS == 1 ? 5 : (TPS == 2 ? 3 : 2));
+  __device__ static uint32_t codes(uint32_t stage, int t) {
+    return stage + static_cast<uint32_t>(t * P::kCodeBytes);
+  }
+  __device__ static uint32_t scales(uint32_t stage, int t) {
+    return stage + static_cast<uint32_t>(TPS * P::kCodeBytes + t * P::kScaleBytes);
+  }
+};
+
+constexpr int kMaxStages = 5;
+constexpr int kMaxTPS = 4;
 
 struct TileMeta {
   uint32_t valid[4];  // row r holds a key
@@ -82,26 +123,29 @@ struct QSlot {
 };
 
 struct Shared {
-  uint64_t raw_full[2][6], raw_empty[2][6];
+  uint64_t raw_full[2][kMaxStages], raw_empty[2][kMaxStages];
   uint64_t op_full[kSlots], acc_full[kSlots];
   uint32_t tmem_base;
   int abort;
-  TileMeta meta[2][6];
+  TileMeta meta[2][kMaxStages][kMaxTPS];
   QSlot qs[2][kQRing];
 };
 
-template <int FMT>
+template <int FMT, int TPS>
 struct Layout {
-  using P = Plan<FMT>;
-  static constexpr int kRawStride = (P::kStageBytes + 1023) / 1024 * 1024;
-  static constexpr int kRaw = 0;                                // [half][stage]
-  static constexpr int kQ = kRaw + 2 * P::kStages * kRawStride;  // [set][ring] x 4 KB B operands
+  using R = Ring<FMT, TPS>;
+  static_assert(R::kStages <= kMaxStages && TPS <= kMaxTPS, "ring plan");
+  static constexpr int kRaw = 0;                                    // [half][stage]
+  static constexpr int kQ = kRaw + 2 * R::kStages * R::kRawStride;  // [set][ring] x 4 KB B operands
   static constexpr int kShared = kQ + 2 * kQRing * 4096;
   static constexpr int kBytes = kShared + static_cast<int>(sizeof(Shared));
+  static_assert(kBytes + 1024 <= 232448, "shared memory");
 };
 
 struct Maps {
-  CUtensorMap keys;  // bf16: {128 elems, rows}, box {64, R}; MXFP8: {128 B, rows}, box {128, R}
+  // bf16: {128 elems, rows}, box {64, R}; MXFP8: {128 B, rows}, box {128, R};
+  // MXFP4: {128 B, rows / 2} (two keys a row), box {128, R / 2}
+  CUtensorMap keys;
 };
 
 __device__ __forceinline__ int visible_latents(const ScanArgs& a, int b) {
@@ -123,8 +167,8 @@ __device__ __forceinline__ int64_t contiguous_rows(const ScanArgs& a, int n_vis)
 }
 
 // Position of a CTA's tile: query b and first row r0 of that query's rows.
-// Tiles advance by a fixed step without divisions (the step is at most two
-// tiles, so at most two queries are crossed).
+// Tiles advance by a small fixed step (at most 2 x TPS tiles) without
+// divisions.
 struct TilePos {
   int b;
   int64_t r0;
@@ -141,149 +185,215 @@ struct TilePos {
   }
 };
 
-template <int FMT>
+template <int FMT, int TPS>
 __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32_t sbase,
                          int64_t t_begin, int64_t n_tiles, int64_t tpq, int half) {
   using P = Plan<FMT>;
-  using Lo = Layout<FMT>;
+  using R = Ring<FMT, TPS>;
+  using Lo = Layout<FMT, TPS>;
   const int lane = threadIdx.x & 31;
   if (lane == 0) tma_prefetch_map(&maps.keys);
-  if (half >= n_tiles) return;
+  const int64_t n_own = n_tiles > half ? (n_tiles - half + 1) / 2 : 0;  // tiles half, half + 2, ...
+  if (n_own == 0) return;
   const int64_t q_rows = tpq * kTile;
   const bool gather = a.mode == ROWS_GATHER;
-  // MXFP8 scales of 8 (gathered block) or 128 (contiguous tile) consecutive
-  // rows are 32 or 512 contiguous bytes, copied whole when 16-byte aligned.
+  // MX scales of 8 (gathered block) or 128 (contiguous tile) consecutive rows
+  // are 32 or 512 contiguous bytes, copied whole when 16-byte aligned.
   const bool scale_vec =
       ((reinterpret_cast<uintptr_t>(a.key_scales) | static_cast<uintptr_t>(a.key_stride * 4)) &
        15u) == 0;
-  TilePos pos, nxt;
-  pos.init(t_begin + half, tpq);
-  nxt = pos;
-  // Gathered mode: lane j < 16 holds the j-th block id of a tile; the ids of
-  // the half's next tile are loaded one iteration ahead.
-  auto fetch_block = [&](const TilePos& tp, bool exists) -> int {
-    if (!gather || lane >= kTile / kBlock || !exists) return -1;
-    const int64_t bi = (tp.r0 >> 3) + lane;
-    if (bi >= a.k_blocks) return -1;
-    return a.block_ids[static_cast<int64_t>(tp.b) * a.k_blocks + bi];
+  // Gathered mode: in round k lane l serves block slot l % 16 of the stage's
+  // tile 2k + l / 16 (16 candidate blocks of 8 keys per tile). Block ids of the
+  // next stage are loaded one stage ahead.
+  constexpr int kRounds = (TPS * 16 + 31) / 32;
+  auto fetch_blocks = [&](const TilePos& first, int64_t j0, int (&ids)[kRounds]) {
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+      const int t = 2 * k + (lane >> 4);
+      ids[k] = -1;
+      if (!gather || t >= TPS || j0 + t >= n_own) continue;
+      TilePos tp = first;
+      tp.advance(2 * t, q_rows);
+      const int64_t bi = (tp.r0 >> 3) + (lane & 15);
+      if (bi < a.k_blocks) ids[k] = a.block_ids[static_cast<int64_t>(tp.b) * a.k_blocks + bi];
+    }
   };
-  int blk_next = fetch_block(pos, true);
-  int nv_b = -1, n_vis = 0;
+  TilePos first;  // the stage's first tile
+  first.init(t_begin + half, tpq);
+  int blk[kRounds];
+  fetch_blocks(first, 0, blk);
+  // Visible latents of a query, cached for the last query asked about: a
+  // lane's tiles move through the queries in order.
+  int nv_b = -1, nv = 0;
+  auto n_vis_of = [&](int b) -> int {
+    if (b != nv_b) {
+      nv = visible_latents(a, b);
+      nv_b = b;
+    }
+    return nv;
+  };
   int s = 0;           // stage of this iteration
   uint32_t kpar = 0;   // parity of the stage's use count
-  for (int64_t i = half, j = 0; i < n_tiles; i += 2, ++j) {
-    const int blk = blk_next;
-    nxt.advance(2, q_rows);
-    blk_next = fetch_block(nxt, i + 2 < n_tiles);
-    if (j >= P::kStages &&
+  for (int64_t j0 = 0; j0 < n_own; j0 += TPS) {
+    TilePos next = first;
+    next.advance(2 * TPS, q_rows);
+    int blk_next[kRounds];
+    fetch_blocks(next, j0 + TPS, blk_next);
+    if (j0 >= static_cast<int64_t>(TPS) * R::kStages &&
         !mbar_wait_abortable(&sh.raw_empty[half][s], kpar ^ 1u, &sh.abort, a.status, SITE_SCAN)) {
       return;
     }
-    const int b = pos.b;
-    const int64_t r0 = pos.r0;
-    if (b != nv_b) {
-      n_vis = visible_latents(a, b);
-      nv_b = b;
-    }
-    const int64_t seq = static_cast<int64_t>(b) * a.key_stride;
-    const uint32_t raw = sbase + Lo::kRaw + (half * P::kStages + s) * Lo::kRawStride;
-    uint32_t vm[4];
-    uint32_t bytes;
+    const uint32_t stage = sbase + Lo::kRaw + (half * R::kStages + s) * R::kRawStride;
+    uint64_t* full = &sh.raw_full[half][s];
     if (gather) {
-      // This lane's block: rows [8 lane, 8 lane + nrows) of the tile.
-      int nrows = 0;
-      int64_t y = 0;
-      if (blk >= 0) {
-        const int64_t t0 = static_cast<int64_t>(blk) * kBlock;
-        const int64_t v = n_vis - t0;
-        if (v > 0) {
-          nrows = static_cast<int>(v < kBlock ? v : kBlock);
-          y = seq + t0;
+      int nrows[kRounds];
+      int64_t y[kRounds];
+      uint32_t vm[kRounds][4];
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int k = 0; k < kRounds; ++k) {
+        const int t = 2 * k + (lane >> 4);
+        nrows[k] = 0;
+        y[k] = 0;
+        if (blk[k] >= 0) {
+          TilePos tp = first;
+          tp.advance(2 * t, q_rows);
+          const int64_t t0 = static_cast<int64_t>(blk[k]) * kBlock;
+          const int64_t v = n_vis_of(tp.b) - t0;
+          if (v > 0) {
+            nrows[k] = static_cast<int>(v < kBlock ? v : kBlock);
+            y[k] = static_cast<int64_t>(tp.b) * a.key_stride + t0;
+          }
+        }
+        const int row0 = (lane & 15) * kBlock;
+        bytes += nrows[k] > 0 ? kBlock * P::kRowBytes : 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) vm[k][w] = range_bits(w, row0, row0 + nrows[k]);
+        // the tile's rows: OR over its 16 lanes
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) vm[k][w] |= __shfl_xor_sync(0xFFFFFFFFu, vm[k][w], o);
         }
       }
-      const int row0 = lane * kBlock;
-      bytes = nrows > 0 ? kBlock * P::kRowBytes : 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) vm[k] = range_bits(k, row0, row0 + nrows);
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, o);
+      // lane 0 records every tile's rows (tile 2k + 1's come from lane 16)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, o);
+      for (int k = 0; k < kRounds; ++k) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) vm[k] |= __shfl_xor_sync(0xFFFFFFFFu, vm[k], o);
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t hi = __shfl_sync(0xFFFFFFFFu, vm[k][w], 16);
+          if (lane == 0) {
+            sh.meta[half][s][2 * k].valid[w] = vm[k][w];
+            if (2 * k + 1 < TPS) sh.meta[half][s][2 * k + 1].valid[w] = hi;
+          }
+        }
       }
-      if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = vm[k];
-        mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
-      if (nrows > 0) {
+#pragma unroll
+      for (int k = 0; k < kRounds; ++k) {
+        if (nrows[k] <= 0) continue;
+        const int t = 2 * k + (lane >> 4);
+        const int row0 = (lane & 15) * kBlock;
+        const uint32_t codes = R::codes(stage, t);
         if constexpr (FMT == DSA_FMT_BF16) {
           // two K halves (64 elements = 128 bytes each) into the two K-atoms
-          tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
-          tma_load_2d(raw + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y),
-                      &sh.raw_full[half][s]);
+          tma_load_2d(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full);
+          tma_load_2d(codes + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y[k]),
+                      full);
         } else {
-          tma_load_2d(raw + row0 * 128, &maps.keys, 0, static_cast<int>(y), &sh.raw_full[half][s]);
-          const uint32_t sc_dst = raw + kTile * 128 + row0 * 4;
-          const uint8_t* sc_src = a.key_scales + y * 4;
-          if (scale_vec && nrows == kBlock) {
+          if constexpr (FMT == DSA_FMT_MXFP8) {
+            tma_load_2d(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full);
+          } else {
+            tma_load_2d(codes + row0 * 64, &maps.keys, 0, static_cast<int>(y[k] >> 1), full);
+          }
+          const uint32_t sc_dst = R::scales(stage, t) + row0 * 4;
+          const uint8_t* sc_src = a.key_scales + y[k] * 4;
+          if (scale_vec && nrows[k] == kBlock) {
             cp_async_16(sc_dst, sc_src);
             cp_async_16(sc_dst + 16, sc_src + 16);
           } else {
-            for (int r = 0; r < nrows; ++r) cp_async_4(sc_dst + r * 4, sc_src + r * 4);
+            for (int r = 0; r < nrows[k]; ++r) cp_async_4(sc_dst + r * 4, sc_src + r * 4);
           }
         }
       }
     } else {
-      // Contiguous rows: uniform across the warp, lane 0 issues.
-      int64_t v = contiguous_rows(a, n_vis) - r0;
-      v = v < 0 ? 0 : (v > kTile ? kTile : v);
-      const int nrows = static_cast<int>(v);
-      const bool bulk_sc = FMT == DSA_FMT_MXFP8 && scale_vec && nrows == kTile;
-      bytes = (nrows > 0 ? kTile * P::kRowBytes : 0) + (bulk_sc ? kTile * 4 : 0);
+      // Contiguous rows: the same values in every lane; lane 0 issues the boxes.
+      int nrows[TPS];
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int t = 0; t < TPS; ++t) {
+        nrows[t] = 0;
+        if (j0 + t < n_own) {
+          TilePos tp = first;
+          tp.advance(2 * t, q_rows);
+          int64_t v = contiguous_rows(a, n_vis_of(tp.b)) - tp.r0;
+          v = v < 0 ? 0 : (v > kTile ? kTile : v);
+          nrows[t] = static_cast<int>(v);
+        }
+        const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
+        bytes += (nrows[t] > 0 ? P::kCodeBytes : 0) + (bulk_sc ? P::kScaleBytes : 0);
+      }
       if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sh.meta[half][s].valid[k] = range_bits(k, 0, nrows);
-        mbar_arrive_expect_tx(&sh.raw_full[half][s], bytes);
-        if (nrows > 0) {
-          const int yy = static_cast<int>(seq + r0);
+        for (int t = 0; t < TPS; ++t) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) sh.meta[half][s][t].valid[w] = range_bits(w, 0, nrows[t]);
+        }
+        mbar_arrive_expect_tx(full, bytes);
+      }
+#pragma unroll
+      for (int t = 0; t < TPS; ++t) {
+        if (nrows[t] == 0) continue;
+        TilePos tp = first;
+        tp.advance(2 * t, q_rows);
+        const int64_t row = static_cast<int64_t>(tp.b) * a.key_stride + tp.r0;
+        const uint32_t codes = R::codes(stage, t);
+        const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
+        if (lane == 0) {
           if constexpr (FMT == DSA_FMT_BF16) {
-            tma_load_2d(raw, &maps.keys, 0, yy, &sh.raw_full[half][s]);
-            tma_load_2d(raw + kTile * 128, &maps.keys, 64, yy, &sh.raw_full[half][s]);
+            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row), full);
+            tma_load_2d(codes + kTile * 128, &maps.keys, 64, static_cast<int>(row), full);
+          } else if constexpr (FMT == DSA_FMT_MXFP8) {
+            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row), full);
           } else {
-            tma_load_2d(raw, &maps.keys, 0, yy, &sh.raw_full[half][s]);
-            if (bulk_sc) {
-              bulk_g2s(raw + kTile * 128, a.key_scales + (seq + r0) * 4, kTile * 4,
-                       &sh.raw_full[half][s]);
+            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row >> 1), full);
+          }
+          if (bulk_sc) bulk_g2s(R::scales(stage, t), a.key_scales + row * 4, P::kScaleBytes, full);
+        }
+        if constexpr (FMT != DSA_FMT_BF16) {
+          if (!bulk_sc) {
+            // lane l copies the scales of rows l, l + 32, l + 64, l + 96
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = lane + 32 * k;
+              if (r < nrows[t]) {
+                cp_async_4(R::scales(stage, t) + r * 4, a.key_scales + (row + r) * 4);
+              }
             }
           }
         }
       }
-      if constexpr (FMT == DSA_FMT_MXFP8) {
-        if (!bulk_sc) {
-          // lane l copies the scales of rows l, l + 32, l + 64, l + 96
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = lane + 32 * k;
-            if (r < nrows) cp_async_4(raw + kTile * 128 + r * 4, a.key_scales + (seq + r0 + r) * 4);
-          }
-        }
-      }
     }
-    cp_async_mbar_arrive_noinc(&sh.raw_full[half][s]);
-    pos = nxt;
-    if (++s == P::kStages) {
+    cp_async_mbar_arrive_noinc(full);
+    first = next;
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) blk[k] = blk_next[k];
+    if (++s == R::kStages) {
       s = 0;
       kpar ^= 1u;
     }
   }
 }
 
-template <int FMT>
+template <int FMT, int TPS>
 __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_tiles, int set) {
   using P = Plan<FMT>;
-  using Lo = Layout<FMT>;
+  using R = Ring<FMT, TPS>;
+  using Lo = Layout<FMT, TPS>;
+  static_assert(FMT != DSA_FMT_BF16 || TPS == 1, "bf16 tiles are read by the MMA, one a stage");
   constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, FMT == DSA_FMT_BF16, false, false);
   const uint32_t tmem = sh.tmem_base;
   int ring = 0;   // index-query ring slot of the set's tile i (advances per own tile)
@@ -300,7 +410,7 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
     const uint64_t bd0 = sw128_desc(qb, 16, 1024);
     const uint32_t slot = tmem + q * P::kSlotCols;
     if constexpr (FMT == DSA_FMT_BF16) {
-      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + stage) * Lo::kRawStride;
+      const uint32_t raw = sbase + Lo::kRaw + (set * R::kStages + stage) * R::kRawStride;
       const uint64_t ad0 = sw128_desc(raw, 16, 1024);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {  // K = 128 in steps of 16
@@ -321,15 +431,15 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
       mma_commit(&sh.acc_full[q]);
     }
     if (++ring == kQRing) ring = 0;
-    if (++stage == P::kStages) stage = 0;
+    if (++stage == R::kStages) stage = 0;
   }
 }
 
 // Index query of query b -> ring slot [set][ring] (one math set, 128 threads).
-template <int FMT>
+template <int FMT, int TPS>
 __device__ void build_query(const ScanArgs& a, Shared& sh, uint32_t sbase, int b, int mt,
                             int set, int ring) {
-  using Lo = Layout<FMT>;
+  using Lo = Layout<FMT, TPS>;
   const uint16_t* q = a.q_idx + static_cast<int64_t>(b) * kIdxHeads * kIdxDim;
   const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
   QSlot& slot = sh.qs[set][ring];
@@ -379,11 +489,12 @@ __device__ void build_query(const ScanArgs& a, Shared& sh, uint32_t sbase, int b
   }
 }
 
-template <int FMT>
+template <int FMT, int TPS>
 __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_begin,
                      int n_tiles, int64_t tpq) {
   using P = Plan<FMT>;
-  using Lo = Layout<FMT>;
+  using R = Ring<FMT, TPS>;
+  using Lo = Layout<FMT, TPS>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int set = (warp - kMathWarp0) >> 2;               // tiles i with i % 2 == set
   const int mt = threadIdx.x - 32 * kMathWarp0 - kMathThreads * set;  // 0..127 within the set
@@ -398,7 +509,9 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
   TilePos prep, epi;  // positions of this set's next prepared and next finished tile
   prep.init(t_begin + set, tpq);
   epi = prep;
-  int ring = 0, stage = 0;       // of the tile being prepared (advance per own tile)
+  int ring = 0;                  // of the tile being prepared (advances per own tile)
+  int stage = 0;                 // ring stage of the tile being prepared (advances per TPS
+  uint32_t spar = 0;             // own tiles) and the parity of that stage's use
   int ring_e = 0;                // of the tile being finished
 
   auto epilogue = [&](int e) -> bool {
@@ -448,16 +561,17 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
 
   // Own tiles i = set, set + 2, ...: the epilogue of tile i - 4 (which shares
   // tile i's pending entry and TMEM slot), then the preparation of tile i.
-  // The loop is unrolled by two own tiles so that the two pending entries
-  // (parity pi) are distinct registers: the MXFP8 scale load issued here is
-  // first used two own tiles later and its latency stays hidden.
-  auto own_tile = [&](int i, auto pic) -> bool {
+  // The loop is unrolled by U = max(2, TPS) own tiles so that the two pending
+  // entries (parity pi) are distinct registers (the MX scale load issued here
+  // is first used two own tiles later and its latency stays hidden) and the
+  // tile's place t in its ring stage is known at compile time.
+  auto own_tile = [&](int i, auto pic, auto tc) -> bool {
     constexpr int pi = decltype(pic)::value;
+    constexpr int t = decltype(tc)::value;
     if (i >= 4 && i - 4 < n_tiles) {
       if (!epilogue(i - 4)) return false;
     }
     if (i >= n_tiles) return true;
-    const int s = stage;
     const int q = i & (kSlots - 1);
     const int b = prep.b;
     const int held = ring == 0 ? ring_b0 : (ring == 1 ? ring_b1 : ring_b2);
@@ -465,48 +579,69 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       // The ring slot last served tile i - 6, whose epilogue every thread of
       // the set has finished once all of them reach this barrier.
       named_sync(1 + set, kMathThreads);
-      build_query<FMT>(a, sh, sbase, b, mt, set, ring);
+      build_query<FMT, TPS>(a, sh, sbase, b, mt, set, ring);
       fence_proxy_async_smem();
       named_sync(1 + set, kMathThreads);
       if (ring == 0) ring_b0 = b; else if (ring == 1) ring_b1 = b; else ring_b2 = b;
     }
-    if (!mbar_wait_abortable(&sh.raw_full[set][s],
-                             static_cast<uint32_t>(((i >> 1) / P::kStages) & 1), &sh.abort,
-                             a.status, SITE_SCAN)) {
+    if (t == 0 && !mbar_wait_abortable(&sh.raw_full[set][stage], spar, &sh.abort, a.status,
+                                       SITE_SCAN)) {
       return false;
     }
-    const TileMeta& m = sh.meta[set][s];
+    const TileMeta& m = sh.meta[set][stage][t];
     const bool valid_i = (m.valid[row >> 5] >> (row & 31)) & 1u;
     if constexpr (pi) pend_valid1 = valid_i; else pend_valid0 = valid_i;
-    if constexpr (FMT == DSA_FMT_MXFP8) {
-      const uint32_t raw = sbase + Lo::kRaw + (set * P::kStages + s) * Lo::kRawStride;
+    if constexpr (FMT != DSA_FMT_BF16) {
+      const uint32_t st_base = sbase + Lo::kRaw + (set * R::kStages + stage) * R::kRawStride;
+      const uint32_t raw = R::codes(st_base, t);
       // The A slot of tile i was last read by the MMA of tile i - 4, which the
       // epilogue above has already seen complete (its acc_full commit).
-      // own row: 8 chunks of 16 codes at their swizzled positions
+      // Own row to f16 pairs: word j holds elements 2j, 2j + 1.
       uint32_t f[64];
+      if constexpr (FMT == DSA_FMT_MXFP8) {
+        // 8 chunks of 16 codes at their swizzled positions
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = ld_shared_v4(raw + sw128_off(row, c));
-        asm("{\n .reg .b16 a, b, c, d, e, f, g, h;\n"
-            " mov.b32 {a, b}, %8;\n mov.b32 {c, d}, %9;\n"
-            " mov.b32 {e, f}, %10;\n mov.b32 {g, h}, %11;\n"
-            " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
-            " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n"
-            " cvt.rn.f16x2.e4m3x2 %4, e;\n cvt.rn.f16x2.e4m3x2 %5, f;\n"
-            " cvt.rn.f16x2.e4m3x2 %6, g;\n cvt.rn.f16x2.e4m3x2 %7, h;\n}\n"
-            : "=r"(f[8 * c + 0]), "=r"(f[8 * c + 1]), "=r"(f[8 * c + 2]), "=r"(f[8 * c + 3]),
-              "=r"(f[8 * c + 4]), "=r"(f[8 * c + 5]), "=r"(f[8 * c + 6]), "=r"(f[8 * c + 7])
-            : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = ld_shared_v4(raw + sw128_off(row, c));
+          asm("{\n .reg .b16 a, b, c, d, e, f, g, h;\n"
+              " mov.b32 {a, b}, %8;\n mov.b32 {c, d}, %9;\n"
+              " mov.b32 {e, f}, %10;\n mov.b32 {g, h}, %11;\n"
+              " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
+              " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n"
+              " cvt.rn.f16x2.e4m3x2 %4, e;\n cvt.rn.f16x2.e4m3x2 %5, f;\n"
+              " cvt.rn.f16x2.e4m3x2 %6, g;\n cvt.rn.f16x2.e4m3x2 %7, h;\n}\n"
+              : "=r"(f[8 * c + 0]), "=r"(f[8 * c + 1]), "=r"(f[8 * c + 2]), "=r"(f[8 * c + 3]),
+                "=r"(f[8 * c + 4]), "=r"(f[8 * c + 5]), "=r"(f[8 * c + 6]), "=r"(f[8 * c + 7])
+              : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+        }
+      } else {
+        // the row is half of 128-byte row row / 2: its 4 chunks of 32 codes
+        // (two a byte, element 2j in the low nibble of byte j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = ld_shared_v4(raw + sw128_off(row >> 1, 4 * (row & 1) + c));
+          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            asm("{\n .reg .b8 a, b, c, d;\n mov.b32 {a, b, c, d}, %4;\n"
+                " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n"
+                " cvt.rn.f16x2.e2m1x2 %2, c;\n cvt.rn.f16x2.e2m1x2 %3, d;\n}\n"
+                : "=r"(f[16 * c + 4 * k + 0]), "=r"(f[16 * c + 4 * k + 1]),
+                  "=r"(f[16 * c + 4 * k + 2]), "=r"(f[16 * c + 4 * k + 3])
+                : "r"(vw[k]));
+          }
+        }
       }
       // The row's four group scales (one 32-bit word): loaded now, used by the
-      // epilogue two own tiles later, so the global load's latency is hidden.
+      // epilogue two own tiles later, so the load's latency is hidden.
       uint32_t& sc_i = pi ? pend_sc1 : pend_sc0;
-      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sc_i) : "r"(raw + kTile * 128 + row * 4));
+      asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(sc_i) : "r"(R::scales(st_base, t) + row * 4));
       tmem_st64(tmem + lane_base + q * P::kSlotCols, f);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sh.raw_empty[set][s]);
+        // the stage is free once its last tile is converted
+        if (t == TPS - 1) mbar_arrive(&sh.raw_empty[set][stage]);
         mbar_arrive(&sh.op_full[q]);
       }
     } else {
@@ -515,21 +650,40 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     }
     prep.advance(2, q_rows);
     if (++ring == kQRing) ring = 0;
-    if (++stage == P::kStages) stage = 0;
+    if (t == TPS - 1 && ++stage == R::kStages) {
+      stage = 0;
+      spar ^= 1u;
+    }
     return true;
   };
-  // Own tiles i = set, set + 2, ... taken two at a time (parities 0, 1).
-  for (int i = set; i < n_tiles + 4; i += 4) {
-    if (!own_tile(i, std::integral_constant<int, 0>{})) return;
-    if (!own_tile(i + 2, std::integral_constant<int, 1>{})) return;
+  using I0 = std::integral_constant<int, 0>;
+  using I1 = std::integral_constant<int, 1>;
+  using I2 = std::integral_constant<int, 2>;
+  using I3 = std::integral_constant<int, 3>;
+  if constexpr (TPS <= 2) {
+    // Own tiles taken two at a time (parities 0, 1; stage places 0, TPS - 1).
+    using T1 = std::integral_constant<int, TPS - 1>;
+    for (int i = set; i < n_tiles + 4; i += 4) {
+      if (!own_tile(i, I0{}, I0{})) return;
+      if (!own_tile(i + 2, I1{}, T1{})) return;
+    }
+  } else {
+    // Four at a time: one ring stage.
+    for (int i = set; i < n_tiles + 4; i += 8) {
+      if (!own_tile(i, I0{}, I0{})) return;
+      if (!own_tile(i + 2, I1{}, I1{})) return;
+      if (!own_tile(i + 4, I0{}, I2{})) return;
+      if (!own_tile(i + 6, I1{}, I3{})) return;
+    }
   }
 }
 
-template <int FMT>
+template <int FMT, int TPS>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kernel(ScanArgs a, const __grid_constant__ Maps maps, int64_t tpq, int64_t total) {
   using P = Plan<FMT>;
-  using Lo = Layout<FMT>;
+  using R = Ring<FMT, TPS>;
+  using Lo = Layout<FMT, TPS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -544,9 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int h = 0; h < 2; ++h) {
-      for (int s = 0; s < P::kStages; ++s) {
+      for (int s = 0; s < R::kStages; ++s) {
         // raw_full: the producer's expect_tx arrival + one cp.async arrival per lane
         mbar_init(&sh.raw_full[h][s], 1 + 32);
+        // raw_empty: the MMA's commit (bf16), or the four warps of the math set
+        // once they converted the stage's last tile (MX formats)
         mbar_init(&sh.raw_empty[h][s], FMT == DSA_FMT_BF16 ? 1 : 4);
       }
     }
@@ -564,12 +720,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();  // the previous kernel's outputs (scores, ids, pooled keys) are final
 
   if (warp < kMmaWarp) {
-    producer<FMT>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
+    producer<FMT, TPS>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
   } else if (warp == kMmaWarp || warp == kMmaWarp2) {
-    if ((threadIdx.x & 31) == 0) mma_issuer<FMT>(a, sh, sbase, n_tiles, warp == kMmaWarp ? 0 : 1);
+    if ((threadIdx.x & 31) == 0) {
+      mma_issuer<FMT, TPS>(a, sh, sbase, n_tiles, warp == kMmaWarp ? 0 : 1);
+    }
     __syncwarp();
   } else {
-    math<FMT>(a, sh, sbase, t_begin, n_tiles, tpq);
+    math<FMT, TPS>(a, sh, sbase, t_begin, n_tiles, tpq);
   }
   tc_fence_before();
   __syncthreads();
@@ -579,14 +737,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int FMT>
+template <int FMT, int TPS>
 cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
-  using Lo = Layout<FMT>;
+  using Lo = Layout<FMT, TPS>;
   const int64_t tpq = (a.n_rows + kTile - 1) / kTile;
   const int64_t total = tpq * a.B;
   if (total == 0) return cudaSuccess;
   // Rows the tensor map covers: every sequence's stride, and only the last
-  // sequence's own rows (a box reaching past them reads zeros).
+  // sequence's own rows (a box reaching past them reads zeros). MXFP4 arrays
+  // are read in pairs of rows; the caller's buffer holds whole pairs.
   int64_t last_rows;
   if (a.mode == ROWS_BLOCKS) {
     last_rows = a.prefill ? a.max_latents / 8 : (a.max_latents + 7) / 8;
@@ -602,25 +761,39 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
     if (FMT == DSA_FMT_BF16) {
       e = encode_tma_2d(&maps.keys, a.key_data, /*elem_bytes=*/2, /*inner=*/128, rows,
                         /*row_bytes=*/256, /*box_inner=*/64, box_rows);
-    } else {
+    } else if (FMT == DSA_FMT_MXFP8) {
       e = encode_tma_2d(&maps.keys, a.key_data, 1, 128, rows, 128, 128, box_rows);
+    } else {
+      e = encode_tma_2d(&maps.keys, a.key_data, 1, 128, (rows + 1) / 2, 128, 128, box_rows / 2);
     }
     if (e != cudaSuccess) return e;
   }
   const int smem = Lo::kBytes + 1024;
   static std::atomic<int> smem_set[64]{};
-  e = ensure_smem(reinterpret_cast<const void*>(scan_kernel<FMT>), smem, smem_set);
+  e = ensure_smem(reinterpret_cast<const void*>(scan_kernel<FMT, TPS>), smem, smem_set);
   if (e != cudaSuccess) return e;
   const int64_t grid = total < num_sms ? total : num_sms;
-  return launch_pdl(scan_kernel<FMT>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1,
-                    a, maps, tpq, total);
+  return launch_pdl(scan_kernel<FMT, TPS>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem,
+                    s, 1, a, maps, tpq, total);
 }
 
 }  // namespace
 
+// Tiles per ring stage: bf16 tiles are 32 KB already; MXFP8 tiles (16.5 KB)
+// go two a stage and MXFP4 tiles (8.5 KB) four a stage over contiguous rows;
+// gathered scans take DSA_SCAN_GATHER_TPS MXFP8 tiles (twice as many MXFP4).
 cudaError_t launch_scan(const ScanArgs& a, int num_sms, cudaStream_t s) {
-  if (a.fmt == DSA_FMT_BF16) return launch_fmt<DSA_FMT_BF16>(a, num_sms, s);
-  return launch_fmt<DSA_FMT_MXFP8>(a, num_sms, s);
+  const bool gather = a.mode == ROWS_GATHER;
+  if (a.fmt == DSA_FMT_BF16) return launch_fmt<DSA_FMT_BF16, 1>(a, num_sms, s);
+  if (a.fmt == DSA_FMT_MXFP8) {
+    if (gather) return launch_fmt<DSA_FMT_MXFP8, DSA_SCAN_GATHER_TPS>(a, num_sms, s);
+    return launch_fmt<DSA_FMT_MXFP8, 2>(a, num_sms, s);
+  }
+  if (a.fmt == DSA_FMT_MXFP4) {
+    if (gather) return launch_fmt<DSA_FMT_MXFP4, 2 * DSA_SCAN_GATHER_TPS>(a, num_sms, s);
+    return launch_fmt<DSA_FMT_MXFP4, 4>(a, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dsa
