@@ -104,15 +104,15 @@ T* at(void* ws, size_t off) {
 dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 // Launch shape of an attention call over n queries: split-KV over the most
-// CTAs per query (8, 4 or 2) that still fit the SMs in one wave, else one;
-// 64-row tiles for prefill chunks, 32-row tiles for decode.
+// CTAs per query (8, 4 or 2) whose n clusters are all resident at once, else
+// one; 64-row tiles for prefill chunks, 32-row tiles for decode.
 void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
   (void)c;
   a.tile_rows = a.prefill ? 64 : 32;
-  const int sms = device_sm_count();
   a.splits = 1;
+  const int sms = device_sm_count();
   for (int sp = kMaxAttnSplits; sp >= 2; sp /= 2) {
-    if (static_cast<int64_t>(sp) * n <= sms) {
+    if (static_cast<int64_t>(sp) * n <= sms && n <= attn_max_clusters(sp)) {
       a.splits = sp;
       break;
     }

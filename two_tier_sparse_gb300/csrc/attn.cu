@@ -13,8 +13,9 @@
 // Warp roles: warps 0-3 math (softmax for the 64 heads by warps 0-1, one head
 // per thread; O rescaling and the epilogue by all four, thread = TMEM lane),
 // warps 4-7 loaders (warp 4 + w owns ring slot w: cp.async gathers of random
-// 1 KB rows, waited by the warp and announced on the slot's mbarrier; each
-// also loads a quarter of Q), warp 8 issues the QK^T MMAs and warp 9 the PV
+// 1 KB rows, waited by the warp and announced on the slot's mbarrier; Q comes
+// by eight TMA boxes that land in the swizzled operand layout), warp 8 issues
+// the QK^T MMAs and warp 9 the PV
 // MMAs (a barrier wait costs a single thread a few hundred cycles; two issuers
 // overlap their waits). Random rows reach shared memory
 // fastest through several slots with independent completion, hence four
@@ -31,8 +32,15 @@
 // rows and the selected latents of a query are each cut in S parts handled by
 // the S CTAs of a cluster. CTA r finishes the latent dims [r D, r D + D),
 // D = 512 / S: every CTA stores, into each peer's then idle ring (distributed
-// shared memory), its unnormalised O for that peer's dims and its (max, sum);
-// after a cluster barrier each merges its dims and writes them.
+// shared memory), its O for that peer's dims and its (max, sum); after a
+// cluster barrier each merges its dims and writes them.
+//
+// The epilogue works in chunks of 16 heads in rolled loops and writes the
+// output from registers (a warp stores 32 consecutive dims of a head at a
+// time): it runs once per CTA, so its code is fetched cold, and a compact
+// loop costs far less than a fully unrolled one.
+#include <cstddef>
+
 #include "kernels.h"
 
 namespace dsa {
@@ -71,8 +79,8 @@ constexpr int kMisc = kIds + kMaxKTokens * 4;
 constexpr int kMiscBytes = 2048;
 constexpr int kSmemBytes = kMisc + kMiscBytes + 1024;  // + alignment slack of the base
 constexpr int kTmemCols = 512;  // S[b]: cols [64 b, 64 b + 32); O^T slice m: [128 + 64 m, ...)
-constexpr uint32_t kOutBytes = kHeads * kLatent * 2;  // one query's bf16 output, [64 h][512]
-static_assert(kP - kQ == static_cast<int>(kOutBytes), "the Q region stages the output");
+constexpr uint32_t kQBytes = kHeads * kLatent * 2;  // one query's bf16 Q, 8 atoms
+static_assert(kP - kQ == static_cast<int>(kQBytes), "Q region");
 // Split-KV exchange payload from a sender to the CTA finishing dims
 // [p D, p D + D): the sender's O for those dims divided by its own sum, bf16,
 // one 128-byte row of 64 heads per dim (16-byte chunk c of row dd stored at
@@ -92,10 +100,12 @@ struct Misc {
   int abort;
   int n_sel;
   int warp_cnt[4];
-  float alpha[kHeads];
-  float inv_l[kHeads];
+  alignas(16) float alpha[kHeads];
+  alignas(16) float inv_l[kHeads];  // read four at a time (16-byte loads)
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
+static_assert(offsetof(Misc, inv_l) % 16 == 0 && kMisc % 16 == 0 && kWgt % 16 == 0,
+              "16-byte loads of inv_l and of the merge weights");
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m,
                                          DeviceStatus* st) {
@@ -103,7 +113,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
 }
 
 template <int ROWS>
-__global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                const __grid_constant__ CUtensorMap wmap) {
   using TS = TileShape<ROWS>;
   constexpr int kRows = ROWS;
   constexpr int kSlots = TS::kSlots;
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       mbar_init(&misc->p_full[i], 2);
       mbar_init(&misc->p_empty[i], 1);
     }
-    mbar_init(&misc->q_done, 128);  // every loader thread, once its quarter of Q landed
+    mbar_init(&misc->q_done, 1);    // the TMA loads of Q (expect-tx arrival + 64 KB)
     mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
     mbar_init(&misc->xchg, 1);       // the receiver's expect-tx arrival + the S - 1 copies
     misc->abort = 0;
@@ -150,12 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
   // This query's visible latents and window rows.
   int n_vis, n_sw;
   const uint16_t* win;
+  int64_t wrow0;  // row of the window buffer holding this query's first window row
   if (a.prefill) {
     const int64_t P = a.ctx + b;
     n_vis = static_cast<int>((P + 1) / a.ratio);
     const int64_t first = P - a.window + 1 > 0 ? P - a.window + 1 : 0;
     const int64_t base_pos = a.ctx - a.window + 1;
-    win = a.swa + (first - base_pos) * kLatent;
+    wrow0 = first - base_pos;
+    win = a.swa + wrow0 * kLatent;
     n_sw = static_cast<int>(P - first + 1);
   } else {
     n_vis = a.n_latents[b];
@@ -164,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       if (tid == 0 && split == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
       n_sw = n_sw < 0 ? 0 : a.window;
     }
-    win = a.swa + static_cast<int64_t>(b) * a.window * kLatent;
+    wrow0 = static_cast<int64_t>(b) * a.window;
+    win = a.swa + wrow0 * kLatent;
   }
   if (n_vis > a.lat_stride) n_vis = static_cast<int>(a.lat_stride);
   const uint16_t* lat =
@@ -196,19 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     cluster_arrive();
   };
 
-  const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * kHeads * kLatent;
-  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
-    // Q does not depend on the ids: its copies start at once (64 heads x 64
-    // chunks of 16 B, a quarter per loader warp); each loader thread reports
-    // its part on q_done once it landed.
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-      const int c = lane + 32 * (32 * (warp - kLoadWarp0) + j);
-      const int h = c >> 6, cr = c & 63;
-      cp_async_16(sbase + kQ + (cr >> 3) * (kHeads * 128) + sw128_off(h, cr & 7),
-                  qsrc + h * kLatent + cr * 8);
+  if (warp == kLoadWarp0 && lane == 0) {
+    // Q does not depend on the ids: eight boxes of 64 heads x 64 dims, each
+    // landing as one 128-byte-swizzled atom of the QK^T A operand.
+    tma_prefetch_map(&qmap);
+    mbar_arrive_expect_tx(&misc->q_done, kQBytes);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      tma_load_2d(sbase + kQ + c * (kHeads * 128), &qmap, 64 * c, b * kHeads, &misc->q_done);
     }
-    cp_async_commit();
   }
 
   // Compact the valid token ids (>= 0 and < n_vis) in order (math threads,
@@ -260,10 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     // (tiles sl, sl + kSlots, ...): it waits for its own copies of a tile,
     // fences them into the async proxy (the tensor core's view) and then
     // arrives, while the other slots' tiles are in flight. Tiles made only of
-    // window rows need no ids.
+    // window rows need no ids. A part of 32 window rows (contiguous in the
+    // window buffer) comes by eight TMA boxes instead, which complete on the
+    // slot's barrier by themselves: the warp moves on at once and leaves the
+    // cp.async path to the gathered rows.
     const int w = warp - kLoadWarp0;
     const int sl = w % kSlots, part = w / kSlots;
-    bool q_reported = false, have_ids = false;
+    bool have_ids = false;
     int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
     for (int t = sl;; t += kSlots) {
       const int g0 = t * kRows;
@@ -284,6 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         break;
       }
       const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
+      const int r0 = g0 + 32 * part;  // this warp's first row of the tile
+      if (r0 + 32 <= w_cnt) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&misc->kv_full[sl], 32 * 1024);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            tma_load_2d(dstb + c * kAtomBytes + 32 * part * 128, &wmap, 64 * c,
+                        static_cast<int>(wrow0 + w_begin + r0), &misc->kv_full[sl]);
+          }
+        } else {
+          mbar_arrive(&misc->kv_full[sl]);
+        }
+        continue;
+      }
 #pragma unroll 8
       for (int j = 0; j < 64; ++j) {  // 32 rows x 64 chunks of 16 B
         const int c = lane + 32 * j;
@@ -300,20 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
       }
       cp_async_commit();
-      if (!q_reported) {  // the Q group is the older one
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(&misc->q_done);
-        q_reported = true;
-      }
       cp_async_wait<0>();
       fence_proxy_async_smem();
       mbar_arrive(&misc->kv_full[sl]);
-    }
-    if (!q_reported) {
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&misc->q_done);
     }
     if (paired) exchange_phases();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -503,33 +520,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
     }
     tc_fence_after();
     const bool have_o = ok && n_tiles > 0;
-    uint16_t* stage_o = reinterpret_cast<uint16_t*>(gbase + kQ);  // bf16 [64 h][512]
     uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
-    // O^T slice m: the 64 heads at dim m * 128 + tid (zeros without rows),
-    // one tensor-memory load of 64 columns.
-    auto load_o = [&](int m, float (&v)[64]) {
+    // Heads [16 hc, 16 hc + 16) of O^T slice m (dim 128 m + tid in this
+    // thread's lane), zeros without rows.
+    auto load16 = [&](int m, int hc, float (&v)[16]) {
       if (have_o) {
-        tmem_ld64(la + 128 + 64 * m, v);
+        tmem_ld16(la + 128 + 64 * m + 16 * hc, v);
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.f;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
       }
     };
-    auto put_out = [&](int m, const float (&v)[64]) {
+    // v[i] *= f[16 hc + i], f in shared memory
+    auto scale16 = [&](float (&v)[16], uint32_t f, int hc) {
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) {
-        stage_o[h * kLatent + m * 128 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
+      for (int i = 0; i < 16; i += 4) {
+        const float4 w4 = ld_shared_f4(f + (16 * hc + i) * 4);
+        v[i] *= w4.x;
+        v[i + 1] *= w4.y;
+        v[i + 2] *= w4.z;
+        v[i + 3] *= w4.w;
       }
     };
-    auto store_out = [&]() {
-      fence_proxy_async_smem();
-      named_sync(kMathBar, 128);
-      if (tid == 0) {
-        bulk_s2g(out, sbase + kQ, kOutBytes);
-        bulk_commit();
-        bulk_wait_read();
+    // out[16 hc + i][d] = v[i]: each store instruction of a warp writes 32
+    // consecutive dims of one head.
+    auto store16 = [&](int d, int hc, const float (&v)[16]) {
+      uint16_t* o = out + static_cast<int64_t>(16 * hc) * kLatent + d;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[static_cast<int64_t>(i) * kLatent] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
       }
     };
+    const uint32_t inv_l_s = smem_u32(misc->inv_l);
     if (!paired) {
       if (warp < 2) {
         misc->inv_l[tid] = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -541,13 +563,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
       named_sync(kMathBar, 128);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-        float v[64];
-        load_o(m, v);
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) v[h] *= misc->inv_l[h];
-        put_out(m, v);
+#pragma unroll 1
+        for (int hc = 0; hc < 4; ++hc) {
+          float v[16];
+          load16(m, hc, v);
+          scale16(v, inv_l_s, hc);
+          store16(128 * m + tid, hc, v);
+        }
       }
-      store_out();
     } else {
       // CTA `split` finishes latent dims [split D, split D + D). O^T slice m
       // holds dim 128 m + tid in this thread's lane, so the thread's four dims
@@ -566,22 +589,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         const int d = 128 * m + tid;
         const int p = d / D;
         if (p == split) continue;
-        float v[64];
-        load_o(m, v);
         const int dd = d - p * D;
         const uint32_t row = send_slot(p) + static_cast<uint32_t>(dd) * 128;
+#pragma unroll 1
+        for (int hc = 0; hc < 4; ++hc) {
+          float v[16];
+          load16(m, hc, v);
+          scale16(v, inv_l_s, hc);
+          uint32_t w8[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int h = 8 * c + 2 * e;
-            const __nv_bfloat162 x =
-                __floats2bfloat162_rn(v[h] * misc->inv_l[h], v[h + 1] * misc->inv_l[h + 1]);
-            w4[e] = *reinterpret_cast<const uint32_t*>(&x);
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 x = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w8[e] = *reinterpret_cast<const uint32_t*>(&x);
           }
-          st_shared_v4(row + static_cast<uint32_t>(c ^ (dd & 7)) * 16,
-                       make_uint4(w4[0], w4[1], w4[2], w4[3]));
+          st_shared_v4(row + static_cast<uint32_t>((2 * hc) ^ (dd & 7)) * 16,
+                       make_uint4(w8[0], w8[1], w8[2], w8[3]));
+          st_shared_v4(row + static_cast<uint32_t>((2 * hc + 1) ^ (dd & 7)) * 16,
+                       make_uint4(w8[4], w8[5], w8[6], w8[7]));
         }
       }
       if (warp < 2) {
@@ -646,47 +670,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
         }
       }
       named_sync(kMathBar, 128);
-      // bf16 [64 h][D] in the ring past the receive slots (the staged
-      // payloads may still be read by the partners' copies until phase 2).
-      const uint32_t part_off = kRecv + static_cast<uint32_t>(S) * pay;
-      uint16_t* part_o = reinterpret_cast<uint16_t*>(gbase + part_off);
+      const uint32_t wgt_s = sbase + kWgt;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         const int d = 128 * m + tid;
         if (d / D != split) continue;
         const int dd = d - split * D;
-        float v[64];
-        load_o(m, v);
+#pragma unroll 1
+        for (int hc = 0; hc < 4; ++hc) {
+          float v[16];
+          load16(m, hc, v);
+          scale16(v, wgt_s + static_cast<uint32_t>(split * kHeads * 4), hc);
+#pragma unroll 1
+          for (int q = 0; q < S; ++q) {
+            if (q == split || !ok) continue;
+            const uint32_t row = sbase + kRecv + static_cast<uint32_t>(q) * pay +
+                                 static_cast<uint32_t>(dd) * 128;
+            const uint4 x0 = ld_shared_v4(row + static_cast<uint32_t>((2 * hc) ^ (dd & 7)) * 16);
+            const uint4 x1 =
+                ld_shared_v4(row + static_cast<uint32_t>((2 * hc + 1) ^ (dd & 7)) * 16);
+            const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const uint32_t wq = wgt_s + static_cast<uint32_t>(q * kHeads * 4);
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) v[h] *= wgt[split * kHeads + h];
-        for (int q = 0; q < S; ++q) {
-          if (q == split || !ok) continue;
-          const uint32_t row = sbase + kRecv + static_cast<uint32_t>(q) * pay +
-                               static_cast<uint32_t>(dd) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 x = ld_shared_v4(row + static_cast<uint32_t>(c ^ (dd & 7)) * 16);
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int h = 8 * c + 2 * e;
-              v[h] = fmaf(wgt[q * kHeads + h], bf16_bits_to_float(xs[e] & 0xFFFF), v[h]);
-              v[h + 1] = fmaf(wgt[q * kHeads + h + 1], bf16_bits_to_float(xs[e] >> 16), v[h + 1]);
+            for (int i = 0; i < 16; i += 4) {
+              const float4 w4 = ld_shared_f4(wq + (16 * hc + i) * 4);
+              v[i] = fmaf(w4.x, bf16_bits_to_float(xs[i / 2] & 0xFFFF), v[i]);
+              v[i + 1] = fmaf(w4.y, bf16_bits_to_float(xs[i / 2] >> 16), v[i + 1]);
+              v[i + 2] = fmaf(w4.z, bf16_bits_to_float(xs[i / 2 + 1] & 0xFFFF), v[i + 2]);
+              v[i + 3] = fmaf(w4.w, bf16_bits_to_float(xs[i / 2 + 1] >> 16), v[i + 3]);
             }
           }
+          store16(d, hc, v);
         }
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          part_o[h * D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
-        }
-      }
-      named_sync(kMathBar, 128);
-      // 64 rows of 2 D bytes, 16 bytes a store
-      const int per_row = D / 8;
-      for (int i = tid; i < kHeads * per_row; i += 128) {
-        const int hh = i / per_row, ch = i - hh * per_row;
-        const uint4 v = *reinterpret_cast<const uint4*>(gbase + part_off + hh * 2 * D + ch * 16);
-        *reinterpret_cast<uint4*>(out + hh * kLatent + D * split + ch * 8) = v;
       }
     }
   }
@@ -702,24 +717,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnArgs a) {
 
 }  // namespace
 
+// Clusters of `splits` CTAs (32-row tiles) that can be resident at once on
+// the current device (clusters must fit a GPC; several GPCs cannot hold as
+// many 8-CTA clusters as SMs / 8). Cached per device and size.
+int attn_max_clusters(int splits) {
+  static std::atomic<int> cache[64][4]{};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int k = splits == 2 ? 0 : splits == 4 ? 1 : splits == 8 ? 2 : 3;
+  int n = cache[dev][k].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  static std::atomic<int> smem_set[64]{};
+  if (ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set) !=
+      cudaSuccess) {
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 1;
+  attr.val.clusterDim.y = static_cast<unsigned>(splits);
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<32>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the error the failed query left behind
+    n = device_sm_count() / splits;
+  }
+  cache[dev][k].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
   if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) {
     return cudaErrorInvalidValue;
   }
+  // Q as rows of 512 bf16 (one per query head), boxes of 64 heads x 64 dims.
+  CUtensorMap qmap;
+  memset(&qmap, 0, sizeof(qmap));
+  cudaError_t e = encode_tma_2d(&qmap, a.q, 2, kLatent, static_cast<uint64_t>(a.B) * kHeads,
+                                kLatent * 2, 64, kHeads);
+  if (e != cudaSuccess) return e;
+  // Window rows (decode: B x window rows; prefill: n_q + window - 1), boxes of
+  // 32 rows x 64 dims.
+  CUtensorMap wmap;
+  memset(&wmap, 0, sizeof(wmap));
+  const uint64_t wrows = a.prefill ? static_cast<uint64_t>(a.B) + a.window - 1
+                                   : static_cast<uint64_t>(a.B) * a.window;
+  e = encode_tma_2d(&wmap, a.swa, 2, kLatent, wrows, kLatent * 2, 64, 32);
+  if (e != cudaSuccess) return e;
   if (a.tile_rows == 64) {
     static std::atomic<int> smem_set[64]{};
-    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
+    e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                      a.splits, a);
+                      a.splits, a, qmap, wmap);
   }
   if (a.tile_rows != 32) return cudaErrorInvalidValue;
   static std::atomic<int> smem_set[64]{};
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
+  e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                    a.splits, a);
+                    a.splits, a, qmap, wmap);
 }
 
 }  // namespace dsa

@@ -78,6 +78,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+// Four fp32 values from shared memory (no compiler memory barrier: callers
+// order it against writes with a named barrier or __syncthreads).
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor-core operand reads) after this fence and a barrier.
 __device__ __forceinline__ void fence_proxy_async_smem() {

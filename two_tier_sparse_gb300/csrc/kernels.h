@@ -180,9 +180,10 @@ struct AttnArgs {
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
-// Split-KV runs S CTAs per query, the largest S in {8, 4, 2} for which S x
-// queries fits the SMs in one wave.
+// Split-KV runs S CTAs per query, the largest S in {8, 4, 2} for which the
+// queries' clusters fit the device at once (attn_max_clusters).
 constexpr int kMaxAttnSplits = 8;
+int attn_max_clusters(int splits);
 
 // block_ids[b] = 0, 1, ..., ceil(n_latents[b] / 8) - 1, then -1.
 cudaError_t launch_identity_blocks(const int32_t* n_latents, int B, int k_blocks,
