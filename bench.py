@@ -322,6 +322,7 @@ def run_ours(args):
     if spec["kind"] == "prefill":
         return run_prefill(args, spec, dsa, synth, dev, rank, world)
     B, T, ratio, fmt = spec["B"], spec["T"], spec["ratio"], spec["key_fmt"]
+    page_rows = spec.get("page_rows", 0)
     if args.batch:
         B = args.batch
     # Every rank decodes its own batch: seeds differ per rank.
@@ -341,14 +342,42 @@ def run_ours(args):
     keys = dsa.Keys(fmt, d(inp.keys.data), None if inp.keys.scales is None else
                     d(inp.keys.scales))
     del inp
+    pages = None
+    if page_rows:
+        # Every cache in pages of page_rows tokens: sequence b's logical page p
+        # is physical page table[b, p] of a pool, a seeded permutation of the
+        # B x cap / page_rows pages plus a few spare ones.
+        pps = cap // page_rows
+        n_pages = B * pps + 4
+        gen = torch.Generator().manual_seed(shard_seed(spec["seed"], rank))
+        table = torch.randperm(n_pages, generator=gen)[:B * pps].to(torch.int32).view(B, pps)
+        flat = table.view(-1).to(dev, torch.int64)
+
+        def paged(t):
+            if t.dtype == torch.uint16:  # bf16 bit patterns: copied as int16
+                t = t.view(torch.int16)
+            pool = torch.zeros((n_pages * page_rows,) + tuple(t.shape[2:]), dtype=t.dtype,
+                               device=dev)
+            pool.view(n_pages, page_rows, *t.shape[2:])[flat] = t.view(B * pps, page_rows,
+                                                                       *t.shape[2:])
+            return pool
+        pages = dsa.Pages(table.to(dev), page_rows, n_pages)
+        latents = paged(latents)
+        keys = dsa.Keys(fmt, paged(keys.data), None if keys.scales is None else
+                        paged(keys.scales), pages)
+        torch.cuda.empty_cache()
     nbc = cap // 8
+    # block keys: [B, nbc, ...], or (paged) a pool of page_rows / 8 rows a page
+    lead = (pages.c.n_pages * page_rows // 8,) if pages is not None else (B, nbc)
     if fmt == "bf16":
-        pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.int16, device=dev))
+        pooled = dsa.Keys(fmt, torch.empty(lead + (128,), dtype=torch.int16, device=dev),
+                          pages=pages)
     else:
-        nbc += nbc & 1 if fmt == "mxfp4" else 0  # MXFP4 rows are read in pairs
+        if pages is None and fmt == "mxfp4":
+            lead = (B, nbc + (nbc & 1))  # MXFP4 rows are read in pairs
         width = 64 if fmt == "mxfp4" else 128
-        pooled = dsa.Keys(fmt, torch.empty((B, nbc, width), dtype=torch.uint8, device=dev),
-                          torch.empty((B, nbc, 4), dtype=torch.uint8, device=dev))
+        pooled = dsa.Keys(fmt, torch.empty(lead + (width,), dtype=torch.uint8, device=dev),
+                          torch.empty(lead + (4,), dtype=torch.uint8, device=dev), pages)
     ws = dsa.workspace(cfg, B, cap, dev)
     out = torch.empty((B, 64, 512), dtype=torch.int16, device=dev)
     lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
@@ -605,6 +634,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "batch_per_gpu": B, "tokens": T, "ratio": ratio,
                    "latents": L, "blocks": nb, "k_blocks": cfg.k_blocks,
+                   "layout": f"paged, {page_rows}-token pages" if page_rows else "contiguous",
                    "k_tokens": cfg.k_tokens, "window": cfg.window, "key_fmt": fmt,
                    "l2": L2Flush.DESCRIPTION,
                    "step_algorithmic_bytes": step_bytes,

@@ -94,14 +94,44 @@ typedef struct {
   float sm_scale;  /* softmax scale tau; <= 0 selects 1/sqrt(latent_dim) */
 } dsa_config_t;
 
-/* A key cache (index keys or block-pooled keys) of B sequences. Sequence b's
- * row r is at data + (b * seq_stride_rows + r) * row_bytes; MXFP8 scales are
- * laid out the same way with 4 bytes per row. */
+/*
+ * Paged layout of a decode batch's caches (a block table, as serving engines
+ * keep KV caches in fixed-size pages; the candidate-block indexer reads its
+ * keys through one, miles.radixark.com "DeepSeek-V4.1 Flash", §4.1). Each
+ * cache is a pool of physical pages shared by the B sequences: logical row r
+ * of sequence b lives in physical page
+ *     page_table[b * pages_per_seq + r / R]   at row r % R of that page,
+ * with R = page_rows for index keys and latents and R = page_rows / 8 for
+ * block keys (a page of page_rows tokens holds page_rows / 8 blocks). So the
+ * pools are laid out as [n_pages * R] rows of the cache's own row format
+ * (latents: 512 bf16; keys: their dsa_fmt_t row, MX scales [n_pages * R, 4]).
+ *   page_table:    device int32 [B, pages_per_seq]; an entry outside
+ *                  [0, n_pages) is a device-detected error (DSA_ERR_DEVICE_CHECK,
+ *                  the rows of that page are skipped)
+ *   page_rows:     tokens per page, a positive multiple of 64
+ *   pages_per_seq: row stride of page_table, at least ceil(max_latents / page_rows)
+ *   n_pages:       physical pages in each pool; n_pages * page_rows < 2^31
+ */
+typedef struct {
+  const int32_t* page_table;
+  int32_t page_rows;
+  int32_t pages_per_seq;
+  int64_t n_pages;
+} dsa_pages_t;
+
+/* A key cache (index keys or block-pooled keys) of B sequences. Contiguous
+ * (pages == NULL): sequence b's row r is at data + (b * seq_stride_rows + r) *
+ * row_bytes, and MX scales are laid out the same way with 4 bytes per row.
+ * Paged (pages != NULL): rows are found through the page table above and
+ * seq_stride_rows is not used. Paged caches are taken by dsa_pool_index_keys,
+ * dsa_index_blocks, dsa_topk, dsa_topk_noalloc and dsa_decode_step (decode
+ * only; prefill reads one contiguous sequence). */
 typedef struct {
   dsa_fmt_t fmt;
   const void* data;
   const uint8_t* scales;
   int64_t seq_stride_rows;
+  const dsa_pages_t* pages;
 } dsa_keys_t;
 
 /* The writable form, for dsa_pool_index_keys' output. */
@@ -110,6 +140,7 @@ typedef struct {
   void* data;
   uint8_t* scales;
   int64_t seq_stride_rows;
+  const dsa_pages_t* pages;
 } dsa_keys_out_t;
 
 /* Fills *cfg with the DeepSeek-V4.1 values above (ratio 1, sm_scale 0). */
@@ -207,6 +238,19 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
                                     dsa_stream_t stream);
 
 /*
+ * dsa_sparse_attn_decode over a paged latent pool: latent id t of sequence b
+ * is row page_table[b * pages_per_seq + t / page_rows] * page_rows + t % page_rows
+ * of `latents` (bf16 [pages->n_pages * page_rows, 512]). Ids whose page entry
+ * is out of range are skipped and reported like ids past n_latents.
+ */
+dsa_status_t dsa_sparse_attn_decode_paged(const dsa_config_t* cfg, const void* q,
+                                          const void* latents, const dsa_pages_t* pages,
+                                          const int32_t* n_latents, const int32_t* token_ids,
+                                          const void* swa, const int32_t* swa_len, int B,
+                                          void* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * The whole decode step for B sequences, the query of sequence b at position
  * T_b - 1 with n_latents[b] = T_b / ratio visible latents: pool the newest
  * block (when update_pool != 0), the candidate-block stage (skipped when no
@@ -214,6 +258,9 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
  * attention, as the four calls above would in sequence.
  *   pooled:        block keys, read by the block stage; also written (newest
  *                  block only) when update_pool != 0
+ *   keys, pooled:  both contiguous, or both paged with the same page table;
+ *                  paged keys make the latents paged by that table too (and
+ *                  latent_seq_stride_rows is then not used)
  *   block_ids:     out (optional), device int32 [B, k_blocks]
  *   token_ids:     out (optional), device int32 [B, k_tokens]
  */

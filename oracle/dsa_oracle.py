@@ -427,6 +427,19 @@ def attend_query(cfg: StepConfig, q_bits, latents_bits: np.ndarray, token_ids: n
 # ---------------------------------------------------------------------------
 
 
+def gather_paged(pool: np.ndarray, page_table_row: np.ndarray, page_rows: int,
+                 n_rows: int) -> np.ndarray:
+    """Logical rows 0 .. n_rows - 1 of one sequence of a paged cache: row r is row
+    r mod page_rows of physical page page_table_row[r // page_rows] of the pool
+    [n_pages * page_rows, ...] (the block-table layout serving engines keep KV
+    caches in; miles.radixark.com "DeepSeek-V4.1 Flash", §4.1, names a paged
+    indexer). The step computes on these rows exactly as on a contiguous
+    sequence."""
+    r = np.arange(n_rows, dtype=np.int64)
+    page = np.asarray(page_table_row, np.int64)[r // page_rows]
+    return np.asarray(pool)[page * page_rows + r % page_rows]
+
+
 def decoded_key_cache(keys_fmt: str, data: np.ndarray, scales) -> np.ndarray:
     return decode_keys(keys_fmt, data, scales)
 

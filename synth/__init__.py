@@ -299,6 +299,32 @@ def prefill_inputs(n_q: int, ctx: int, ratio: int, key_fmt: str, seed: int,
                          keys=keys, swa=swa.reshape(n_sw, LATENT_DIM), window=window)
 
 
+def paginate(arr: np.ndarray, page_rows: int, seed: int, spare_pages: int = 3,
+             poison: int = 0xFF):
+    """Lays a per-sequence cache arr [B, cap, ...] out as a pool of pages, the
+    way a serving engine's block table does: sequence b's logical page p (rows
+    [p * page_rows, (p + 1) * page_rows)) goes to physical page table[b, p] of
+    pool [n_pages * page_rows, ...]. Physical pages are a seeded permutation of
+    B * pages_per_seq + spare_pages pages; the spare ones and the rows past cap
+    are filled with the byte `poison`. Returns (pool, table int32 [B, pages_per_seq]).
+    Holds no arithmetic of the method: only where bytes go."""
+    arr = np.asarray(arr)
+    B, cap = arr.shape[0], arr.shape[1]
+    pps = max(1, -(-cap // page_rows))
+    n_pages = B * pps + spare_pages
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(n_pages)
+    table = perm[:B * pps].reshape(B, pps).astype(np.int32)
+    pool = np.empty((n_pages * page_rows,) + arr.shape[2:], arr.dtype)
+    pool.view(np.uint8)[...] = poison
+    for b in range(B):
+        for p in range(pps):
+            lo, hi = p * page_rows, min(cap, (p + 1) * page_rows)
+            dst = int(table[b, p]) * page_rows
+            pool[dst:dst + hi - lo] = arr[b, lo:hi]
+    return pool, table
+
+
 # The workloads, named by what they are (tokens per sequence, batch,
 # compression ratio, index-key format) with their seeds.
 WORKLOADS = {
@@ -315,12 +341,17 @@ WORKLOADS = {
     # (recipes.vllm.ai "DeepSeek-V4.1-Flash", indexer_kv_dtype mxfp4).
     "decode_b64_t131072_r1_mxfp4": dict(kind="decode", B=64, T=131072, ratio=1,
                                         key_fmt="mxfp4", seed=2),
+    # The same batch with every cache in shuffled pages of 64 tokens behind a
+    # block table (the paged layout serving engines use).
+    "decode_b64_t131072_r1_mxfp8_paged64": dict(kind="decode", B=64, T=131072, ratio=1,
+                                                key_fmt="mxfp8", seed=2, page_rows=64),
 }
 
 
 def workload_inputs(name: str, **kw):
     spec = dict(WORKLOADS[name])
     kind = spec.pop("kind")
+    spec.pop("page_rows", None)  # the layout, not the values
     spec.update(kw)
     if kind == "decode":
         B, T = spec.pop("B"), spec.pop("T")

@@ -242,6 +242,41 @@ def test_topk_noalloc_capacity_and_errors(lib):
     assert call(B=0) == 0
 
 
+def test_paged_cache_argument_errors(lib):
+    cfg = dsa.config()
+
+    def pages(table=A, rows=64, per_seq=2, n=10):
+        return dsa._Pages(table, rows, per_seq, n)
+
+    def call_topk(pg, L=100):
+        keys = dsa._Keys(0, A, None, 0, ctypes.pointer(pg) if pg is not None else None)
+        return lib.dsa_topk(ctypes.byref(cfg), A, A, ctypes.byref(keys), None, A, 2, L, A, None,
+                            A, 16, None)   # workspace too small: nothing may launch
+    assert call_topk(pages()) == 4                     # valid pages, then the workspace check
+    assert call_topk(pages(rows=32)) == 1              # pages of a multiple of 64 tokens
+    assert call_topk(pages(rows=0)) == 1
+    assert call_topk(pages(table=None)) == 1
+    assert call_topk(pages(table=A + 2)) == 2
+    assert call_topk(pages(per_seq=1), L=100) == 1     # 64 tokens a sequence < 100
+    assert call_topk(pages(n=0)) == 1
+    assert call_topk(pages(n=1 << 26)) == 1            # more than 2^31 rows in the pool
+    pg = pages()
+    # prefill reads one contiguous sequence
+    keys = dsa._Keys(0, A, None, 0, ctypes.pointer(pg))
+    assert lib.dsa_sparse_attn_prefill(ctypes.byref(dsa.config(ratio=2)), 16, 100, A, A, A, A,
+                                       ctypes.byref(keys), ctypes.byref(keys), A, A, None, None,
+                                       A, 1 << 30, None) == 1
+    # the step's keys and block keys: both paged by the same table, or neither
+    flat = dsa._Keys(0, A, None, 13, None)
+    assert lib.dsa_decode_step(ctypes.byref(cfg), A, A, A, ctypes.byref(keys), ctypes.byref(flat),
+                               1, A, 0, A, 100, A, A, 2, None, None, A, None, A, 16,
+                               None) == 1
+    assert lib.dsa_sparse_attn_decode_paged(ctypes.byref(cfg), A, A, None, A, A, A, A, 2, A,
+                                            None, A, 1 << 30, None) == 1
+    assert lib.dsa_sparse_attn_decode_paged(ctypes.byref(cfg), A, A, ctypes.byref(pages(rows=100)),
+                                            A, A, A, A, 2, A, None, A, 1 << 30, None) == 1
+
+
 def test_hooks_and_self_test_argument_errors(lib):
     n_kinds = len(dsa.KERNEL_KINDS)
     assert lib.dsa_profile_events(-1, None, None, 0) == 1

@@ -33,7 +33,7 @@ EXPORTS = ("dsa_default_config", "dsa_status_string", "dsa_workspace_size",
            "dsa_pool_index_keys", "dsa_index_blocks", "dsa_topk", "dsa_sparse_attn_decode",
            "dsa_decode_step", "dsa_sparse_attn_prefill", "dsa_read_device_status",
            "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc",
-           "dsa_selftest_timeout")
+           "dsa_selftest_timeout", "dsa_sparse_attn_decode_paged")
 
 TOPK_NOALLOC_MAX_SCORES = 1 << 21
 
@@ -54,10 +54,16 @@ class Config(ctypes.Structure):
                 ("window", ctypes.c_int), ("ratio", ctypes.c_int), ("sm_scale", ctypes.c_float)]
 
 
+class _Pages(ctypes.Structure):
+    """dsa_pages_t."""
+    _fields_ = [("page_table", ctypes.c_void_p), ("page_rows", ctypes.c_int32),
+                ("pages_per_seq", ctypes.c_int32), ("n_pages", ctypes.c_int64)]
+
+
 class _Keys(ctypes.Structure):
     """dsa_keys_t / dsa_keys_out_t (same layout)."""
     _fields_ = [("fmt", ctypes.c_int), ("data", ctypes.c_void_p), ("scales", ctypes.c_void_p),
-                ("seq_stride_rows", ctypes.c_int64)]
+                ("seq_stride_rows", ctypes.c_int64), ("pages", ctypes.POINTER(_Pages))]
 
 
 _lib = None
@@ -93,6 +99,8 @@ def load() -> ctypes.CDLL:
         lib.dsa_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
         lib.dsa_topk_noalloc.argtypes = [cp, vp, vp, kp, vp, vp, i32, i64, vp, vp]
         lib.dsa_selftest_timeout.argtypes = [vp, sz, vp]
+        lib.dsa_sparse_attn_decode_paged.argtypes = [cp, vp, vp, ctypes.POINTER(_Pages), vp, vp,
+                                                     vp, vp, i32, vp, vp, vp, sz, vp]
         for f in EXPORTS:
             if f not in ("dsa_default_config", "dsa_status_string"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -124,6 +132,16 @@ def config(k_blocks=2048, k_tokens=512, window=128, ratio=1, sm_scale=0.0) -> Co
     return c
 
 
+class Pages:
+    """A page table (dsa_pages_t) over pools of n_pages pages of page_rows tokens:
+    table is a device int32 tensor [B, pages_per_seq]."""
+
+    def __init__(self, table: torch.Tensor, page_rows: int, n_pages: int):
+        assert table.dtype == torch.int32 and table.dim() == 2
+        self.table = table
+        self.c = _Pages(table.data_ptr(), page_rows, table.shape[1], n_pages)
+
+
 @dataclass
 class Keys:
     """A key cache on the device: data [B, rows, 128] (bf16 as 16-bit words, or
@@ -132,11 +150,14 @@ class Keys:
     fmt: str
     data: torch.Tensor
     scales: Optional[torch.Tensor] = None
+    pages: Optional[Pages] = None  # paged pool (data rows = n_pages x rows per page)
 
     def c(self) -> _Keys:
         stride = self.data.shape[-2] if self.data.dim() >= 3 else 0
+        pages = ctypes.pointer(self.pages.c) if self.pages is not None else None
         return _Keys(_FMT[self.fmt], self.data.data_ptr(),
-                     self.scales.data_ptr() if self.scales is not None else None, stride)
+                     self.scales.data_ptr() if self.scales is not None else None, stride,
+                     pages)
 
 
 def workspace_size(cfg: Config, n_queries: int, max_latents: int) -> int:
@@ -154,7 +175,7 @@ def workspace(cfg: Config, n_queries: int, max_latents: int, device="cuda") -> t
 
 def pool_index_keys(cfg, keys: Keys, n_latents, max_latents, pooled: Keys, ws, tail_only=False,
                     stream=None):
-    B = keys.data.shape[0]
+    B = n_latents.shape[0]
     _check(load().dsa_pool_index_keys(ctypes.byref(cfg), ctypes.byref(keys.c()), _p(n_latents), B,
                                       max_latents, int(tail_only), ctypes.byref(pooled.c()),
                                       _p(ws), ws.numel(), _stream(stream)), "dsa_pool_index_keys")
@@ -197,13 +218,25 @@ def sparse_attn_decode(cfg, q, latents, n_latents, token_ids, swa, swa_len, out,
            "dsa_sparse_attn_decode")
 
 
+def sparse_attn_decode_paged(cfg, q, latents, pages: Pages, n_latents, token_ids, swa, swa_len,
+                             out, ws, lse=None, stream=None):
+    """dsa_sparse_attn_decode over a paged latent pool (latents [n_pages * page_rows, 512])."""
+    B = q.shape[0]
+    _check(load().dsa_sparse_attn_decode_paged(ctypes.byref(cfg), _p(q), _p(latents),
+                                               ctypes.byref(pages.c), _p(n_latents),
+                                               _p(token_ids), _p(swa), _p(swa_len), B, _p(out),
+                                               _p(lse), _p(ws), ws.numel(), _stream(stream)),
+           "dsa_sparse_attn_decode_paged")
+
+
 def decode_step(cfg, q, q_idx, w, keys: Keys, pooled: Keys, latents, n_latents, max_latents, swa,
                 swa_len, out, ws, lse=None, block_ids=None, token_ids=None, update_pool=False,
                 stream=None):
     B = q.shape[0]
+    lat_stride = latents.shape[1] if keys.pages is None else 0
     _check(load().dsa_decode_step(ctypes.byref(cfg), _p(q), _p(q_idx), _p(w),
                                   ctypes.byref(keys.c()), ctypes.byref(pooled.c()),
-                                  int(update_pool), _p(latents), latents.shape[1], _p(n_latents),
+                                  int(update_pool), _p(latents), lat_stride, _p(n_latents),
                                   max_latents, _p(swa), _p(swa_len), B, _p(block_ids),
                                   _p(token_ids), _p(out), _p(lse), _p(ws), ws.numel(),
                                   _stream(stream)), "dsa_decode_step")

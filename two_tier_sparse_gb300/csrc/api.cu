@@ -71,7 +71,43 @@ float tau(const dsa_config_t& c) {
   return c.sm_scale > 0.f ? c.sm_scale : 1.0f / sqrtf(static_cast<float>(c.latent_dim));
 }
 
-dsa_status_t check_keys(const dsa_keys_t* k, int64_t min_stride, bool need_stride) {
+// A page table covering sequences of up to max_latents latents.
+dsa_status_t check_pages(const dsa_pages_t* pg, int64_t max_latents) {
+  if (pg->page_table == nullptr || pg->page_rows <= 0 || pg->page_rows % 64 != 0 ||
+      pg->n_pages < 1 || pg->pages_per_seq < 1) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(pg->page_table) & 3u) return DSA_ERR_MISALIGNED;
+  if (static_cast<int64_t>(pg->pages_per_seq) * pg->page_rows < max_latents) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (pg->n_pages * pg->page_rows >= (int64_t(1) << 31)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+// Paged addressing of a cache with `div` tokens per row (1: keys, latents;
+// 8: block keys); a null table for a contiguous cache.
+Paging paging_of(const dsa_pages_t* pg, int div) {
+  Paging p{};
+  if (pg != nullptr) {
+    p.table = pg->page_table;
+    p.rows = pg->page_rows / div;
+    p.per_seq = pg->pages_per_seq;
+    p.n_pages = pg->n_pages;
+  }
+  return p;
+}
+
+bool same_pages(const dsa_pages_t* a, const dsa_pages_t* b) {
+  if (a == nullptr || b == nullptr) return a == b;
+  return a->page_table == b->page_table && a->page_rows == b->page_rows &&
+         a->pages_per_seq == b->pages_per_seq && a->n_pages == b->n_pages;
+}
+
+// Key cache checks. Contiguous: at least min_stride rows per sequence (when
+// need_stride). Paged: a valid table for sequences of max_latents latents.
+dsa_status_t check_keys(const dsa_keys_t* k, int64_t min_stride, bool need_stride,
+                        int64_t max_latents = 0) {
   if (k == nullptr || k->data == nullptr) return DSA_ERR_INVALID_ARG;
   if (k->fmt != DSA_FMT_BF16 && k->fmt != DSA_FMT_MXFP8 && k->fmt != DSA_FMT_MXFP4) {
     return DSA_ERR_INVALID_ARG;
@@ -80,6 +116,7 @@ dsa_status_t check_keys(const dsa_keys_t* k, int64_t min_stride, bool need_strid
   if (mx && k->scales == nullptr) return DSA_ERR_INVALID_ARG;
   if (!aligned16(k->data)) return DSA_ERR_MISALIGNED;
   if (mx && (reinterpret_cast<uintptr_t>(k->scales) & 3u)) return DSA_ERR_MISALIGNED;
+  if (k->pages != nullptr) return check_pages(k->pages, max_latents);
   if (need_stride && k->seq_stride_rows < min_stride) return DSA_ERR_INVALID_ARG;
   // MXFP4 rows are read two at a time (128 bytes): sequences start on a pair.
   if (k->fmt == DSA_FMT_MXFP4 && need_stride && (k->seq_stride_rows & 1)) {
@@ -204,6 +241,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     sa.n_latents = n_lat;
     sa.max_latents = max_latents;
     sa.mode = ROWS_BLOCKS;
+    sa.pages = paging_of(pooled.pages, kBlock);
     sa.n_rows = nb_max;
     sa.scores = scores;
     sa.B = B;
@@ -274,6 +312,7 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     sa.w = w;
     sa.n_latents = n_lat;
     sa.max_latents = max_latents;
+    sa.pages = paging_of(keys.pages, 1);
     if (block_ids) {
       sa.mode = ROWS_GATHER;
       sa.block_ids = block_ids;
@@ -422,10 +461,12 @@ dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys
   if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || pooled == nullptr) {
     return DSA_ERR_INVALID_ARG;
   }
-  DSA_TRY(check_keys(keys, max_latents, true));
-  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows};
-  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true));
+  DSA_TRY(check_keys(keys, max_latents, true, max_latents));
+  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows,
+                      pooled->pages};
+  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true, max_latents));
   if (pooled->fmt != keys->fmt || n_latents == nullptr) return DSA_ERR_INVALID_ARG;
+  if (!same_pages(keys->pages, pooled->pages)) return DSA_ERR_INVALID_ARG;
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0 || max_latents == 0) return DSA_OK;
@@ -441,6 +482,8 @@ dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys
   a.out_data = pooled->data;
   a.out_scales = pooled->scales;
   a.out_stride = pooled->seq_stride_rows;
+  a.key_pages = paging_of(keys->pages, 1);
+  a.out_pages = paging_of(pooled->pages, kBlock);
   a.status = at<DeviceStatus>(workspace, L.status);
   DSA_CUDA(launch(DSA_KERNEL_POOL, static_cast<cudaStream_t>(stream), [&](int*) { return launch_pool(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
@@ -459,7 +502,7 @@ dsa_status_t dsa_index_blocks(const dsa_config_t* cfg, const void* q_idx, const 
       (block_scores && !aligned16(block_scores))) {
     return DSA_ERR_MISALIGNED;
   }
-  DSA_TRY(check_keys(pooled, (max_latents + 7) / 8, true));
+  DSA_TRY(check_keys(pooled, (max_latents + 7) / 8, true, max_latents));
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
@@ -484,7 +527,7 @@ dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w
       (block_ids && !aligned16(block_ids)) || (token_scores && !aligned16(token_scores))) {
     return DSA_ERR_MISALIGNED;
   }
-  DSA_TRY(check_keys(keys, max_latents, true));
+  DSA_TRY(check_keys(keys, max_latents, true, max_latents));
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
@@ -495,12 +538,16 @@ dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w
                          static_cast<cudaStream_t>(stream), 0, 0);
 }
 
-dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, const void* latents,
-                                    int64_t latent_seq_stride_rows, const int32_t* n_latents,
-                                    const int32_t* token_ids, const void* swa,
-                                    const int32_t* swa_len, int B, void* out, float* lse,
-                                    void* workspace, size_t workspace_bytes,
-                                    dsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// dsa_sparse_attn_decode and its paged form (pages != nullptr).
+dsa_status_t attn_decode(const dsa_config_t* cfg, const void* q, const void* latents,
+                         int64_t latent_seq_stride_rows, const dsa_pages_t* pages,
+                         const int32_t* n_latents, const int32_t* token_ids, const void* swa,
+                         const int32_t* swa_len, int B, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
   if (B < 0 || latent_seq_stride_rows < 0) return DSA_ERR_INVALID_ARG;
   if (q == nullptr || latents == nullptr || n_latents == nullptr || token_ids == nullptr ||
@@ -511,6 +558,7 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
       !aligned16(token_ids) || (lse && !aligned16(lse))) {
     return DSA_ERR_MISALIGNED;
   }
+  if (pages != nullptr) DSA_TRY(check_pages(pages, 0));
   Layout L;
   DSA_TRY(check_ws(*cfg, B, 0, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
@@ -518,6 +566,10 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = latent_seq_stride_rows;
+  if (pages != nullptr) {
+    a.pages = paging_of(pages, 1);
+    a.lat_stride = static_cast<int64_t>(pages->pages_per_seq) * pages->page_rows;
+  }
   a.n_latents = n_latents;
   a.token_ids = token_ids;
   a.k_tokens = cfg->k_tokens;
@@ -534,6 +586,31 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
   return DSA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, const void* latents,
+                                    int64_t latent_seq_stride_rows, const int32_t* n_latents,
+                                    const int32_t* token_ids, const void* swa,
+                                    const int32_t* swa_len, int B, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    dsa_stream_t stream) {
+  return attn_decode(cfg, q, latents, latent_seq_stride_rows, nullptr, n_latents, token_ids, swa,
+                     swa_len, B, out, lse, workspace, workspace_bytes, stream);
+}
+
+dsa_status_t dsa_sparse_attn_decode_paged(const dsa_config_t* cfg, const void* q,
+                                          const void* latents, const dsa_pages_t* pages,
+                                          const int32_t* n_latents, const int32_t* token_ids,
+                                          const void* swa, const int32_t* swa_len, int B,
+                                          void* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, dsa_stream_t stream) {
+  if (pages == nullptr) return DSA_ERR_INVALID_ARG;
+  return attn_decode(cfg, q, latents, 0, pages, n_latents, token_ids, swa, swa_len, B, out, lse,
+                     workspace, workspace_bytes, stream);
+}
+
 dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void* q_idx,
                              const float* w, const dsa_keys_t* keys, const dsa_keys_out_t* pooled,
                              int update_pool, const void* latents,
@@ -545,7 +622,9 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || pooled == nullptr) {
     return DSA_ERR_INVALID_ARG;
   }
-  if (latent_seq_stride_rows < max_latents) return DSA_ERR_INVALID_ARG;
+  if (keys != nullptr && keys->pages == nullptr && latent_seq_stride_rows < max_latents) {
+    return DSA_ERR_INVALID_ARG;
+  }
   if (q == nullptr || q_idx == nullptr || w == nullptr || latents == nullptr ||
       n_latents == nullptr || swa == nullptr || swa_len == nullptr || out == nullptr) {
     return DSA_ERR_INVALID_ARG;
@@ -555,10 +634,12 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
       (block_ids && !aligned16(block_ids)) || (token_ids && !aligned16(token_ids))) {
     return DSA_ERR_MISALIGNED;
   }
-  DSA_TRY(check_keys(keys, max_latents, true));
-  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows};
-  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true));
+  DSA_TRY(check_keys(keys, max_latents, true, max_latents));
+  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows,
+                      pooled->pages};
+  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true, max_latents));
   if (pooled->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  if (!same_pages(keys->pages, pooled->pages)) return DSA_ERR_INVALID_ARG;
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
@@ -577,6 +658,8 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
     a.out_data = pooled->data;
     a.out_scales = pooled->scales;
     a.out_stride = pooled->seq_stride_rows;
+    a.key_pages = paging_of(keys->pages, 1);
+    a.out_pages = paging_of(pooled->pages, kBlock);
     a.status = st;
     DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_pool(a, s); }));
   }
@@ -599,6 +682,10 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = latent_seq_stride_rows;
+  if (keys->pages) {  // the latents share the keys' page table
+    a.pages = paging_of(keys->pages, 1);
+    a.lat_stride = static_cast<int64_t>(keys->pages->pages_per_seq) * keys->pages->page_rows;
+  }
   a.n_latents = n_latents;
   a.token_ids = tids;
   a.k_tokens = cfg->k_tokens;
@@ -637,6 +724,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   DSA_TRY(check_keys(keys, 0, false));
   DSA_TRY(check_keys(pooled, 0, false));
   if (pooled->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  if (keys->pages != nullptr || pooled->pages != nullptr) return DSA_ERR_INVALID_ARG;
   Layout L;
   DSA_TRY(check_ws(*cfg, n_q, n_lat, workspace, workspace_bytes, &L));
   if (n_q == 0) return DSA_OK;
@@ -771,7 +859,7 @@ extern "C" dsa_status_t dsa_topk_noalloc(const dsa_config_t* cfg, const void* q_
       (block_ids && !aligned16(block_ids))) {
     return DSA_ERR_MISALIGNED;
   }
-  DSA_TRY(check_keys(keys, max_latents, true));
+  DSA_TRY(check_keys(keys, max_latents, true, max_latents));
   const int64_t n_cand = block_ids ? static_cast<int64_t>(cfg->k_blocks) * kBlock
                                    : (max_latents + 7) / 8 * 8;
   if (static_cast<int64_t>(B) * n_cand > DSA_TOPK_NOALLOC_MAX_SCORES) return DSA_ERR_WORKSPACE;

@@ -182,8 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     win = a.swa + wrow0 * kLatent;
   }
   if (n_vis > a.lat_stride) n_vis = static_cast<int>(a.lat_stride);
+  // Latent rows: ids index this sequence's rows, or (paged) the compaction
+  // below turns them into rows of the shared pool.
+  const bool paged = a.pages.table != nullptr;
   const uint16_t* lat =
-      a.latents + (a.prefill ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
+      a.latents +
+      (a.prefill || paged ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
   // This CTA's rows: its part of the window rows first (they are inputs of the
   // step, so they stream while the previous kernel still selects the tokens),
   // then its part of the selected latents (known once the ids are compacted).
@@ -241,6 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
           }
           id = -1;
+        }
+        if (paged && id >= 0) {
+          const int64_t row = paged_row(a.pages, b, id);
+          if (row < 0 && split == 0) {
+            record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+          }
+          id = static_cast<int>(row);
         }
       }
       my[j] = id;

@@ -24,6 +24,28 @@ constexpr int kMaxKBlocks = 4096;
 constexpr int kMaxKTokens = 512;
 constexpr int kMaxWindow = 128;
 
+// Paged addressing of one cache (dsa_pages_t with this cache's rows per page:
+// page_rows for index keys and latents, page_rows / 8 for block keys); a null
+// table means the cache is contiguous.
+struct Paging {
+  const int32_t* table;  // [B, per_seq]
+  int rows;              // rows per page of this cache
+  int per_seq;
+  int64_t n_pages;
+};
+// Physical row of logical row r of sequence b, or -1 when the page entry is
+// outside the pool (or r outside the table).
+// (Logical rows are below 2^30, so the page arithmetic is 32-bit.)
+__device__ __forceinline__ int64_t paged_row(const Paging& p, int b, int64_t r) {
+  if (r < 0 || r >= (int64_t{1} << 30)) return -1;
+  const int ri = static_cast<int>(r);
+  const int pi = ri / p.rows;
+  if (pi >= p.per_seq) return -1;
+  const int pg = p.table[static_cast<int64_t>(b) * p.per_seq + pi];
+  if (pg < 0 || pg >= p.n_pages) return -1;
+  return static_cast<int64_t>(pg) * p.rows + (ri - pi * p.rows);
+}
+
 struct PoolArgs {
   int fmt;
   const void* key_data;
@@ -36,6 +58,7 @@ struct PoolArgs {
   void* out_data;
   uint8_t* out_scales;
   int64_t out_stride;
+  Paging key_pages, out_pages;  // paged caches (table null: contiguous)
   DeviceStatus* status;
 };
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s);
@@ -70,6 +93,9 @@ struct ScanArgs {
   int prefill;
   int64_t ctx;
   int ratio;
+  // Paged cache (table null: contiguous, key_stride rows per sequence). Rows
+  // are then read in groups of 8 (one TMA box each), like gathered blocks.
+  Paging pages;
   DeviceStatus* status;
 };
 // In prefill ROWS_BLOCKS mode only complete blocks are scored; a query's
@@ -177,6 +203,8 @@ struct AttnArgs {
   // KV rows per tile: 32 (four ring slots) or 64 (two ring slots; half the
   // QK^T instructions per row).
   int tile_rows;
+  // Paged latent pool (table null: contiguous, lat_stride rows per sequence).
+  Paging pages;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);

@@ -168,11 +168,21 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
     if (blk >= nb) return;
   }
   const int c = min(8, n - blk * 8);
+  // The block's member rows (consecutive: a page holds whole blocks) and its
+  // block-key row, contiguous or through the page table.
+  int64_t row0 = static_cast<int64_t>(b) * a.key_stride + blk * 8;
+  int64_t orow = static_cast<int64_t>(b) * a.out_stride + blk;
+  if (a.key_pages.table) {
+    row0 = paged_row(a.key_pages, b, static_cast<int64_t>(blk) * 8);
+    orow = paged_row(a.out_pages, b, blk);
+    if (row0 < 0 || orow < 0) {
+      if (lane == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_POOL, b);
+      return;
+    }
+  }
   float acc[4], dec[4];
-  block_mean(a.fmt, a.key_data, a.key_scales, static_cast<int64_t>(b) * a.key_stride + blk * 8, c,
-             lane, acc);
+  block_mean(a.fmt, a.key_data, a.key_scales, row0, c, lane, acc);
   const Stored st = round_to_format(a.fmt, acc, dec);
-  const int64_t orow = static_cast<int64_t>(b) * a.out_stride + blk;
   if (a.fmt == DSA_FMT_BF16) {
     uint16_t* o = static_cast<uint16_t*>(a.out_data);
     *reinterpret_cast<uint2*>(o + orow * 128 + lane * 4) = make_uint2(st.w0, st.w1);

@@ -196,15 +196,20 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
   const int64_t n_own = n_tiles > half ? (n_tiles - half + 1) / 2 : 0;  // tiles half, half + 2, ...
   if (n_own == 0) return;
   const int64_t q_rows = tpq * kTile;
-  const bool gather = a.mode == ROWS_GATHER;
+  // Gathered blocks, and every row of a paged cache, come in groups of 8 rows
+  // (one TMA box each: a page holds whole groups).
+  const bool paged = a.pages.table != nullptr;
+  const bool gather = a.mode == ROWS_GATHER || paged;
   // MX scales of 8 (gathered block) or 128 (contiguous tile) consecutive rows
   // are 32 or 512 contiguous bytes, copied whole when 16-byte aligned.
   const bool scale_vec =
       ((reinterpret_cast<uintptr_t>(a.key_scales) | static_cast<uintptr_t>(a.key_stride * 4)) &
        15u) == 0;
-  // Gathered mode: in round k lane l serves block slot l % 16 of the stage's
-  // tile 2k + l / 16 (16 candidate blocks of 8 keys per tile). Block ids of the
-  // next stage are loaded one stage ahead.
+  // Grouped mode: in round k lane l serves 8-row group l % 16 of the stage's
+  // tile 2k + l / 16 (16 groups of 8 rows per tile): the candidate block
+  // (gathered) or the group's own place in the query's rows (paged). Block ids
+  // are loaded two stages ahead and (paged) their page-table entries one stage
+  // ahead, each from a value that has had a whole stage to arrive.
   constexpr int kRounds = (TPS * 16 + 31) / 32;
   auto fetch_blocks = [&](const TilePos& first, int64_t j0, int (&ids)[kRounds]) {
 #pragma unroll
@@ -215,13 +220,33 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
       TilePos tp = first;
       tp.advance(2 * t, q_rows);
       const int64_t bi = (tp.r0 >> 3) + (lane & 15);
-      if (bi < a.k_blocks) ids[k] = a.block_ids[static_cast<int64_t>(tp.b) * a.k_blocks + bi];
+      if (a.mode != ROWS_GATHER) {
+        ids[k] = static_cast<int>(bi);
+      } else if (bi < a.k_blocks) {
+        ids[k] = a.block_ids[static_cast<int64_t>(tp.b) * a.k_blocks + bi];
+      }
+    }
+  };
+  auto fetch_pages = [&](const TilePos& first, const int (&ids)[kRounds],
+                         int64_t (&phys)[kRounds]) {
+#pragma unroll
+    for (int k = 0; k < kRounds; ++k) {
+      phys[k] = -1;
+      if (!paged || ids[k] < 0) continue;
+      TilePos tp = first;
+      tp.advance(2 * (2 * k + (lane >> 4)), q_rows);
+      phys[k] = paged_row(a.pages, tp.b, int64_t{ids[k]} * kBlock);
     }
   };
   TilePos first;  // the stage's first tile
   first.init(t_begin + half, tpq);
-  int blk[kRounds];
+  int blk[kRounds], blk1[kRounds];  // groups of this stage and of the next
+  int64_t phys[kRounds];            // (paged) their rows in the pool
   fetch_blocks(first, 0, blk);
+  fetch_pages(first, blk, phys);
+  TilePos next = first;
+  next.advance(2 * TPS, q_rows);
+  fetch_blocks(next, TPS, blk1);
   // Visible latents of a query, cached for the last query asked about: a
   // lane's tiles move through the queries in order.
   int nv_b = -1, nv = 0;
@@ -235,10 +260,12 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
   int s = 0;           // stage of this iteration
   uint32_t kpar = 0;   // parity of the stage's use count
   for (int64_t j0 = 0; j0 < n_own; j0 += TPS) {
-    TilePos next = first;
-    next.advance(2 * TPS, q_rows);
-    int blk_next[kRounds];
-    fetch_blocks(next, j0 + TPS, blk_next);
+    TilePos next2 = next;
+    next2.advance(2 * TPS, q_rows);
+    int blk2[kRounds];
+    fetch_blocks(next2, j0 + 2 * TPS, blk2);
+    int64_t phys1[kRounds];
+    fetch_pages(next, blk1, phys1);
     if (j0 >= static_cast<int64_t>(TPS) * R::kStages &&
         !mbar_wait_abortable(&sh.raw_empty[half][s], kpar ^ 1u, &sh.abort, a.status, SITE_SCAN)) {
       return;
@@ -258,11 +285,20 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         if (blk[k] >= 0) {
           TilePos tp = first;
           tp.advance(2 * t, q_rows);
+          // logical first row of the group and the rows the query has there
           const int64_t t0 = static_cast<int64_t>(blk[k]) * kBlock;
-          const int64_t v = n_vis_of(tp.b) - t0;
+          const int n_vis = n_vis_of(tp.b);
+          const int64_t v = (a.mode == ROWS_BLOCKS ? contiguous_rows(a, n_vis) : n_vis) - t0;
           if (v > 0) {
             nrows[k] = static_cast<int>(v < kBlock ? v : kBlock);
             y[k] = static_cast<int64_t>(tp.b) * a.key_stride + t0;
+            if (paged) {
+              y[k] = phys[k];
+              if (y[k] < 0) {
+                nrows[k] = 0;  // its scores stay -inf
+                record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SCAN, static_cast<uint32_t>(tp.b));
+              }
+            }
           }
         }
         const int row0 = (lane & 15) * kBlock;
@@ -379,8 +415,13 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
     }
     cp_async_mbar_arrive_noinc(full);
     first = next;
+    next = next2;
 #pragma unroll
-    for (int k = 0; k < kRounds; ++k) blk[k] = blk_next[k];
+    for (int k = 0; k < kRounds; ++k) {
+      blk[k] = blk1[k];
+      phys[k] = phys1[k];
+      blk1[k] = blk2[k];
+    }
     if (++s == R::kStages) {
       s = 0;
       kpar ^= 1u;
@@ -752,10 +793,12 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
   } else {
     last_rows = a.max_latents;
   }
-  const int64_t rows = (a.prefill ? 0 : (a.B - 1) * a.key_stride) + last_rows;
+  // A paged cache: the whole pool.
+  const int64_t rows = a.pages.table ? a.pages.n_pages * a.pages.rows
+                                     : (a.prefill ? 0 : (a.B - 1) * a.key_stride) + last_rows;
   Maps maps;
   memset(&maps, 0, sizeof(maps));
-  const int box_rows = (a.mode == ROWS_GATHER) ? kBlock : kTile;
+  const int box_rows = (a.mode == ROWS_GATHER || a.pages.table) ? kBlock : kTile;
   cudaError_t e = cudaSuccess;
   if (rows > 0) {
     if (FMT == DSA_FMT_BF16) {
@@ -783,7 +826,7 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
 // go two a stage and MXFP4 tiles (8.5 KB) four a stage over contiguous rows;
 // gathered scans take DSA_SCAN_GATHER_TPS MXFP8 tiles (twice as many MXFP4).
 cudaError_t launch_scan(const ScanArgs& a, int num_sms, cudaStream_t s) {
-  const bool gather = a.mode == ROWS_GATHER;
+  const bool gather = a.mode == ROWS_GATHER || a.pages.table != nullptr;
   if (a.fmt == DSA_FMT_BF16) return launch_fmt<DSA_FMT_BF16, 1>(a, num_sms, s);
   if (a.fmt == DSA_FMT_MXFP8) {
     if (gather) return launch_fmt<DSA_FMT_MXFP8, DSA_SCAN_GATHER_TPS>(a, num_sms, s);
