@@ -41,6 +41,8 @@ METRIC = "sparse-attn decode queries/s at 128K ctx; achieved HBM GB/s vs rooflin
 PREFILL_METRIC = ("sparse-attn prefill queries/s (4096 queries on 64K context); achieved bf16 "
                   "TFLOP/s vs roofline")
 PREFILL_CPU_SAMPLE = 512  # oracle queries timed for a prefill chunk's CPU figure
+MULTI_METRIC = ("sparse-attn multi-query decode queries/s at 128K ctx (5 queries a sequence); "
+                "achieved HBM GB/s vs roofline")
 DEFAULT_WORKLOAD = "decode_b64_t131072_r1_mxfp8"
 PREFILL_WORKLOAD = "prefill_q4096_ctx65536_r2_bf16"
 L2_FLUSH_BYTES = 512 << 20
@@ -249,6 +251,35 @@ def cpu_oracle_prefill_rate(workload: str, n_sample: int, steps: int = 1):
     return len(picks) / t, t, threads, sample
 
 
+def cpu_oracle_multi_rate(workload: str, n_seq: int, steps: int = 1):
+    """Times the oracle, as it stands, on n_seq sequences of a multi-query
+    workload (all of each sequence's queries, its block keys built inside the
+    timed region as the decode leg does). Returns (queries/s, seconds per step,
+    threads, sample description)."""
+    import oracle as O
+    import synth
+    spec = dict(synth.WORKLOADS[workload])
+    assert spec.pop("kind") == "multi"
+    m = synth.multi_inputs([spec["T"]] * n_seq, spec["n_q"], spec["ratio"], spec["key_fmt"],
+                           spec["seed"])
+    cfg = O.StepConfig(ratio=spec["ratio"])
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for b in range(n_seq):
+            view = synth.multi_as_prefill(m, b)
+            kv, pooled, _ = O.prefill_caches(cfg, view)
+            for i in range(m.n_q):
+                O.prefill_query(cfg, view, i, kv, pooled)
+        times.append(time.perf_counter() - t0)
+    threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or os.cpu_count() or 1
+    sample = (f"{n_seq} sequence(s) x {m.n_q} queries of the workload ({spec['T']} tokens, ratio "
+              f"{spec['ratio']}, {spec['key_fmt']} keys); each sequence's block keys are built "
+              "in the timed region")
+    t = float(np.median(times))
+    return n_seq * m.n_q / t, t, threads, sample
+
+
 def auto_cpu_sample(workload: str) -> int:
     import synth
     T = synth.WORKLOADS[workload]["T"]
@@ -261,6 +292,25 @@ def run_reference(args):
         return
     import synth
     spec = synth.WORKLOADS[args.workload]
+    if spec["kind"] == "multi":
+        n = args.cpu_sample or 2
+        for _ in range(args.warmup):
+            cpu_oracle_multi_rate(args.workload, n)
+        qps, t, threads, sample = cpu_oracle_multi_rate(args.workload, n, steps=max(1, args.steps))
+        line = {
+            "impl": "reference", "metric": MULTI_METRIC, "value": qps, "unit": "queries/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": spec["B"], "queries_per_seq": spec["n_q"],
+                       "tokens": spec["T"], "ratio": spec["ratio"], "key_fmt": spec["key_fmt"]},
+            "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     if spec["kind"] == "prefill":
         n = args.cpu_sample or PREFILL_CPU_SAMPLE
         for _ in range(args.warmup):
@@ -321,6 +371,8 @@ def run_ours(args):
     spec = dict(synth.WORKLOADS[args.workload])
     if spec["kind"] == "prefill":
         return run_prefill(args, spec, dsa, synth, dev, rank, world)
+    if spec["kind"] == "multi":
+        return run_multi(args, spec, dsa, synth, dev, rank, world)
     B, T, ratio, fmt = spec["B"], spec["T"], spec["ratio"], spec["key_fmt"]
     page_rows = spec.get("page_rows", 0)
     if args.batch:
@@ -853,6 +905,140 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world, workload=None, steps=N
     if world > 1 and emit:
         torch.distributed.destroy_process_group()
     return line if rank == 0 else None
+
+
+def run_multi(args, spec, dsa, synth, dev, rank, world):
+    """Multi-query decode: every sequence's n_q queries at its last n_q
+    positions, one dsa_decode_multi call a step (inputs resident in HBM, the
+    block-key cache built once outside the step)."""
+    import torch
+    B, T, n_q, ratio, fmt = spec["B"], spec["T"], spec["n_q"], spec["ratio"], spec["key_fmt"]
+    if args.batch:
+        B = args.batch
+    t0 = time.time()
+    m = synth.multi_inputs([T] * B, n_q, ratio, fmt, shard_seed(spec["seed"], rank))
+    gen_s = time.time() - t0
+    cfg = dsa.config(ratio=ratio)
+    cap = m.cap
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, q_idx, w, latents, swa = d(m.q), d(m.q_idx), d(m.w), d(m.latents), d(m.swa)
+    n_tok, n_lat = d(m.T.astype(np.int32)), d(m.n_latents)
+    keys = dsa.Keys(fmt, d(m.keys.data), None if m.keys.scales is None else d(m.keys.scales))
+    L = int(m.n_latents.max())
+    del m
+    nbc = cap // 8
+    width = 64 if fmt == "mxfp4" else 128
+    nbc += nbc & 1 if fmt == "mxfp4" else 0
+    if fmt == "bf16":
+        pooled = dsa.Keys(fmt, torch.empty((B, nbc, 128), dtype=torch.int16, device=dev))
+    else:
+        pooled = dsa.Keys(fmt, torch.empty((B, nbc, width), dtype=torch.uint8, device=dev),
+                          torch.empty((B, nbc, 4), dtype=torch.uint8, device=dev))
+    ws = dsa.workspace(cfg, B * n_q, cap, dev)
+    dsa.pool_index_keys(cfg, keys, n_lat, cap, pooled, ws)
+    out = torch.empty((B, n_q, 64, 512), dtype=torch.int16, device=dev)
+    lse = torch.empty((B, n_q, 64), dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+
+    def step():
+        dsa.decode_multi(cfg, n_tok, q, q_idx, w, keys, pooled, latents, cap, swa, out, ws, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        step()
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+    g = torch.cuda.CUDAGraph()
+    dsa.launch_counts(reset=True)
+    with torch.cuda.graph(g):
+        step()
+    per_replay = dsa.launch_counts(reset=True)
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clocks:
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            for _ in range(10):
+                flush()
+                g.replay()
+            torch.cuda.synchronize()
+        for i in range(K):
+            flush()
+            ev_s[i].record()
+            g.replay()
+            ev_e[i].record()
+        torch.cuda.synchronize()
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(ev_s, ev_e)]
+    ms = reduce_max([float(np.mean(step_ms))], dev)[0]
+    kinds = {"pool": 1, "scan": 2, "select": 2, "attn": 1}
+    kev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n * K)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(n * K)])
+           for k, n in kinds.items()}
+    for k, (a_, b_) in kev.items():
+        dsa.profile_events(k, a_, b_)
+    dsa.launch_counts(reset=True)
+    for i in range(K):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    for k in kinds:
+        dsa.profile_events(k, [], [])
+    n_launch = dsa.launch_counts(reset=True)
+    kern_ms = {k: [s_.elapsed_time(e_) for s_, e_ in zip(*kev[k])][:n_launch[k]] for k in kinds}
+    kernel_ms = {k: float(sum(v) / K) for k, v in kern_ms.items()}
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+    # Scan roofline. Every query scans its sequence's block keys and its own
+    # 2048 candidate blocks; the n_q queries of a sequence read the same block
+    # keys, so the algorithmic bytes count those once per sequence (the
+    # candidate blocks, mostly shared too, are counted per query: an upper
+    # bound of the unique bytes).
+    row_bytes = {"mxfp8": 132, "mxfp4": 68}.get(fmt, 256)
+    nb = -(-L // 8)
+    blk_bytes = B * nb * row_bytes
+    tok_bytes = B * n_q * min(nb, cfg.k_blocks) * 8 * row_bytes
+    scan_ms = kern_ms["scan"]
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved_blk = blk_bytes / (float(np.mean(scan_ms[0::2])) * 1e-3) / 1e9
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            qps, _, threads, sample = cpu_oracle_multi_rate(args.workload, args.cpu_sample or 2)
+            cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
+                   "sample": sample}
+        line = {
+            "metric": MULTI_METRIC, "value": job_rate(B * n_q, world, ms), "unit": "queries/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch_per_gpu": B, "queries_per_seq": n_q,
+                       "tokens": T, "ratio": ratio, "key_fmt": fmt, "latents": L,
+                       "l2": L2Flush.DESCRIPTION, "input_gen_s": round(gen_s, 1)},
+            "roofline": {"kernel": "scan, block stage (the block keys shared by a sequence's "
+                                   "queries, counted once)", "bound": "hbm",
+                         "achieved": achieved_blk, "peak": hbm_peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": achieved_blk / hbm_peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": blk_bytes,
+                         "token_stage_bytes_upper_bound": tok_bytes,
+                         "launch_ms_block_stage": float(np.mean(scan_ms[0::2])),
+                         "launch_ms_token_stage": float(np.mean(scan_ms[1::2]))},
+            "cpu_baseline": cpu,
+            "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q_)) for q_ in (10, 50, 90)],
+            "kernel_ms_per_step": kernel_ms,
+            "gpu_launches": int(sum(per_replay.values())) * K,
+            "gpu_launches_by_kind": {k: v * K for k, v in per_replay.items()},
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
 
 def main():

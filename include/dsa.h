@@ -296,6 +296,41 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
                                      size_t workspace_bytes, dsa_stream_t stream);
 
 /*
+ * Multi-query decode: n_q queries per sequence at its last n_q positions, as
+ * when a block of draft tokens is verified in one pass (recipes.vllm.ai
+ * "DeepSeek-V4.1-Flash", Overview, bullet "DSpark draft head"). Sequence b
+ * holds T_b = n_tokens[b] tokens and its query i sits at position
+ * P = T_b - n_q + i. Each query is causal with its own two-tier selection over
+ * floor((P + 1) / ratio) latents (a block it sees in part is pooled over its
+ * visible members on the fly, as in prefill) and its own window of positions
+ * max(0, P - window + 1) .. P; the queries of a sequence read the same caches.
+ *   n_tokens:    device int32 [B], each >= n_q (the queries of a shorter
+ *                sequence that have no position get no rows, reported as
+ *                DSA_ERR_DEVICE_CHECK)
+ *   q:           device bf16 [B, n_q, 64, 512]; q_idx bf16 [B, n_q, 16, 128];
+ *                w fp32 [B, n_q, 16]
+ *   keys:        index keys of each sequence, contiguous (seq_stride_rows >=
+ *                max_latents)
+ *   pooled:      block keys of each sequence's complete blocks, as
+ *                dsa_pool_index_keys writes them (seq_stride_rows >= max_latents / 8)
+ *   latents:     bf16, sequence b's row r at (b * latent_seq_stride_rows + r) * 512
+ *   max_latents: at least floor(n_tokens[b] / ratio) for every b
+ *   swa:         device bf16 [B, window + n_q - 1, 512]; row r of sequence b
+ *                holds position T_b - n_q - window + 1 + r (rows before
+ *                position 0 are never read)
+ *   out:         out, bf16 [B, n_q, 64, 512]; lse: out (optional) fp32 [B, n_q, 64]
+ *   token_ids:   out (optional), int32 [B, n_q, k_tokens]
+ * The workspace is sized for B * n_q queries (dsa_workspace_size).
+ */
+dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n_tokens,
+                              const void* q, const void* q_idx, const float* w,
+                              const dsa_keys_t* keys, const dsa_keys_t* pooled,
+                              const void* latents, int64_t latent_seq_stride_rows,
+                              int64_t max_latents, const void* swa, int B, void* out, float* lse,
+                              int32_t* token_ids, void* workspace, size_t workspace_bytes,
+                              dsa_stream_t stream);
+
+/*
  * dsa_topk without a workspace. The pages have no counterpart to this call; it
  * serves callers that cannot allocate device memory: a plugin that runs inside
  * a host framework which owns all device memory and lends it none, or a

@@ -246,6 +246,73 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
 
 
 @dataclass
+class MultiInputs:
+    """A multi-query decode batch: sequence b holds T[b] tokens and its n_q
+    queries sit at positions T[b] - n_q + i. Caches are those of a DecodeInputs
+    batch; q, q_idx and w gain a query axis, and window row r of sequence b
+    holds position T[b] - n_q - window + 1 + r (zero rows before position 0)."""
+    T: np.ndarray
+    n_q: int
+    ratio: int
+    q: np.ndarray          # uint16 bf16 [B, n_q, 64, 512]
+    q_idx: np.ndarray      # uint16 bf16 [B, n_q, 16, 128]
+    w: np.ndarray          # float32 [B, n_q, 16]
+    latents: np.ndarray    # uint16 bf16 [B, cap, 512]
+    keys: Keys             # [B, cap, ...]
+    swa: np.ndarray        # uint16 bf16 [B, window + n_q - 1, 512]
+    n_latents: np.ndarray  # int32 [B] = T // ratio
+    window: int = WINDOW
+
+    @property
+    def B(self) -> int:
+        return int(self.T.shape[0])
+
+    @property
+    def cap(self) -> int:
+        return int(self.latents.shape[1])
+
+
+def multi_inputs(T, n_q: int, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
+                 q_scale: float = 1.0) -> MultiInputs:
+    """A multi-query decode batch over the caches decode_inputs builds for the
+    same T (its own query, index-query, weight and window streams)."""
+    base = decode_inputs(T, ratio, key_fmt, seed, window=window, q_scale=q_scale)
+    B = base.B
+    s512 = 1.0 / np.sqrt(512.0)
+    s128 = 1.0 / np.sqrt(128.0)
+    q = np.empty((B, n_q, N_HEADS, LATENT_DIM), np.uint16)
+    q_idx = np.empty((B, n_q, N_IDX_HEADS, IDX_DIM), np.uint16)
+    w = np.empty((B, n_q, N_IDX_HEADS), np.float32)
+    n_sw = window + n_q - 1
+    swa = np.empty((B, n_sw, LATENT_DIM), np.uint16)
+    for b in range(B):
+        off = _seq_offset(b) + (1 << 39)  # apart from decode_inputs' streams
+        normal_bf16(seed, TAG_Q, off, n_q * N_HEADS * LATENT_DIM, s512 * q_scale,
+                    out=q[b].reshape(-1))
+        normal_bf16(seed, TAG_QIDX, off, n_q * N_IDX_HEADS * IDX_DIM, s128,
+                    out=q_idx[b].reshape(-1))
+        w[b] = uniform_f32(seed, TAG_W, off, n_q * N_IDX_HEADS).reshape(n_q, N_IDX_HEADS)
+        normal_bf16(seed, TAG_SWA, off, n_sw * LATENT_DIM, s512, out=swa[b].reshape(-1))
+        first_pos = int(base.T[b]) - n_q - window + 1
+        if first_pos < 0:
+            swa[b, :min(n_sw, -first_pos)] = 0
+    return MultiInputs(T=base.T, n_q=n_q, ratio=ratio, q=q, q_idx=q_idx, w=w,
+                       latents=base.latents, keys=base.keys, swa=swa, n_latents=base.n_latents,
+                       window=window)
+
+
+def multi_as_prefill(inp: MultiInputs, b: int) -> "PrefillInputs":
+    """Sequence b of a multi-query batch seen as a prefill chunk: n_q queries
+    appended after T[b] - n_q tokens, with the same bytes (no copy of values)."""
+    n_lat = int(inp.n_latents[b])
+    keys = Keys(inp.keys.fmt, inp.keys.data[b], None if inp.keys.scales is None
+                else inp.keys.scales[b])
+    return PrefillInputs(ctx=int(inp.T[b]) - inp.n_q, ratio=inp.ratio, q=inp.q[b],
+                         q_idx=inp.q_idx[b], w=inp.w[b], latents=inp.latents[b],
+                         keys=keys, swa=inp.swa[b], window=inp.window)
+
+
+@dataclass
 class PrefillInputs:
     """A prefill chunk of n_q queries appended after ctx tokens of one sequence.
 
@@ -345,6 +412,10 @@ WORKLOADS = {
     # block table (the paged layout serving engines use).
     "decode_b64_t131072_r1_mxfp8_paged64": dict(kind="decode", B=64, T=131072, ratio=1,
                                                 key_fmt="mxfp8", seed=2, page_rows=64),
+    # Multi-query decode: the 64 x 131072 batch with 5 queries a sequence (a
+    # DSpark block of draft tokens verified in one pass).
+    "decode_mq5_b64_t131072_r1_mxfp8": dict(kind="multi", B=64, n_q=5, T=131072, ratio=1,
+                                            key_fmt="mxfp8", seed=2),
 }
 
 
@@ -356,4 +427,7 @@ def workload_inputs(name: str, **kw):
     if kind == "decode":
         B, T = spec.pop("B"), spec.pop("T")
         return decode_inputs([T] * B, **spec)
+    if kind == "multi":
+        B, T, n_q = spec.pop("B"), spec.pop("T"), spec.pop("n_q")
+        return multi_inputs([T] * B, n_q, **spec)
     return prefill_inputs(**spec)

@@ -33,7 +33,7 @@ EXPORTS = ("dsa_default_config", "dsa_status_string", "dsa_workspace_size",
            "dsa_pool_index_keys", "dsa_index_blocks", "dsa_topk", "dsa_sparse_attn_decode",
            "dsa_decode_step", "dsa_sparse_attn_prefill", "dsa_read_device_status",
            "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc",
-           "dsa_selftest_timeout", "dsa_sparse_attn_decode_paged")
+           "dsa_selftest_timeout", "dsa_sparse_attn_decode_paged", "dsa_decode_multi")
 
 TOPK_NOALLOC_MAX_SCORES = 1 << 21
 
@@ -101,6 +101,8 @@ def load() -> ctypes.CDLL:
         lib.dsa_selftest_timeout.argtypes = [vp, sz, vp]
         lib.dsa_sparse_attn_decode_paged.argtypes = [cp, vp, vp, ctypes.POINTER(_Pages), vp, vp,
                                                      vp, vp, i32, vp, vp, vp, sz, vp]
+        lib.dsa_decode_multi.argtypes = [cp, i32, vp, vp, vp, vp, kp, kp, vp, i64, i64, vp, i32,
+                                         vp, vp, vp, vp, sz, vp]
         for f in EXPORTS:
             if f not in ("dsa_default_config", "dsa_status_string"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -240,6 +242,18 @@ def decode_step(cfg, q, q_idx, w, keys: Keys, pooled: Keys, latents, n_latents, 
                                   max_latents, _p(swa), _p(swa_len), B, _p(block_ids),
                                   _p(token_ids), _p(out), _p(lse), _p(ws), ws.numel(),
                                   _stream(stream)), "dsa_decode_step")
+
+
+def decode_multi(cfg, n_tokens, q, q_idx, w, keys: Keys, pooled: Keys, latents, max_latents, swa,
+                 out, ws, lse=None, token_ids=None, stream=None):
+    """Multi-query decode: q [B, n_q, 64, 512], each sequence's n_q queries at its
+    last n_q positions (n_tokens [B] device int32)."""
+    B, n_q = q.shape[0], q.shape[1]
+    _check(load().dsa_decode_multi(ctypes.byref(cfg), n_q, _p(n_tokens), _p(q), _p(q_idx), _p(w),
+                                   ctypes.byref(keys.c()), ctypes.byref(pooled.c()), _p(latents),
+                                   latents.shape[1], max_latents, _p(swa), B, _p(out), _p(lse),
+                                   _p(token_ids), _p(ws), ws.numel(), _stream(stream)),
+           "dsa_decode_multi")
 
 
 def sparse_attn_prefill(cfg, ctx_len, q, q_idx, w, latents, keys: Keys, pooled: Keys, swa, out,

@@ -208,15 +208,23 @@ bool prefill_batched(const dsa_keys_t& k, int prefill, int64_t rows) {
   return prefill && k.fmt == DSA_FMT_BF16 && rows > 0;
 }
 
+// Multi-query decode: mq queries per sequence, each sequence holding
+// n_tokens[s] tokens (mq = 0: a plain decode batch or one prefill chunk).
+struct MultiQuery {
+  int mq = 0;
+  const int32_t* n_tokens = nullptr;
+};
+
 // Launch sequences shared by the public calls. `sel_tmp`: scratch of
 // 32768 ids per query for two-pass selections (may be null).
 dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const float* w,
                              const dsa_keys_t& pooled, const int32_t* n_lat, int B,
                              int64_t max_latents, int32_t* block_ids, float* scores,
                              DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s, int prefill,
-                             int64_t ctx, const dsa_keys_t* partial_keys) {
+                             int64_t ctx, const dsa_keys_t* partial_keys,
+                             MultiQuery m = MultiQuery{}) {
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
-  if (prefill_batched(pooled, prefill, max_latents / kBlock)) {
+  if (m.mq == 0 && prefill_batched(pooled, prefill, max_latents / kBlock)) {
     BatchedScanArgs ba{};
     ba.key_data = static_cast<const uint16_t*>(pooled.data);
     ba.key_rows = max_latents / kBlock;  // complete blocks
@@ -235,11 +243,13 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     sa.fmt = pooled.fmt;
     sa.key_data = pooled.data;
     sa.key_scales = pooled.scales;
-    sa.key_stride = prefill ? 0 : pooled.seq_stride_rows;
+    sa.key_stride = prefill && m.mq == 0 ? 0 : pooled.seq_stride_rows;
     sa.q_idx = q_idx;
     sa.w = w;
     sa.n_latents = n_lat;
     sa.max_latents = max_latents;
+    sa.mq = m.mq;
+    sa.n_tokens = m.n_tokens;
     sa.mode = ROWS_BLOCKS;
     sa.pages = paging_of(pooled.pages, kBlock);
     sa.n_rows = nb_max;
@@ -261,6 +271,9 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     pa.n_q = B;
     pa.ctx = ctx;
     pa.ratio = c.ratio;
+    pa.mq = m.mq;
+    pa.n_tokens = m.n_tokens;
+    pa.key_stride = m.mq > 0 ? partial_keys->seq_stride_rows : 0;
     pa.scores = scores;
     pa.n_rows = nb_max;
     DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_prefill_partial(pa, s); }));
@@ -281,9 +294,9 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              const dsa_keys_t& keys, const int32_t* block_ids,
                              const int32_t* n_lat, int B, int64_t max_latents, int32_t* token_ids,
                              float* scores, DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s,
-                             int prefill, int64_t ctx) {
+                             int prefill, int64_t ctx, MultiQuery m = MultiQuery{}) {
   SelectArgs se{};
-  if (block_ids && prefill_batched(keys, prefill, max_latents)) {
+  if (block_ids && m.mq == 0 && prefill_batched(keys, prefill, max_latents)) {
     // Dense token scores over every latent, read by the selection through
     // the block ids.
     BatchedScanArgs ba{};
@@ -307,11 +320,13 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     sa.fmt = keys.fmt;
     sa.key_data = keys.data;
     sa.key_scales = keys.scales;
-    sa.key_stride = prefill ? 0 : keys.seq_stride_rows;
+    sa.key_stride = prefill && m.mq == 0 ? 0 : keys.seq_stride_rows;
     sa.q_idx = q_idx;
     sa.w = w;
     sa.n_latents = n_lat;
     sa.max_latents = max_latents;
+    sa.mq = m.mq;
+    sa.n_tokens = m.n_tokens;
     sa.pages = paging_of(keys.pages, 1);
     if (block_ids) {
       sa.mode = ROWS_GATHER;
@@ -756,6 +771,70 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   a.ratio = cfg->ratio;
   a.status = st;
   set_splits(a, *cfg, n_q);
+  DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
+  return DSA_OK;
+}
+
+dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n_tokens,
+                              const void* q, const void* q_idx, const float* w,
+                              const dsa_keys_t* keys, const dsa_keys_t* pooled,
+                              const void* latents, int64_t latent_seq_stride_rows,
+                              int64_t max_latents, const void* swa, int B, void* out, float* lse,
+                              int32_t* token_ids, void* workspace, size_t workspace_bytes,
+                              dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (n_q < 1 || B < 0 || max_latents < 0 || max_latents > kMaxLatents ||
+      latent_seq_stride_rows < max_latents || static_cast<int64_t>(B) * n_q > (1 << 30)) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (n_tokens == nullptr || q == nullptr || q_idx == nullptr || w == nullptr ||
+      latents == nullptr || swa == nullptr || out == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(w) || !aligned16(latents) ||
+      !aligned16(swa) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (token_ids && !aligned16(token_ids)) || (reinterpret_cast<uintptr_t>(n_tokens) & 3u)) {
+    return DSA_ERR_MISALIGNED;
+  }
+  DSA_TRY(check_keys(keys, max_latents, true));
+  DSA_TRY(check_keys(pooled, max_latents / kBlock, true));
+  if (pooled->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  if (keys->pages != nullptr || pooled->pages != nullptr) return DSA_ERR_INVALID_ARG;
+  const int nq_total = B * n_q;
+  Layout L;
+  DSA_TRY(check_ws(*cfg, nq_total, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
+  const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
+  const MultiQuery m{n_q, n_tokens};
+  int32_t* bids = at<int32_t>(workspace, L.block_ids);
+  DSA_TRY(run_block_stage(*cfg, qi, w, *pooled, nullptr, nq_total, max_latents, bids,
+                          at<float>(workspace, L.block_scores), st, select_tmp(workspace, L), s, 1,
+                          0, keys, m));
+  int32_t* tids = token_ids ? token_ids : at<int32_t>(workspace, L.token_ids);
+  DSA_TRY(run_token_stage(*cfg, qi, w, *keys, bids, nullptr, nq_total, max_latents, tids,
+                          at<float>(workspace, L.token_scores), st, select_tmp(workspace, L), s, 1,
+                          0, m));
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.latents = static_cast<const uint16_t*>(latents);
+  a.lat_stride = latent_seq_stride_rows;
+  a.token_ids = tids;
+  a.k_tokens = cfg->k_tokens;
+  a.swa = static_cast<const uint16_t*>(swa);
+  a.window = cfg->window;
+  a.B = nq_total;
+  a.scale_log2 = tau(*cfg) * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.prefill = 1;
+  a.ratio = cfg->ratio;
+  a.mq = n_q;
+  a.n_tokens = n_tokens;
+  a.swa_seq_rows = cfg->window + n_q - 1;
+  a.status = st;
+  set_splits(a, *cfg, nq_total);
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }

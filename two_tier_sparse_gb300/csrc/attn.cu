@@ -164,11 +164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint16_t* win;
   int64_t wrow0;  // row of the window buffer holding this query's first window row
   if (a.prefill) {
-    const int64_t P = a.ctx + b;
+    int64_t P = query_pos(a.ctx, a.mq, a.n_tokens, b);
+    if (P < 0) {
+      // a multi-query sequence with fewer tokens than queries: this query has
+      // no position, hence no rows
+      if (tid == 0 && split == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
+      P = -1;
+    }
     n_vis = static_cast<int>((P + 1) / a.ratio);
     const int64_t first = P - a.window + 1 > 0 ? P - a.window + 1 : 0;
-    const int64_t base_pos = a.ctx - a.window + 1;
-    wrow0 = first - base_pos;
+    // the window buffer's row 0 holds position (first query's position) - window + 1
+    const int64_t base_pos = (a.mq > 0 ? P - b % a.mq : a.ctx) - a.window + 1;
+    wrow0 = static_cast<int64_t>(query_seq(a.mq, b)) * a.swa_seq_rows + (first - base_pos);
     win = a.swa + wrow0 * kLatent;
     n_sw = static_cast<int>(P - first + 1);
   } else {
@@ -185,9 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Latent rows: ids index this sequence's rows, or (paged) the compaction
   // below turns them into rows of the shared pool.
   const bool paged = a.pages.table != nullptr;
-  const uint16_t* lat =
-      a.latents +
-      (a.prefill || paged ? 0 : static_cast<int64_t>(b) * a.lat_stride * kLatent);
+  const int lat_seq = a.prefill ? query_seq(a.mq, b) : (paged ? 0 : b);
+  const uint16_t* lat = a.latents + static_cast<int64_t>(lat_seq) * a.lat_stride * kLatent;
   // This CTA's rows: its part of the window rows first (they are inputs of the
   // step, so they stream while the previous kernel still selects the tokens),
   // then its part of the selected latents (known once the ids are compacted).
@@ -777,8 +783,10 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   // 32 rows x 64 dims.
   CUtensorMap wmap;
   memset(&wmap, 0, sizeof(wmap));
-  const uint64_t wrows = a.prefill ? static_cast<uint64_t>(a.B) + a.window - 1
-                                   : static_cast<uint64_t>(a.B) * a.window;
+  const uint64_t wrows =
+      a.prefill ? (a.mq > 0 ? static_cast<uint64_t>(a.B / a.mq) * a.swa_seq_rows
+                            : static_cast<uint64_t>(a.B) + a.window - 1)
+                : static_cast<uint64_t>(a.B) * a.window;
   e = encode_tma_2d(&wmap, a.swa, 2, kLatent, wrows, kLatent * 2, 64, 32);
   if (e != cudaSuccess) return e;
   if (a.tile_rows == 64) {

@@ -46,6 +46,16 @@ __device__ __forceinline__ int64_t paged_row(const Paging& p, int b, int64_t r) 
   return static_cast<int64_t>(pg) * p.rows + (ri - pi * p.rows);
 }
 
+// Position of query b of a prefill-mode call: ctx + b for a chunk of one
+// sequence; in a multi-query decode batch (mq queries per sequence, sequence
+// s holding n_tokens[s] tokens) the (b % mq)-th of sequence b / mq's last mq
+// positions.
+__device__ __forceinline__ int64_t query_pos(int64_t ctx, int mq, const int32_t* n_tokens,
+                                             int b) {
+  return mq > 0 ? int64_t{n_tokens[b / mq]} - mq + b % mq : ctx + b;
+}
+__device__ __forceinline__ int query_seq(int mq, int b) { return mq > 0 ? b / mq : 0; }
+
 struct PoolArgs {
   int fmt;
   const void* key_data;
@@ -89,10 +99,13 @@ struct ScanArgs {
   float* scores;   // [B, n_rows]
   int B;
   // Prefill: query b sees n_latents = (ctx + b + 1) / ratio latents of one
-  // shared key array (key_stride 0).
+  // shared key array (key_stride 0). Multi-query decode (mq > 0): prefill mode
+  // over B / mq sequences of key_stride rows, query b at query_pos().
   int prefill;
   int64_t ctx;
   int ratio;
+  int mq;
+  const int32_t* n_tokens;
   // Paged cache (table null: contiguous, key_stride rows per sequence). Rows
   // are then read in groups of 8 (one TMA box each), like gathered blocks.
   Paging pages;
@@ -137,6 +150,9 @@ struct PartialArgs {
   int n_q;
   int64_t ctx;
   int ratio;
+  int mq;                    // multi-query decode: queries per sequence (0: one sequence)
+  const int32_t* n_tokens;   //   [n_q / mq] tokens per sequence
+  int64_t key_stride;        //   key rows per sequence
   float* scores;
   int64_t n_rows;
 };
@@ -192,10 +208,15 @@ struct AttnArgs {
   uint16_t* out;     // bf16 [B, 64, 512]
   float* lse;        // [B, 64] or null
   // Prefill: query b is at position ctx + b, n_latents = (ctx + b + 1) / ratio,
-  // window rows from the shared buffer.
+  // window rows from the shared buffer. Multi-query decode (mq > 0): query b
+  // at query_pos(), sequence b / mq's latents at lat_stride rows a sequence
+  // and its window buffer at swa_seq_rows rows a sequence.
   int prefill;
   int64_t ctx;
   int ratio;
+  int mq;
+  const int32_t* n_tokens;
+  int64_t swa_seq_rows;
   // Split-KV: with splits = S in {2, 4, 8} each query's window rows and
   // selected latents are each cut in S parts handled by the S CTAs of a
   // cluster (merged on chip); 1: one CTA per query.

@@ -197,19 +197,23 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
   }
 }
 
-// One warp per prefill query: pool its partially visible last block and score it.
+// One warp per prefill query (or multi-query decode query): pool its
+// partially visible last block and score it.
 __global__ void __launch_bounds__(256) prefill_partial_kernel(PartialArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= a.n_q) return;
-  const int n = static_cast<int>((a.ctx + b + 1) / a.ratio);
+  const int64_t P = query_pos(a.ctx, a.mq, a.n_tokens, b);
+  if (P < 0) return;  // a sequence shorter than its queries (reported by the attention)
+  const int n = static_cast<int>((P + 1) / a.ratio);
   const int c = n & 7;
   if (c == 0) return;
   const int blk = n >> 3;
   float acc[4], key[4];
-  block_mean(a.fmt, a.key_data, a.key_scales, static_cast<int64_t>(blk) * 8, c, lane, acc);
+  const int64_t row0 = static_cast<int64_t>(query_seq(a.mq, b)) * a.key_stride;
+  block_mean(a.fmt, a.key_data, a.key_scales, row0 + static_cast<int64_t>(blk) * 8, c, lane, acc);
   round_to_format(a.fmt, acc, key);
   // dot_h = q_h . key: each lane's 4 products, then a fixed xor-tree sum.
   const uint16_t* q = a.q_idx + static_cast<int64_t>(b) * kIdxHeads * kIdxDim;

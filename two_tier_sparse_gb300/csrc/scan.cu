@@ -149,7 +149,8 @@ struct Maps {
 };
 
 __device__ __forceinline__ int visible_latents(const ScanArgs& a, int b) {
-  int n = a.prefill ? static_cast<int>((a.ctx + b + 1) / a.ratio) : a.n_latents[b];
+  int n = a.prefill ? static_cast<int>((query_pos(a.ctx, a.mq, a.n_tokens, b) + 1) / a.ratio)
+                    : a.n_latents[b];
   if (n > a.max_latents) n = static_cast<int>(a.max_latents);
   return n < 0 ? 0 : n;
 }
@@ -164,6 +165,11 @@ __device__ __forceinline__ int64_t contiguous_rows(const ScanArgs& a, int n_vis)
     n = n_vis;
   }
   return n < a.n_rows ? n : a.n_rows;
+}
+
+// First key row of query b's sequence in a contiguous cache.
+__device__ __forceinline__ int64_t seq_row0(const ScanArgs& a, int b) {
+  return static_cast<int64_t>(a.mq > 0 ? b / a.mq : b) * a.key_stride;
 }
 
 // Position of a CTA's tile: query b and first row r0 of that query's rows.
@@ -291,7 +297,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
           const int64_t v = (a.mode == ROWS_BLOCKS ? contiguous_rows(a, n_vis) : n_vis) - t0;
           if (v > 0) {
             nrows[k] = static_cast<int>(v < kBlock ? v : kBlock);
-            y[k] = static_cast<int64_t>(tp.b) * a.key_stride + t0;
+            y[k] = seq_row0(a, tp.b) + t0;
             if (paged) {
               y[k] = phys[k];
               if (y[k] < 0) {
@@ -385,7 +391,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         if (nrows[t] == 0) continue;
         TilePos tp = first;
         tp.advance(2 * t, q_rows);
-        const int64_t row = static_cast<int64_t>(tp.b) * a.key_stride + tp.r0;
+        const int64_t row = seq_row0(a, tp.b) + tp.r0;
         const uint32_t codes = R::codes(stage, t);
         const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
         if (lane == 0) {
@@ -794,8 +800,9 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
     last_rows = a.max_latents;
   }
   // A paged cache: the whole pool.
+  const int64_t n_seqs = a.mq > 0 ? a.B / a.mq : (a.prefill ? 1 : a.B);
   const int64_t rows = a.pages.table ? a.pages.n_pages * a.pages.rows
-                                     : (a.prefill ? 0 : (a.B - 1) * a.key_stride) + last_rows;
+                                     : (n_seqs - 1) * a.key_stride + last_rows;
   Maps maps;
   memset(&maps, 0, sizeof(maps));
   const int box_rows = (a.mode == ROWS_GATHER || a.pages.table) ? kBlock : kTile;
