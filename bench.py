@@ -280,6 +280,26 @@ def cpu_oracle_multi_rate(workload: str, n_seq: int, steps: int = 1):
     return n_seq * m.n_q / t, t, threads, sample
 
 
+THREADS_NOTE = ("the oracle's loops run in one Python thread; numpy's BLAS calls inside them may "
+                "use up to `cores` threads")
+
+
+def cpu_oracle_one_thread(workload: str, n_seq: int):
+    """The decode oracle timed again in a child process whose BLAS and OpenMP
+    are held to one thread (environment set before numpy loads). Returns
+    {"value", "unit", "threads": 1, "sample"} or None if the child failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_oracle_rate(%r, %d)))" % (ROOT, workload, n_seq))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=900)
+        qps, _, _, sample = json.loads(p.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": qps, "unit": "queries/s", "threads": 1, "sample": sample}
+
+
 def auto_cpu_sample(workload: str) -> int:
     import synth
     T = synth.WORKLOADS[workload]["T"]
@@ -678,7 +698,8 @@ def run_ours(args):
         n = args.cpu_sample or auto_cpu_sample(args.workload)
         qps, t, threads, sample = cpu_oracle_rate(args.workload, n)
         cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
-               "sample": sample}
+               "sample": sample, "threads_note": THREADS_NOTE,
+               "one_thread": cpu_oracle_one_thread(args.workload, max(1, min(n, 4)))}
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -874,7 +895,7 @@ def run_prefill(args, spec, dsa, synth, dev, rank, world, workload=None, steps=N
             qps, _, threads, sample = cpu_oracle_prefill_rate(
                 workload, (args.cpu_sample if emit else 0) or PREFILL_CPU_SAMPLE)
             cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
-                   "sample": sample}
+                   "sample": sample, "threads_note": THREADS_NOTE}
         line = {
             "metric": PREFILL_METRIC,
             "value": job_rate(n_q, world, ms), "unit": "queries/s", "n_gpus": world, "steps": K,
@@ -1012,7 +1033,7 @@ def run_multi(args, spec, dsa, synth, dev, rank, world):
         if not args.no_cpu_baseline and world == 1:
             qps, _, threads, sample = cpu_oracle_multi_rate(args.workload, args.cpu_sample or 2)
             cpu = {"value": qps, "unit": "queries/s", "cores": threads, "kind": "oracle",
-                   "sample": sample}
+                   "sample": sample, "threads_note": THREADS_NOTE}
         line = {
             "metric": MULTI_METRIC, "value": job_rate(B * n_q, world, ms), "unit": "queries/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,

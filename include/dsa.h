@@ -42,6 +42,10 @@
  *     dsa_read_device_status reports DSA_ERR_DEVICE_CHECK.
  *   - Determinism: results are bit-identical from run to run (no floating-point
  *     atomics; every reduction has a fixed order).
+ *   - Tracing: each call marks its phases as NVTX ranges (dsa.decode_step,
+ *     dsa.decode_multi, dsa.prefill, dsa.pool, dsa.block_stage,
+ *     dsa.token_stage, dsa.attention) that a profiler shows on its timeline;
+ *     with no tool attached a range costs two calls into empty stubs.
  */
 #ifndef DSA_H_
 #define DSA_H_

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <mutex>
@@ -13,6 +14,16 @@
 namespace dsa {
 
 namespace {
+
+// NVTX range over a scope: the call's phases show by name in a profiler's
+// timeline (Nsight Systems, ncu --nvtx); without a tool attached a push or pop
+// is one call into an empty stub.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -96,6 +107,14 @@ Paging paging_of(const dsa_pages_t* pg, int div) {
     p.n_pages = pg->n_pages;
   }
   return p;
+}
+
+// Rows of a cache array of B sequences that hold at most `rows` rows each
+// (contiguous: every sequence's stride but the last's own rows; paged: the
+// pool), for the debug checks of the kernels.
+int64_t cache_rows(const dsa_pages_t* pg, int div, int B, int64_t stride, int64_t rows) {
+  if (pg != nullptr) return pg->n_pages * (pg->page_rows / div);
+  return B > 0 ? (B - 1) * stride + rows : 0;
 }
 
 bool same_pages(const dsa_pages_t* a, const dsa_pages_t* b) {
@@ -223,6 +242,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s, int prefill,
                              int64_t ctx, const dsa_keys_t* partial_keys,
                              MultiQuery m = MultiQuery{}) {
+  Range range("dsa.block_stage");
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
   if (m.mq == 0 && prefill_batched(pooled, prefill, max_latents / kBlock)) {
     BatchedScanArgs ba{};
@@ -274,6 +294,8 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     pa.mq = m.mq;
     pa.n_tokens = m.n_tokens;
     pa.key_stride = m.mq > 0 ? partial_keys->seq_stride_rows : 0;
+    pa.key_rows = m.mq > 0 ? cache_rows(nullptr, 1, B / m.mq, pa.key_stride, max_latents)
+                           : max_latents;
     pa.scores = scores;
     pa.n_rows = nb_max;
     DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_prefill_partial(pa, s); }));
@@ -295,6 +317,7 @@ dsa_status_t run_token_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              const int32_t* n_lat, int B, int64_t max_latents, int32_t* token_ids,
                              float* scores, DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s,
                              int prefill, int64_t ctx, MultiQuery m = MultiQuery{}) {
+  Range range("dsa.token_stage");
   SelectArgs se{};
   if (block_ids && m.mq == 0 && prefill_batched(keys, prefill, max_latents)) {
     // Dense token scores over every latent, read by the selection through
@@ -485,6 +508,7 @@ dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0 || max_latents == 0) return DSA_OK;
+  Range range("dsa.pool");
   PoolArgs a{};
   a.fmt = keys->fmt;
   a.key_data = keys->data;
@@ -499,6 +523,9 @@ dsa_status_t dsa_pool_index_keys(const dsa_config_t* cfg, const dsa_keys_t* keys
   a.out_stride = pooled->seq_stride_rows;
   a.key_pages = paging_of(keys->pages, 1);
   a.out_pages = paging_of(pooled->pages, kBlock);
+  a.key_rows = cache_rows(keys->pages, 1, B, keys->seq_stride_rows, max_latents);
+  a.out_rows = cache_rows(pooled->pages, kBlock, B, pooled->seq_stride_rows,
+                          (max_latents + kBlock - 1) / kBlock);
   a.status = at<DeviceStatus>(workspace, L.status);
   DSA_CUDA(launch(DSA_KERNEL_POOL, static_cast<cudaStream_t>(stream), [&](int*) { return launch_pool(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
@@ -581,9 +608,11 @@ dsa_status_t attn_decode(const dsa_config_t* cfg, const void* q, const void* lat
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = latent_seq_stride_rows;
+  a.lat_rows = static_cast<int64_t>(B) * latent_seq_stride_rows;
   if (pages != nullptr) {
     a.pages = paging_of(pages, 1);
     a.lat_stride = static_cast<int64_t>(pages->pages_per_seq) * pages->page_rows;
+    a.lat_rows = pages->n_pages * pages->page_rows;
   }
   a.n_latents = n_latents;
   a.token_ids = token_ids;
@@ -597,6 +626,7 @@ dsa_status_t attn_decode(const dsa_config_t* cfg, const void* q, const void* lat
   a.lse = lse;
   a.status = at<DeviceStatus>(workspace, L.status);
   set_splits(a, *cfg, B);
+  Range range("dsa.attention");
   DSA_CUDA(launch(DSA_KERNEL_ATTN, static_cast<cudaStream_t>(stream), [&](int*) { return launch_attn(a, static_cast<cudaStream_t>(stream)); }));
   return DSA_OK;
 }
@@ -658,9 +688,11 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   Layout L;
   DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
+  Range range("dsa.decode_step");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
   if (update_pool && max_latents > 0) {
+    Range pool_range("dsa.pool");
     PoolArgs a{};
     a.fmt = keys->fmt;
     a.key_data = keys->data;
@@ -675,6 +707,9 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
     a.out_stride = pooled->seq_stride_rows;
     a.key_pages = paging_of(keys->pages, 1);
     a.out_pages = paging_of(pooled->pages, kBlock);
+    a.key_rows = cache_rows(keys->pages, 1, B, keys->seq_stride_rows, max_latents);
+    a.out_rows = cache_rows(pooled->pages, kBlock, B, pooled->seq_stride_rows,
+                            (max_latents + kBlock - 1) / kBlock);
     a.status = st;
     DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_pool(a, s); }));
   }
@@ -697,9 +732,11 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = latent_seq_stride_rows;
+  a.lat_rows = static_cast<int64_t>(B) * latent_seq_stride_rows;
   if (keys->pages) {  // the latents share the keys' page table
     a.pages = paging_of(keys->pages, 1);
     a.lat_stride = static_cast<int64_t>(keys->pages->pages_per_seq) * keys->pages->page_rows;
+    a.lat_rows = keys->pages->n_pages * keys->pages->page_rows;
   }
   a.n_latents = n_latents;
   a.token_ids = tids;
@@ -713,6 +750,7 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   a.lse = lse;
   a.status = st;
   set_splits(a, *cfg, B);
+  Range attn_range("dsa.attention");
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }
@@ -743,6 +781,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   Layout L;
   DSA_TRY(check_ws(*cfg, n_q, n_lat, workspace, workspace_bytes, &L));
   if (n_q == 0) return DSA_OK;
+  Range range("dsa.prefill");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
   const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
@@ -758,6 +797,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = n_lat;
+  a.lat_rows = n_lat;
   a.token_ids = tids;
   a.k_tokens = cfg->k_tokens;
   a.swa = static_cast<const uint16_t*>(swa);
@@ -771,6 +811,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
   a.ratio = cfg->ratio;
   a.status = st;
   set_splits(a, *cfg, n_q);
+  Range attn_range("dsa.attention");
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }
@@ -804,6 +845,7 @@ dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n
   Layout L;
   DSA_TRY(check_ws(*cfg, nq_total, max_latents, workspace, workspace_bytes, &L));
   if (B == 0) return DSA_OK;
+  Range range("dsa.decode_multi");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
   const uint16_t* qi = static_cast<const uint16_t*>(q_idx);
@@ -820,6 +862,7 @@ dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n
   a.q = static_cast<const uint16_t*>(q);
   a.latents = static_cast<const uint16_t*>(latents);
   a.lat_stride = latent_seq_stride_rows;
+  a.lat_rows = static_cast<int64_t>(B) * latent_seq_stride_rows;
   a.token_ids = tids;
   a.k_tokens = cfg->k_tokens;
   a.swa = static_cast<const uint16_t*>(swa);
@@ -835,6 +878,7 @@ dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n
   a.swa_seq_rows = cfg->window + n_q - 1;
   a.status = st;
   set_splits(a, *cfg, nq_total);
+  Range attn_range("dsa.attention");
   DSA_CUDA(launch(DSA_KERNEL_ATTN, s, [&](int*) { return launch_attn(a, s); }));
   return DSA_OK;
 }

@@ -316,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
       const int r0 = g0 + 32 * part;  // this warp's first row of the tile
-      if (r0 + 32 <= w_cnt) {
+      if (r0 + 32 <= w_cnt &&
+          DSA_DCHECK(wrow0 + w_begin + r0 + 32 <= a.swa_rows, a.status, SITE_ATTN,
+                     wrow0 + w_begin + r0)) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&misc->kv_full[sl], 32 * 1024);
 #pragma unroll
@@ -335,10 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * part + (c >> 6), cr = c & 63;
         const int g = g0 + row;
         const uint32_t dst = dstb + (cr >> 3) * kAtomBytes + sw128_off(row, cr & 7);
-        if (g < n_rows_cta) {
-          const uint16_t* src = (g < w_cnt)
-                                    ? win + static_cast<int64_t>(w_begin + g) * kLatent
-                                    : lat + static_cast<int64_t>(ids[s_begin + g - w_cnt]) * kLatent;
+        bool copy = g < n_rows_cta;
+        const uint16_t* src = nullptr;
+        if (copy) {
+          // the row's place in its whole array (window buffer or latents)
+          const int64_t arow = (g < w_cnt) ? wrow0 + w_begin + g
+                                           : (lat - a.latents) / kLatent + ids[s_begin + g - w_cnt];
+          copy = DSA_DCHECK(arow >= 0 && arow < (g < w_cnt ? a.swa_rows : a.lat_rows), a.status,
+                            SITE_ATTN, arow);
+          src = ((g < w_cnt) ? a.swa : a.latents) + arow * kLatent;
+        }
+        if (copy) {
           cp_async_16(dst, src + cr * 8);
         } else {
           st_shared_v4(dst, make_uint4(0, 0, 0, 0));
@@ -789,19 +798,21 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                 : static_cast<uint64_t>(a.B) * a.window;
   e = encode_tma_2d(&wmap, a.swa, 2, kLatent, wrows, kLatent * 2, 64, 32);
   if (e != cudaSuccess) return e;
+  AttnArgs args = a;
+  args.swa_rows = static_cast<int64_t>(wrows);
   if (a.tile_rows == 64) {
     static std::atomic<int> smem_set[64]{};
     e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                      a.splits, a, qmap, wmap);
+                      a.splits, args, qmap, wmap);
   }
   if (a.tile_rows != 32) return cudaErrorInvalidValue;
   static std::atomic<int> smem_set[64]{};
   e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                    a.splits, a, qmap, wmap);
+                    a.splits, args, qmap, wmap);
 }
 
 }  // namespace dsa

@@ -42,6 +42,17 @@ __device__ __forceinline__ void record_status(DeviceStatus* st, uint32_t code, u
   }
 }
 
+// Debug builds (-DDSA_DEBUG) check each computed row of a global array
+// against that array's extent before it is read or written: a failed check
+// records DSA_ERR_DEVICE_CHECK (site, detail) and the caller skips the access.
+// Release builds compile the checks to `true`.
+#ifdef DSA_DEBUG
+#define DSA_DCHECK(cond, st, site, detail) \
+  ((cond) ? true : (record_status((st), DSA_ERR_DEVICE_CHECK, (site), static_cast<uint32_t>(detail)), false))
+#else
+#define DSA_DCHECK(cond, st, site, detail) true
+#endif
+
 // ---------------------------------------------------------------------------
 // Shared-memory addressing, cp.async, fences
 // ---------------------------------------------------------------------------

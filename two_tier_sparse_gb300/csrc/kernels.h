@@ -69,6 +69,7 @@ struct PoolArgs {
   uint8_t* out_scales;
   int64_t out_stride;
   Paging key_pages, out_pages;  // paged caches (table null: contiguous)
+  int64_t key_rows, out_rows;   // rows of the key and block-key arrays (debug checks)
   DeviceStatus* status;
 };
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s);
@@ -109,6 +110,7 @@ struct ScanArgs {
   // Paged cache (table null: contiguous, key_stride rows per sequence). Rows
   // are then read in groups of 8 (one TMA box each), like gathered blocks.
   Paging pages;
+  int64_t key_rows;  // rows of the key array (set by launch_scan; debug checks)
   DeviceStatus* status;
 };
 // In prefill ROWS_BLOCKS mode only complete blocks are scored; a query's
@@ -153,6 +155,7 @@ struct PartialArgs {
   int mq;                    // multi-query decode: queries per sequence (0: one sequence)
   const int32_t* n_tokens;   //   [n_q / mq] tokens per sequence
   int64_t key_stride;        //   key rows per sequence
+  int64_t key_rows;          // rows of the key array (debug checks)
   float* scores;
   int64_t n_rows;
 };
@@ -226,6 +229,8 @@ struct AttnArgs {
   int tile_rows;
   // Paged latent pool (table null: contiguous, lat_stride rows per sequence).
   Paging pages;
+  int64_t lat_rows;  // rows of the latent array (debug checks)
+  int64_t swa_rows;  // rows of the window buffer (set by launch_attn; debug checks)
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);

@@ -180,6 +180,10 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
       return;
     }
   }
+  if (!DSA_DCHECK(row0 >= 0 && row0 + c <= a.key_rows && orow >= 0 && orow < a.out_rows,
+                  a.status, SITE_POOL, b)) {
+    return;
+  }
   float acc[4], dec[4];
   block_mean(a.fmt, a.key_data, a.key_scales, row0, c, lane, acc);
   const Stored st = round_to_format(a.fmt, acc, dec);
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(256) prefill_partial_kernel(PartialArgs a) {
   const int blk = n >> 3;
   float acc[4], key[4];
   const int64_t row0 = static_cast<int64_t>(query_seq(a.mq, b)) * a.key_stride;
+  if (!DSA_DCHECK(row0 + int64_t{blk} * 8 + c <= a.key_rows, nullptr, SITE_PREFILL, b)) return;
   block_mean(a.fmt, a.key_data, a.key_scales, row0 + static_cast<int64_t>(blk) * 8, c, lane, acc);
   round_to_format(a.fmt, acc, key);
   // dot_h = q_h . key: each lane's 4 products, then a fixed xor-tree sum.

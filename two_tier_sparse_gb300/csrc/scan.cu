@@ -305,6 +305,10 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
                 record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SCAN, static_cast<uint32_t>(tp.b));
               }
             }
+            if (nrows[k] > 0 &&
+                !DSA_DCHECK(y[k] >= 0 && y[k] + nrows[k] <= a.key_rows, a.status, SITE_SCAN, y[k])) {
+              nrows[k] = 0;
+            }
           }
         }
         const int row0 = (lane & 15) * kBlock;
@@ -374,6 +378,11 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
           int64_t v = contiguous_rows(a, n_vis_of(tp.b)) - tp.r0;
           v = v < 0 ? 0 : (v > kTile ? kTile : v);
           nrows[t] = static_cast<int>(v);
+          const int64_t row = seq_row0(a, tp.b) + tp.r0;
+          if (nrows[t] > 0 &&
+              !DSA_DCHECK(row >= 0 && row + nrows[t] <= a.key_rows, a.status, SITE_SCAN, row)) {
+            nrows[t] = 0;
+          }
         }
         const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
         bytes += (nrows[t] > 0 ? P::kCodeBytes : 0) + (bulk_sc ? P::kScaleBytes : 0);
@@ -785,7 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int FMT, int TPS>
-cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_fmt(const ScanArgs& args, int num_sms, cudaStream_t s) {
+  ScanArgs a = args;
   using Lo = Layout<FMT, TPS>;
   const int64_t tpq = (a.n_rows + kTile - 1) / kTile;
   const int64_t total = tpq * a.B;
@@ -803,6 +813,7 @@ cudaError_t launch_fmt(const ScanArgs& a, int num_sms, cudaStream_t s) {
   const int64_t n_seqs = a.mq > 0 ? a.B / a.mq : (a.prefill ? 1 : a.B);
   const int64_t rows = a.pages.table ? a.pages.n_pages * a.pages.rows
                                      : (n_seqs - 1) * a.key_stride + last_rows;
+  a.key_rows = rows;
   Maps maps;
   memset(&maps, 0, sizeof(maps));
   const int box_rows = (a.mode == ROWS_GATHER || a.pages.table) ? kBlock : kTile;
