@@ -43,7 +43,7 @@
  *   - Determinism: results are bit-identical from run to run (no floating-point
  *     atomics; every reduction has a fixed order).
  *   - Tracing: each call marks its phases as NVTX ranges (dsa.decode_step,
- *     dsa.decode_multi, dsa.prefill, dsa.pool, dsa.block_stage,
+ *     dsa.decode_multi, dsa.prefill, dsa.compress_append, dsa.pool, dsa.block_stage,
  *     dsa.token_stage, dsa.attention) that a profiler shows on its timeline;
  *     with no tool attached a range costs two calls into empty stubs.
  */
@@ -298,6 +298,37 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
                                      const dsa_keys_t* pooled, const void* swa, void* out,
                                      float* lse, int32_t* token_ids, void* workspace,
                                      size_t workspace_bytes, dsa_stream_t stream);
+
+/*
+ * Cache append at the compression step (recipes.vllm.ai "DeepSeek-V4.1-Flash",
+ * Overview, "Two-tier sparse attention": layers with a compression ratio keep
+ * latents "pooled by a learned softmax gate", one latent per ratio positions).
+ * For each sequence b whose token count T_b = n_tokens[b] completes a latent
+ * (T_b % ratio == 0), latent j = T_b / ratio - 1 becomes
+ *     RN_bf16( sum_i softmax(gate[b])_i * kv[b][i] ),   i = 0 .. ratio - 1
+ * (softmax over the group's ratio logits, in fp32), its index key row becomes
+ * new_keys' row b, and the block key of the block holding j is re-pooled as
+ * dsa_pool_index_keys(tail_only) does. Sequences that complete no latent are
+ * left as they are. The gate's learned projection is not on the pages: its
+ * logits are inputs.
+ *   n_tokens:  device int32 [B]
+ *   kv:        device bf16 [B, ratio, 512]: the group's per-position KV vectors
+ *   gate:      device fp32 [B, ratio]
+ *   new_keys:  the new index key of each sequence, one row per sequence (data
+ *              [B, row], MX scales [B, 4]; seq_stride_rows not used)
+ *   latents:   bf16, contiguous with latent_seq_stride_rows rows a sequence, or
+ *              paged by keys->pages like the keys
+ *   keys, pooled: the index-key and block-key caches (written)
+ *   max_latents: the caches' capacity; a latent at or past it is a device check
+ * ratio must be at most 32 (DSA_ERR_UNSUPPORTED otherwise). The workspace is
+ * sized for B queries.
+ */
+dsa_status_t dsa_compress_append(const dsa_config_t* cfg, int B, const int32_t* n_tokens,
+                                 const void* kv, const float* gate, const dsa_keys_t* new_keys,
+                                 void* latents, int64_t latent_seq_stride_rows,
+                                 const dsa_keys_out_t* keys, const dsa_keys_out_t* pooled,
+                                 int64_t max_latents, void* workspace, size_t workspace_bytes,
+                                 dsa_stream_t stream);
 
 /*
  * Multi-query decode: n_q queries per sequence at its last n_q positions, as

@@ -317,6 +317,26 @@ def store_f32(v32: np.ndarray, fmt: str):
 
 
 # ---------------------------------------------------------------------------
+# Cache append: the compressed latent of a group of `ratio` positions
+# ---------------------------------------------------------------------------
+
+
+def compress_latent(kv_bits: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    """The latent of one group of positions, pooled by a softmax gate
+    (recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse
+    attention": compressed KV latents "pooled by a learned softmax gate"; ratio
+    1 or 2 positions a latent). kv_bits: bf16 [ratio, D] (the group's per-position
+    KV vectors, in position order); gate: the group's ratio gate logits (the
+    learned projection that makes them is not on the pages, so they are given).
+    latent = RN_bf16(sum_i softmax(gate)_i * kv_i), computed in float64."""
+    g = np.asarray(gate, np.float32).astype(np.float64)
+    e = np.exp(g - g.max())
+    wts = e / e.sum()
+    v = wts @ bf16_to_f64(kv_bits)
+    return f32_to_bf16_rne(v.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
 # S1 / S3: indexer scores;  S2 / S4: top-k selection
 # ---------------------------------------------------------------------------
 

@@ -277,6 +277,22 @@ def test_paged_cache_argument_errors(lib):
                                             A, A, A, A, 2, A, None, A, 1 << 30, None) == 1
 
 
+def test_compress_append_argument_errors(lib):
+    def call(c=dsa.config(ratio=2), B=2, n=A, kv=A, g=A, new=_k(stride=1), lat=A, stride=100,
+             keys=_k(), pooled=_k(stride=13), L=100, ws=A, wsb=16):
+        return lib.dsa_compress_append(ctypes.byref(c), B, n, kv, g, _ref(new), lat, stride,
+                                       _ref(keys), _ref(pooled), L, ws, wsb, None)
+    assert call() == 4                                  # valid, then the (tiny) workspace
+    assert call(c=dsa.config(ratio=33)) == 3            # groups of more than 32 positions
+    assert call(n=None) == 1 and call(kv=None) == 1 and call(g=None) == 1
+    assert call(new=None) == 1 and call(keys=None) == 1 and call(pooled=None) == 1
+    assert call(kv=A + 8) == 2
+    assert call(g=A + 2) == 2
+    assert call(stride=99) == 1                         # latent rows a sequence < capacity
+    assert call(new=_k(fmt=1, scales=A, stride=1)) == 1  # formats differ
+    assert call(B=-1) == 1
+
+
 def test_hooks_and_self_test_argument_errors(lib):
     n_kinds = len(dsa.KERNEL_KINDS)
     assert lib.dsa_profile_events(-1, None, None, 0) == 1

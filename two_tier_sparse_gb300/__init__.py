@@ -33,7 +33,8 @@ EXPORTS = ("dsa_default_config", "dsa_status_string", "dsa_workspace_size",
            "dsa_pool_index_keys", "dsa_index_blocks", "dsa_topk", "dsa_sparse_attn_decode",
            "dsa_decode_step", "dsa_sparse_attn_prefill", "dsa_read_device_status",
            "dsa_profile_events", "dsa_launch_counts", "dsa_topk_noalloc",
-           "dsa_selftest_timeout", "dsa_sparse_attn_decode_paged", "dsa_decode_multi")
+           "dsa_selftest_timeout", "dsa_sparse_attn_decode_paged", "dsa_decode_multi",
+           "dsa_compress_append")
 
 TOPK_NOALLOC_MAX_SCORES = 1 << 21
 
@@ -103,6 +104,8 @@ def load() -> ctypes.CDLL:
                                                      vp, vp, i32, vp, vp, vp, sz, vp]
         lib.dsa_decode_multi.argtypes = [cp, i32, vp, vp, vp, vp, kp, kp, vp, i64, i64, vp, i32,
                                          vp, vp, vp, vp, sz, vp]
+        lib.dsa_compress_append.argtypes = [cp, i32, vp, vp, vp, kp, vp, i64, kp, kp, i64, vp,
+                                            sz, vp]
         for f in EXPORTS:
             if f not in ("dsa_default_config", "dsa_status_string"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -254,6 +257,19 @@ def decode_multi(cfg, n_tokens, q, q_idx, w, keys: Keys, pooled: Keys, latents, 
                                    latents.shape[1], max_latents, _p(swa), B, _p(out), _p(lse),
                                    _p(token_ids), _p(ws), ws.numel(), _stream(stream)),
            "dsa_decode_multi")
+
+
+def compress_append(cfg, n_tokens, kv, gate, new_keys: Keys, latents, keys: Keys, pooled: Keys,
+                    max_latents, ws, stream=None):
+    """The cache append at the compression step: kv bf16 [B, ratio, 512], gate
+    fp32 [B, ratio], new_keys one index-key row per sequence."""
+    B = n_tokens.shape[0]
+    lat_stride = latents.shape[1] if keys.pages is None else 0
+    _check(load().dsa_compress_append(ctypes.byref(cfg), B, _p(n_tokens), _p(kv), _p(gate),
+                                      ctypes.byref(new_keys.c()), _p(latents), lat_stride,
+                                      ctypes.byref(keys.c()), ctypes.byref(pooled.c()),
+                                      max_latents, _p(ws), ws.numel(), _stream(stream)),
+           "dsa_compress_append")
 
 
 def sparse_attn_prefill(cfg, ctx_len, q, q_idx, w, latents, keys: Keys, pooled: Keys, swa, out,

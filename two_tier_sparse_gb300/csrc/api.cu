@@ -883,6 +883,84 @@ dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n
   return DSA_OK;
 }
 
+dsa_status_t dsa_compress_append(const dsa_config_t* cfg, int B, const int32_t* n_tokens,
+                                 const void* kv, const float* gate, const dsa_keys_t* new_keys,
+                                 void* latents, int64_t latent_seq_stride_rows,
+                                 const dsa_keys_out_t* keys, const dsa_keys_out_t* pooled,
+                                 int64_t max_latents, void* workspace, size_t workspace_bytes,
+                                 dsa_stream_t stream) {
+  DSA_TRY(check_config(cfg));
+  if (cfg->ratio > 32) return DSA_ERR_UNSUPPORTED;
+  if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || keys == nullptr ||
+      pooled == nullptr || new_keys == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (n_tokens == nullptr || kv == nullptr || gate == nullptr || latents == nullptr ||
+      new_keys->data == nullptr) {
+    return DSA_ERR_INVALID_ARG;
+  }
+  const bool paged = keys->pages != nullptr;
+  if (!paged && latent_seq_stride_rows < max_latents) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(latents) || !aligned16(new_keys->data) ||
+      (reinterpret_cast<uintptr_t>(n_tokens) & 3u) || (reinterpret_cast<uintptr_t>(gate) & 3u)) {
+    return DSA_ERR_MISALIGNED;
+  }
+  const dsa_keys_t kk{keys->fmt, keys->data, keys->scales, keys->seq_stride_rows, keys->pages};
+  DSA_TRY(check_keys(&kk, max_latents, true, max_latents));
+  const dsa_keys_t pk{pooled->fmt, pooled->data, pooled->scales, pooled->seq_stride_rows,
+                      pooled->pages};
+  DSA_TRY(check_keys(&pk, (max_latents + 7) / 8, true, max_latents));
+  if (pooled->fmt != keys->fmt || new_keys->fmt != keys->fmt) return DSA_ERR_INVALID_ARG;
+  if (new_keys->fmt != DSA_FMT_BF16 && new_keys->scales == nullptr) return DSA_ERR_INVALID_ARG;
+  if (!same_pages(keys->pages, pooled->pages)) return DSA_ERR_INVALID_ARG;
+  Layout L;
+  DSA_TRY(check_ws(*cfg, B, max_latents, workspace, workspace_bytes, &L));
+  if (B == 0) return DSA_OK;
+  Range range("dsa.compress_append");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(workspace, L.status);
+  int32_t* n_lat = at<int32_t>(workspace, L.token_ids);  // B entries: the new latent counts
+  AppendArgs ap{};
+  ap.B = B;
+  ap.ratio = cfg->ratio;
+  ap.n_tokens = n_tokens;
+  ap.kv = static_cast<const uint16_t*>(kv);
+  ap.gate = gate;
+  ap.fmt = keys->fmt;
+  ap.new_key = static_cast<const uint8_t*>(new_keys->data);
+  ap.new_scales = new_keys->scales;
+  ap.latents = static_cast<uint16_t*>(latents);
+  ap.lat_stride = latent_seq_stride_rows;
+  ap.key_data = static_cast<uint8_t*>(keys->data);
+  ap.key_scales = keys->scales;
+  ap.key_stride = keys->seq_stride_rows;
+  ap.pages = paging_of(keys->pages, 1);
+  ap.max_latents = max_latents;
+  ap.n_lat_out = n_lat;
+  ap.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_append(ap, s); }));
+  PoolArgs a{};
+  a.fmt = keys->fmt;
+  a.key_data = keys->data;
+  a.key_scales = keys->scales;
+  a.key_stride = keys->seq_stride_rows;
+  a.n_latents = n_lat;
+  a.max_latents = max_latents;
+  a.B = B;
+  a.tail_only = 1;
+  a.out_data = pooled->data;
+  a.out_scales = pooled->scales;
+  a.out_stride = pooled->seq_stride_rows;
+  a.key_pages = paging_of(keys->pages, 1);
+  a.out_pages = paging_of(pooled->pages, kBlock);
+  a.key_rows = cache_rows(keys->pages, 1, B, keys->seq_stride_rows, max_latents);
+  a.out_rows = cache_rows(pooled->pages, kBlock, B, pooled->seq_stride_rows,
+                          (max_latents + kBlock - 1) / kBlock);
+  a.status = st;
+  DSA_CUDA(launch(DSA_KERNEL_POOL, s, [&](int*) { return launch_pool(a, s); }));
+  return DSA_OK;
+}
+
 dsa_status_t dsa_profile_events(int kind, void* const* starts, void* const* ends, int n) {
   if (kind < 0 || kind >= DSA_KERNEL_KINDS || n < 0) return DSA_ERR_INVALID_ARG;
   if (n > 0 && (starts == nullptr || ends == nullptr)) return DSA_ERR_INVALID_ARG;

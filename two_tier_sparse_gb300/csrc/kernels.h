@@ -74,6 +74,31 @@ struct PoolArgs {
 };
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s);
 
+// Cache append at the compression step: for each sequence whose token count
+// n completes a latent (n % ratio == 0), latent n / ratio - 1 becomes
+// RN_bf16(sum_i softmax(gate)_i kv_i) over its ratio positions, and its index
+// key row is copied in; n_lat_out[b] = n / ratio for the tail pooling after.
+struct AppendArgs {
+  int B;
+  int ratio;                 // 1..32
+  const int32_t* n_tokens;   // [B]
+  const uint16_t* kv;        // bf16 [B, ratio, 512]
+  const float* gate;         // [B, ratio]
+  int fmt;
+  const uint8_t* new_key;    // [B, row bytes] in the key format
+  const uint8_t* new_scales; // [B, 4] (MX formats)
+  uint16_t* latents;
+  int64_t lat_stride;
+  uint8_t* key_data;
+  uint8_t* key_scales;
+  int64_t key_stride;
+  Paging pages;              // latents and keys paged by one table (table null: contiguous)
+  int64_t max_latents;
+  int32_t* n_lat_out;        // [B]
+  DeviceStatus* status;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
 // Indexer scores of key rows, one row per MMA lane:
 //   score = sum_h w_h * max(0, q_idx_h . key)
 // Row r of query b is

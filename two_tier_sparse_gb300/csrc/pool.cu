@@ -236,7 +236,78 @@ __global__ void __launch_bounds__(256) prefill_partial_kernel(PartialArgs a) {
   if (lane == 0) a.scores[static_cast<int64_t>(b) * a.n_rows + blk] = score;
 }
 
+// One warp per sequence: the compressed latent of its last ratio positions
+// (softmax of the gate logits in fp32, lane i < ratio holding logit i; lane l
+// sums dims [16 l, 16 l + 16) over the positions in order) and its index key.
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= a.B) return;
+  const int n = a.n_tokens[b];
+  const int n_lat = n >= 0 ? n / a.ratio : 0;
+  if (lane == 0) a.n_lat_out[b] = n_lat;
+  if (n <= 0 || n % a.ratio != 0) return;  // no latent completes at this step
+  const int j = n_lat - 1;
+  int64_t lrow = static_cast<int64_t>(b) * a.lat_stride + j;
+  int64_t krow = static_cast<int64_t>(b) * a.key_stride + j;
+  if (a.pages.table) lrow = krow = paged_row(a.pages, b, j);
+  if (j >= a.max_latents || lrow < 0) {
+    if (lane == 0) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_POOL, b);
+    return;
+  }
+  const float g = lane < a.ratio ? a.gate[static_cast<int64_t>(b) * a.ratio + lane] : -INFINITY;
+  float m = g;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const float e = lane < a.ratio ? expf(g - m) : 0.f;
+  float sum = e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  const float wl = e / sum;
+  float acc[16];
+#pragma unroll
+  for (int d = 0; d < 16; ++d) acc[d] = 0.f;
+  for (int i = 0; i < a.ratio; ++i) {
+    const float wi = __shfl_sync(0xFFFFFFFFu, wl, i);
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.kv + (static_cast<int64_t>(b) * a.ratio + i) * kLatent + 16 * lane);
+    const uint4 x0 = src[0], x1 = src[1];
+    const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[2 * k] = fmaf(wi, bf16_bits_to_float(xs[k] & 0xFFFF), acc[2 * k]);
+      acc[2 * k + 1] = fmaf(wi, bf16_bits_to_float(xs[k] >> 16), acc[2 * k + 1]);
+    }
+  }
+  uint32_t out[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
+    out[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.latents + lrow * kLatent + 16 * lane);
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  // the index key row (and its scales)
+  const int row_bytes = a.fmt == DSA_FMT_BF16 ? 256 : (a.fmt == DSA_FMT_MXFP8 ? 128 : 64);
+  if (lane * 16 < row_bytes) {
+    *reinterpret_cast<uint4*>(a.key_data + krow * row_bytes + lane * 16) =
+        *reinterpret_cast<const uint4*>(a.new_key + static_cast<int64_t>(b) * row_bytes + lane * 16);
+  }
+  if (a.fmt != DSA_FMT_BF16 && lane < 4) {
+    a.key_scales[krow * 4 + lane] = a.new_scales[static_cast<int64_t>(b) * 4 + lane];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  const int grid = (a.B + 7) / 8;
+  return launch_pdl(append_kernel, dim3(grid), dim3(256), 0, s, 1, a);
+}
 
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t s) {
   const int64_t nb_max = (a.max_latents + 7) / 8;
