@@ -11,7 +11,8 @@
 //   O^T += KV^T . P^T (four M = 128 slices of the 512 latent dims, N = 64 heads,
 //                      K = 32 rows; the KV tile is read as an MN-major operand)
 // Warp roles: warps 0-3 math (softmax for the 64 heads by warps 0-1, one head
-// per thread; O rescaling and the epilogue by all four, thread = TMEM lane),
+// per thread; O rescaling by all four, thread = TMEM lane; the epilogue by
+// these four and the four loader warps, which are idle by then),
 // warps 4-7 loaders (warp 4 + w owns ring slot w: cp.async gathers of random
 // 1 KB rows, waited by the warp and announced on the slot's mbarrier; Q comes
 // by eight TMA boxes that land in the swizzled operand layout), warp 8 issues
@@ -31,8 +32,9 @@
 // Split-KV: while S x queries CTAs fit the SMs (S = 8, 4 or 2), the window
 // rows and the selected latents of a query are each cut in S parts handled by
 // the S CTAs of a cluster. CTA r finishes the latent dims [r D, r D + D),
-// D = 512 / S: every CTA stores, into each peer's then idle ring (distributed
-// shared memory), its O for that peer's dims and its (max, sum); after a
+// D = 512 / S: once every CTA's MMAs are done (a cluster barrier), each stores
+// straight into each peer's idle ring (distributed shared memory) its
+// unnormalised O for that peer's dims and its (max, sum); after a second
 // cluster barrier each merges its dims and writes them.
 //
 // The epilogue works in chunks of 16 heads in rolled loops and writes the
@@ -54,6 +56,8 @@ constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;  // 8: QK^T issuer (and TMEM o
 constexpr int kPvWarp = kMmaWarp + 1;          // 9: PV issuer
 constexpr int kThreads = 32 * (kPvWarp + 1);   // 320
 constexpr int kMathBar = 1;         // named barrier of the 128 math threads
+constexpr int kEpiBar = 2;          // named barrier of the epilogue (math + loader warps)
+constexpr int kEpiThreads = 32 * kMmaWarp;  // 256
 
 // Shared-memory plan (offsets from a 1024-aligned base). The QK^T MMA reads
 // 64 rows past each Q atom (they only feed unused accumulator lanes); past
@@ -82,20 +86,21 @@ constexpr int kTmemCols = 512;  // S[b]: cols [64 b, 64 b + 32); O^T slice m: [1
 constexpr uint32_t kQBytes = kHeads * kLatent * 2;  // one query's bf16 Q, 8 atoms
 static_assert(kP - kQ == static_cast<int>(kQBytes), "Q region");
 // Split-KV exchange payload from a sender to the CTA finishing dims
-// [p D, p D + D): the sender's O for those dims divided by its own sum, bf16,
-// one 128-byte row of 64 heads per dim (16-byte chunk c of row dd stored at
-// chunk c ^ (dd & 7)), then the sender's (max, sum) per head.
+// [p D, p D + D): the sender's unnormalised O for those dims, bf16, one
+// 128-byte row of 64 heads per dim (16-byte chunk c of row dd stored at chunk
+// c ^ (dd & 7)), then the sender's (max, sum) per head.
 __host__ __device__ constexpr int xchg_bytes(int S) { return (kLatent / S) * 128 + kHeads * 8; }
-constexpr int kSend = kQ;    // outgoing payloads, S - 1 of them, in the Q region
 constexpr int kRecv = kKV;   // incoming payloads: slot s from sender s, in the ring
-static_assert((kMaxAttnSplits - 1) * xchg_bytes(kMaxAttnSplits) <= kP - kQ, "send staging");
-static_assert(xchg_bytes(2) <= kP - kQ, "send staging");
+static_assert(2 * xchg_bytes(2) <= kKVBytes && 4 * xchg_bytes(4) <= kKVBytes &&
+                  kMaxAttnSplits * xchg_bytes(kMaxAttnSplits) <= kKVBytes,
+              "receive areas fit the ring");
 constexpr int kWgt = kP;     // [S][64 h] merge weights, in the P buffers
 static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge weights fit the P buffers");
 
 struct Misc {
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
-  uint64_t q_done, ids_ready, xchg;  // xchg: the split-KV payloads received
+  uint64_t q_done, ids_ready;
+  uint64_t o_done;                   // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort;
   int n_sel;
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&misc->q_done, 1);    // the TMA loads of Q (expect-tx arrival + 64 KB)
     mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
-    mbar_init(&misc->xchg, 1);       // the receiver's expect-tx arrival + the S - 1 copies
+    mbar_init(&misc->o_done, 1);     // the PV issuer's last commit
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -282,6 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) mbar_arrive(&misc->ids_ready);
   }
 
+  // State the epilogue warps (math and loaders) share: the softmax statistics
+  // of head tid (threads 0..63), whether every wait succeeded, and the tile count.
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  int n_tiles_e = 0;
+
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
     // ---------------- loaders ----------------
     // Warp 4 + w fills 32 rows (part w / kSlots) of slot w % kSlots's tiles
@@ -300,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g0 = t * kRows;
       if (!have_ids && g0 + kRows > w_cnt) {
         if (!wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
+          ok = false;
           break;
         }
         int s_cnt;
@@ -312,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t >= kSlots &&
           !wait_bar(&misc->kv_empty[sl], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
+        ok = false;
         break;
       }
       const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
@@ -358,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&misc->kv_full[sl]);
     }
-    if (paired) exchange_phases();
+    n_tiles_e = have_ids ? n_tiles : 0;
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ---------------- MMA issuers ----------------
     int n_tiles = 0;
@@ -396,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&misc->kv_empty[t % kSlots]);
         mma_commit(&misc->p_empty[sb]);
       }
+      if (n_tiles > 0) mma_commit(&misc->o_done);  // arrives once every MMA has completed
     }
     if (lane == 0 && warp == kMmaWarp) {
       constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (paired) exchange_phases();
   } else {
-    // ---------------- math: softmax, rescale, epilogue ----------------
+    // ---------------- math: softmax, rescale ----------------
     int s_begin, s_cnt;
     sel_range(misc->n_sel, s_begin, s_cnt);
     const int n_rows_cta = w_cnt + s_cnt;
@@ -436,9 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A failed (timed-out) wait makes `ok` false for good; the thread then
     // skips the work but still reaches every named barrier, so the math warps
     // never part ways at a barrier.
-    float m_run = -INFINITY, l_run = 0.f;  // threads 0..63: head tid
+    n_tiles_e = n_tiles;
     const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
-    bool ok = true;
     // PV(j) is known complete through p_empty[j & 1], whose phases a thread
     // consumes in order (at most one phase ahead of its last wait), so a
     // parity wait is never more than one phase off; waiting on PV(j) early (to
@@ -532,14 +545,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&misc->p_full[sb]);
       }
     }
+  }
 
-    // ---------------- epilogue ----------------
-    // Once the last PV has completed every MMA has: Q, P and the ring are free.
-    // (Warps 2-3 have waited on no p_empty phase unless they rescaled: their
-    // own waits run in order up to the last PV here.)
+  if (warp < kMmaWarp) {
+    // ---------------- epilogue (math and loader warps) ----------------
+    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (dims 128 m + 32 (w % 4) + lane of O^T
+    // slice m) and heads [32 (w / 4), 32 (w / 4) + 32): the math warps take heads
+    // 0..31, the loader warps (idle by now) heads 32..63, so eight warps share the
+    // work that runs once per CTA.
+    const int half = warp >> 2;
+    const int et = 32 * (warp & 3) + lane;  // dim within a slice = TMEM lane
+    const uint32_t lq = tmem_addr(tmem, static_cast<uint32_t>(32 * (warp & 3)), 0);
+    const int n_tiles = n_tiles_e;
+    // Once the PV issuer's last commit has arrived, every MMA has completed:
+    // Q, P and the ring are free.
     if (n_tiles > 0) {
-      if (warp >= 2 && n_tiles >= 2) wait_pv(n_tiles - 2);
-      wait_pv(n_tiles - 1);
+      if (ok) ok = wait_bar(&misc->o_done, 0u, misc, a.status);
     } else if (ok) {
       // no tiles: nothing ordered the Q copies before the staging writes below
       ok = wait_bar(&misc->q_done, 0u, misc, a.status);
@@ -547,11 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const bool have_o = ok && n_tiles > 0;
     uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
-    // Heads [16 hc, 16 hc + 16) of O^T slice m (dim 128 m + tid in this
+    // Heads [16 hc, 16 hc + 16) of O^T slice m (dim 128 m + et in this
     // thread's lane), zeros without rows.
     auto load16 = [&](int m, int hc, float (&v)[16]) {
       if (have_o) {
-        tmem_ld16(la + 128 + 64 * m + 16 * hc, v);
+        tmem_ld16(lq + 128 + 64 * m + 16 * hc, v);
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -586,132 +607,122 @@ __global__ void __launch_bounds__(kThreads, 1)
               l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
       }
-      named_sync(kMathBar, 128);
+      named_sync(kEpiBar, kEpiThreads);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
 #pragma unroll 1
-        for (int hc = 0; hc < 4; ++hc) {
+        for (int hc = 2 * half; hc < 2 * half + 2; ++hc) {
           float v[16];
           load16(m, hc, v);
           scale16(v, inv_l_s, hc);
-          store16(128 * m + tid, hc, v);
+          store16(128 * m + et, hc, v);
         }
       }
     } else {
       // CTA `split` finishes latent dims [split D, split D + D). O^T slice m
-      // holds dim 128 m + tid in this thread's lane, so the thread's four dims
-      // go to CTAs (128 m + tid) / D (a warp's 32 dims always go to one CTA).
+      // holds dim 128 m + et in this thread's lane, so the thread's four dims
+      // go to CTAs (128 m + et) / D (a warp's 32 dims always go to one CTA).
+      // Each CTA writes, straight into each peer's receive area (its ring, free
+      // once the peer's MMAs are done), its unnormalised O for the peer's dims
+      // in bf16 and its (max, sum) per head; its own (max, sum) go to its own
+      // area, so the merge reads every CTA's the same way.
       const int D = kLatent / S;
       const uint32_t pay = static_cast<uint32_t>(xchg_bytes(S));
       const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
-      auto send_slot = [&](int p) -> uint32_t {  // staging of the payload for CTA p
-        return sbase + kSend + static_cast<uint32_t>(p < split ? p : p - 1) * pay;
+      auto recv_slot = [&](int q) -> uint32_t {  // payload from CTA q, in this CTA
+        return sbase + kRecv + static_cast<uint32_t>(q) * pay;
       };
       cluster_wait();  // phase 0
-      if (warp < 2) misc->inv_l[tid] = l_own > 0.f ? 1.f / l_own : 0.f;
-      named_sync(kMathBar, 128);
+      if (warp < 2) {
+        float* t = reinterpret_cast<float*>(gbase + (recv_slot(split) - sbase) + D * 128);
+        t[2 * tid] = m_own;
+        t[2 * tid + 1] = l_own;
+      }
+      cluster_arrive();  // phase 1: every CTA's MMAs are done, so its ring may be written
+      cluster_wait();
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + tid;
+        const int d = 128 * m + et;
         const int p = d / D;
         if (p == split) continue;
         const int dd = d - p * D;
-        const uint32_t row = send_slot(p) + static_cast<uint32_t>(dd) * 128;
+        const uint32_t row =
+            mapa_shared(recv_slot(split) + static_cast<uint32_t>(dd) * 128, static_cast<uint32_t>(p));
 #pragma unroll 1
-        for (int hc = 0; hc < 4; ++hc) {
+        for (int hc = 2 * half; hc < 2 * half + 2; ++hc) {
           float v[16];
           load16(m, hc, v);
-          scale16(v, inv_l_s, hc);
           uint32_t w8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const __nv_bfloat162 x = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
             w8[e] = *reinterpret_cast<const uint32_t*>(&x);
           }
-          st_shared_v4(row + static_cast<uint32_t>((2 * hc) ^ (dd & 7)) * 16,
-                       make_uint4(w8[0], w8[1], w8[2], w8[3]));
-          st_shared_v4(row + static_cast<uint32_t>((2 * hc + 1) ^ (dd & 7)) * 16,
-                       make_uint4(w8[4], w8[5], w8[6], w8[7]));
+          st_cluster_u4(row + static_cast<uint32_t>((2 * hc) ^ (dd & 7)) * 16,
+                        make_uint4(w8[0], w8[1], w8[2], w8[3]));
+          st_cluster_u4(row + static_cast<uint32_t>((2 * hc + 1) ^ (dd & 7)) * 16,
+                        make_uint4(w8[4], w8[5], w8[6], w8[7]));
         }
       }
       if (warp < 2) {
         for (int p = 0; p < S; ++p) {
           if (p == split) continue;
-          float* t = reinterpret_cast<float*>(gbase + (send_slot(p) - sbase) + D * 128);
-          t[2 * tid] = m_own;
-          t[2 * tid + 1] = l_own;
+          st_cluster_f32x2(mapa_shared(recv_slot(split) + D * 128 + 8 * tid, static_cast<uint32_t>(p)),
+                           m_own, l_own);
         }
       }
-      fence_proxy_async_smem();  // the staged payloads, for the copy engine
-      if (tid == 0) mbar_arrive_expect_tx(&misc->xchg, static_cast<uint32_t>(S - 1) * pay);
-      named_sync(kMathBar, 128);
-      cluster_arrive();  // phase 1
-      cluster_wait();
-      if (tid == 0) {
-        for (int p = 0; p < S; ++p) {
-          if (p == split) continue;
-          bulk_s2cluster(mapa_shared(sbase + kRecv + static_cast<uint32_t>(split) * pay,
-                                     static_cast<uint32_t>(p)),
-                         send_slot(p), pay,
-                         mapa_shared(smem_u32(&misc->xchg), static_cast<uint32_t>(p)));
-        }
-      }
-      if (ok) ok = wait_bar(&misc->xchg, 0u, misc, a.status);
-      cluster_arrive();  // phase 2: this CTA's payloads have all landed
-      // out = sum_s w_s O_s with w_s = 2^(m_s - M) / L, M = max_s m_s,
-      // L = sum_s 2^(m_s - M) l_s (a range without rows has l_s = 0); a
-      // received O_s comes divided by l_s, so its weight takes l_s back.
+      cluster_arrive();  // phase 2: every payload is written (release) ...
+      cluster_wait();    // ... and visible here (acquire)
+      // out = sum_q w_q O_q with w_q = 2^(m_q - M) / L, M = max_q m_q,
+      // L = sum_q 2^(m_q - M) l_q (a range without rows has l_q = 0), O_q the
+      // unnormalised accumulator of CTA q.
       float* wgt = reinterpret_cast<float*>(gbase + kWgt);  // [S][64]
       if (warp < 2) {
-        auto ml_of = [&](int q, float& mq, float& lq) {
-          if (q == split) {
-            mq = m_own;
-            lq = l_own;
-          } else {
-            const float* t = reinterpret_cast<const float*>(
-                gbase + kRecv + static_cast<uint32_t>(q) * pay + D * 128);
-            mq = ok ? t[2 * tid] : -INFINITY;
-            lq = ok ? t[2 * tid + 1] : 0.f;
-          }
-        };
+        float mq[kMaxAttnSplits], lqs[kMaxAttnSplits];
         float M = -INFINITY;
-        for (int q = 0; q < S; ++q) {
-          float mq, lq;
-          ml_of(q, mq, lq);
-          if (lq > 0.f) M = fmaxf(M, mq);
+#pragma unroll
+        for (int q = 0; q < kMaxAttnSplits; ++q) {
+          mq[q] = -INFINITY;
+          lqs[q] = 0.f;
+          if (q < S) {
+            const float* t = reinterpret_cast<const float*>(gbase + (recv_slot(q) - sbase) + D * 128);
+            mq[q] = t[2 * tid];
+            lqs[q] = t[2 * tid + 1];
+          }
+          if (lqs[q] > 0.f) M = fmaxf(M, mq[q]);
         }
-        float L = 0.f;
-        for (int q = 0; q < S; ++q) {
-          float mq, lq;
-          ml_of(q, mq, lq);
-          const float eq = lq > 0.f ? exp2f(mq - M) : 0.f;
-          L = fmaf(eq, lq, L);
-          wgt[q * kHeads + tid] = q == split ? eq : eq * lq;
+        float L = 0.f, eq[kMaxAttnSplits];
+#pragma unroll
+        for (int q = 0; q < kMaxAttnSplits; ++q) {
+          eq[q] = lqs[q] > 0.f ? exp2f(mq[q] - M) : 0.f;
+          L = fmaf(eq[q], lqs[q], L);
         }
         const float inv_L = L > 0.f ? 1.f / L : 0.f;
-        for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
+#pragma unroll
+        for (int q = 0; q < kMaxAttnSplits; ++q) {
+          if (q < S) wgt[q * kHeads + tid] = eq[q] * inv_L;
+        }
         if (a.lse && split == 0) {
           a.lse[static_cast<int64_t>(b) * kHeads + tid] =
               L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
         }
       }
-      named_sync(kMathBar, 128);
+      named_sync(kEpiBar, kEpiThreads);
       const uint32_t wgt_s = sbase + kWgt;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + tid;
+        const int d = 128 * m + et;
         if (d / D != split) continue;
         const int dd = d - split * D;
 #pragma unroll 1
-        for (int hc = 0; hc < 4; ++hc) {
+        for (int hc = 2 * half; hc < 2 * half + 2; ++hc) {
           float v[16];
           load16(m, hc, v);
           scale16(v, wgt_s + static_cast<uint32_t>(split * kHeads * 4), hc);
 #pragma unroll 1
           for (int q = 0; q < S; ++q) {
-            if (q == split || !ok) continue;
-            const uint32_t row = sbase + kRecv + static_cast<uint32_t>(q) * pay +
-                                 static_cast<uint32_t>(dd) * 128;
+            if (q == split) continue;
+            const uint32_t row = recv_slot(q) + static_cast<uint32_t>(dd) * 128;
             const uint4 x0 = ld_shared_v4(row + static_cast<uint32_t>((2 * hc) ^ (dd & 7)) * 16);
             const uint4 x1 =
                 ld_shared_v4(row + static_cast<uint32_t>((2 * hc + 1) ^ (dd & 7)) * 16);
@@ -738,7 +749,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (paired) cluster_wait();  // phase 2: no copy touches this CTA any more
+  // The epilogue warps have waited for phase 2 (no peer writes this CTA any
+  // more); the MMA warps, which only arrived there, wait now.
+  if (paired && warp >= kMmaWarp) cluster_wait();
 }
 
 }  // namespace

@@ -255,6 +255,14 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                "f"(c), "f"(d)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
   asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(a) : "memory");
 }

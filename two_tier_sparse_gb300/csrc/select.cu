@@ -348,25 +348,68 @@ struct RegShared {
   uint32_t bin_idx[kRankMax];
   uint32_t taken[kThreads];  // bit i: candidate i of the final bin is selected (n <= 32 x 1024)
   uint32_t warp_a[kWarps], warp_b[kWarps], warp_c[kWarps];
-  uint32_t kmin, kmax, n_valid, bstar, need, count, total;
+  uint32_t bstar, need, count, nbin;
 };
+
+// Exclusive prefix, over the warps before this one, of the per-warp values
+// v[w] (v read from shared memory at lane w), with the total; every warp
+// computes it itself, so no second barrier is needed.
+__device__ __forceinline__ uint32_t warps_before(uint32_t v_lane, int warp, uint32_t* total) {
+  const uint32_t incl = warp_incl_scan(v_lane);
+  *total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  return __shfl_sync(0xFFFFFFFFu, incl - v_lane, warp);
+}
 
 template <int KPT>
 __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   __shared__ RegShared sh;
   extern __shared__ int32_t bids[];  // token stage: the query's block ids
   griddep_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // State that depends on no input is cleared while the previous kernel ends.
+  for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
+  sh.taken[tid] = 0u;
+  if (tid == 0) sh.nbin = 0;
   griddep_wait();
   // The CTA's candidates: all of query b's (plain), chunk c of them (first
   // pass of a two-pass selection), or the ids the first pass kept (second).
   const int b = a.chunks ? static_cast<int>(blockIdx.x / a.chunks) : static_cast<int>(blockIdx.x);
   const int64_t base = a.chunks ? static_cast<int64_t>(blockIdx.x % a.chunks) * a.chunk : 0;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n);
   const uint32_t k = static_cast<uint32_t>(a.k);
   const float* sc = a.scores + static_cast<int64_t>(b) * a.n;
   const int32_t* ids_in = a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in : nullptr;
+  const bool dense = a.dense_stride && a.block_ids;
 
+  uint32_t key[KPT];
+  const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
+  // Scores that do not go through the block ids are requested first, so their
+  // latency overlaps the block-id copy below.
+  if (ids_in) {
+    // Second pass: the kept ids ascend along the list (chunks in order, each
+    // ascending, -1 padded), so list order is id order for the tie rule.
+    // (The key registers hold the ids first: no second array.)
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t i = wbase + 32 * j;
+      key[j] = static_cast<uint32_t>(i < n ? ids_in[i] : -1);
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int32_t id = static_cast<int32_t>(key[j]);
+      key[j] = score_key(id >= 0 ? sc[id] : -INFINITY);
+    }
+  } else if (!dense) {
+    // all KPT loads go out before any is used (indices clamped into the row)
+    float v[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t i = wbase + 32 * j;
+      v[j] = __ldg(sc + base + (i < n ? i : 0));
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) key[j] = score_key(wbase + 32 * j < n ? v[j] : -INFINITY);
+  }
   if (a.block_ids) {
     // Ascending block ids with -1 padding at the end are required: the tie
     // rule and the ascending output rely on it.
@@ -381,38 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         }
       }
     }
-    if (a.dense_stride) __syncthreads();  // the keys below are read through the block ids
+    if (dense) __syncthreads();  // the keys below are read through the block ids
   }
-  sh.taken[tid] = 0u;
-  uint32_t key[KPT];
-  const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
-  if (a.dense_stride && a.block_ids) {
+  if (dense) {
     const float* row = a.scores + static_cast<int64_t>(b) * a.dense_stride;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       const int64_t i = wbase + 32 * j;
       const int blk = i < n ? bids[i >> 3] : -1;
       key[j] = score_key(blk >= 0 ? row[static_cast<int64_t>(blk) * 8 + (i & 7)] : -INFINITY);
-    }
-  } else if (ids_in) {
-    // Second pass: the kept ids ascend along the list (chunks in order, each
-    // ascending, -1 padded), so list order is id order for the tie rule.
-    // (The key registers hold the ids first: no second array.)
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const int64_t i = wbase + 32 * j;
-      key[j] = static_cast<uint32_t>(i < n ? ids_in[i] : -1);
-    }
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const int32_t id = static_cast<int32_t>(key[j]);
-      key[j] = score_key(id >= 0 ? sc[id] : -INFINITY);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const int64_t i = wbase + 32 * j;
-      key[j] = score_key(i < n ? sc[base + i] : -INFINITY);
     }
   }
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
@@ -433,24 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     sh.warp_c[warp] = cnt;
   }
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t mn = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
-    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
-    const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, sh.warp_c[lane]);
-    if (lane == 0) {
-      sh.kmin = mn;
-      sh.kmax = mx;
-      sh.n_valid = c;
-    }
-  }
-  __syncthreads();
-  kmin = sh.kmin;
-  const bool take_all = sh.n_valid <= k;
-  const uint32_t span = sh.kmax - kmin;
+  // every warp reduces the 32 warps' values itself
+  kmin = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
+  const uint32_t n_valid = __reduce_add_sync(0xFFFFFFFFu, sh.warp_c[lane]);
+  const bool take_all = n_valid <= k;
+  const uint32_t span = kmax - kmin;
   uint32_t P = 0, s_cur = 32, need = k;
   bool ties = false;
   // Threshold search over a histogram in sh.hist: the bin holding the
-  // need-th largest key, counted from the top bin down.
+  // nd-th largest key, counted from the top bin down. The caller has synced
+  // after filling the histogram; this ends with a barrier after which
+  // sh.bstar / sh.need / sh.count hold the bin, the count still needed in it
+  // and its size. (sh.warp_a is rewritten: its readers are behind a barrier.)
   auto find_threshold = [&](uint32_t nd) {
     uint32_t h[4], local = 0;
 #pragma unroll
@@ -461,12 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     const uint32_t incl = warp_incl_scan(local);
     if (lane == 31) sh.warp_a[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-      const uint32_t x = sh.warp_a[lane];
-      sh.warp_b[lane] = warp_incl_scan(x) - x;
-    }
-    __syncthreads();
-    uint32_t run = incl - local + sh.warp_b[warp];
+    uint32_t total;
+    uint32_t run = incl - local + warps_before(sh.warp_a[lane], warp, &total);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (run < nd && run + h[j] >= nd) {
@@ -491,11 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   for (int j = 0; j < (KPT + 1) / 2; ++j) binp[j] = 0;
   if (!take_all) {
     const float vmin = key_value(kmin);
-    const float vspan = key_value(sh.kmax) - vmin;
+    const float vspan = key_value(kmax) - vmin;
     const float vscale = static_cast<float>(kBins) / vspan;
     if (vspan > 0.f && isfinite(vspan) && isfinite(vscale)) {
-      for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
-      __syncthreads();
 #pragma unroll
       for (int j = 0; j < KPT; ++j) {
         if (key[j] > kInvalidKey) {
@@ -511,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         vbin = sh.bstar;
         need = sh.need;
       }
-      __syncthreads();
     }
   }
   auto bin_of = [&](int j) -> uint32_t { return (binp[j >> 1] >> (16 * (j & 1))) & 0xFFFFu; };
@@ -545,98 +553,102 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       __syncthreads();
     }
   }
-  // Candidate j's position relative to the threshold bin: 1 above, 0 in it, -1 below.
-  auto side = [&](int j) -> int {
-    if (vspace) {
-      const uint32_t bj = bin_of(j);
-      return bj > vbin ? 1 : (bj == vbin ? 0 : -1);
-    }
-    const uint32_t hi = (key[j] - kmin) >> s_cur;
-    return hi > P ? 1 : (hi == P ? 0 : -1);
-  };
-  // Final bin: rank its members exactly (unless they all tie), 16 threads per
-  // member, and mark the taken ones in sh.taken by candidate index.
-  if (!take_all && !ties) {
-    __syncthreads();  // every thread has read the last level's bin count
-    if (tid == 0) sh.count = 0;
-    __syncthreads();
+  // Classification against the threshold bin, as warp ballots over slot j:
+  // gt_mask[j] = candidates strictly above the bin. The bin's members either
+  // all tie (then the first `need` of them in index order are taken, and
+  // sh.taken holds their ballots) or are collected here, ranked below and
+  // their taken ones marked in sh.taken. Candidate wbase + 32 j is bit `lane`
+  // of word warp * KPT + j, so a warp reads its slot-j word of sh.taken at once.
+  uint32_t gt_mask[KPT];
+  uint32_t e_w = 0;  // tied bin members in this warp
+  const bool collect = !take_all && !ties;
+  if (take_all) {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) gt_mask[j] = __ballot_sync(0xFFFFFFFFu, key[j] > kInvalidKey);
+  } else if (vspace) {
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      if (key[j] > kInvalidKey && side(j) == 0) {
-        const uint32_t slot = atomicAdd(&sh.count, 1u);
+      const bool valid = key[j] > kInvalidKey;
+      const uint32_t bj = bin_of(j);
+      gt_mask[j] = __ballot_sync(0xFFFFFFFFu, valid && bj > vbin);
+      if (valid && bj == vbin) {  // a value-space bin is always ranked (never ties)
+        const uint32_t slot = atomicAdd(&sh.nbin, 1u);
         sh.bin_key[slot] = key[j];
         sh.bin_idx[slot] = static_cast<uint32_t>(wbase + 32 * j);
       }
     }
-    __syncthreads();
-    const uint32_t c = sh.count;
-    const uint32_t mi = static_cast<uint32_t>(tid >> 4), part = static_cast<uint32_t>(tid & 15);
-    uint32_t rank = 0, ke = 0, ie = 0;
-    if (mi < c) {
-      ke = sh.bin_key[mi];
-      ie = sh.bin_idx[mi];
-      for (uint32_t o = part; o < c; o += 16) {
-        const uint32_t ko = sh.bin_key[o];
-        rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const bool valid = key[j] > kInvalidKey;
+      const uint32_t hi = (key[j] - kmin) >> s_cur;
+      const bool inb = valid && hi == P;
+      gt_mask[j] = __ballot_sync(0xFFFFFFFFu, valid && hi > P);
+      if (ties) {
+        const uint32_t e = __ballot_sync(0xFFFFFFFFu, inb);
+        if (lane == 0) sh.taken[warp * KPT + j] = e;
+        e_w += __popc(e);
+      } else if (inb) {
+        const uint32_t slot = atomicAdd(&sh.nbin, 1u);
+        sh.bin_key[slot] = key[j];
+        sh.bin_idx[slot] = static_cast<uint32_t>(wbase + 32 * j);
       }
     }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
-    if (part == 0 && mi < c && rank < need) atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
-    __syncthreads();
+    if (ties) __syncwarp();  // lane 0's words, read by the whole warp below
   }
-  // Selection masks per slot run, then the warps' totals -> output offsets.
-  uint32_t gt_mask[KPT], eq_mask[KPT];
-  uint32_t g_w = 0, e_w = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    bool gt = false, eq = false;
-    if (key[j] > kInvalidKey) {
-      if (take_all) {
-        gt = true;
-      } else {
-        const int sd = side(j);
-        if (sd > 0) {
-          gt = true;
-        } else if (sd == 0) {
-          if (ties) {
-            eq = true;
-          } else {
-            const uint32_t i = static_cast<uint32_t>(wbase + 32 * j);
-            gt = (sh.taken[i >> 5] >> (i & 31)) & 1u;
-          }
+  if (collect) {
+    __syncthreads();
+    const uint32_t c = sh.nbin;
+    if (need >= c) {
+      // every member is taken
+      if (static_cast<uint32_t>(tid) < c) {
+        const uint32_t ie = sh.bin_idx[tid];
+        atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
+      }
+    } else {
+      const uint32_t mi = static_cast<uint32_t>(tid >> 4), part = static_cast<uint32_t>(tid & 15);
+      uint32_t rank = 0, ke = 0, ie = 0;
+      if (mi < c) {
+        ke = sh.bin_key[mi];
+        ie = sh.bin_idx[mi];
+        for (uint32_t o = part; o < c; o += 16) {
+          const uint32_t ko = sh.bin_key[o];
+          rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
         }
       }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+      if (part == 0 && mi < c && rank < need) atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
     }
-    gt_mask[j] = __ballot_sync(0xFFFFFFFFu, gt);
-    eq_mask[j] = ties ? __ballot_sync(0xFFFFFFFFu, eq) : 0u;
-    g_w += __popc(gt_mask[j]);
-    e_w += __popc(eq_mask[j]);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) gt_mask[j] |= sh.taken[warp * KPT + j];
   }
-  // Warp totals -> block scan (in warp order = index order) -> each warp's
-  // output offset and its share of the ties taken at the threshold.
+  uint32_t g_w = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) g_w += __popc(gt_mask[j]);
+  // Warp totals -> (every warp scans them itself, in warp order = index
+  // order) this warp's output offset and its share of the ties taken at the
+  // threshold.
   if (lane == 0) {
     sh.warp_a[warp] = g_w;
     sh.warp_b[warp] = e_w;
   }
   __syncthreads();
-  if (warp == 0) {
+  uint32_t total, te_w;
+  uint32_t pos;
+  {
     const uint32_t take_eq_total = ties ? need : 0u;
     const uint32_t e = sh.warp_b[lane], g = sh.warp_a[lane];
-    const uint32_t e_incl = warp_incl_scan(e);
-    const uint32_t e_before = e_incl - e;
+    const uint32_t e_before = warp_incl_scan(e) - e;  // ties in the warps before warp `lane`
     const uint32_t te = take_eq_total > e_before ? min(e, take_eq_total - e_before) : 0u;
     const uint32_t sel = g + te;
-    const uint32_t sel_incl = warp_incl_scan(sel);
-    sh.warp_a[lane] = sel_incl - sel;  // output offset of the warp
-    sh.warp_b[lane] = te;              // ties the warp takes
-    if (lane == 31) sh.total = sel_incl;
+    pos = warps_before(sel, warp, &total);  // output offset of this warp
+    te_w = __shfl_sync(0xFFFFFFFFu, te, warp);  // ties this warp takes
   }
-  __syncthreads();
   // First pass: row b * chunks + c of the scratch, i.e. row blockIdx.x.
   int32_t* out = a.out_ids + static_cast<int64_t>(blockIdx.x) * a.k;
   const uint32_t lt = (1u << lane) - 1u;
-  uint32_t pos = sh.warp_a[warp];
   auto out_id = [&](int j) -> int32_t {
     const int64_t i = wbase + 32 * j;
     if (ids_in) return ids_in[i];
@@ -650,22 +662,21 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       pos += __popc(gt_mask[j]);
     }
   } else {
-    const uint32_t te_w = sh.warp_b[warp];
     uint32_t eq_seen = 0;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
+      const uint32_t eqm = sh.taken[warp * KPT + j];  // the tied members of slot j
       // ties taken in this run: the first (te_w - eq_seen) tied lanes, if any left
       const uint32_t left = te_w > eq_seen ? te_w - eq_seen : 0u;
-      const uint32_t eq_rank = __popc(eq_mask[j] & lt);
+      const uint32_t eq_rank = __popc(eqm & lt);
       const bool is_gt = (gt_mask[j] >> lane) & 1u;
-      const bool is_eq = ((eq_mask[j] >> lane) & 1u) && eq_rank < left;
+      const bool is_eq = ((eqm >> lane) & 1u) && eq_rank < left;
       if (is_gt || is_eq) out[pos + __popc(gt_mask[j] & lt) + min(eq_rank, left)] = out_id(j);
-      const uint32_t taken_eq = min(static_cast<uint32_t>(__popc(eq_mask[j])), left);
+      const uint32_t taken_eq = min(static_cast<uint32_t>(__popc(eqm)), left);
       pos += __popc(gt_mask[j]) + taken_eq;
-      eq_seen += __popc(eq_mask[j]);
+      eq_seen += __popc(eqm);
     }
   }
-  const uint32_t total = sh.total;
   for (int64_t j = total + tid; j < a.k; j += kThreads) out[j] = -1;
 }
 
