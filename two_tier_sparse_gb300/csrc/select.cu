@@ -335,11 +335,13 @@ constexpr int kRankMax = 64;  // final bins at most this large are ranked exactl
 __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
-// Value-space histogram bin: non-decreasing in v for v >= vmin.
+// Value-space histogram bin: non-decreasing in v for v >= vmin. t =
+// (v - vmin) * vscale lies in [0, ~kBins]; adding 2^23 rounds it to an
+// integer held in the low mantissa bits (every step is monotone, so the bin
+// is), which avoids a float-to-integer conversion.
 __device__ __forceinline__ uint32_t value_bin(float v, float vmin, float vscale) {
-  const float t = (v - vmin) * vscale;
-  return t >= static_cast<float>(kBins - 1) ? static_cast<uint32_t>(kBins - 1)
-                                             : static_cast<uint32_t>(t);
+  const float t = (v - vmin) * vscale + 8388608.f;
+  return min(__float_as_uint(t) - 0x4B000000u, static_cast<uint32_t>(kBins - 1));
 }
 
 struct RegShared {
@@ -411,19 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     for (int j = 0; j < KPT; ++j) key[j] = score_key(wbase + 32 * j < n ? v[j] : -INFINITY);
   }
   if (a.block_ids) {
-    // Ascending block ids with -1 padding at the end are required: the tie
-    // rule and the ascending output rely on it.
+    // copied to shared memory; their order is checked after the next barrier
     const int32_t* bl = a.block_ids + static_cast<int64_t>(b) * a.k_blocks;
-    for (int i = tid; i < a.k_blocks; i += kThreads) {
-      const int x = bl[i];
-      bids[i] = x;
-      if (i + 1 < a.k_blocks) {
-        const int y = bl[i + 1];
-        if (y >= 0 && (x < 0 || y <= x)) {
-          record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
-        }
-      }
-    }
+    for (int i = tid; i < a.k_blocks; i += kThreads) bids[i] = bl[i];
     if (dense) __syncthreads();  // the keys below are read through the block ids
   }
   if (dense) {
@@ -453,6 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     sh.warp_c[warp] = cnt;
   }
   __syncthreads();
+  if (a.block_ids) {
+    // Ascending block ids with -1 padding at the end are required: the tie
+    // rule and the ascending output rely on it.
+    for (int i = tid; i + 1 < a.k_blocks; i += kThreads) {
+      const int x = bids[i], y = bids[i + 1];
+      if (y >= 0 && (x < 0 || y <= x)) {
+        record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
+      }
+    }
+  }
   // every warp reduces the 32 warps' values itself
   kmin = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
   kmax = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
