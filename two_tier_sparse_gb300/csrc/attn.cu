@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // below turns them into rows of the shared pool.
   const bool paged = a.pages.table != nullptr;
   const int lat_seq = a.prefill ? query_seq(a.mq, b) : (paged ? 0 : b);
-  const uint16_t* lat = a.latents + static_cast<int64_t>(lat_seq) * a.lat_stride * kLatent;
+  const int64_t lat_row0 = static_cast<int64_t>(lat_seq) * a.lat_stride;  // its first row
   // This CTA's rows: its part of the window rows first (they are inputs of the
   // step, so they stream while the previous kernel still selects the tokens),
   // then its part of the selected latents (known once the ids are compacted).
@@ -344,26 +344,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-#pragma unroll 8
-      for (int j = 0; j < 64; ++j) {  // 32 rows x 64 chunks of 16 B
-        const int c = lane + 32 * j;
-        const int row = 32 * part + (c >> 6), cr = c & 63;
-        const int g = g0 + row;
-        const uint32_t dst = dstb + (cr >> 3) * kAtomBytes + sw128_off(row, cr & 7);
-        bool copy = g < n_rows_cta;
-        const uint16_t* src = nullptr;
-        if (copy) {
-          // the row's place in its whole array (window buffer or latents)
-          const int64_t arow = (g < w_cnt) ? wrow0 + w_begin + g
-                                           : (lat - a.latents) / kLatent + ids[s_begin + g - w_cnt];
-          copy = DSA_DCHECK(arow >= 0 && arow < (g < w_cnt ? a.swa_rows : a.lat_rows), a.status,
-                            SITE_ATTN, arow);
-          src = ((g < w_cnt) ? a.swa : a.latents) + arow * kLatent;
+      // Lane l works out the source of the warp's row l once (its place in the
+      // window buffer or the latents; -1: none, zero-filled); each row is then
+      // copied by the whole warp, lane l taking 16-byte chunks l and l + 32, so
+      // a copy instruction of the warp covers 512 contiguous bytes.
+      int64_t arow_l = -1;
+      {
+        const int gl = r0 + lane;
+        if (gl < n_rows_cta) {
+          arow_l = gl < w_cnt ? wrow0 + w_begin + gl : lat_row0 + ids[s_begin + gl - w_cnt];
+          if (!DSA_DCHECK(arow_l >= 0 && arow_l < (gl < w_cnt ? a.swa_rows : a.lat_rows), a.status,
+                          SITE_ATTN, arow_l)) {
+            arow_l = -1;
+          }
         }
-        if (copy) {
-          cp_async_16(dst, src + cr * 8);
+      }
+      // chunk lane of a row: atom lane / 8, 16-byte unit lane % 8; chunk
+      // lane + 32: atom 4 + lane / 8, same unit
+      const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) {
+        const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
+        const int row = 32 * part + r;
+        const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
+        const uint32_t d1 = d0 + 4 * kAtomBytes;
+        if (arow >= 0) {
+          const uint16_t* src = (r0 + r < w_cnt ? a.swa : a.latents) + arow * kLatent + lane * 8;
+          cp_async_16(d0, src);
+          cp_async_16(d1, src + 256);
         } else {
-          st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+          st_shared_v4(d0, make_uint4(0, 0, 0, 0));
+          st_shared_v4(d1, make_uint4(0, 0, 0, 0));
         }
       }
       cp_async_commit();
