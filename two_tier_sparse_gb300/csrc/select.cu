@@ -330,6 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a, int u
 // slot j, so every pass runs on registers and each warp lays out its own part
 // of the output; only the warps' totals need a block-wide scan.
 constexpr int kRankMax = 64;  // final bins at most this large are ranked exactly
+// Dense score rows of at most this many tokens are staged whole in shared
+// memory (after the block ids) before their kept blocks are read: at the
+// densities where rows are dense (a prefill chunk's kept blocks are about
+// half of its blocks), one coalesced pass over the row costs less than a
+// scattered 32-byte read per kept block.
+constexpr int64_t kStagedRowMax = 48640;
+constexpr int kStageIters = static_cast<int>((kStagedRowMax / 4 + 1023) / 1024);  // float4 a thread
 
 // The score a valid order-preserving key stands for (inverse of score_key).
 __device__ __forceinline__ float key_value(uint32_t key) {
@@ -412,6 +419,30 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
 #pragma unroll
     for (int j = 0; j < KPT; ++j) key[j] = score_key(wbase + 32 * j < n ? v[j] : -INFINITY);
   }
+  const bool staged = dense && a.dense_stride <= kStagedRowMax;
+  const float* row = dense ? a.scores + static_cast<int64_t>(b) * a.dense_stride : nullptr;
+  float* row_s = reinterpret_cast<float*>(bids + kMaxKBlocks);  // staged row (16-byte aligned)
+  if (staged) {
+    // the whole row, in two rounds of float4 loads (each round's loads all
+    // issued before any is stored)
+    const int n4 = static_cast<int>(a.dense_stride / 4);
+    const float4* src = reinterpret_cast<const float4*>(row);
+    constexpr int kRound = (kStageIters + 1) / 2;
+#pragma unroll
+    for (int u0 = 0; u0 < kStageIters; u0 += kRound) {
+      float4 v4[kRound];
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        const int i = tid + (u0 + u) * kThreads;
+        if (u0 + u < kStageIters && i < n4) v4[u] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        const int i = tid + (u0 + u) * kThreads;
+        if (u0 + u < kStageIters && i < n4) reinterpret_cast<float4*>(row_s)[i] = v4[u];
+      }
+    }
+  }
   if (a.block_ids) {
     // copied to shared memory; their order is checked after the next barrier
     const int32_t* bl = a.block_ids + static_cast<int64_t>(b) * a.k_blocks;
@@ -419,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     if (dense) __syncthreads();  // the keys below are read through the block ids
   }
   if (dense) {
-    const float* row = a.scores + static_cast<int64_t>(b) * a.dense_stride;
+    const float* rsrc = staged ? row_s : row;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       const int64_t i = wbase + 32 * j;
       const int blk = i < n ? bids[i >> 3] : -1;
-      key[j] = score_key(blk >= 0 ? row[static_cast<int64_t>(blk) * 8 + (i & 7)] : -INFINITY);
+      key[j] = score_key(blk >= 0 ? rsrc[static_cast<int64_t>(blk) * 8 + (i & 7)] : -INFINITY);
     }
   }
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
@@ -686,10 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
 
 template <int KPT>
 cudaError_t launch_reg(const SelectArgs& a, unsigned grid, cudaStream_t s) {
-  const size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
+  // block ids, then (dense rows that fit) the staged row
+  size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
+  if (a.block_ids && a.dense_stride && a.dense_stride <= kStagedRowMax) {
+    smem = static_cast<size_t>(kMaxKBlocks) * 4 + static_cast<size_t>(a.dense_stride) * 4;
+  }
   static std::atomic<int> smem_set[64]{};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
-                              static_cast<int>(kMaxKBlocks * 4), smem_set);
+                              static_cast<int>(kMaxKBlocks * 4 + kStagedRowMax * 4), smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(select_reg_kernel<KPT>, dim3(grid), dim3(kThreads), smem, s, 1, a);
 }
