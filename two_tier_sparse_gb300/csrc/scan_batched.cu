@@ -18,8 +18,10 @@
 //              each group's index queries (B operand, 64 KB) and weights;
 //   warp 1     MMA issuer (one thread), tensor-memory owner: two accumulators
 //              of 256 columns, so one tile's epilogue overlaps the next MMA;
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its key
-//              rows) and columns of queries 8 ((w - 2) / 4) .. + 7.
+//   warps 2-17 epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its key
+//              rows) and the columns of queries 4 ((w - 2) / 4) .. + 3 (the
+//              head sums of 16 queries per key row are the kernel's longest
+//              step, so they are spread over sixteen warps).
 #include "kernels.h"
 
 namespace dsa {
@@ -31,7 +33,7 @@ constexpr int kGroup = 16;       // queries per group
 constexpr int kN = kGroup * kIdxHeads;  // 256 MMA columns
 constexpr int kStages = 4;
 constexpr int kEpiWarp0 = 2;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // 320
 constexpr int kTileBytes = kTile * kIdxDim * 2;          // 32 KB: two K-atoms of 16 KB
 constexpr int kQBytes = kN * kIdxDim * 2;                // 64 KB: two K-atoms of 32 KB
@@ -203,14 +205,14 @@ __device__ void mma_issuer(const BatchedScanArgs& a, Shared& sh, uint32_t sbase,
 __device__ void epilogue(const BatchedScanArgs& a, Shared& sh, int64_t i0, int64_t i1, int64_t T) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;                   // TMEM lanes this warp may read
-  const int half = (warp - kEpiWarp0) >> 2;    // queries 8 half .. 8 half + 7 of the group
+  const int quarter = (warp - kEpiWarp0) >> 2;  // queries 4 quarter .. + 3 of the group
   const int row = 32 * quad + lane;
   const uint32_t tmem = sh.tmem_base;
   const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
   int64_t n_done = 0;
-  // Per group: this warp's eight queries' visible rows (-1: no such query).
+  // Per group: this warp's four queries' visible rows (-1: no such query).
   int cur_g = -1;
-  int vis[8];
+  int vis[4];
   Walk it;
   it.init(a, i0, T);
   for (int64_t i = i0; i < i1; ++i, it.next(a, T)) {
@@ -218,8 +220,8 @@ __device__ void epilogue(const BatchedScanArgs& a, Shared& sh, int64_t i0, int64
     if (it.g != cur_g) {
       cur_g = it.g;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t q = static_cast<int64_t>(cur_g) * kGroup + 8 * half + j;
+      for (int j = 0; j < 4; ++j) {
+        const int64_t q = static_cast<int64_t>(cur_g) * kGroup + 4 * quarter + j;
         vis[j] = q < a.n_q ? static_cast<int>(visible_rows(a, q)) : -1;
       }
     }
@@ -231,17 +233,16 @@ __device__ void epilogue(const BatchedScanArgs& a, Shared& sh, int64_t i0, int64
     tc_fence_after();
     const int r = it.t * kTile + row;
     const bool in_cols = r < a.n_cols;
-    float* out = a.scores + (static_cast<int64_t>(it.g) * kGroup + 8 * half) * a.n_cols + r;
-    // Two tensor-memory loads of four queries' 64 columns each (one wait per
-    // load), then the ReLU-weighted head sums in head order.
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
+    float* out = a.scores + (static_cast<int64_t>(it.g) * kGroup + 4 * quarter) * a.n_cols + r;
+    // One tensor-memory load of the four queries' 64 columns, then the
+    // ReLU-weighted head sums in head order.
+    {
       float v[64];
-      tmem_ld64(tmem + lane_base + static_cast<uint32_t>(slot * kN + 16 * (8 * half + 4 * jj)), v);
+      tmem_ld64(tmem + lane_base + static_cast<uint32_t>(slot * kN + 16 * (4 * quarter)), v);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int j = 4 * jj + k;
-        const int qj = 8 * half + j;  // query within the group
+        const int j = k;
+        const int qj = 4 * quarter + j;  // query within the group
         if (vis[j] >= 0 && in_cols) {
           float sc = -INFINITY;
           if (r < vis[j]) {
