@@ -241,7 +241,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
                              int64_t max_latents, int32_t* block_ids, float* scores,
                              DeviceStatus* st, int32_t* sel_tmp, cudaStream_t s, int prefill,
                              int64_t ctx, const dsa_keys_t* partial_keys,
-                             MultiQuery m = MultiQuery{}) {
+                             MultiQuery m = MultiQuery{}, int after_tail_pool = 0) {
   Range range("dsa.block_stage");
   const int64_t nb_max = (max_latents + kBlock - 1) / kBlock;
   if (m.mq == 0 && prefill_batched(pooled, prefill, max_latents / kBlock)) {
@@ -278,6 +278,7 @@ dsa_status_t run_block_stage(const dsa_config_t& c, const uint16_t* q_idx, const
     sa.prefill = prefill;
     sa.ctx = ctx;
     sa.ratio = c.ratio;
+    sa.defer_wait = after_tail_pool;
     sa.status = st;
     DSA_CUDA(launch(DSA_KERNEL_SCAN, s, [&](int*) { return launch_scan(sa, device_sm_count(), s); }));
   }
@@ -717,9 +718,12 @@ dsa_status_t dsa_decode_step(const dsa_config_t* cfg, const void* q, const void*
   int32_t* bids = block_ids ? block_ids : at<int32_t>(workspace, L.block_ids);
   const int32_t* gather_ids = nullptr;
   if (L.nb_max > cfg->k_blocks) {
+    // right after the tail pool, the block scan streams every block the pool
+    // does not rewrite before it waits for the pool
     DSA_TRY(run_block_stage(*cfg, qi, w, pk, n_latents, B, max_latents, bids,
                             at<float>(workspace, L.block_scores), st, select_tmp(workspace, L), s,
-                            0, 0, nullptr));
+                            0, 0, nullptr, MultiQuery{},
+                            update_pool && max_latents > 0 && !pk.pages ? 1 : 0));
     gather_ids = bids;
   } else if (block_ids) {
     DSA_CUDA(launch(DSA_KERNEL_OTHER, s, [&](int*) { return launch_identity_blocks(n_latents, B, cfg->k_blocks, block_ids, s); }));

@@ -136,6 +136,12 @@ struct ScanArgs {
   // are then read in groups of 8 (one TMA box each), like gathered blocks.
   Paging pages;
   int64_t key_rows;  // rows of the key array (set by launch_scan; debug checks)
+  // Block stage of a decode step whose previous kernel is the tail pool
+  // (which rewrites only each sequence's last block): the dependency wait is
+  // taken by the producer just before the first tile that holds a sequence's
+  // last block, so every other tile streams while the pool still runs.
+  // Contiguous caches only.
+  int defer_wait;
   DeviceStatus* status;
 };
 // In prefill ROWS_BLOCKS mode only complete blocks are scored; a query's

@@ -146,10 +146,13 @@ __device__ __forceinline__ Stored round_to_format(int fmt, const float (&v)[4], 
   return st;
 }
 
-// One warp per (sequence, block).
+// One warp per (sequence, block). The dependent kernel is released only once
+// this kernel's own dependency wait has returned: a decode step's block scan
+// reads the blocks this kernel does not write before its own wait, and those
+// blocks must be final (every earlier kernel complete).
 __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y;

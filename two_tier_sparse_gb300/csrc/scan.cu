@@ -264,6 +264,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
     return nv;
   };
   int s = 0;           // stage of this iteration
+  bool waited = !a.defer_wait;  // the dependency wait has been taken
   uint32_t kpar = 0;   // parity of the stage's use count
   for (int64_t j0 = 0; j0 < n_own; j0 += TPS) {
     TilePos next2 = next;
@@ -369,6 +370,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
       // Contiguous rows: the same values in every lane; lane 0 issues the boxes.
       int nrows[TPS];
       uint32_t bytes = 0;
+      bool tail = false;  // a tile of the stage reaches its sequence's last row
 #pragma unroll
       for (int t = 0; t < TPS; ++t) {
         nrows[t] = 0;
@@ -376,6 +378,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
           TilePos tp = first;
           tp.advance(2 * t, q_rows);
           int64_t v = contiguous_rows(a, n_vis_of(tp.b)) - tp.r0;
+          tail = tail || (v > 0 && v <= kTile);
           v = v < 0 ? 0 : (v > kTile ? kTile : v);
           nrows[t] = static_cast<int>(v);
           const int64_t row = seq_row0(a, tp.b) + tp.r0;
@@ -386,6 +389,10 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         }
         const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
         bytes += (nrows[t] > 0 ? P::kCodeBytes : 0) + (bulk_sc ? P::kScaleBytes : 0);
+      }
+      if (tail && !waited) {
+        griddep_wait();  // the tail pool has written the last blocks (all lanes)
+        waited = true;
       }
       if (lane == 0) {
 #pragma unroll
@@ -773,7 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  griddep_wait();  // the previous kernel's outputs (scores, ids, pooled keys) are final
+  // The previous kernel's outputs (scores, ids, pooled keys) are final past
+  // this wait; with defer_wait only the producer takes it, before the tiles
+  // that the tail pool writes (nothing else here reads a library output).
+  if (!a.defer_wait) griddep_wait();
 
   if (warp < kMmaWarp) {
     producer<FMT, TPS>(a, maps, sh, sbase, t_begin, n_tiles, tpq, warp);
@@ -843,8 +853,11 @@ cudaError_t launch_fmt(const ScanArgs& args, int num_sms, cudaStream_t s) {
 // Tiles per ring stage: bf16 tiles are 32 KB already; MXFP8 tiles (16.5 KB)
 // go two a stage and MXFP4 tiles (8.5 KB) four a stage over contiguous rows;
 // gathered scans take DSA_SCAN_GATHER_TPS MXFP8 tiles (twice as many MXFP4).
-cudaError_t launch_scan(const ScanArgs& a, int num_sms, cudaStream_t s) {
-  const bool gather = a.mode == ROWS_GATHER || a.pages.table != nullptr;
+cudaError_t launch_scan(const ScanArgs& args, int num_sms, cudaStream_t s) {
+  const bool gather = args.mode == ROWS_GATHER || args.pages.table != nullptr;
+  ScanArgs a = args;
+  // the deferred wait covers the contiguous decode block stage only
+  if (gather || a.mode != ROWS_BLOCKS || a.prefill || a.mq > 0) a.defer_wait = 0;
   if (a.fmt == DSA_FMT_BF16) return launch_fmt<DSA_FMT_BF16, 1>(a, num_sms, s);
   if (a.fmt == DSA_FMT_MXFP8) {
     if (gather) return launch_fmt<DSA_FMT_MXFP8, DSA_SCAN_GATHER_TPS>(a, num_sms, s);
