@@ -41,6 +41,7 @@
 // output from registers (a warp stores 32 consecutive dims of a head at a
 // time): it runs once per CTA, so its code is fetched cold, and a compact
 // loop costs far less than a fully unrolled one.
+#include <algorithm>
 #include <cstddef>
 
 #include "kernels.h"
@@ -765,6 +766,584 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (paired && warp >= kMmaWarp) cluster_wait();
 }
 
+// ---------------------------------------------------------------------------
+// Unsplit attention (one CTA per query: prefill chunks, multi-query batches,
+// decode batches too large to split), persistent: grid = min(queries, SMs),
+// CTA c takes queries c, c + grid, ... and runs them through one pipeline, so
+// the next query's index list, Q and first tiles load while the current
+// query's last tiles and its epilogue run. The roles are those of attn_kernel
+// (4 math warps, 4 loaders, QK^T and PV issuers); barrier phases follow a
+// per-CTA count of tiles across the CTA's queries (tile g: ring slot g mod
+// kSlots, S and P buffer g & 1).
+//   * index lists: double-buffered; the math warps compact query i + 1's
+//     right after their last softmax of query i, before its epilogue;
+//   * Q: the QK^T issuer loads query i + 1's Q once query i's last QK^T has
+//     completed (q_free);
+//   * O^T: the math warps' epilogue of query i reads it before their first
+//     softmax of query i + 1, which precedes PV(i + 1, 0) (the only MMA that
+//     overwrites it), so no extra barrier is needed; the epilogue runs on the
+//     math warps alone while the loaders stream the next query.
+// ---------------------------------------------------------------------------
+constexpr int kIdsB = kMisc + kMiscBytes;  // second index-list buffer
+constexpr int kSmemStream = kIdsB + kMaxKTokens * 4 + 1024;
+
+struct MiscS {
+  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
+  uint64_t q_done, q_free, o_done;
+  uint32_t tmem_base;
+  int abort;
+  // Per-query hand-offs are counters, not barrier phases: a query without rows
+  // lets a role run ahead by more than one phase.
+  int ids_seq;  // queries whose index lists are compacted (math warps)
+  int ld_seq;   // queries finished by loader warps (one count per warp)
+  int mma_seq;  // queries whose tile count the QK^T issuer has read
+  int pv_seq;   // queries whose tile count the PV issuer has read
+  int epi_seq;  // queries whose epilogue is done (math warps)
+  int n_sel[2];
+  int warp_cnt[4];
+  alignas(16) float alpha[kHeads];
+  alignas(16) float inv_l[kHeads];
+};
+static_assert(sizeof(MiscS) <= kMiscBytes, "misc block");
+static_assert(offsetof(MiscS, inv_l) % 16 == 0, "16-byte loads of inv_l");
+
+__device__ __forceinline__ bool wait_bar_s(uint64_t* bar, uint32_t parity, MiscS* m,
+                                           DeviceStatus* st) {
+  return mbar_wait_abortable(bar, parity, &m->abort, st, SITE_ATTN);
+}
+
+// A query's rows in the window buffer and the latents (unsplit).
+struct QueryRows {
+  int n_vis;      // visible latents (ids must be below)
+  int n_sw;       // window rows
+  int64_t wrow0;  // row of the window buffer holding its first window row
+  int64_t lat_row0;  // first row of its sequence's latents (0 when paged)
+};
+
+__device__ __forceinline__ QueryRows query_rows(const AttnArgs& a, int b, bool report) {
+  QueryRows r;
+  if (a.prefill) {
+    int64_t P = query_pos(a.ctx, a.mq, a.n_tokens, b);
+    if (P < 0) {
+      // a multi-query sequence with fewer tokens than queries: no rows
+      if (report) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
+      P = -1;
+    }
+    r.n_vis = static_cast<int>((P + 1) / a.ratio);
+    const int64_t first = P - a.window + 1 > 0 ? P - a.window + 1 : 0;
+    // the window buffer's row 0 holds position (first query's position) - window + 1
+    const int64_t base_pos = (a.mq > 0 ? P - b % a.mq : a.ctx) - a.window + 1;
+    r.wrow0 = static_cast<int64_t>(query_seq(a.mq, b)) * a.swa_seq_rows + (first - base_pos);
+    r.n_sw = static_cast<int>(P - first + 1);
+  } else {
+    r.n_vis = a.n_latents[b];
+    r.n_sw = a.swa_len[b];
+    if (r.n_sw < 0 || r.n_sw > a.window) {
+      if (report) record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, b);
+      r.n_sw = r.n_sw < 0 ? 0 : a.window;
+    }
+    r.wrow0 = static_cast<int64_t>(b) * a.window;
+  }
+  if (r.n_vis > a.lat_stride) r.n_vis = static_cast<int>(a.lat_stride);
+  const bool paged = a.pages.table != nullptr;
+  const int lat_seq = a.prefill ? query_seq(a.mq, b) : (paged ? 0 : b);
+  r.lat_row0 = static_cast<int64_t>(lat_seq) * a.lat_stride;
+  return r;
+}
+
+// Bounded wait (all threads that call it) until *p >= v, a counter in shared
+// memory that another role raises; false once it times out or the CTA aborts.
+__device__ __forceinline__ bool wait_count(int* p, int v, MiscS* m, DeviceStatus* st) {
+  volatile int* vp = p;
+  if (*vp >= v) {
+    __threadfence_block();
+    return true;
+  }
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (*vp >= v) {
+      __threadfence_block();
+      return true;
+    }
+    if ((it & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&m->abort)) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        record_status(st, DSA_ERR_TIMEOUT, SITE_ATTN, smem_u32(p));
+        m->abort = 1;
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+// Raises a counter after this thread's earlier shared-memory writes.
+__device__ __forceinline__ void raise_count(int* p, int v) {
+  __threadfence_block();
+  *reinterpret_cast<volatile int*>(p) = v;
+}
+
+template <int ROWS>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_stream_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap wmap) {
+  using TS = TileShape<ROWS>;
+  constexpr int kRows = ROWS;
+  constexpr int kSlots = TS::kSlots;
+  constexpr int kAtomBytes = TS::kAtomBytes;
+  constexpr int kSlotBytes = TS::kSlotBytes;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  MiscS* misc = reinterpret_cast<MiscS*>(gbase + kMisc);
+  // index-list buffer of query index qi
+  auto ids_buf = [&](int qi) -> int32_t* {
+    return reinterpret_cast<int32_t*>(gbase + ((qi & 1) ? kIdsB : kIds));
+  };
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b0 = blockIdx.x, gstep = gridDim.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&misc->kv_full[i], 32 * TS::kWarpsPerSlot);
+      mbar_init(&misc->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&misc->s_full[i], 1);
+      mbar_init(&misc->s_free[i], 2);
+      mbar_init(&misc->p_full[i], 2);
+      mbar_init(&misc->p_empty[i], 1);
+    }
+    mbar_init(&misc->q_done, 1);  // a query's Q: expect-tx arrival + 64 KB
+    mbar_init(&misc->q_free, 1);  // a query's QK^Ts have completed
+    mbar_init(&misc->o_done, 1);  // a query's PVs have completed
+    misc->abort = 0;
+    misc->ids_seq = misc->ld_seq = misc->mma_seq = misc->pv_seq = misc->epi_seq = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&misc->tmem_base, kTmemCols);
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+
+  // Tile count of query index qi (its lists compacted): window rows + ids.
+  auto tiles_of = [&](int b, int qi) -> int {
+    const QueryRows qr = query_rows(a, b, false);
+    return (qr.n_sw + misc->n_sel[qi & 1] + kRows - 1) / kRows;
+  };
+
+  if (warp < kLoadWarp0) {
+    // ---------------- math: index lists, softmax, epilogue ----------------
+    griddep_wait();  // the previous kernel's token ids are final
+    const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
+    bool ok = true;
+    // Compacts query index qi's valid token ids (>= 0 and < n_vis; pool rows
+    // when the latents are paged) in order into buffer qi & 1.
+    auto compact = [&](int b, int qi) {
+      if (qi >= 2) {
+        // every other role is done with query qi - 2, whose buffer this reuses
+        if (tid == 0 && ok) {
+          ok = wait_count(&misc->ld_seq, kLoadWarps * (qi - 1), misc, a.status) &&
+               wait_count(&misc->mma_seq, qi - 1, misc, a.status) &&
+               wait_count(&misc->pv_seq, qi - 1, misc, a.status);
+        }
+        named_sync(kMathBar, 128);
+      }
+      const QueryRows qr = query_rows(a, b, tid == 0);
+      const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
+      int32_t* ids = ids_buf(qi);
+      constexpr int kPer = kMaxKTokens / 128;  // 4
+      int my[kPer];
+      int cnt = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = tid * kPer + j;
+        int id = -1;
+        if (i < a.k_tokens) {
+          id = tk[i];
+          if (id >= qr.n_vis) {
+            record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+            id = -1;
+          }
+          if (a.pages.table != nullptr && id >= 0) {
+            const int64_t row = paged_row(a.pages, b, id);
+            if (row < 0) {
+              record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+            }
+            id = static_cast<int>(row);
+          }
+        }
+        my[j] = id;
+        cnt += id >= 0 ? 1 : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) misc->warp_cnt[warp] = incl;
+      named_sync(kMathBar, 128);
+      int before = incl - cnt;
+      for (int w = 0; w < warp; ++w) before += misc->warp_cnt[w];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (my[j] >= 0) ids[before++] = my[j];
+      }
+      if (tid == 127) misc->n_sel[qi & 1] = before;
+      named_sync(kMathBar, 128);
+      if (tid == 0) raise_count(&misc->ids_seq, qi + 1);
+    };
+    if (b0 < a.B) compact(b0, 0);
+    int64_t gq = 0;  // this CTA's tile count before the current query
+    int qi = 0;
+    for (int b = b0; b < a.B; b += gstep, ++qi) {
+      const QueryRows qr = query_rows(a, b, false);
+      const int n_rows = qr.n_sw + misc->n_sel[qi & 1];
+      const int n_tiles = (n_rows + kRows - 1) / kRows;
+      float m_run = -INFINITY, l_run = 0.f;  // threads 0..63: head tid
+      // PV(j) is known complete through p_empty[j & 1]; the next phase of that
+      // barrier needs P(j + 2), written after every wait below, so a parity
+      // wait is never more than one phase off.
+      auto wait_pv = [&](int64_t j) {
+        if (ok) {
+          ok = wait_bar_s(&misc->p_empty[j & 1], static_cast<uint32_t>((j >> 1) & 1), misc,
+                          a.status);
+        }
+      };
+      for (int t = 0; t < n_tiles; ++t) {
+        const int64_t g = gq + t;
+        const int sb = static_cast<int>(g & 1);
+        const int valid = min(kRows, n_rows - t * kRows);
+        float z[kRows];
+        float alpha = 1.f;
+        bool resc = false;
+        if (warp < 2) {
+          if (ok) {
+            ok = wait_bar_s(&misc->s_full[sb], static_cast<uint32_t>((g >> 1) & 1), misc, a.status);
+          }
+          tc_fence_after();
+          if (ok) {
+#pragma unroll
+            for (int c = 0; c < kRows / 16; ++c) {
+              float v[16];
+              tmem_ld16(la + 64 * sb + c * 16, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                z[c * 16 + i] = (c * 16 + i < valid) ? v[i] * a.scale_log2 : -INFINITY;
+              }
+            }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) mt = fmaxf(mt, z[i]);
+            if (t == 0) {
+              m_run = mt;
+            } else if (mt > m_run + 8.f) {
+              alpha = exp2f(m_run - mt);
+              m_run = mt;
+              resc = true;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&misc->s_free[sb]);
+          misc->alpha[tid] = alpha;
+        }
+        // O^T holds this query's PV(0..t-1); if any head's maximum moved,
+        // scale every head's column by its alpha.
+        const bool any_resc = named_sync_or(kMathBar, 128, resc);
+        if (any_resc) {
+          if (t > 0) wait_pv(g - 1);
+          tc_fence_after();
+          if (ok && t > 0) {
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                float v[16];
+                const uint32_t addr = la + 128 + 64 * m + 16 * c;
+                tmem_ld16(addr, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= misc->alpha[16 * c + i];
+                tmem_st16(addr, v);
+              }
+            }
+          }
+          tc_fence_before();
+          named_sync(kMathBar, 128);  // alpha is read by all before the next tile rewrites it
+        }
+        if (warp < 2) {
+          // P[sb] was last read by PV(g - 2), of this query or the previous one
+          if (g >= 2) wait_pv(g - 2);
+          if (ok) {
+            float sum = 0.f;
+            uint32_t pk[kRows / 2];
+#pragma unroll
+            for (int i = 0; i < kRows; i += 2) {
+              const float p0 = exp2f(z[i] - m_run), p1 = exp2f(z[i + 1] - m_run);
+              sum += p0 + p1;  // the denominator sums the fp32 probabilities
+              const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
+              pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
+            l_run = l_run * alpha + sum;
+            const uint32_t pb = sbase + kP + sb * kPBytes;
+#pragma unroll
+            for (int c = 0; c < kRows / 8; ++c) {
+              st_shared_v4(pb + sw128_off(tid, c),
+                           make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&misc->p_full[sb]);
+        }
+      }
+      // The next query's index list first, so the loaders and the issuers go
+      // on with it while this query's epilogue runs.
+      if (b + gstep < a.B) compact(b + gstep, qi + 1);
+      // ---------------- epilogue (math warps) ----------------
+      if (ok) ok = wait_bar_s(&misc->o_done, static_cast<uint32_t>(qi & 1), misc, a.status);
+      tc_fence_after();
+      const bool have_o = ok && n_tiles > 0;
+      uint16_t* out = a.out + static_cast<int64_t>(b) * kHeads * kLatent;
+      if (warp < 2) {
+        misc->inv_l[tid] = have_o && l_run > 0.f ? 1.f / l_run : 0.f;
+        if (a.lse) {
+          a.lse[static_cast<int64_t>(b) * kHeads + tid] =
+              have_o && l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+      named_sync(kMathBar, 128);
+      const uint32_t inv_l_s = smem_u32(misc->inv_l);
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+#pragma unroll 1
+        for (int hc = 0; hc < 4; ++hc) {
+          float v[16];
+          if (have_o) {
+            tmem_ld16(la + 128 + 64 * m + 16 * hc, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 w4 = ld_shared_f4(inv_l_s + (16 * hc + i) * 4);
+            v[i] *= w4.x;
+            v[i + 1] *= w4.y;
+            v[i + 2] *= w4.z;
+            v[i + 3] *= w4.w;
+          }
+          uint16_t* o = out + static_cast<int64_t>(16 * hc) * kLatent + 128 * m + tid;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            o[static_cast<int64_t>(i) * kLatent] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+          }
+        }
+      }
+      tc_fence_before();
+      named_sync(kMathBar, 128);  // every read of O^T is done
+      if (tid == 0) raise_count(&misc->epi_seq, qi + 1);
+      gq += n_tiles;
+    }
+  }
+  else if (warp < kMmaWarp) {
+    // ---------------- loaders ----------------
+    // Warp 4 + w fills 32 rows (part w / kSlots) of ring slot w % kSlots for
+    // the CTA's tiles g = slot, slot + kSlots, ... across its queries.
+    const int w = warp - kLoadWarp0;
+    const int sl = w % kSlots, part = w / kSlots;
+    const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
+    bool ok = true;
+    int64_t gq = 0;
+    int qi = 0;
+    for (int b = b0; b < a.B && ok; b += gstep, ++qi) {
+      if (!wait_count(&misc->ids_seq, qi + 1, misc, a.status)) {
+        ok = false;
+        break;
+      }
+      const QueryRows qr = query_rows(a, b, false);
+      const int32_t* ids = ids_buf(qi);
+      const int w_cnt = qr.n_sw;
+      const int n_rows = w_cnt + misc->n_sel[qi & 1];
+      const int n_tiles = (n_rows + kRows - 1) / kRows;
+      for (int t = static_cast<int>(((sl - gq) % kSlots + kSlots) % kSlots); t < n_tiles;
+           t += kSlots) {
+        const int64_t g = gq + t;
+        const uint32_t u = static_cast<uint32_t>(g / kSlots);
+        if (g >= kSlots &&
+            !wait_bar_s(&misc->kv_empty[sl], (u - 1) & 1u, misc, a.status)) {
+          ok = false;
+          break;
+        }
+        const int r0 = t * kRows + 32 * part;  // this warp's first row of the tile
+        if (r0 + 32 <= w_cnt &&
+            DSA_DCHECK(qr.wrow0 + r0 + 32 <= a.swa_rows, a.status, SITE_ATTN, qr.wrow0 + r0)) {
+          // 32 window rows (contiguous): eight TMA boxes, completing on the slot
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&misc->kv_full[sl], 32 * 1024);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              tma_load_2d(dstb + c * kAtomBytes + 32 * part * 128, &wmap, 64 * c,
+                          static_cast<int>(qr.wrow0 + r0), &misc->kv_full[sl]);
+            }
+          } else {
+            mbar_arrive(&misc->kv_full[sl]);
+          }
+          continue;
+        }
+        // Lane l works out the source of the warp's row l once (-1: none,
+        // zero-filled); each row is then copied by the whole warp, lane l
+        // taking 16-byte chunks l and l + 32.
+        int64_t arow_l = -1;
+        {
+          const int gl = r0 + lane;
+          if (gl < n_rows) {
+            arow_l = gl < w_cnt ? qr.wrow0 + gl : qr.lat_row0 + ids[gl - w_cnt];
+            if (!DSA_DCHECK(arow_l >= 0 && arow_l < (gl < w_cnt ? a.swa_rows : a.lat_rows),
+                            a.status, SITE_ATTN, arow_l)) {
+              arow_l = -1;
+            }
+          }
+        }
+        const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
+          const int row = 32 * part + r;
+          const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
+          const uint32_t d1 = d0 + 4 * kAtomBytes;
+          if (arow >= 0) {
+            const uint16_t* src = (r0 + r < w_cnt ? a.swa : a.latents) + arow * kLatent + lane * 8;
+            cp_async_16(d0, src);
+            cp_async_16(d1, src + 256);
+          } else {
+            st_shared_v4(d0, make_uint4(0, 0, 0, 0));
+            st_shared_v4(d1, make_uint4(0, 0, 0, 0));
+          }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&misc->kv_full[sl]);
+      }
+      __syncwarp();
+      if (ok && lane == 0) {
+        __threadfence_block();
+        atomicAdd(&misc->ld_seq, 1);  // this warp no longer reads query qi's list
+      }
+      gq += n_tiles;
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- QK^T issuer (and Q loads) ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
+      auto load_q = [&](int b) {
+        mbar_arrive_expect_tx(&misc->q_done, kQBytes);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          tma_load_2d(sbase + kQ + c * (kHeads * 128), &qmap, 64 * c, b * kHeads, &misc->q_done);
+        }
+      };
+      tma_prefetch_map(&qmap);
+      tma_prefetch_map(&wmap);
+      if (b0 < a.B) load_q(b0);
+      bool ok = true;
+      int64_t gq = 0;
+      int qi = 0;
+      for (int b = b0; b < a.B && ok; b += gstep, ++qi) {
+        if (!wait_count(&misc->ids_seq, qi + 1, misc, a.status)) break;
+        const int n_tiles = tiles_of(b, qi);
+        raise_count(&misc->mma_seq, qi + 1);
+        ok = wait_bar_s(&misc->q_done, static_cast<uint32_t>(qi & 1), misc, a.status);
+        for (int t = 0; t < n_tiles && ok; ++t) {
+          const int64_t g = gq + t;
+          const int slot = static_cast<int>(g % kSlots), sb = static_cast<int>(g & 1);
+          if (!wait_bar_s(&misc->kv_full[slot], static_cast<uint32_t>((g / kSlots) & 1), misc,
+                          a.status)) {
+            ok = false;
+            break;
+          }
+          if (g >= 2 && !wait_bar_s(&misc->s_free[sb], static_cast<uint32_t>(((g >> 1) - 1) & 1),
+                                    misc, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          fence_proxy_async_smem();
+          const uint64_t ad0 = sw128_desc(sbase + kQ, 16, 1024);
+          const uint64_t bd0 = sw128_desc(sbase + kKV + slot * kSlotBytes, 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < kLatent / 16; ++ks) {
+            const uint64_t ad = ad0 + (((ks >> 2) * (kHeads * 128) + (ks & 3) * 32) >> 4);
+            const uint64_t bd = bd0 + (((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
+            mma_f16(tmem + 64 * sb, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&misc->s_full[sb]);
+        }
+        mma_commit(&misc->q_free);  // arrives once this query's QK^Ts have completed
+        gq += n_tiles;
+        if (ok && b + gstep < a.B) {
+          ok = wait_bar_s(&misc->q_free, static_cast<uint32_t>(qi & 1), misc, a.status);
+          if (ok) load_q(b + gstep);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- PV issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = mma_idesc(128, kHeads, true, true, false);
+      bool ok = true;
+      int64_t gq = 0;
+      int qi = 0;
+      for (int b = b0; b < a.B && ok; b += gstep, ++qi) {
+        if (!wait_count(&misc->ids_seq, qi + 1, misc, a.status)) break;
+        const int n_tiles = tiles_of(b, qi);
+        raise_count(&misc->pv_seq, qi + 1);
+        for (int t = 0; t < n_tiles && ok; ++t) {
+          const int64_t g = gq + t;
+          const int slot = static_cast<int>(g % kSlots), sb = static_cast<int>(g & 1);
+          if (!wait_bar_s(&misc->p_full[sb], static_cast<uint32_t>((g >> 1) & 1), misc,
+                          a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          fence_proxy_async_smem();
+          const uint64_t ad0 = sw128_desc(sbase + kKV + slot * kSlotBytes, kAtomBytes, 1024);
+          const uint64_t bd0 = sw128_desc(sbase + kP + sb * kPBytes, 16, 1024);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int ks = 0; ks < kRows / 16; ++ks) {
+              const uint64_t ad = ad0 + ((m * 2 * kAtomBytes + ks * 16 * 128) >> 4);
+              const uint64_t bd = bd0 + ((ks * 32) >> 4);
+              mma_f16(tmem + 128 + 64 * m, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&misc->kv_empty[slot]);
+          mma_commit(&misc->p_empty[sb]);
+        }
+        // o_done's phases stay one per query in step with the epilogues:
+        // this query's commit waits for the previous query's epilogue.
+        if (ok) ok = wait_count(&misc->epi_seq, qi, misc, a.status);
+        mma_commit(&misc->o_done);  // arrives once this query's PVs have completed
+        gq += n_tiles;
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
 }  // namespace
 
 // Clusters of `splits` CTAs (32-row tiles) that can be resident at once on
@@ -824,6 +1403,23 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   AttnArgs args = a;
   args.swa_rows = static_cast<int64_t>(wrows);
+  if (a.splits == 1) {
+    // unsplit: persistent CTAs, one per SM at most, each walking its queries
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(a.B, device_sm_count()));
+    if (a.tile_rows == 64) {
+      static std::atomic<int> smem_set[64]{};
+      e = ensure_smem(reinterpret_cast<const void*>(attn_stream_kernel<64>), kSmemStream, smem_set);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(attn_stream_kernel<64>, dim3(grid), dim3(kThreads), kSmemStream, s, 1, args,
+                        qmap, wmap);
+    }
+    if (a.tile_rows != 32) return cudaErrorInvalidValue;
+    static std::atomic<int> smem_set[64]{};
+    e = ensure_smem(reinterpret_cast<const void*>(attn_stream_kernel<32>), kSmemStream, smem_set);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_stream_kernel<32>, dim3(grid), dim3(kThreads), kSmemStream, s, 1, args,
+                      qmap, wmap);
+  }
   if (a.tile_rows == 64) {
     static std::atomic<int> smem_set[64]{};
     e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
