@@ -561,6 +561,68 @@ def run_ours(args):
                                 "ms_per_step": st_ms}
     dsa.launch_counts(reset=True)
 
+    # Stage costs inside a replay: CUDA graphs of growing prefixes of the step,
+    # made of the C ABI's separate calls (tail pool + dsa_index_blocks, then
+    # + dsa_topk, then + the attention), each timed like the step. The
+    # per-kernel breakdown above brackets every launch with events, which adds
+    # a launch's latency to each kernel and cuts their programmatic overlap.
+    stages = {}
+    try:
+        nb_s = -(-L // 8)
+        has_block = nb_s > cfg.k_blocks
+        bids_p = torch.empty((B, cfg.k_blocks), dtype=torch.int32, device=dev)
+        tids_p = torch.empty((B, cfg.k_tokens), dtype=torch.int32, device=dev)
+        out_p = torch.empty_like(out)
+        lse_p = torch.empty_like(lse)
+
+        def p_pool():
+            dsa.pool_index_keys(cfg, keys, n_lat, cap, pooled, ws, tail_only=True)
+
+        def p_block():
+            dsa.index_blocks(cfg, q_idx, w, pooled, n_lat, cap, bids_p, ws)
+
+        def p_token():
+            dsa.topk(cfg, q_idx, w, keys, bids_p if has_block else None, n_lat, cap, tids_p, ws)
+
+        def p_attn():
+            if pages is not None:
+                dsa.sparse_attn_decode_paged(cfg, q, latents, pages, n_lat, tids_p, swa, swa_len,
+                                             out_p, ws, lse=lse_p)
+            else:
+                dsa.sparse_attn_decode(cfg, q, latents, n_lat, tids_p, swa, swa_len, out_p, ws,
+                                       lse=lse_p)
+
+        first = [p_pool, p_block] if has_block else [p_pool]
+        prefixes = [first, first + [p_token], first + [p_token, p_attn]]
+        times = []
+        for fns in prefixes:
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                for f in fns:
+                    f()
+            for _ in range(3):
+                flush()
+                gp.replay()
+            for i in range(K):
+                flush()
+                ev_s[i].record()
+                gp.replay()
+                ev_e[i].record()
+            torch.cuda.synchronize()
+            times.append(sum(s.elapsed_time(e) for s, e in zip(ev_s, ev_e)) / K)
+        stages = {"pool + block stage" if has_block else "pool": times[0],
+                  "token stage": times[1] - times[0], "attention": times[2] - times[1],
+                  "all three prefixes' last (the calls one by one)": times[2],
+                  "how": "CUDA graphs of growing prefixes of the step made of the C ABI's "
+                         "separate calls; a stage is the difference of two prefixes' replay "
+                         "times (ms)"}
+    except RuntimeError as e:
+        stages = {"error": str(e).splitlines()[0][:200] if str(e) else type(e).__name__}
+    code, info = dsa.read_device_status(ws)
+    if code != 0:
+        raise SystemExit(f"device status {code} info {info:#x}")
+    dsa.launch_counts(reset=True)
+
     # Roofline of the dominant kernel: the indexer scan. Algorithmic bytes per
     # launch = rows scanned x bytes per key row (MXFP8: 128 codes + 4 scale
     # bytes; MXFP4: 64 + 4; bf16: 256); both launches of a step scan 2048 x 8 = 16384 rows per
@@ -733,6 +795,7 @@ def run_ours(args):
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
         "graph": graph,
         "kernel_ms_per_step": kernel_ms,
+        "stage_ms_in_graph": stages,
         "gpu_launches": int(sum(counts.values())),
         "gpu_launches_by_kind": counts,
         "clocks": clocks.summary(),
