@@ -499,28 +499,64 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
 }
 
 // Index query of query b -> ring slot [set][ring] (one math set, 128 threads).
-template <int FMT, int TPS>
-__device__ void build_query(const ScanArgs& a, Shared& sh, uint32_t sbase, int b, int mt,
-                            int set, int ring) {
-  using Lo = Layout<FMT, TPS>;
+// A query's index vectors and weight as one math thread of a set loads them
+// (the loads go out when the fetch is made and are used when the query's ring
+// slot is built, so a fetch made a tile ahead hides their latency).
+struct QFetch {
+  int b;  // the query (-1: none)
+  uint4 v0, v1;
+  float w;
+};
+__device__ __forceinline__ uint4 ld_global_v4_early(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+template <int FMT>
+__device__ __forceinline__ QFetch fetch_query(const ScanArgs& a, int b, int mt) {
+  QFetch f;
+  f.b = b;
   const uint16_t* q = a.q_idx + static_cast<int64_t>(b) * kIdxHeads * kIdxDim;
+  if constexpr (FMT == DSA_FMT_BF16) {
+    // thread mt: 16-byte chunks c = mt and mt + 128 (head c / 16, chunk c % 16)
+    f.v0 = ld_global_v4_early(q + (mt >> 4) * kIdxDim + (mt & 15) * 8);
+    const int c1 = mt + kMathThreads;
+    f.v1 = ld_global_v4_early(q + (c1 >> 4) * kIdxDim + (c1 & 15) * 8);
+  } else {
+    const int h = mt >> 3, part = mt & 7;  // 8 threads per head, 16 elements each
+    f.v0 = ld_global_v4_early(q + h * kIdxDim + part * 16);
+    f.v1 = ld_global_v4_early(q + h * kIdxDim + part * 16 + 8);
+  }
+  f.w = 0.f;
+  if (mt < kIdxHeads) {
+    asm volatile("ld.global.nc.f32 %0, [%1];\n"
+                 : "=f"(f.w)
+                 : "l"(a.w + static_cast<int64_t>(b) * kIdxHeads + mt));
+  }
+  return f;
+}
+
+// Query f.b's index vectors -> ring slot [set][ring] (one math set, 128 threads).
+template <int FMT, int TPS>
+__device__ void build_query(Shared& sh, uint32_t sbase, const QFetch& f, int mt, int set,
+                            int ring) {
+  using Lo = Layout<FMT, TPS>;
   const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
   QSlot& slot = sh.qs[set][ring];
-  if (mt < kIdxHeads) slot.w[mt] = a.w[static_cast<int64_t>(b) * kIdxHeads + mt];
+  if (mt < kIdxHeads) slot.w[mt] = f.w;
   if constexpr (FMT == DSA_FMT_BF16) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int c = mt + kMathThreads * j;
       const int h = c >> 4, cr = c & 15;
-      const uint4 v = *reinterpret_cast<const uint4*>(q + h * kIdxDim + cr * 8);
-      st_shared_v4(qb + (cr >> 3) * 2048 + sw128_off(h, cr & 7), v);
+      st_shared_v4(qb + (cr >> 3) * 2048 + sw128_off(h, cr & 7), j == 0 ? f.v0 : f.v1);
     }
     if (mt < kIdxHeads) slot.qinv[mt] = 1.0f;
   } else {
     const int h = mt >> 3, part = mt & 7;  // 8 threads per head, 16 elements each
-    const uint4 v0 = *reinterpret_cast<const uint4*>(q + h * kIdxDim + part * 16);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(q + h * kIdxDim + part * 16 + 8);
-    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint32_t wv[8] = {f.v0.x, f.v0.y, f.v0.z, f.v0.w, f.v1.x, f.v1.y, f.v1.z, f.v1.w};
     float x[16];
     float amax = 0.f;
 #pragma unroll
@@ -576,6 +612,11 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
   int stage = 0;                 // ring stage of the tile being prepared (advances per TPS
   uint32_t spar = 0;             // own tiles) and the parity of that stage's use
   int ring_e = 0;                // of the tile being finished
+  // The query of this set's next tile of another query, fetched one own tile
+  // ahead (and kept while the ring's slots are rebuilt for it).
+  QFetch nq;
+  nq.b = -1;
+  if (set < n_tiles) nq = fetch_query<FMT>(a, prep.b, mt);
 
   auto epilogue = [&](int e) -> bool {
     const int q = e & (kSlots - 1);
@@ -641,8 +682,9 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     if (held != b) {
       // The ring slot last served tile i - 6, whose epilogue every thread of
       // the set has finished once all of them reach this barrier.
+      if (nq.b != b) nq = fetch_query<FMT>(a, b, mt);
       named_sync(1 + set, kMathThreads);
-      build_query<FMT, TPS>(a, sh, sbase, b, mt, set, ring);
+      build_query<FMT, TPS>(sh, sbase, nq, mt, set, ring);
       fence_proxy_async_smem();
       named_sync(1 + set, kMathThreads);
       if (ring == 0) ring_b0 = b; else if (ring == 1) ring_b1 = b; else ring_b2 = b;
@@ -712,6 +754,7 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       if (lane == 0) mbar_arrive(&sh.op_full[q]);
     }
     prep.advance(2, q_rows);
+    if (i + 2 < n_tiles && prep.b != b && nq.b != prep.b) nq = fetch_query<FMT>(a, prep.b, mt);
     if (++ring == kQRing) ring = 0;
     if (t == TPS - 1 && ++stage == R::kStages) {
       stage = 0;
