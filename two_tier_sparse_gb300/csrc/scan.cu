@@ -265,6 +265,7 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
   };
   int s = 0;           // stage of this iteration
   bool waited = !a.defer_wait;  // the dependency wait has been taken
+  const uint64_t pol = l2_evict_first_policy();  // keys are read once a launch
   uint32_t kpar = 0;   // parity of the stage's use count
   for (int64_t j0 = 0; j0 < n_own; j0 += TPS) {
     TilePos next2 = next;
@@ -347,20 +348,22 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         const uint32_t codes = R::codes(stage, t);
         if constexpr (FMT == DSA_FMT_BF16) {
           // two K halves (64 elements = 128 bytes each) into the two K-atoms
-          tma_load_2d(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full);
-          tma_load_2d(codes + kTile * 128 + row0 * 128, &maps.keys, 64, static_cast<int>(y[k]),
-                      full);
+          tma_load_2d_hint(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full, pol);
+          tma_load_2d_hint(codes + kTile * 128 + row0 * 128, &maps.keys, 64,
+                           static_cast<int>(y[k]), full, pol);
         } else {
           if constexpr (FMT == DSA_FMT_MXFP8) {
-            tma_load_2d(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full);
+            tma_load_2d_hint(codes + row0 * 128, &maps.keys, 0, static_cast<int>(y[k]), full,
+                             pol);
           } else {
-            tma_load_2d(codes + row0 * 64, &maps.keys, 0, static_cast<int>(y[k] >> 1), full);
+            tma_load_2d_hint(codes + row0 * 64, &maps.keys, 0, static_cast<int>(y[k] >> 1), full,
+                             pol);
           }
           const uint32_t sc_dst = R::scales(stage, t) + row0 * 4;
           const uint8_t* sc_src = a.key_scales + y[k] * 4;
           if (scale_vec && nrows[k] == kBlock) {
-            cp_async_16(sc_dst, sc_src);
-            cp_async_16(sc_dst + 16, sc_src + 16);
+            cp_async_16_hint(sc_dst, sc_src, pol);
+            cp_async_16_hint(sc_dst + 16, sc_src + 16, pol);
           } else {
             for (int r = 0; r < nrows[k]; ++r) cp_async_4(sc_dst + r * 4, sc_src + r * 4);
           }
@@ -412,14 +415,18 @@ __device__ void producer(const ScanArgs& a, const Maps& maps, Shared& sh, uint32
         const bool bulk_sc = FMT != DSA_FMT_BF16 && scale_vec && nrows[t] == kTile;
         if (lane == 0) {
           if constexpr (FMT == DSA_FMT_BF16) {
-            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row), full);
-            tma_load_2d(codes + kTile * 128, &maps.keys, 64, static_cast<int>(row), full);
+            tma_load_2d_hint(codes, &maps.keys, 0, static_cast<int>(row), full, pol);
+            tma_load_2d_hint(codes + kTile * 128, &maps.keys, 64, static_cast<int>(row), full,
+                             pol);
           } else if constexpr (FMT == DSA_FMT_MXFP8) {
-            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row), full);
+            tma_load_2d_hint(codes, &maps.keys, 0, static_cast<int>(row), full, pol);
           } else {
-            tma_load_2d(codes, &maps.keys, 0, static_cast<int>(row >> 1), full);
+            tma_load_2d_hint(codes, &maps.keys, 0, static_cast<int>(row >> 1), full, pol);
           }
-          if (bulk_sc) bulk_g2s(R::scales(stage, t), a.key_scales + row * 4, P::kScaleBytes, full);
+          if (bulk_sc) {
+            bulk_g2s_hint(R::scales(stage, t), a.key_scales + row * 4, P::kScaleBytes, full,
+                          pol);
+          }
         }
         if constexpr (FMT != DSA_FMT_BF16) {
           if (!bulk_sc) {

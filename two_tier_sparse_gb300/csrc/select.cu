@@ -390,6 +390,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   const int32_t* ids_in = a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in : nullptr;
   const bool dense = a.dense_stride && a.block_ids;
 
+  // The block ids (token stage) are requested first, so their latency
+  // overlaps the score loads; they go to shared memory further down.
+  constexpr int kBidRegs = kMaxKBlocks / kThreads;
+  static_assert(kMaxKBlocks % kThreads == 0, "block ids: whole registers a thread");
+  const int32_t* bl = a.block_ids ? a.block_ids + static_cast<int64_t>(b) * a.k_blocks : nullptr;
+  int32_t bid_r[kBidRegs];
+  if (bl) {
+#pragma unroll
+    for (int u = 0; u < kBidRegs; ++u) {
+      const int i = tid + u * kThreads;
+      bid_r[u] = i < a.k_blocks ? __ldg(bl + i) : -1;
+    }
+  }
   uint32_t key[KPT];
   const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
   // Scores that do not go through the block ids are requested first, so their
@@ -443,10 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       }
     }
   }
-  if (a.block_ids) {
-    // copied to shared memory; their order is checked after the next barrier
-    const int32_t* bl = a.block_ids + static_cast<int64_t>(b) * a.k_blocks;
-    for (int i = tid; i < a.k_blocks; i += kThreads) bids[i] = bl[i];
+  if (bl) {
+    // to shared memory; their order is checked after the next barrier
+#pragma unroll
+    for (int u = 0; u < kBidRegs; ++u) {
+      const int i = tid + u * kThreads;
+      if (i < a.k_blocks) bids[i] = bid_r[u];
+    }
     if (dense) __syncthreads();  // the keys below are read through the block ids
   }
   if (dense) {
