@@ -113,6 +113,43 @@ static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 static_assert(offsetof(Misc, inv_l) % 16 == 0 && kMisc % 16 == 0 && kWgt % 16 == 0,
               "16-byte loads of inv_l and of the merge weights");
 
+// A tile's scores of this thread's head (TMEM columns [addr, addr + R)), in
+// log2 units, -inf past the tile's valid rows: one TMEM load, one wait.
+template <int R>
+__device__ __forceinline__ void load_scores(uint32_t addr, int valid, float scale_log2,
+                                            float (&z)[R]) {
+  if constexpr (R == 64) {
+    tmem_ld64(addr, z);
+  } else {
+    static_assert(R == 32, "tile rows");
+    tmem_ld32(addr, z);
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i) z[i] = i < valid ? z[i] * scale_log2 : -INFINITY;
+}
+// max_i z[i], as four independent chains
+template <int R>
+__device__ __forceinline__ float max_scores(const float (&z)[R]) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < R; ++i) m4[i & 3] = fmaxf(m4[i & 3], z[i]);
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+// p_i = 2^(z_i - m) packed as bf16 pairs into pk; returns sum_i p_i over the
+// fp32 probabilities (four partial sums)
+template <int R>
+__device__ __forceinline__ float exp_pack(const float (&z)[R], float m, uint32_t (&pk)[R / 2]) {
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < R; i += 2) {
+    const float p0 = exp2f(z[i] - m), p1 = exp2f(z[i + 1] - m);
+    s4[(i >> 1) & 3] += p0 + p1;
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
+    pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+  }
+  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m,
                                          DeviceStatus* st) {
   return mbar_wait_abortable(bar, parity, &m->abort, st, SITE_ATTN);
@@ -483,18 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = wait_bar(&misc->s_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status);
         tc_fence_after();
         if (ok) {
-#pragma unroll
-          for (int c = 0; c < kRows / 16; ++c) {
-            float v[16];
-            tmem_ld16(la + 64 * sb + c * 16, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              z[c * 16 + i] = (c * 16 + i < valid) ? v[i] * a.scale_log2 : -INFINITY;
-            }
-          }
-          float mt = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kRows; ++i) mt = fmaxf(mt, z[i]);
+          load_scores<kRows>(la + 64 * sb, valid, a.scale_log2, z);
+          const float mt = max_scores<kRows>(z);
           if (t == 0) {
             m_run = mt;
           } else if (mt > m_run + 8.f) {
@@ -535,16 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P[sb] was last read by PV(t - 2)
         if (t >= 2) wait_pv(t - 2);
         if (ok) {
-          float sum = 0.f;
           uint32_t pk[kRows / 2];
-#pragma unroll
-          for (int i = 0; i < kRows; i += 2) {
-            const float p0 = exp2f(z[i] - m_run), p1 = exp2f(z[i + 1] - m_run);
-            sum += p0 + p1;  // the denominator sums the fp32 probabilities
-            const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
-            pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
-          }
-          l_run = l_run * alpha + sum;
+          // the denominator sums the fp32 probabilities
+          l_run = l_run * alpha + exp_pack<kRows>(z, m_run, pk);
           const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
           for (int c = 0; c < kRows / 8; ++c) {
@@ -1026,18 +1046,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (ok) {
-#pragma unroll
-            for (int c = 0; c < kRows / 16; ++c) {
-              float v[16];
-              tmem_ld16(la + 64 * sb + c * 16, v);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                z[c * 16 + i] = (c * 16 + i < valid) ? v[i] * a.scale_log2 : -INFINITY;
-              }
-            }
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kRows; ++i) mt = fmaxf(mt, z[i]);
+            load_scores<kRows>(la + 64 * sb, valid, a.scale_log2, z);
+            const float mt = max_scores<kRows>(z);
             if (t == 0) {
               m_run = mt;
             } else if (mt > m_run + 8.f) {
@@ -1078,16 +1088,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P[sb] was last read by PV(g - 2), of this query or the previous one
           if (g >= 2) wait_pv(g - 2);
           if (ok) {
-            float sum = 0.f;
             uint32_t pk[kRows / 2];
-#pragma unroll
-            for (int i = 0; i < kRows; i += 2) {
-              const float p0 = exp2f(z[i] - m_run), p1 = exp2f(z[i + 1] - m_run);
-              sum += p0 + p1;  // the denominator sums the fp32 probabilities
-              const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
-              pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
-            }
-            l_run = l_run * alpha + sum;
+            // the denominator sums the fp32 probabilities
+            l_run = l_run * alpha + exp_pack<kRows>(z, m_run, pk);
             const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
             for (int c = 0; c < kRows / 8; ++c) {
