@@ -330,13 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectArgs a, int u
 // slot j, so every pass runs on registers and each warp lays out its own part
 // of the output; only the warps' totals need a block-wide scan.
 constexpr int kRankMax = 64;  // final bins at most this large are ranked exactly
-// Dense score rows of at most this many tokens are staged whole in shared
-// memory (after the block ids) before their kept blocks are read: at the
-// densities where rows are dense (a prefill chunk's kept blocks are about
-// half of its blocks), one coalesced pass over the row costs less than a
-// scattered 32-byte read per kept block.
-constexpr int64_t kStagedRowMax = 48640;
-constexpr int kStageIters = static_cast<int>((kStagedRowMax / 4 + 1023) / 1024);  // float4 a thread
+// Dense score rows (a prefill chunk's token stage scores every latent): each
+// kept block's 8 scores (32 bytes) are copied to shared memory in candidate
+// order by asynchronous 16-byte copies, issued as soon as the block ids are in
+// registers; the keys are then read without bank conflicts.
 
 // The score a valid order-preserving key stands for (inverse of score_key).
 __device__ __forceinline__ float key_value(uint32_t key) {
@@ -384,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   // pass of a two-pass selection), or the ids the first pass kept (second).
   const int b = a.chunks ? static_cast<int>(blockIdx.x / a.chunks) : static_cast<int>(blockIdx.x);
   const int64_t base = a.chunks ? static_cast<int64_t>(blockIdx.x % a.chunks) * a.chunk : 0;
-  const int64_t n = a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n);
+  // at most KPT x 1024 candidates: 32-bit indices from here on
+  const int n = static_cast<int>(a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n));
   const uint32_t k = static_cast<uint32_t>(a.k);
   const float* sc = a.scores + static_cast<int64_t>(b) * a.n;
   const int32_t* ids_in = a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in : nullptr;
@@ -404,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     }
   }
   uint32_t key[KPT];
-  const int64_t wbase = static_cast<int64_t>(warp) * (32 * KPT) + lane;  // + 32 j
+  const int wbase = warp * (32 * KPT) + lane;  // + 32 j
   // Scores that do not go through the block ids are requested first, so their
   // latency overlaps the block-id copy below.
   if (ids_in) {
@@ -413,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     // (The key registers hold the ids first: no second array.)
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      const int64_t i = wbase + 32 * j;
+      const int i = wbase + 32 * j;
       key[j] = static_cast<uint32_t>(i < n ? ids_in[i] : -1);
     }
 #pragma unroll
@@ -426,35 +424,28 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
     float v[KPT];
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      const int64_t i = wbase + 32 * j;
+      const int i = wbase + 32 * j;
       v[j] = __ldg(sc + base + (i < n ? i : 0));
     }
 #pragma unroll
     for (int j = 0; j < KPT; ++j) key[j] = score_key(wbase + 32 * j < n ? v[j] : -INFINITY);
   }
-  const bool staged = dense && a.dense_stride <= kStagedRowMax;
-  const float* row = dense ? a.scores + static_cast<int64_t>(b) * a.dense_stride : nullptr;
-  float* row_s = reinterpret_cast<float*>(bids + kMaxKBlocks);  // staged row (16-byte aligned)
-  if (staged) {
-    // the whole row, in two rounds of float4 loads (each round's loads all
-    // issued before any is stored)
-    const int n4 = static_cast<int>(a.dense_stride / 4);
-    const float4* src = reinterpret_cast<const float4*>(row);
-    constexpr int kRound = (kStageIters + 1) / 2;
+  // kept blocks' scores in candidate order, after the block ids (16-byte aligned)
+  float* cand_s = reinterpret_cast<float*>(bids + kMaxKBlocks);
+  const int n_row_blocks = dense ? static_cast<int>(a.dense_stride / 8) : 0;
+  if (dense) {
+    const float* row = a.scores + static_cast<int64_t>(b) * a.dense_stride;
 #pragma unroll
-    for (int u0 = 0; u0 < kStageIters; u0 += kRound) {
-      float4 v4[kRound];
-#pragma unroll
-      for (int u = 0; u < kRound; ++u) {
-        const int i = tid + (u0 + u) * kThreads;
-        if (u0 + u < kStageIters && i < n4) v4[u] = __ldg(src + i);
-      }
-#pragma unroll
-      for (int u = 0; u < kRound; ++u) {
-        const int i = tid + (u0 + u) * kThreads;
-        if (u0 + u < kStageIters && i < n4) reinterpret_cast<float4*>(row_s)[i] = v4[u];
+    for (int u = 0; u < kBidRegs; ++u) {
+      const int kb = tid + u * kThreads;
+      if (kb < a.k_blocks && bid_r[u] >= 0 && bid_r[u] < n_row_blocks) {
+        const float* src = row + static_cast<int64_t>(bid_r[u]) * 8;
+        const uint32_t dst = smem_u32(cand_s + kb * 8);
+        cp_async_16(dst, src);
+        cp_async_16(dst + 16, src + 4);
       }
     }
+    cp_async_commit();
   }
   if (bl) {
     // to shared memory; their order is checked after the next barrier
@@ -463,15 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       const int i = tid + u * kThreads;
       if (i < a.k_blocks) bids[i] = bid_r[u];
     }
-    if (dense) __syncthreads();  // the keys below are read through the block ids
   }
   if (dense) {
-    const float* rsrc = staged ? row_s : row;
+    cp_async_wait<0>();
+    __syncthreads();  // every thread's copies and block ids are visible
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      const int64_t i = wbase + 32 * j;
+      const int i = wbase + 32 * j;
       const int blk = i < n ? bids[i >> 3] : -1;
-      key[j] = score_key(blk >= 0 ? rsrc[static_cast<int64_t>(blk) * 8 + (i & 7)] : -INFINITY);
+      key[j] = score_key(blk >= 0 && blk < n_row_blocks ? cand_s[i] : -INFINITY);
     }
   }
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, cnt = 0;
@@ -699,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   int32_t* out = a.out_ids + static_cast<int64_t>(blockIdx.x) * a.k;
   const uint32_t lt = (1u << lane) - 1u;
   auto out_id = [&](int j) -> int32_t {
-    const int64_t i = wbase + 32 * j;
+    const int i = wbase + 32 * j;
     if (ids_in) return ids_in[i];
     return a.block_ids ? bids[i >> 3] * 8 + static_cast<int32_t>(i & 7)
                        : static_cast<int32_t>(base + i);
@@ -726,21 +717,21 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       eq_seen += __popc(eqm);
     }
   }
-  for (int64_t j = total + tid; j < a.k; j += kThreads) out[j] = -1;
+  for (int j = static_cast<int>(total) + tid; j < a.k; j += kThreads) out[j] = -1;
 }
 
 }  // namespace
 
 template <int KPT>
 cudaError_t launch_reg(const SelectArgs& a, unsigned grid, cudaStream_t s) {
-  // block ids, then (dense rows that fit) the staged row
+  // block ids, then (dense rows) the kept blocks' scores
   size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
-  if (a.block_ids && a.dense_stride && a.dense_stride <= kStagedRowMax) {
-    smem = static_cast<size_t>(kMaxKBlocks) * 4 + static_cast<size_t>(a.dense_stride) * 4;
+  if (a.block_ids && a.dense_stride) {
+    smem = static_cast<size_t>(kMaxKBlocks) * 4 + static_cast<size_t>(a.k_blocks) * 8 * 4;
   }
   static std::atomic<int> smem_set[64]{};
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
-                              static_cast<int>(kMaxKBlocks * 4 + kStagedRowMax * 4), smem_set);
+                              static_cast<int>(kMaxKBlocks * 4 + kMaxKBlocks * 8 * 4), smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(select_reg_kernel<KPT>, dim3(grid), dim3(kThreads), smem, s, 1, a);
 }
