@@ -696,10 +696,34 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
                        : static_cast<int32_t>(base + i);
   };
   if (!ties) {
+    // one loop per id source (the source is the same for every slot): slot
+    // j's lanes with their bit set write at ow + (set bits below them)
+    int32_t* ow = out + pos;
+    if (ids_in) {
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      if ((gt_mask[j] >> lane) & 1u) out[pos + __popc(gt_mask[j] & lt)] = out_id(j);
-      pos += __popc(gt_mask[j]);
+      for (int j = 0; j < KPT; ++j) {
+        const uint32_t m = gt_mask[j];
+        if ((m >> lane) & 1u) ow[__popc(m & lt)] = ids_in[wbase + 32 * j];
+        ow += __popc(m);
+      }
+    } else if (a.block_ids) {
+      // candidate wbase + 32 j is token (lane & 7) of kept block (wbase >> 3) + 4 j
+      const int32_t* bw = bids + (wbase >> 3);
+      const int32_t r = lane & 7;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const uint32_t m = gt_mask[j];
+        if ((m >> lane) & 1u) ow[__popc(m & lt)] = bw[4 * j] * 8 + r;
+        ow += __popc(m);
+      }
+    } else {
+      const int32_t id0 = static_cast<int32_t>(base) + wbase;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const uint32_t m = gt_mask[j];
+        if ((m >> lane) & 1u) ow[__popc(m & lt)] = id0 + 32 * j;
+        ow += __popc(m);
+      }
     }
   } else {
     uint32_t eq_seen = 0;
