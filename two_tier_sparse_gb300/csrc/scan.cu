@@ -129,6 +129,7 @@ struct Shared {
   int abort;
   TileMeta meta[2][kMaxStages][kMaxTPS];
   QSlot qs[2][kQRing];
+  int tile_slot[kSlots];  // index-query slot of the tile in each TMEM slot (set by its math set)
 };
 
 template <int FMT, int TPS>
@@ -466,7 +467,6 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
   static_assert(FMT != DSA_FMT_BF16 || TPS == 1, "bf16 tiles are read by the MMA, one a stage");
   constexpr uint32_t idesc = mma_idesc(kTile, kIdxHeads, FMT == DSA_FMT_BF16, false, false);
   const uint32_t tmem = sh.tmem_base;
-  int ring = 0;   // index-query ring slot of the set's tile i (advances per own tile)
   int stage = 0;  // bf16: raw stage of the half of tile i (advances per own tile)
   for (int i = set; i < n_tiles; i += 2) {
     const int q = i & (kSlots - 1);
@@ -476,7 +476,8 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
     // with the tcgen05 fence before its arrival).
     if (!mbar_wait_abortable(&sh.op_full[q], u & 1, &sh.abort, a.status, SITE_SCAN)) return;
     tc_fence_after();
-    const uint32_t qb = sbase + Lo::kQ + (set * kQRing + ring) * 4096;
+    // the tile's index query: the slot its math set wrote before arriving
+    const uint32_t qb = sbase + Lo::kQ + (set * kQRing + sh.tile_slot[q]) * 4096;
     const uint64_t bd0 = sw128_desc(qb, 16, 1024);
     const uint32_t slot = tmem + q * P::kSlotCols;
     if constexpr (FMT == DSA_FMT_BF16) {
@@ -500,7 +501,6 @@ __device__ void mma_issuer(const ScanArgs& a, Shared& sh, uint32_t sbase, int n_
       }
       mma_commit(&sh.acc_full[q]);
     }
-    if (++ring == kQRing) ring = 0;
     if (++stage == R::kStages) stage = 0;
   }
 }
@@ -608,19 +608,21 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
   const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   const uint32_t tmem = sh.tmem_base;
   const int64_t q_rows = tpq * kTile;
-  int ring_b0 = -1, ring_b1 = -1, ring_b2 = -1;  // query held by each ring slot
   // per-thread state of this set's two tiles waiting for their epilogue
   uint32_t pend_sc0 = 0, pend_sc1 = 0;
   bool pend_valid0 = false, pend_valid1 = false;
   TilePos prep, epi;  // positions of this set's next prepared and next finished tile
   prep.init(t_begin + set, tpq);
   epi = prep;
-  int ring = 0;                  // of the tile being prepared (advances per own tile)
+  // Index-query slots follow the queries: a query's tiles share one slot,
+  // and a tile of another query builds the next slot (last used by a tile at
+  // least three own tiles back, whose epilogue is done).
+  int cur_b = -1, cur_slot = kQRing - 1;
+  int pend_slot0 = 0, pend_slot1 = 0;  // of the two tiles waiting for their epilogue
   int stage = 0;                 // ring stage of the tile being prepared (advances per TPS
   uint32_t spar = 0;             // own tiles) and the parity of that stage's use
-  int ring_e = 0;                // of the tile being finished
   // The query of this set's next tile of another query, fetched one own tile
-  // ahead (and kept while the ring's slots are rebuilt for it).
+  // ahead.
   QFetch nq;
   nq.b = -1;
   if (set < n_tiles) nq = fetch_query<FMT>(a, prep.b, mt);
@@ -653,7 +655,7 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       }
     }
     tc_fence_before();
-    const QSlot& slot = sh.qs[set][ring_e];
+    const QSlot& slot = sh.qs[set][pe ? pend_slot1 : pend_slot0];
     if (r < a.n_rows) {
       float s = -INFINITY;
       if (pe ? pend_valid1 : pend_valid0) {
@@ -666,7 +668,6 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
       a.scores[static_cast<int64_t>(b) * a.n_rows + r] = s;
     }
     epi.advance(2, q_rows);
-    if (++ring_e == kQRing) ring_e = 0;
     return true;
   };
 
@@ -685,17 +686,22 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     if (i >= n_tiles) return true;
     const int q = i & (kSlots - 1);
     const int b = prep.b;
-    const int held = ring == 0 ? ring_b0 : (ring == 1 ? ring_b1 : ring_b2);
-    if (held != b) {
-      // The ring slot last served tile i - 6, whose epilogue every thread of
-      // the set has finished once all of them reach this barrier.
+    if (b != cur_b) {
+      // The next slot last served a tile at most i - 6 (each slot holds one
+      // query, and the two slots since hold the queries of tiles i - 4 and
+      // i - 2 at the latest), whose epilogue every thread of the set has
+      // finished once all of them reach this barrier.
+      const int ns = cur_slot + 1 == kQRing ? 0 : cur_slot + 1;
       if (nq.b != b) nq = fetch_query<FMT>(a, b, mt);
       named_sync(1 + set, kMathThreads);
-      build_query<FMT, TPS>(sh, sbase, nq, mt, set, ring);
+      build_query<FMT, TPS>(sh, sbase, nq, mt, set, ns);
       fence_proxy_async_smem();
       named_sync(1 + set, kMathThreads);
-      if (ring == 0) ring_b0 = b; else if (ring == 1) ring_b1 = b; else ring_b2 = b;
+      cur_b = b;
+      cur_slot = ns;
     }
+    if constexpr (pi) pend_slot1 = cur_slot; else pend_slot0 = cur_slot;
+    if (mt == 0) sh.tile_slot[q] = cur_slot;  // read by the MMA issuer after op_full[q]
     if (t == 0 && !mbar_wait_abortable(&sh.raw_full[set][stage], spar, &sh.abort, a.status,
                                        SITE_SCAN)) {
       return false;
@@ -762,7 +768,6 @@ __device__ void math(const ScanArgs& a, Shared& sh, uint32_t sbase, int64_t t_be
     }
     prep.advance(2, q_rows);
     if (i + 2 < n_tiles && prep.b != b && nq.b != prep.b) nq = fetch_query<FMT>(a, prep.b, mt);
-    if (++ring == kQRing) ring = 0;
     if (t == TPS - 1 && ++stage == R::kStages) {
       stage = 0;
       spar ^= 1u;
