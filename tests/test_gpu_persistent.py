@@ -81,3 +81,23 @@ def test_unsplit_decode_step_is_deterministic_across_replays():
         outs.append(host_u16(out))
     assert d.status()[0] == 0
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "bf16"])
+def test_scan_query_switches_in_every_cta(fmt):
+    """600 short sequences (1-2 tiles of each stage per query): every scan CTA's
+    tile range spans several queries, so each math set keeps building the next
+    query's index vectors while the previous query's tiles are still in
+    flight. Both tiers run (k_blocks 16, k_tokens 40); every sequence is
+    checked against the oracle."""
+    from test_gpu_parity import check_step, run_step
+    rng = np.random.default_rng(96)
+    T = [int(t) for t in rng.integers(100, 1200, size=600)]
+    inp = synth.decode_inputs(T, 1, fmt, seed=97, q_scale=8.0)
+    cfg = dsa.config(k_blocks=16, k_tokens=40, ratio=1, sm_scale=1.0)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    outs = run_step(d, cfg)
+    code, info = d.status()
+    assert code == 0, hex(info)
+    check_step(inp, cfg, outs, range(inp.B))
