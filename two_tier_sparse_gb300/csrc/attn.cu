@@ -710,30 +710,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unnormalised accumulator of CTA q.
       float* wgt = reinterpret_cast<float*>(gbase + kWgt);  // [S][64]
       if (warp < 2) {
-        float mq[kMaxAttnSplits], lqs[kMaxAttnSplits];
+        // Rolled loops over the S senders: this code runs once per CTA and is
+        // fetched cold, so its size costs more than its work.
+        auto ml = [&](int q) {  // sender q's (max, sum) of head tid
+          return reinterpret_cast<const float2*>(gbase + (recv_slot(q) - sbase) + D * 128)[tid];
+        };
         float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMaxAttnSplits; ++q) {
-          mq[q] = -INFINITY;
-          lqs[q] = 0.f;
-          if (q < S) {
-            const float* t = reinterpret_cast<const float*>(gbase + (recv_slot(q) - sbase) + D * 128);
-            mq[q] = t[2 * tid];
-            lqs[q] = t[2 * tid + 1];
-          }
-          if (lqs[q] > 0.f) M = fmaxf(M, mq[q]);
+#pragma unroll 1
+        for (int q = 0; q < S; ++q) {
+          const float2 x = ml(q);
+          if (x.y > 0.f) M = fmaxf(M, x.x);
         }
-        float L = 0.f, eq[kMaxAttnSplits];
-#pragma unroll
-        for (int q = 0; q < kMaxAttnSplits; ++q) {
-          eq[q] = lqs[q] > 0.f ? exp2f(mq[q] - M) : 0.f;
-          L = fmaf(eq[q], lqs[q], L);
+        float L = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < S; ++q) {
+          const float2 x = ml(q);
+          const float e = x.y > 0.f ? exp2f(x.x - M) : 0.f;
+          wgt[q * kHeads + tid] = e;
+          L = fmaf(e, x.y, L);
         }
         const float inv_L = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxAttnSplits; ++q) {
-          if (q < S) wgt[q * kHeads + tid] = eq[q] * inv_L;
-        }
+#pragma unroll 1
+        for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
         if (a.lse && split == 0) {
           a.lse[static_cast<int64_t>(b) * kHeads + tid] =
               L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
