@@ -923,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&misc->kv_full[i], 32 * TS::kWarpsPerSlot);
+      mbar_init(&misc->kv_full[i], 32 * kLoadWarps);  // every loader thread, per tile
       mbar_init(&misc->kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1152,11 +1152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   else if (warp < kMmaWarp) {
     // ---------------- loaders ----------------
-    // Warp 4 + w fills 32 rows (part w / kSlots) of ring slot w % kSlots for
-    // the CTA's tiles g = slot, slot + kSlots, ... across its queries.
+    // Loader warp w fills rows [kWarpRows w, kWarpRows (w + 1)) of every tile
+    // g = 0, 1, ... of the CTA's queries (ring slot g % kSlots): the four
+    // warps' copies of a tile are in flight together, and each lane's
+    // completion arrives on the slot by itself (rows without a source are
+    // zero-filled through the same path), so no warp waits for its own
+    // copies: it goes on to the next tile once that tile's slot is free.
+    constexpr int kWarpRows = kRows / kLoadWarps;
     const int w = warp - kLoadWarp0;
-    const int sl = w % kSlots, part = w / kSlots;
-    const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
     bool ok = true;
     int64_t gq = 0;
     int qi = 0;
@@ -1170,38 +1173,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w_cnt = qr.n_sw;
       const int n_rows = w_cnt + misc->n_sel[qi & 1];
       const int n_tiles = (n_rows + kRows - 1) / kRows;
-      for (int t = static_cast<int>(((sl - gq) % kSlots + kSlots) % kSlots); t < n_tiles;
-           t += kSlots) {
+      for (int t = 0; t < n_tiles; ++t) {
         const int64_t g = gq + t;
+        const int sl = static_cast<int>(g % kSlots);
         const uint32_t u = static_cast<uint32_t>(g / kSlots);
         if (g >= kSlots &&
             !wait_bar_s(&misc->kv_empty[sl], (u - 1) & 1u, misc, a.status)) {
           ok = false;
           break;
         }
-        const int r0 = t * kRows + 32 * part;  // this warp's first row of the tile
-        if (r0 + 32 <= w_cnt &&
-            DSA_DCHECK(qr.wrow0 + r0 + 32 <= a.swa_rows, a.status, SITE_ATTN, qr.wrow0 + r0)) {
-          // 32 window rows (contiguous): eight TMA boxes, completing on the slot
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&misc->kv_full[sl], 32 * 1024);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              tma_load_2d(dstb + c * kAtomBytes + 32 * part * 128, &wmap, 64 * c,
-                          static_cast<int>(qr.wrow0 + r0), &misc->kv_full[sl]);
-            }
-          } else {
-            mbar_arrive(&misc->kv_full[sl]);
-          }
-          continue;
-        }
-        // Lane l works out the source of the warp's row l once (-1: none,
-        // zero-filled); each row is then copied by the whole warp, lane l
-        // taking 16-byte chunks l and l + 32.
+        const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
+        const int r0 = t * kRows + kWarpRows * w;  // this warp's first row of the tile
+        // Lane l < kWarpRows works out the source of the warp's row l once
+        // (-1: none, zero-filled); each row is then copied by the whole warp,
+        // lane l taking 16-byte chunks l and l + 32.
         int64_t arow_l = -1;
         {
           const int gl = r0 + lane;
-          if (gl < n_rows) {
+          if (lane < kWarpRows && gl < n_rows) {
             arow_l = gl < w_cnt ? qr.wrow0 + gl : qr.lat_row0 + ids[gl - w_cnt];
             if (!DSA_DCHECK(arow_l >= 0 && arow_l < (gl < w_cnt ? a.swa_rows : a.lat_rows),
                             a.status, SITE_ATTN, arow_l)) {
@@ -1211,9 +1200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
 #pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < kWarpRows; ++r) {
           const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
-          const int row = 32 * part + r;
+          const int row = kWarpRows * w + r;
           const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
           const uint32_t d1 = d0 + 4 * kAtomBytes;
           if (arow >= 0) {
@@ -1221,14 +1210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_16(d0, src);
             cp_async_16(d1, src + 256);
           } else {
-            st_shared_v4(d0, make_uint4(0, 0, 0, 0));
-            st_shared_v4(d1, make_uint4(0, 0, 0, 0));
+            cp_async_16_zero(d0, a.latents);
+            cp_async_16_zero(d1, a.latents);
           }
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&misc->kv_full[sl]);
+        cp_async_mbar_arrive_noinc(&misc->kv_full[sl]);
       }
       __syncwarp();
       if (ok && lane == 0) {

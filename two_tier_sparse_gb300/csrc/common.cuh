@@ -346,6 +346,12 @@ __device__ __forceinline__ void cluster_wait() {
 
 // Arrives (without raising the expected count) on `bar` once every cp.async
 // this thread issued before has landed.
+// 16 zero bytes written through the cp.async path (source size 0: nothing is
+// read from `src`, which must still be a valid global address), so that a
+// cp.async completion arrival also covers them.
+__device__ __forceinline__ void cp_async_16_zero(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;\n" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
                : "memory");
