@@ -13,14 +13,14 @@
 // Warp roles: warps 0-3 math (softmax for the 64 heads by warps 0-1, one head
 // per thread; O rescaling by all four, thread = TMEM lane; the epilogue by
 // these four and the four loader warps, which are idle by then),
-// warps 4-7 loaders (warp 4 + w owns ring slot w: cp.async gathers of random
-// 1 KB rows, waited by the warp and announced on the slot's mbarrier; Q comes
-// by eight TMA boxes that land in the swizzled operand layout), warp 8 issues
-// the QK^T MMAs and warp 9 the PV
-// MMAs (a barrier wait costs a single thread a few hundred cycles; two issuers
-// overlap their waits). Random rows reach shared memory
-// fastest through several slots with independent completion, hence four
-// 32 KB slots. S is double-buffered in tensor memory so QK^T of tile t + 1
+// warps 4-7 loaders (every loader warp copies its quarter of the rows of each
+// tile by cp.async, the 1 KB rows gathered at random; each lane's completion
+// arrives on the slot's mbarrier by itself, so the four warps' copies of a
+// tile are in flight together and no warp waits for its own; Q comes by
+// eight TMA boxes that land in the swizzled operand layout), warp 8 issues
+// the QK^T MMAs and warp 9 the PV MMAs (a barrier wait costs a single thread
+// a few hundred cycles; two issuers overlap their waits). Four 32 KB slots
+// keep several tiles in flight. S is double-buffered in tensor memory so QK^T of tile t + 1
 // runs while the softmax of tile t does. The running maximum only moves when
 // it grows by more than 2^8 (the stale maximum keeps every P value <= 256,
 // exact enough in bf16 and fp32), so rescaling O is rare.
@@ -78,7 +78,6 @@ struct TileShape {
   static constexpr int kSlots = kKVBytes / (ROWS * 1024);
   static constexpr int kAtomBytes = ROWS * 128;
   static constexpr int kSlotBytes = 8 * kAtomBytes;
-  static constexpr int kWarpsPerSlot = kLoadWarps / kSlots;
 };
 constexpr int kMisc = kIds + kMaxKTokens * 4;
 constexpr int kMiscBytes = 2048;
@@ -157,8 +156,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
 
 template <int ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                const __grid_constant__ CUtensorMap wmap) {
+    attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   using TS = TileShape<ROWS>;
   constexpr int kRows = ROWS;
   constexpr int kSlots = TS::kSlots;
@@ -178,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&misc->kv_full[i], 32 * TS::kWarpsPerSlot);  // the slot's loader threads
+      mbar_init(&misc->kv_full[i], 32 * kLoadWarps);  // every loader thread, per tile
       mbar_init(&misc->kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -333,19 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
     // ---------------- loaders ----------------
-    // Warp 4 + w fills 32 rows (part w / kSlots) of slot w % kSlots's tiles
-    // (tiles sl, sl + kSlots, ...): it waits for its own copies of a tile,
-    // fences them into the async proxy (the tensor core's view) and then
-    // arrives, while the other slots' tiles are in flight. Tiles made only of
-    // window rows need no ids. A part of 32 window rows (contiguous in the
-    // window buffer) comes by eight TMA boxes instead, which complete on the
-    // slot's barrier by themselves: the warp moves on at once and leaves the
-    // cp.async path to the gathered rows.
+    // Loader warp w fills rows [kWarpRows w, kWarpRows (w + 1)) of every tile
+    // t (ring slot t % kSlots): the four warps' copies of a tile are in
+    // flight together, and each lane's completion arrives on the slot by
+    // itself (rows without a source are zero-filled through the same path),
+    // so no warp waits for its own copies. Tiles made only of window rows
+    // need no ids: they load while the previous kernel still selects.
+    constexpr int kWarpRows = kRows / kLoadWarps;
     const int w = warp - kLoadWarp0;
-    const int sl = w % kSlots, part = w / kSlots;
     bool have_ids = false;
     int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
-    for (int t = sl;; t += kSlots) {
+    for (int t = 0;; ++t) {
       const int g0 = t * kRows;
       if (!have_ids && g0 + kRows > w_cnt) {
         if (!wait_bar(&misc->ids_ready, 0u, misc, a.status)) {
@@ -359,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         have_ids = true;
       }
       if (have_ids && t >= n_tiles) break;
+      const int sl = t % kSlots;
       if (t >= kSlots &&
           !wait_bar(&misc->kv_empty[sl], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
@@ -366,30 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint32_t dstb = sbase + kKV + sl * kSlotBytes;
-      const int r0 = g0 + 32 * part;  // this warp's first row of the tile
-      if (r0 + 32 <= w_cnt &&
-          DSA_DCHECK(wrow0 + w_begin + r0 + 32 <= a.swa_rows, a.status, SITE_ATTN,
-                     wrow0 + w_begin + r0)) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&misc->kv_full[sl], 32 * 1024);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            tma_load_2d(dstb + c * kAtomBytes + 32 * part * 128, &wmap, 64 * c,
-                        static_cast<int>(wrow0 + w_begin + r0), &misc->kv_full[sl]);
-          }
-        } else {
-          mbar_arrive(&misc->kv_full[sl]);
-        }
-        continue;
-      }
-      // Lane l works out the source of the warp's row l once (its place in the
-      // window buffer or the latents; -1: none, zero-filled); each row is then
-      // copied by the whole warp, lane l taking 16-byte chunks l and l + 32, so
-      // a copy instruction of the warp covers 512 contiguous bytes.
+      const int r0 = g0 + kWarpRows * w;  // this warp's first row of the tile
+      // Lane l < kWarpRows works out the source of the warp's row l once (its
+      // place in the window buffer or the latents; -1: none, zero-filled);
+      // each row is then copied by the whole warp, lane l taking 16-byte
+      // chunks l and l + 32, so a copy instruction covers 512 contiguous bytes.
       int64_t arow_l = -1;
       {
         const int gl = r0 + lane;
-        if (gl < n_rows_cta) {
+        if (lane < kWarpRows && gl < n_rows_cta) {
           arow_l = gl < w_cnt ? wrow0 + w_begin + gl : lat_row0 + ids[s_begin + gl - w_cnt];
           if (!DSA_DCHECK(arow_l >= 0 && arow_l < (gl < w_cnt ? a.swa_rows : a.lat_rows), a.status,
                           SITE_ATTN, arow_l)) {
@@ -401,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lane + 32: atom 4 + lane / 8, same unit
       const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
 #pragma unroll 4
-      for (int r = 0; r < 32; ++r) {
+      for (int r = 0; r < kWarpRows; ++r) {
         const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
-        const int row = 32 * part + r;
+        const int row = kWarpRows * w + r;
         const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
         const uint32_t d1 = d0 + 4 * kAtomBytes;
         if (arow >= 0) {
@@ -411,14 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(d0, src);
           cp_async_16(d1, src + 256);
         } else {
-          st_shared_v4(d0, make_uint4(0, 0, 0, 0));
-          st_shared_v4(d1, make_uint4(0, 0, 0, 0));
+          cp_async_16_zero(d0, a.latents);
+          cp_async_16_zero(d1, a.latents);
         }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&misc->kv_full[sl]);
+      cp_async_mbar_arrive_noinc(&misc->kv_full[sl]);
     }
     n_tiles_e = have_ids ? n_tiles : 0;
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -902,8 +881,7 @@ __device__ __forceinline__ void raise_count(int* p, int v) {
 
 template <int ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_stream_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap wmap) {
+    attn_stream_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   using TS = TileShape<ROWS>;
   constexpr int kRows = ROWS;
   constexpr int kSlots = TS::kSlots;
@@ -1235,7 +1213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       tma_prefetch_map(&qmap);
-      tma_prefetch_map(&wmap);
       if (b0 < a.B) load_q(b0);
       bool ok = true;
       int64_t gq = 0;
@@ -1378,16 +1355,11 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   cudaError_t e = encode_tma_2d(&qmap, a.q, 2, kLatent, static_cast<uint64_t>(a.B) * kHeads,
                                 kLatent * 2, 64, kHeads);
   if (e != cudaSuccess) return e;
-  // Window rows (decode: B x window rows; prefill: n_q + window - 1), boxes of
-  // 32 rows x 64 dims.
-  CUtensorMap wmap;
-  memset(&wmap, 0, sizeof(wmap));
+  // Rows of the window buffer (decode: B x window rows; prefill: n_q + window - 1).
   const uint64_t wrows =
       a.prefill ? (a.mq > 0 ? static_cast<uint64_t>(a.B / a.mq) * a.swa_seq_rows
                             : static_cast<uint64_t>(a.B) + a.window - 1)
                 : static_cast<uint64_t>(a.B) * a.window;
-  e = encode_tma_2d(&wmap, a.swa, 2, kLatent, wrows, kLatent * 2, 64, 32);
-  if (e != cudaSuccess) return e;
   AttnArgs args = a;
   args.swa_rows = static_cast<int64_t>(wrows);
   if (a.splits == 1) {
@@ -1398,28 +1370,28 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       e = ensure_smem(reinterpret_cast<const void*>(attn_stream_kernel<64>), kSmemStream, smem_set);
       if (e != cudaSuccess) return e;
       return launch_pdl(attn_stream_kernel<64>, dim3(grid), dim3(kThreads), kSmemStream, s, 1, args,
-                        qmap, wmap);
+                        qmap);
     }
     if (a.tile_rows != 32) return cudaErrorInvalidValue;
     static std::atomic<int> smem_set[64]{};
     e = ensure_smem(reinterpret_cast<const void*>(attn_stream_kernel<32>), kSmemStream, smem_set);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_stream_kernel<32>, dim3(grid), dim3(kThreads), kSmemStream, s, 1, args,
-                      qmap, wmap);
+                      qmap);
   }
   if (a.tile_rows == 64) {
     static std::atomic<int> smem_set[64]{};
     e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                      a.splits, args, qmap, wmap);
+                      a.splits, args, qmap);
   }
   if (a.tile_rows != 32) return cudaErrorInvalidValue;
   static std::atomic<int> smem_set[64]{};
   e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
-                    a.splits, args, qmap, wmap);
+                    a.splits, args, qmap);
 }
 
 }  // namespace dsa
