@@ -112,11 +112,11 @@ static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 static_assert(offsetof(Misc, inv_l) % 16 == 0 && kMisc % 16 == 0 && kWgt % 16 == 0,
               "16-byte loads of inv_l and of the merge weights");
 
-// A tile's scores of this thread's head (TMEM columns [addr, addr + R)), in
-// log2 units, -inf past the tile's valid rows: one TMEM load, one wait.
+// A tile's raw scores of this thread's head (TMEM columns [addr, addr + R)),
+// -inf past the tile's valid rows: one TMEM load, one wait. The softmax scale
+// (positive) is applied by max_scores and exp_pack.
 template <int R>
-__device__ __forceinline__ void load_scores(uint32_t addr, int valid, float scale_log2,
-                                            float (&z)[R]) {
+__device__ __forceinline__ void load_scores(uint32_t addr, int valid, float (&z)[R]) {
   if constexpr (R == 64) {
     tmem_ld64(addr, z);
   } else {
@@ -124,24 +124,34 @@ __device__ __forceinline__ void load_scores(uint32_t addr, int valid, float scal
     tmem_ld32(addr, z);
   }
 #pragma unroll
-  for (int i = 0; i < R; ++i) z[i] = i < valid ? z[i] * scale_log2 : -INFINITY;
+  for (int i = 0; i < R; ++i) z[i] = i < valid ? z[i] : -INFINITY;
 }
-// max_i z[i], as four independent chains
+// scale * max_i z[i] (log2 units; equal to max_i (scale * z[i]) for scale > 0),
+// the maximum as four independent chains
 template <int R>
-__device__ __forceinline__ float max_scores(const float (&z)[R]) {
+__device__ __forceinline__ float max_scores(const float (&z)[R], float scale) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int i = 0; i < R; ++i) m4[i & 3] = fmaxf(m4[i & 3], z[i]);
-  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
 }
-// p_i = 2^(z_i - m) packed as bf16 pairs into pk; returns sum_i p_i over the
-// fp32 probabilities (four partial sums)
+// 2^x by the ex2 instruction (flushing subnormal results to zero: a
+// probability below 2^-126 of the running maximum's is dropped)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+// p_i = 2^(scale z_i - m) (one fused multiply-add a score) packed as bf16
+// pairs into pk; returns sum_i p_i over the fp32 probabilities (four partial
+// sums)
 template <int R>
-__device__ __forceinline__ float exp_pack(const float (&z)[R], float m, uint32_t (&pk)[R / 2]) {
+__device__ __forceinline__ float exp_pack(const float (&z)[R], float scale, float m,
+                                          uint32_t (&pk)[R / 2]) {
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < R; i += 2) {
-    const float p0 = exp2f(z[i] - m), p1 = exp2f(z[i + 1] - m);
+    const float p0 = ex2_ftz(fmaf(z[i], scale, -m)), p1 = ex2_ftz(fmaf(z[i + 1], scale, -m));
     s4[(i >> 1) & 3] += p0 + p1;
     const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
     pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
@@ -499,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = wait_bar(&misc->s_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status);
         tc_fence_after();
         if (ok) {
-          load_scores<kRows>(la + 64 * sb, valid, a.scale_log2, z);
-          const float mt = max_scores<kRows>(z);
+          load_scores<kRows>(la + 64 * sb, valid, z);
+          const float mt = max_scores<kRows>(z, a.scale_log2);
           if (t == 0) {
             m_run = mt;
           } else if (mt > m_run + 8.f) {
@@ -543,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           uint32_t pk[kRows / 2];
           // the denominator sums the fp32 probabilities
-          l_run = l_run * alpha + exp_pack<kRows>(z, m_run, pk);
+          l_run = l_run * alpha + exp_pack<kRows>(z, a.scale_log2, m_run, pk);
           const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
           for (int c = 0; c < kRows / 8; ++c) {
@@ -1022,8 +1032,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (ok) {
-            load_scores<kRows>(la + 64 * sb, valid, a.scale_log2, z);
-            const float mt = max_scores<kRows>(z);
+            load_scores<kRows>(la + 64 * sb, valid, z);
+            const float mt = max_scores<kRows>(z, a.scale_log2);
             if (t == 0) {
               m_run = mt;
             } else if (mt > m_run + 8.f) {
@@ -1066,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             uint32_t pk[kRows / 2];
             // the denominator sums the fp32 probabilities
-            l_run = l_run * alpha + exp_pack<kRows>(z, m_run, pk);
+            l_run = l_run * alpha + exp_pack<kRows>(z, a.scale_log2, m_run, pk);
             const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
             for (int c = 0; c < kRows / 8; ++c) {
