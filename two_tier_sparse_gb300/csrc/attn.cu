@@ -58,6 +58,7 @@ constexpr int kPvWarp = kMmaWarp + 1;          // 9: PV issuer
 constexpr int kThreads = 32 * (kPvWarp + 1);   // 320
 constexpr int kMathBar = 1;         // named barrier of the 128 math threads
 constexpr int kEpiBar = 2;          // named barrier of the epilogue (math + loader warps)
+constexpr int kLoadBar = 3;         // named barrier of the 128 loader threads
 constexpr int kEpiThreads = 32 * kMmaWarp;  // 256
 
 // Shared-memory plan (offsets from a 1024-aligned base). The QK^T MMA reads
@@ -801,8 +802,9 @@ struct MiscS {
   int abort;
   // Per-query hand-offs are counters, not barrier phases: a query without rows
   // lets a role run ahead by more than one phase.
-  int ids_seq;  // queries whose index lists are compacted (math warps)
+  int ids_seq;  // queries whose index lists are compacted (loader warps)
   int ld_seq;   // queries finished by loader warps (one count per warp)
+  int math_seq; // queries whose tile count the math warps have read
   int mma_seq;  // queries whose tile count the QK^T issuer has read
   int pv_seq;   // queries whose tile count the PV issuer has read
   int epi_seq;  // queries whose epilogue is done (math warps)
@@ -925,6 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&misc->o_done, 1);  // a query's PVs have completed
     misc->abort = 0;
     misc->ids_seq = misc->ld_seq = misc->mma_seq = misc->pv_seq = misc->epi_seq = 0;
+    misc->math_seq = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&misc->tmem_base, kTmemCols);
@@ -940,75 +943,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (qr.n_sw + misc->n_sel[qi & 1] + kRows - 1) / kRows;
   };
 
+  // Compacts query index qi's valid token ids (>= 0 and < n_vis; pool rows
+  // when the latents are paged) in order into buffer qi & 1: the loader
+  // warps' work (thread ct of 128, warp cw of 4, named barrier kLoadBar),
+  // done for the next query as soon as a query's tiles are out, so that no
+  // role waits for ids at a query switch.
+  auto compact = [&](int b, int qi, bool& ok) {
+    const int ct = tid - 32 * kLoadWarp0, cw = warp - kLoadWarp0;
+    if (qi >= 2) {
+      // every other role is done with query qi - 2, whose buffer this reuses
+      if (ct == 0 && ok) {
+        ok = wait_count(&misc->ld_seq, kLoadWarps * (qi - 1), misc, a.status) &&
+             wait_count(&misc->mma_seq, qi - 1, misc, a.status) &&
+             wait_count(&misc->pv_seq, qi - 1, misc, a.status) &&
+             wait_count(&misc->math_seq, qi - 1, misc, a.status);
+      }
+      named_sync(kLoadBar, 32 * kLoadWarps);
+    }
+    const QueryRows qr = query_rows(a, b, ct == 0);
+    const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
+    int32_t* ids = ids_buf(qi);
+    constexpr int kPer = kMaxKTokens / 128;  // 4
+    int my[kPer];
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = ct * kPer + j;
+      int id = -1;
+      if (i < a.k_tokens) {
+        id = tk[i];
+        if (id >= qr.n_vis) {
+          record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+          id = -1;
+        }
+        if (a.pages.table != nullptr && id >= 0) {
+          const int64_t row = paged_row(a.pages, b, id);
+          if (row < 0) {
+            record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
+          }
+          id = static_cast<int>(row);
+        }
+      }
+      my[j] = id;
+      cnt += id >= 0 ? 1 : 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) misc->warp_cnt[cw] = incl;
+    named_sync(kLoadBar, 32 * kLoadWarps);
+    int before = incl - cnt;
+    for (int w = 0; w < cw; ++w) before += misc->warp_cnt[w];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (my[j] >= 0) ids[before++] = my[j];
+    }
+    if (ct == 127) misc->n_sel[qi & 1] = before;
+    named_sync(kLoadBar, 32 * kLoadWarps);
+    if (ct == 0) raise_count(&misc->ids_seq, qi + 1);
+  };
+
   if (warp < kLoadWarp0) {
     // ---------------- math: index lists, softmax, epilogue ----------------
     griddep_wait();  // the previous kernel's token ids are final
     const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
     bool ok = true;
-    // Compacts query index qi's valid token ids (>= 0 and < n_vis; pool rows
-    // when the latents are paged) in order into buffer qi & 1.
-    auto compact = [&](int b, int qi) {
-      if (qi >= 2) {
-        // every other role is done with query qi - 2, whose buffer this reuses
-        if (tid == 0 && ok) {
-          ok = wait_count(&misc->ld_seq, kLoadWarps * (qi - 1), misc, a.status) &&
-               wait_count(&misc->mma_seq, qi - 1, misc, a.status) &&
-               wait_count(&misc->pv_seq, qi - 1, misc, a.status);
-        }
-        named_sync(kMathBar, 128);
-      }
-      const QueryRows qr = query_rows(a, b, tid == 0);
-      const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
-      int32_t* ids = ids_buf(qi);
-      constexpr int kPer = kMaxKTokens / 128;  // 4
-      int my[kPer];
-      int cnt = 0;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int i = tid * kPer + j;
-        int id = -1;
-        if (i < a.k_tokens) {
-          id = tk[i];
-          if (id >= qr.n_vis) {
-            record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
-            id = -1;
-          }
-          if (a.pages.table != nullptr && id >= 0) {
-            const int64_t row = paged_row(a.pages, b, id);
-            if (row < 0) {
-              record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_ATTN, static_cast<uint32_t>(id));
-            }
-            id = static_cast<int>(row);
-          }
-        }
-        my[j] = id;
-        cnt += id >= 0 ? 1 : 0;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (lane == 31) misc->warp_cnt[warp] = incl;
-      named_sync(kMathBar, 128);
-      int before = incl - cnt;
-      for (int w = 0; w < warp; ++w) before += misc->warp_cnt[w];
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        if (my[j] >= 0) ids[before++] = my[j];
-      }
-      if (tid == 127) misc->n_sel[qi & 1] = before;
-      named_sync(kMathBar, 128);
-      if (tid == 0) raise_count(&misc->ids_seq, qi + 1);
-    };
-    if (b0 < a.B) compact(b0, 0);
     int64_t gq = 0;  // this CTA's tile count before the current query
     int qi = 0;
     for (int b = b0; b < a.B; b += gstep, ++qi) {
+      if (tid == 0 && ok) ok = wait_count(&misc->ids_seq, qi + 1, misc, a.status);
+      named_sync(kMathBar, 128);
       const QueryRows qr = query_rows(a, b, false);
       const int n_rows = qr.n_sw + misc->n_sel[qi & 1];
       const int n_tiles = (n_rows + kRows - 1) / kRows;
+      named_sync(kMathBar, 128);  // every math thread has read the tile count
+      if (tid == 0) raise_count(&misc->math_seq, qi + 1);
       float m_run = -INFINITY, l_run = 0.f;  // threads 0..63: head tid
       // PV(j) is known complete through p_empty[j & 1]; the next phase of that
       // barrier needs P(j + 2), written after every wait below, so a parity
@@ -1089,9 +1101,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&misc->p_full[sb]);
         }
       }
-      // The next query's index list first, so the loaders and the issuers go
-      // on with it while this query's epilogue runs.
-      if (b + gstep < a.B) compact(b + gstep, qi + 1);
       // ---------------- epilogue (math warps) ----------------
       if (ok) ok = wait_bar_s(&misc->o_done, static_cast<uint32_t>(qi & 1), misc, a.status);
       tc_fence_after();
@@ -1149,19 +1158,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kWarpRows = kRows / kLoadWarps;
     const int w = warp - kLoadWarp0;
     bool ok = true;
+    griddep_wait();  // the previous kernel's token ids are final
+    if (b0 < a.B) compact(b0, 0, ok);
     int64_t gq = 0;
     int qi = 0;
-    for (int b = b0; b < a.B && ok; b += gstep, ++qi) {
-      if (!wait_count(&misc->ids_seq, qi + 1, misc, a.status)) {
-        ok = false;
-        break;
-      }
+    // Every loader warp goes through every query (and every compaction's
+    // barriers), also after a failed wait, which only skips its copies.
+    for (int b = b0; b < a.B; b += gstep, ++qi) {
       const QueryRows qr = query_rows(a, b, false);
       const int32_t* ids = ids_buf(qi);
       const int w_cnt = qr.n_sw;
       const int n_rows = w_cnt + misc->n_sel[qi & 1];
       const int n_tiles = (n_rows + kRows - 1) / kRows;
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = 0; t < n_tiles && ok; ++t) {
         const int64_t g = gq + t;
         const int sl = static_cast<int>(g % kSlots);
         const uint32_t u = static_cast<uint32_t>(g / kSlots);
@@ -1210,6 +1219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicAdd(&misc->ld_seq, 1);  // this warp no longer reads query qi's list
       }
       gq += n_tiles;
+      // the next query's list, while this query's last tiles are computed
+      if (b + gstep < a.B) compact(b + gstep, qi + 1, ok);
     }
   } else if (warp == kMmaWarp) {
     // ---------------- QK^T issuer (and Q loads) ----------------
