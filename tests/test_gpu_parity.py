@@ -285,6 +285,39 @@ def test_decode_step_is_deterministic_and_updates_the_pool(fmt, k_blocks):
     assert d.status()[0] == 0
 
 
+@pytest.mark.parametrize("fmt,B,t_max,k_blocks", [
+    ("mxfp8", 40, 40000, 256),   # 40 tiles a sequence: a CTA holds at most one last block
+    ("mxfp4", 300, 1000, 16),    # one tile a sequence: some CTAs hold two last blocks
+    ("bf16", 300, 1000, 16),
+])
+def test_decode_step_tail_update_many_sequences(fmt, B, t_max, k_blocks):
+    """The step's tail update over many sequences, right before a block scan
+    whose CTAs each cover one or several sequences' last blocks. Every
+    sequence's newest block key is clobbered; after the step the block keys
+    equal those the pooling kernel writes for the whole cache, bit for bit,
+    for ragged lengths (multiples of 8, a single token, the longest), and the
+    step's outputs agree with the oracle on a sample."""
+    rng = np.random.default_rng(3000 + B)
+    T = [int(t) for t in rng.integers(1, t_max, B)]
+    T[0], T[1], T[2] = t_max, 8 * (t_max // 16), 1
+    inp = synth.decode_inputs(T, 1, fmt, seed=70 + B)
+    cfg = dsa.config(k_blocks=k_blocks, k_tokens=64)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    ref_pool = d.pooled.data.clone()
+    ref_scales = None if d.pooled.scales is None else d.pooled.scales.clone()
+    for b, n in enumerate(inp.n_latents):
+        d.pooled.data[b, (int(n) - 1) // 8] = 0
+        if d.pooled.scales is not None:
+            d.pooled.scales[b, (int(n) - 1) // 8] = 0
+    outs = run_step(d, cfg, update_pool=True)
+    assert d.status()[0] == 0
+    assert torch.equal(d.pooled.data, ref_pool)
+    if ref_scales is not None:
+        assert torch.equal(d.pooled.scales, ref_scales)
+    check_step(inp, cfg, outs, [0, 1, 2, B // 2, B - 1])
+
+
 @pytest.mark.parametrize("fmt,k_blocks", [("mxfp8", 256), ("bf16", 2048)])
 def test_decode_step_replays_from_a_cuda_graph(fmt, k_blocks):
     """The whole step captured once in a CUDA graph, programmatic launch edges
@@ -565,6 +598,53 @@ def test_select_thousands_of_candidates(T, fmt, k_blocks, outliers):
         r = O.decode_sequence(oc, inp, b, with_attention=False, block_ids=bids_h[b])
         pos = {int(t): s for t, s in zip(r["cand"], r["token_scores"])}
         check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
+
+
+@pytest.mark.parametrize("B", [3, 30, 50, 100])
+def test_select_cluster_paths(B):
+    """A query's candidates are split over a cluster of 4 or 2 CTAs while the
+    B clusters fit the SMs at once (one CTA a query beyond), each CTA holding a
+    contiguous share; the CTAs merge their key ranges, histograms, members of
+    the threshold bin and output offsets. Token selection over every latent of
+    ragged sequences of 200-9000 latents (a share of 4096 candidates a CTA
+    leaves the fourth CTA of a 9000-latent query with none), with: every score
+    tied in some sequences (w = 0: the lowest ids win across the CTAs),
+    outlier keys in others (the value-space bins degenerate and the radix
+    levels run), and a sequence with fewer latents than k (-1 padding). The ids
+    must equal the top-k of the scores the GPU returned (score desc, index
+    asc), and two sequences' scores are checked against the oracle."""
+    rng = np.random.default_rng(2000 + B)
+    T = [int(t) for t in rng.integers(300, 9000, B)]
+    T[0], T[-1] = 9000, 200
+    inp = synth.decode_inputs(T, 1, "mxfp8", seed=60 + B)
+    for b in range(1, B, 5):
+        inp.w[b] = 0.0
+    for b in range(2, B, 5):
+        for t in rng.integers(0, T[b], 3):
+            scale_key_row(inp, b, int(t), 12)
+    cfg = dsa.config(k_tokens=512, ratio=1)
+    d = DecodeOnDevice(inp, cfg)
+    n_cand = (d.cap + 7) // 8 * 8
+    tok = torch.empty((B, 512), dtype=torch.int32, device="cuda")
+    tsc = torch.empty((B, n_cand), dtype=torch.float32, device="cuda")
+    dsa.topk(cfg, d.q_idx, d.w, d.keys, None, d.n_lat, d.cap, tok, d.ws, token_scores=tsc)
+    assert d.status()[0] == 0
+    tok_h, tsc_h = tok.cpu().numpy(), tsc.cpu().numpy()
+    for b in range(B):
+        assert np.isneginf(tsc_h[b, T[b]:]).all(), f"scores past the sequence {b}"
+        assert np.array_equal(tok_h[b], top_k_of(tsc_h[b], 512)), f"tokens {b} vs own scores"
+        if inp.w[b].max() == 0.0:
+            assert tok_h[b].tolist() == list(range(min(512, T[b]))) + [-1] * max(0, 512 - T[b])
+    assert tok_h[B - 1].tolist() == list(range(200)) + [-1] * 312
+    oc = oracle_cfg(cfg)
+    for b in (0, 2):
+        single = O.select_query(O.StepConfig(k_blocks=1 << 20, k_tokens=512), inp.q_idx[b],
+                                inp.w[b], O.decode_keys("mxfp8", inp.keys.data[b][:T[b]],
+                                                        inp.keys.scales[b][:T[b]]),
+                                np.zeros(((T[b] + 7) // 8, 128)), T[b])
+        check_scores(tsc_h[b, :T[b]], single["token_scores"], f"token scores {b}")
+        pos = {int(t): s for t, s in zip(single["cand"], single["token_scores"])}
+        check_ids(tok_h[b], single["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
 
 
 # ---------------------------------------------------------------------------

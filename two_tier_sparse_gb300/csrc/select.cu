@@ -3,8 +3,10 @@
 // recipes.vllm.ai "DeepSeek-V4.1-Flash", Overview, "Two-tier sparse attention";
 // ties to the lower index, the rule this library fixes).
 //
-// One CTA per query. Scores map to order-preserving 32-bit keys (larger score,
-// larger key; -0 as +0). The selection then works on exact integers
+// One CTA per query (the register-resident kernel: a cluster of 2 or 4 CTAs
+// per query while those clusters fit the SMs at once). Scores map to
+// order-preserving 32-bit keys (larger score, larger key; -0 as +0). The
+// selection then works on exact integers
 // t = key - kmin (kmin the smallest valid key of the query):
 //   1. a radix select on t with 12-bit digits taken from the top of t's range
 //      (so the first histogram already spans the keys' own spread) narrows,
@@ -348,12 +350,20 @@ __device__ __forceinline__ uint32_t value_bin(float v, float vmin, float vscale)
   return min(__float_as_uint(t) - 0x4B000000u, static_cast<uint32_t>(kBins - 1));
 }
 
+constexpr int kMaxCluster = 4;  // CTAs a query's selection may be split over
+
+// Arrays indexed [source CTA][...] are filled, for every CTA of a cluster, by
+// the CTA that owns the values (its own entries locally, the others' by
+// stores into their shared memory) before a cluster barrier; after it every
+// CTA reads them locally.
 struct RegShared {
-  uint32_t hist[kBins];
-  uint32_t bin_key[kRankMax];
-  uint32_t bin_idx[kRankMax];
+  alignas(16) uint32_t hist[kBins];
   uint32_t taken[kThreads];  // bit i: candidate i of the final bin is selected (n <= 32 x 1024)
-  uint32_t warp_a[kWarps], warp_b[kWarps], warp_c[kWarps];
+  uint32_t warp_a[kWarps];
+  uint4 stat[kMaxCluster][kWarps];      // per warp: smallest and largest valid key, valid count
+  uint2 bin[kMaxCluster][kRankMax];     // members of the threshold bin: key, candidate index
+  uint2 tot[kMaxCluster][kWarps];       // per warp: candidates output above the bin, tied members
+  uint32_t bin_src[kMaxCluster];        // the threshold bin's members in each CTA's share
   uint32_t bstar, need, count, nbin;
 };
 
@@ -366,7 +376,19 @@ __device__ __forceinline__ uint32_t warps_before(uint32_t v_lane, int warp, uint
   return __shfl_sync(0xFFFFFFFFu, incl - v_lane, warp);
 }
 
-template <int KPT>
+// CL > 1: a query's candidates are split over a cluster of CL CTAs, rank r
+// holding [r * KPT * 1024, (r + 1) * KPT * 1024). Through distributed shared
+// memory the CTAs exchange their key ranges and valid counts, their members
+// of the threshold bin and their output totals (each CTA stores its values
+// into every CTA's copy before a cluster barrier), and read one another's
+// histograms in place (after a cluster barrier; another comes before a
+// histogram is cleared for the next level). Each CTA so takes the decisions
+// one CTA over all the candidates would, and writes its own part of the
+// ascending output. A cluster barrier costs about as much as a remote read
+// round trip (~0.4-0.6 us), so small values are pushed; the 16 KB histogram
+// is cheaper to read in place than to push. (Plain and second-pass
+// selections only.)
+template <int KPT, int CL>
 __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   __shared__ RegShared sh;
   extern __shared__ int32_t bids[];  // token stage: the query's block ids
@@ -378,15 +400,25 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   if (tid == 0) sh.nbin = 0;
   griddep_wait();
   // The CTA's candidates: all of query b's (plain), chunk c of them (first
-  // pass of a two-pass selection), or the ids the first pass kept (second).
-  const int b = a.chunks ? static_cast<int>(blockIdx.x / a.chunks) : static_cast<int>(blockIdx.x);
-  const int64_t base = a.chunks ? static_cast<int64_t>(blockIdx.x % a.chunks) * a.chunk : 0;
+  // pass of a two-pass selection), or the ids the first pass kept (second);
+  // with CL > 1, the rank's share of them.
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  const int b = CL > 1 ? static_cast<int>(blockIdx.x / CL)
+                       : (a.chunks ? static_cast<int>(blockIdx.x / a.chunks)
+                                   : static_cast<int>(blockIdx.x));
+  constexpr int kPerCta = KPT * kThreads;
+  const int cbase = static_cast<int>(crank) * kPerCta;  // first candidate of this CTA
+  const int64_t base =
+      CL > 1 ? cbase : (a.chunks ? static_cast<int64_t>(blockIdx.x % a.chunks) * a.chunk : 0);
   // at most KPT x 1024 candidates: 32-bit indices from here on
-  const int n = static_cast<int>(a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n));
+  const int n_all =
+      static_cast<int>(a.in_ids ? a.n_in : (a.chunks ? min(a.chunk, a.n - base) : a.n));
+  const int n = CL > 1 ? max(0, min(n_all - cbase, kPerCta)) : n_all;
   const uint32_t k = static_cast<uint32_t>(a.k);
   const float* sc = a.scores + static_cast<int64_t>(b) * a.n;
-  const int32_t* ids_in = a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in : nullptr;
-  const bool dense = a.dense_stride && a.block_ids;
+  const int32_t* ids_in =
+      a.in_ids ? a.in_ids + static_cast<int64_t>(b) * a.n_in + (CL > 1 ? cbase : 0) : nullptr;
+  const bool dense = CL == 1 && a.dense_stride && a.block_ids;
 
   // The block ids (token stage) are requested first, so their latency
   // overlaps the score loads; they go to shared memory further down.
@@ -422,10 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   } else if (!dense) {
     // all KPT loads go out before any is used (indices clamped into the row)
     float v[KPT];
+    const float* sb = sc + (n > 0 ? base : 0);  // (a cluster rank may hold no candidate)
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       const int i = wbase + 32 * j;
-      v[j] = __ldg(sc + base + (i < n ? i : 0));
+      v[j] = __ldg(sb + (i < n ? i : 0));
     }
 #pragma unroll
     for (int j = 0; j < KPT; ++j) key[j] = score_key(wbase + 32 * j < n ? v[j] : -INFINITY);
@@ -478,41 +511,80 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
   cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
   if (lane == 0) {
-    sh.warp_a[warp] = kmin;
-    sh.warp_b[warp] = kmax;
-    sh.warp_c[warp] = cnt;
+    const uint4 v = make_uint4(kmin, kmax, cnt, 0u);
+    sh.stat[crank][warp] = v;
+#pragma unroll
+    for (uint32_t p = 1; p < CL; ++p) {
+      st_cluster_u4(mapa_shared(smem_u32(&sh.stat[crank][warp]), (crank + p) % CL), v);
+    }
   }
-  __syncthreads();
+  if constexpr (CL > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (a.block_ids) {
     // Ascending block ids with -1 padding at the end are required: the tie
     // rule and the ascending output rely on it.
-    for (int i = tid; i + 1 < a.k_blocks; i += kThreads) {
+    for (int i = static_cast<int>(crank) * kThreads + tid; i + 1 < a.k_blocks;
+         i += CL * kThreads) {
       const int x = bids[i], y = bids[i + 1];
       if (y >= 0 && (x < 0 || y <= x)) {
         record_status(a.status, DSA_ERR_DEVICE_CHECK, SITE_SELECT, static_cast<uint32_t>(i));
       }
     }
   }
-  // every warp reduces the 32 warps' values itself
-  kmin = __reduce_min_sync(0xFFFFFFFFu, sh.warp_a[lane]);
-  kmax = __reduce_max_sync(0xFFFFFFFFu, sh.warp_b[lane]);
-  const uint32_t n_valid = __reduce_add_sync(0xFFFFFFFFu, sh.warp_c[lane]);
+  // every warp reduces the 32 warps' values (of every CTA of the cluster) itself
+  uint32_t smin = 0xFFFFFFFFu, smax = 0u, scnt = 0u;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) {
+    const uint4 v = sh.stat[r][lane];
+    smin = min(smin, v.x);
+    smax = max(smax, v.y);
+    scnt += v.z;
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, smin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, smax);
+  const uint32_t n_valid = __reduce_add_sync(0xFFFFFFFFu, scnt);
   const bool take_all = n_valid <= k;
   const uint32_t span = kmax - kmin;
   uint32_t P = 0, s_cur = 32, need = k;
   bool ties = false;
+  // A thread's four histogram words: digits 4092 - 4 tid .. 4095 - 4 tid
+  const uint32_t hoff = static_cast<uint32_t>(kBins - 4 - 4 * tid) * 4u;
+  // The histograms are complete: a barrier (CL = 1) or a cluster barrier.
+  auto hist_done = [&]() {
+    if constexpr (CL > 1) {
+      cluster_sync();
+    } else {
+      __syncthreads();
+    }
+  };
   // Threshold search over a histogram in sh.hist: the bin holding the
-  // nd-th largest key, counted from the top bin down. The caller has synced
-  // after filling the histogram; this ends with a barrier after which
+  // nd-th largest key, counted from the top bin down. hist_done has run
+  // after the histogram was filled; this ends with a barrier after which
   // sh.bstar / sh.need / sh.count hold the bin, the count still needed in it
   // and its size. (sh.warp_a is rewritten: its readers are behind a barrier.)
+  // With CL > 1 the histogram is the sum of the cluster's CTAs' ones (read in
+  // place), and sh.bin_src[r] is the bin's count in CTA r's.
   auto find_threshold = [&](uint32_t nd) {
-    uint32_t h[4], local = 0;
+    uint4 hr[CL];  // [p]: the words of CTA (crank + p) % CL
+    hr[0] = ld_shared_v4(smem_u32(sh.hist) + hoff);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      h[j] = sh.hist[kBins - 1 - (4 * tid + j)];
-      local += h[j];
+    for (uint32_t p = 1; p < CL; ++p) {
+      hr[p] = ld_cluster_v4(mapa_shared(smem_u32(sh.hist) + hoff, (crank + p) % CL));
     }
+    uint4 hv = hr[0];
+#pragma unroll
+    for (int p = 1; p < CL; ++p) {
+      hv.x += hr[p].x;
+      hv.y += hr[p].y;
+      hv.z += hr[p].z;
+      hv.w += hr[p].w;
+    }
+    // h[j] = digit 4095 - 4 tid - j
+    uint32_t h[4] = {hv.w, hv.z, hv.y, hv.x};
+    const uint32_t local = h[0] + h[1] + h[2] + h[3];
     const uint32_t incl = warp_incl_scan(local);
     if (lane == 31) sh.warp_a[warp] = incl;
     __syncthreads();
@@ -524,6 +596,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         sh.bstar = static_cast<uint32_t>(kBins - 1 - (4 * tid + j));
         sh.need = nd - run;
         sh.count = h[j];
+        if constexpr (CL > 1) {
+#pragma unroll
+          for (uint32_t p = 0; p < CL; ++p) {
+            const uint4 v = hr[p];
+            sh.bin_src[(crank + p) % CL] = j == 0 ? v.w : (j == 1 ? v.z : (j == 2 ? v.y : v.x));
+          }
+        }
       }
       run += h[j];
     }
@@ -553,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
           atomicAdd(&sh.hist[bj], 1u);
         }
       }
-      __syncthreads();
+      hist_done();
       find_threshold(need);
       if (sh.count <= kRankMax) {
         vspace = true;
@@ -569,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       const uint32_t hs = s_cur, s_lv = s_next;
       const uint32_t width = hs - s_lv;
       const uint32_t dmask = width >= 32 ? 0xFFFFFFFFu : (1u << width) - 1u;
+      // (the cluster's CTAs have read this histogram's previous contents)
+      if constexpr (CL > 1) cluster_sync();
       for (int i = tid; i < kBins; i += kThreads) sh.hist[i] = 0;
       __syncthreads();
 #pragma unroll
@@ -578,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
           if (hs >= 32 || (t >> hs) == P) atomicAdd(&sh.hist[(t >> s_lv) & dmask], 1u);
         }
       }
-      __syncthreads();
+      hist_done();
       find_threshold(need);
       P = (hs < 32 ? (P << width) : 0u) | sh.bstar;
       need = sh.need;
@@ -593,6 +674,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       __syncthreads();
     }
   }
+  // A member of the threshold bin into this CTA's list, and (CL > 1) into the
+  // other CTAs' copies of it.
+  auto list_member = [&](uint32_t key_j, uint32_t idx) {
+    const uint32_t slot = atomicAdd(&sh.nbin, 1u);
+    const uint2 m = make_uint2(key_j, idx);
+    sh.bin[crank][slot] = m;
+#pragma unroll
+    for (uint32_t p = 1; p < CL; ++p) {
+      st_cluster_u2(mapa_shared(smem_u32(&sh.bin[crank][slot]), (crank + p) % CL), m);
+    }
+  };
   // Classification against the threshold bin, as warp ballots over slot j:
   // gt_mask[j] = candidates strictly above the bin. The bin's members either
   // all tie (then the first `need` of them in index order are taken, and
@@ -612,9 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       const uint32_t bj = bin_of(j);
       gt_mask[j] = __ballot_sync(0xFFFFFFFFu, valid && bj > vbin);
       if (valid && bj == vbin) {  // a value-space bin is always ranked (never ties)
-        const uint32_t slot = atomicAdd(&sh.nbin, 1u);
-        sh.bin_key[slot] = key[j];
-        sh.bin_idx[slot] = static_cast<uint32_t>(wbase + 32 * j);
+        list_member(key[j], static_cast<uint32_t>(cbase + wbase + 32 * j));
       }
     }
   } else {
@@ -629,36 +719,61 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         if (lane == 0) sh.taken[warp * KPT + j] = e;
         e_w += __popc(e);
       } else if (inb) {
-        const uint32_t slot = atomicAdd(&sh.nbin, 1u);
-        sh.bin_key[slot] = key[j];
-        sh.bin_idx[slot] = static_cast<uint32_t>(wbase + 32 * j);
+        list_member(key[j], static_cast<uint32_t>(cbase + wbase + 32 * j));
       }
     }
     if (ties) __syncwarp();  // lane 0's words, read by the whole warp below
   }
+  // a candidate index of this CTA's share: its bit in sh.taken
+  auto mark_taken = [&](uint32_t ie) {
+    const uint32_t li = ie - static_cast<uint32_t>(cbase);
+    if (li < static_cast<uint32_t>(kPerCta)) atomicOr(&sh.taken[li >> 5], 1u << (li & 31));
+  };
   if (collect) {
-    __syncthreads();
-    const uint32_t c = sh.nbin;
+    // Members listed by each CTA: this one's own count, or (CL > 1) CTA r's
+    // count in the final level's threshold bin.
+    uint32_t cs[CL];
+    if constexpr (CL > 1) {
+#pragma unroll
+      for (int r = 0; r < CL; ++r) cs[r] = sh.bin_src[r];
+      cluster_sync();  // every CTA's members are in every list
+    } else {
+      __syncthreads();
+      cs[0] = sh.nbin;
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) c += cs[r];
+    // member m of the lists taken in CTA order
+    auto member = [&](uint32_t m) -> uint2 {
+      int r = 0;
+#pragma unroll
+      for (int q = 0; q + 1 < CL; ++q) {
+        if (r == q && m >= cs[q]) {
+          m -= cs[q];
+          r = q + 1;
+        }
+      }
+      return sh.bin[r][m];
+    };
     if (need >= c) {
       // every member is taken
-      if (static_cast<uint32_t>(tid) < c) {
-        const uint32_t ie = sh.bin_idx[tid];
-        atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
-      }
+      if (static_cast<uint32_t>(tid) < c) mark_taken(member(tid).y);
     } else {
       const uint32_t mi = static_cast<uint32_t>(tid >> 4), part = static_cast<uint32_t>(tid & 15);
       uint32_t rank = 0, ke = 0, ie = 0;
       if (mi < c) {
-        ke = sh.bin_key[mi];
-        ie = sh.bin_idx[mi];
+        const uint2 me = member(mi);
+        ke = me.x;
+        ie = me.y;
         for (uint32_t o = part; o < c; o += 16) {
-          const uint32_t ko = sh.bin_key[o];
-          rank += (ko > ke || (ko == ke && sh.bin_idx[o] < ie)) ? 1u : 0u;
+          const uint2 mo = member(o);
+          rank += (mo.x > ke || (mo.x == ke && mo.y < ie)) ? 1u : 0u;
         }
       }
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
-      if (part == 0 && mi < c && rank < need) atomicOr(&sh.taken[ie >> 5], 1u << (ie & 31));
+      if (part == 0 && mi < c && rank < need) mark_taken(ie);
     }
     __syncthreads();
 #pragma unroll
@@ -671,28 +786,60 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
   // order) this warp's output offset and its share of the ties taken at the
   // threshold.
   if (lane == 0) {
-    sh.warp_a[warp] = g_w;
-    sh.warp_b[warp] = e_w;
+    const uint2 v = make_uint2(g_w, e_w);
+    sh.tot[crank][warp] = v;
+#pragma unroll
+    for (uint32_t p = 1; p < CL; ++p) {
+      st_cluster_u2(mapa_shared(smem_u32(&sh.tot[crank][warp]), (crank + p) % CL), v);
+    }
   }
-  __syncthreads();
+  // (CL > 1: the last exchange; no CTA touches another's shared memory after it)
+  if constexpr (CL > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   uint32_t total, te_w;
   uint32_t pos;
   {
     const uint32_t take_eq_total = ties ? need : 0u;
-    const uint32_t e = sh.warp_b[lane], g = sh.warp_a[lane];
-    const uint32_t e_before = warp_incl_scan(e) - e;  // ties in the warps before warp `lane`
+    const uint2 own = sh.tot[crank][lane];
+    const uint32_t e = own.y, g = own.x;
+    // CL > 1: the CTAs of lower rank hold the lower candidate indices, so
+    // their ties come first and their output goes first.
+    uint32_t e_cta = 0, s_cta = 0, s_all = 0;  // ties and output before this CTA; all output
+    if constexpr (CL > 1) {
+      uint32_t e_acc = 0;
+#pragma unroll
+      for (uint32_t r = 0; r < CL; ++r) {
+        const uint2 v = sh.tot[r][lane];
+        const uint32_t e_r = __reduce_add_sync(0xFFFFFFFFu, v.y);
+        const uint32_t g_r = __reduce_add_sync(0xFFFFFFFFu, v.x);
+        const uint32_t te_r = take_eq_total > e_acc ? min(e_r, take_eq_total - e_acc) : 0u;
+        if (r < crank) {
+          e_cta += e_r;
+          s_cta += g_r + te_r;
+        }
+        s_all += g_r + te_r;
+        e_acc += e_r;
+      }
+    }
+    // ties in the warps before warp `lane`
+    const uint32_t e_before = e_cta + warp_incl_scan(e) - e;
     const uint32_t te = take_eq_total > e_before ? min(e, take_eq_total - e_before) : 0u;
     const uint32_t sel = g + te;
-    pos = warps_before(sel, warp, &total);  // output offset of this warp
+    pos = s_cta + warps_before(sel, warp, &total);  // output offset of this warp
+    if constexpr (CL > 1) total = s_all;
     te_w = __shfl_sync(0xFFFFFFFFu, te, warp);  // ties this warp takes
   }
   // First pass: row b * chunks + c of the scratch, i.e. row blockIdx.x.
-  int32_t* out = a.out_ids + static_cast<int64_t>(blockIdx.x) * a.k;
+  int32_t* out = a.out_ids + static_cast<int64_t>(CL > 1 ? b : static_cast<int>(blockIdx.x)) * a.k;
   const uint32_t lt = (1u << lane) - 1u;
   auto out_id = [&](int j) -> int32_t {
     const int i = wbase + 32 * j;
     if (ids_in) return ids_in[i];
-    return a.block_ids ? bids[i >> 3] * 8 + static_cast<int32_t>(i & 7)
+    const int gi = cbase + i;  // the candidate's index within the query
+    return a.block_ids ? bids[gi >> 3] * 8 + static_cast<int32_t>(gi & 7)
                        : static_cast<int32_t>(base + i);
   };
   if (!ties) {
@@ -707,8 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
         ow += __popc(m);
       }
     } else if (a.block_ids) {
-      // candidate wbase + 32 j is token (lane & 7) of kept block (wbase >> 3) + 4 j
-      const int32_t* bw = bids + (wbase >> 3);
+      // candidate cbase + wbase + 32 j is token (lane & 7) of kept block
+      // ((cbase + wbase) >> 3) + 4 j
+      const int32_t* bw = bids + ((cbase + wbase) >> 3);
       const int32_t r = lane & 7;
 #pragma unroll
       for (int j = 0; j < KPT; ++j) {
@@ -741,32 +889,117 @@ __global__ void __launch_bounds__(kThreads, 1) select_reg_kernel(SelectArgs a) {
       eq_seen += __popc(eqm);
     }
   }
-  for (int j = static_cast<int>(total) + tid; j < a.k; j += kThreads) out[j] = -1;
+  for (int j = static_cast<int>(total) + static_cast<int>(crank) * kThreads + tid; j < a.k;
+       j += CL * kThreads) {
+    out[j] = -1;
+  }
 }
 
 }  // namespace
 
-template <int KPT>
+// Dynamic shared memory of a selection CTA: the block ids, then (dense rows,
+// CL = 1 only) the kept blocks' scores.
+constexpr size_t reg_smem_max(int cl) {
+  return static_cast<size_t>(kMaxKBlocks) * 4 + (cl > 1 ? 0 : static_cast<size_t>(kMaxKBlocks) * 8 * 4);
+}
+
+template <int KPT, int CL>
 cudaError_t launch_reg(const SelectArgs& a, unsigned grid, cudaStream_t s) {
-  // block ids, then (dense rows) the kept blocks' scores
   size_t smem = a.block_ids ? static_cast<size_t>(a.k_blocks) * 4 : 0;
-  if (a.block_ids && a.dense_stride) {
+  if (CL == 1 && a.block_ids && a.dense_stride) {
     smem = static_cast<size_t>(kMaxKBlocks) * 4 + static_cast<size_t>(a.k_blocks) * 8 * 4;
   }
   static std::atomic<int> smem_set[64]{};
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT>),
-                              static_cast<int>(kMaxKBlocks * 4 + kMaxKBlocks * 8 * 4), smem_set);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_reg_kernel<KPT, CL>),
+                              static_cast<int>(reg_smem_max(CL)), smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_reg_kernel<KPT>, dim3(grid), dim3(kThreads), smem, s, 1, a);
+  if constexpr (CL == 1) {
+    return launch_pdl(select_reg_kernel<KPT, 1>, dim3(grid), dim3(kThreads), smem, s, 1, a);
+  } else {
+    // clusters of CL consecutive CTAs along x, with programmatic dependent launch
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid * CL);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, select_reg_kernel<KPT, CL>, a);
+  }
 }
 
-// Register-resident selection of m <= 32 * kThreads candidates per CTA.
-cudaError_t launch_reg_for(const SelectArgs& a, int64_t m, unsigned grid, cudaStream_t s) {
-  if (m <= 2 * kThreads) return launch_reg<2>(a, grid, s);
-  if (m <= 4 * kThreads) return launch_reg<4>(a, grid, s);
-  if (m <= 8 * kThreads) return launch_reg<8>(a, grid, s);
-  if (m <= 16 * kThreads) return launch_reg<16>(a, grid, s);
-  return launch_reg<32>(a, grid, s);
+// Register-resident selection of m <= 32 * kThreads candidates per CTA, one
+// CTA (cl = 1) or a cluster of cl CTAs (2 or 4) per query.
+cudaError_t launch_reg_for(const SelectArgs& a, int64_t m, unsigned grid, cudaStream_t s,
+                           int cl = 1) {
+  if (cl == 2 || cl == 4) {
+    const int64_t per = (m + cl - 1) / cl;
+    if (per <= 2 * kThreads) return cl == 2 ? launch_reg<2, 2>(a, grid, s) : launch_reg<2, 4>(a, grid, s);
+    if (per <= 4 * kThreads) return cl == 2 ? launch_reg<4, 2>(a, grid, s) : launch_reg<4, 4>(a, grid, s);
+    if (per <= 8 * kThreads) return cl == 2 ? launch_reg<8, 2>(a, grid, s) : launch_reg<8, 4>(a, grid, s);
+    if (per <= 16 * kThreads && cl == 2) return launch_reg<16, 2>(a, grid, s);
+    return cudaErrorInvalidValue;  // (m <= 32 * kThreads: not reached)
+  }
+  if (m <= 2 * kThreads) return launch_reg<2, 1>(a, grid, s);
+  if (m <= 4 * kThreads) return launch_reg<4, 1>(a, grid, s);
+  if (m <= 8 * kThreads) return launch_reg<8, 1>(a, grid, s);
+  if (m <= 16 * kThreads) return launch_reg<16, 1>(a, grid, s);
+  return launch_reg<32, 1>(a, grid, s);
+}
+
+// CTAs per query of a register-resident selection: a query's candidates are
+// split over a cluster of 2 or 4 CTAs while the clusters of all B queries
+// still fit on the SMs at once and each CTA keeps at least 2048 candidates
+// (the per-candidate work, which bounds the kernel, then shrinks with the
+// split; the cluster exchanges cost a few barriers). Not for first passes
+// (chunks) or dense score rows.
+// Clusters of `cl` selection CTAs (each a whole SM) that can be resident at once.
+int select_max_clusters(int cl) {
+  static std::atomic<int> cache[64][2]{};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int k = cl == 2 ? 0 : 1;
+  int n = cache[dev][k].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = reg_smem_max(cl);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cl);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  const void* kern = cl == 2 ? reinterpret_cast<const void*>(select_reg_kernel<8, 2>)
+                             : reinterpret_cast<const void*>(select_reg_kernel<4, 4>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(reg_smem_max(cl)));
+  if (e == cudaSuccess) {
+    e = cl == 2 ? cudaOccupancyMaxActiveClusters(&n, select_reg_kernel<8, 2>, &cfg)
+                : cudaOccupancyMaxActiveClusters(&n, select_reg_kernel<4, 4>, &cfg);
+  }
+  if (e != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the error the failed query left behind
+    n = device_sm_count() / cl / 2;
+  }
+  cache[dev][k].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int select_cluster(const SelectArgs& a, int64_t m) {
+  if (a.chunks || a.dense_stride) return 1;
+  int cl = 1;
+  while (cl < 4 && m >= int64_t{2048} * cl * 2 && a.B <= select_max_clusters(cl * 2)) cl *= 2;
+  return cl;
 }
 
 constexpr int64_t kRegMax = 32 * kThreads;  // candidates a register-resident CTA holds
@@ -776,7 +1009,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
   if (launches) *launches = 0;
   if (a.B == 0) return cudaSuccess;
   if (launches) *launches = 1;
-  if (a.n <= kRegMax) return launch_reg_for(a, a.n, a.B, s);
+  if (a.n <= kRegMax) return launch_reg_for(a, a.n, a.B, s, select_cluster(a, a.n));
   if (a.dense_stride) return cudaErrorInvalidValue;  // dense rows: register-resident kernel only
   // Two passes over C chunks: every query's best k lies within the best k of
   // its own chunk (same order, same ids), so the second pass over the C * k
@@ -799,7 +1032,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
       p2.in_ids = a.tmp;
       p2.n_in = C * a.k;
       if (launches) *launches = 2;
-      return launch_reg_for(p2, p2.n_in, a.B, s);
+      return launch_reg_for(p2, p2.n_in, a.B, s, select_cluster(p2, p2.n_in));
     }
   }
   const int use_cache = a.n <= kCacheMax ? 1 : 0;
