@@ -600,8 +600,9 @@ def test_select_thousands_of_candidates(T, fmt, k_blocks, outliers):
         check_ids(tok_h[b], r["token_ids"], lambda i: pos[i], 512, f"tokens {b}")
 
 
-@pytest.mark.parametrize("B", [3, 30, 50, 100])
-def test_select_cluster_paths(B):
+@pytest.mark.parametrize("B,t_max", [(3, 9000), (30, 9000), (50, 9000), (100, 9000),
+                                     (100, 5000), (100, 6000)])
+def test_select_cluster_paths(B, t_max):
     """A query's candidates are split over a cluster of 4 or 2 CTAs while the
     B clusters fit the SMs at once (one CTA a query beyond), each CTA holding a
     contiguous share; the CTAs merge their key ranges, histograms, members of
@@ -612,10 +613,12 @@ def test_select_cluster_paths(B):
     outlier keys in others (the value-space bins degenerate and the radix
     levels run), and a sequence with fewer latents than k (-1 padding). The ids
     must equal the top-k of the scores the GPU returned (score desc, index
-    asc), and two sequences' scores are checked against the oracle."""
-    rng = np.random.default_rng(2000 + B)
-    T = [int(t) for t in rng.integers(300, 9000, B)]
-    T[0], T[-1] = 9000, 200
+    asc), and two sequences' scores are checked against the oracle. At 100
+    queries one CTA takes a query; 5000 and 6000 candidates run the 5- and
+    6-slot variants."""
+    rng = np.random.default_rng(2000 + B + t_max)
+    T = [int(t) for t in rng.integers(300, t_max, B)]
+    T[0], T[-1] = t_max, 200
     inp = synth.decode_inputs(T, 1, "mxfp8", seed=60 + B)
     for b in range(1, B, 5):
         inp.w[b] = 0.0

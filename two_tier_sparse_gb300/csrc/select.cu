@@ -949,6 +949,9 @@ cudaError_t launch_reg_for(const SelectArgs& a, int64_t m, unsigned grid, cudaSt
   }
   if (m <= 2 * kThreads) return launch_reg<2, 1>(a, grid, s);
   if (m <= 4 * kThreads) return launch_reg<4, 1>(a, grid, s);
+  // (a prefill chunk's block stage: a few blocks over 4096)
+  if (m <= 5 * kThreads) return launch_reg<5, 1>(a, grid, s);
+  if (m <= 6 * kThreads) return launch_reg<6, 1>(a, grid, s);
   if (m <= 8 * kThreads) return launch_reg<8, 1>(a, grid, s);
   if (m <= 16 * kThreads) return launch_reg<16, 1>(a, grid, s);
   return launch_reg<32, 1>(a, grid, s);
