@@ -433,12 +433,27 @@ def select_query(cfg: StepConfig, q_idx_bits, w, key_vals: np.ndarray, pooled_va
                 cand=cand, token_scores=tscores, token_ids=token_ids)
 
 
+def latent_values(rows: np.ndarray, kv_fmt: str = "bf16", kv_scale: float = 1.0) -> np.ndarray:
+    """Latent or window rows as values. bf16: the bit patterns; fp8: E4M3 codes
+    (OCP 8-bit floating point, the e4m3_value table above) times one scale for
+    the whole cache -- the plainest reading of an "fp8" KV cache dtype
+    (recipes.vllm.ai "DeepSeek-V4.1-Flash", serving configurations,
+    --kv-cache-dtype fp8), which names no scale granularity."""
+    if kv_fmt == "bf16":
+        return bf16_to_f64(rows)
+    if kv_fmt == "fp8":
+        return E4M3_TABLE[np.asarray(rows, np.uint8)] * float(kv_scale)
+    raise ValueError(kv_fmt)
+
+
 def attend_query(cfg: StepConfig, q_bits, latents_bits: np.ndarray, token_ids: np.ndarray,
-                 window_bits: np.ndarray):
-    """Attention of one query over its selected latents ++ its window rows."""
+                 window_bits: np.ndarray, kv_fmt: str = "bf16", kv_scale: float = 1.0):
+    """Attention of one query over its selected latents ++ its window rows
+    (both in the cache format kv_fmt, see latent_values)."""
     ids = np.asarray(token_ids, np.int64)
     ids = ids[ids >= 0]
-    kv = np.concatenate([bf16_to_f64(latents_bits[ids]), bf16_to_f64(window_bits)], axis=0)
+    kv = np.concatenate([latent_values(latents_bits[ids], kv_fmt, kv_scale),
+                         latent_values(window_bits, kv_fmt, kv_scale)], axis=0)
     return attend(bf16_to_f64(q_bits), kv, cfg.tau)
 
 
@@ -492,7 +507,8 @@ def decode_sequence(cfg: StepConfig, inp, b: int, with_attention: bool = True,
     if with_attention:
         sw = int(inp.swa_len[b])
         o, lse = attend_query(cfg, inp.q[b], inp.latents[b], r["token_ids_used"],
-                              inp.swa[b][:sw])
+                              inp.swa[b][:sw], getattr(inp, "kv_fmt", "bf16"),
+                              getattr(inp, "kv_scale", 1.0))
         r["out"], r["lse"] = o, lse
     return r
 

@@ -60,6 +60,7 @@ def _load():
         u64, i64, dbl, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
         lib.synth_normal_bf16.argtypes = [u64, u64, i64, i64, dbl, vp]
         lib.synth_normal_f32.argtypes = [u64, u64, i64, i64, dbl, vp]
+        lib.synth_normal_e4m3.argtypes = [u64, u64, i64, i64, dbl, dbl, vp]
         lib.synth_uniform_f32.argtypes = [u64, u64, i64, i64, vp]
         lib.synth_normal_mxfp8.argtypes = [u64, u64, i64, i64, ctypes.c_int, dbl, vp, vp]
         lib.synth_normal_mxfp4.argtypes = [u64, u64, i64, i64, ctypes.c_int, dbl, vp, vp]
@@ -89,6 +90,16 @@ def normal_f32(seed: int, tag: int, offset: int, n: int, scale: float) -> np.nda
     out = np.empty(n, np.float32)
     if n:
         _load().synth_normal_f32(seed, tag, offset, n, scale, _ptr(out))
+    return out
+
+
+def normal_e4m3(seed: int, tag: int, offset: int, n: int, scale: float, kv_scale: float,
+                out=None) -> np.ndarray:
+    """E4M3 codes (round to nearest even) of fp32(scale * N(0,1)) / kv_scale,
+    the counters of normal_f32: an fp8 cache with one power-of-two scale."""
+    out = np.empty(n, np.uint8) if out is None else out
+    if n:
+        _load().synth_normal_e4m3(seed, tag, offset, n, scale, kv_scale, _ptr(out))
     return out
 
 
@@ -165,6 +176,10 @@ class DecodeInputs:
     swa_len: np.ndarray        # int32 [B]
     window: int = WINDOW
     meta: dict = field(default_factory=dict)
+    # "fp8": latents and window rows are E4M3 codes (uint8 [.., 512]) standing
+    # for code * kv_scale
+    kv_fmt: str = "bf16"
+    kv_scale: float = 1.0
 
     @property
     def B(self) -> int:
@@ -177,7 +192,8 @@ class DecodeInputs:
 
 def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
                   q_scale: float = 1.0, cap: Optional[int] = None,
-                  poison_tail: bool = True) -> DecodeInputs:
+                  poison_tail: bool = True, kv_fmt: str = "bf16",
+                  kv_scale: float = 2.0 ** -6) -> DecodeInputs:
     """Build the synthetic decode workload.
 
     T: tokens per sequence (list). cap: latent rows allocated per sequence
@@ -185,6 +201,8 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
     the N(0,1)/sqrt(512) query (the "sharpened" variants use 8).
     poison_tail fills rows past each sequence's end with +inf (bf16) or the
     largest MXFP8 or MXFP4 value, so a kernel that reads them gives a visibly wrong result.
+    kv_fmt "fp8": latents and window rows are the E4M3 codes of the same
+    N(0,1)/sqrt(512) values divided by kv_scale (rows past the end: 448).
     """
     T = np.asarray(T, np.int64).reshape(-1)
     B = int(T.shape[0])
@@ -197,8 +215,11 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
     q = np.empty((B, N_HEADS, LATENT_DIM), np.uint16)
     q_idx = np.empty((B, N_IDX_HEADS, IDX_DIM), np.uint16)
     w = np.empty((B, N_IDX_HEADS), np.float32)
-    lat = np.empty((B, cap, LATENT_DIM), np.uint16)
-    swa = np.zeros((B, window, LATENT_DIM), np.uint16)
+    if kv_fmt not in ("bf16", "fp8"):
+        raise ValueError(kv_fmt)
+    fp8 = kv_fmt == "fp8"
+    lat = np.empty((B, cap, LATENT_DIM), np.uint8 if fp8 else np.uint16)
+    swa = np.zeros((B, window, LATENT_DIM), np.uint8 if fp8 else np.uint16)
     swa_len = np.minimum(T, window).astype(np.int32)
     if key_fmt == "bf16":
         kdata = np.empty((B, cap, IDX_DIM), np.uint16)
@@ -216,11 +237,18 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
         normal_bf16(seed, TAG_Q, off, N_HEADS * LATENT_DIM, s512 * q_scale, out=q[b].reshape(-1))
         normal_bf16(seed, TAG_QIDX, off, N_IDX_HEADS * IDX_DIM, s128, out=q_idx[b].reshape(-1))
         w[b] = uniform_f32(seed, TAG_W, off, N_IDX_HEADS)
-        normal_bf16(seed, TAG_LAT, off, cap * LATENT_DIM, s512, out=lat[b].reshape(-1))
         n_sw = int(swa_len[b])
-        if n_sw:
-            normal_bf16(seed, TAG_SWA, off, n_sw * LATENT_DIM, s512,
-                        out=swa[b, :n_sw].reshape(-1))
+        if fp8:
+            normal_e4m3(seed, TAG_LAT, off, cap * LATENT_DIM, s512, kv_scale,
+                        out=lat[b].reshape(-1))
+            if n_sw:
+                normal_e4m3(seed, TAG_SWA, off, n_sw * LATENT_DIM, s512, kv_scale,
+                            out=swa[b, :n_sw].reshape(-1))
+        else:
+            normal_bf16(seed, TAG_LAT, off, cap * LATENT_DIM, s512, out=lat[b].reshape(-1))
+            if n_sw:
+                normal_bf16(seed, TAG_SWA, off, n_sw * LATENT_DIM, s512,
+                            out=swa[b, :n_sw].reshape(-1))
         if key_fmt == "bf16":
             normal_bf16(seed, TAG_KEYS, off, cap * IDX_DIM, s128, out=kdata[b].reshape(-1))
         elif key_fmt == "mxfp8":
@@ -231,7 +259,7 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
                          scales=kscales[b])
         if poison_tail:
             n = int(n_lat[b])
-            lat[b, n:] = BF16_POS_INF
+            lat[b, n:] = BF16_POS_INF if kv_fmt == "bf16" else 0x7E
             if key_fmt == "bf16":
                 kdata[b, n:] = BF16_POS_INF
             elif key_fmt == "mxfp8":
@@ -242,7 +270,7 @@ def decode_inputs(T, ratio: int, key_fmt: str, seed: int, window: int = WINDOW,
                 kscales[b, n:] = 254
     return DecodeInputs(T=T, ratio=ratio, q=q, q_idx=q_idx, w=w, latents=lat,
                         keys=Keys(key_fmt, kdata, kscales), swa=swa, n_latents=n_lat,
-                        swa_len=swa_len, window=window)
+                        swa_len=swa_len, window=window, kv_fmt=kv_fmt, kv_scale=kv_scale)
 
 
 @dataclass

@@ -132,6 +132,17 @@ void synth_normal_f32(uint64_t seed, uint64_t tag, int64_t offset, int64_t n, do
 #undef PUT_F32
 }
 
+/* out[i] = e4m3 code of fp32(scale * N(offset + i)) / kv_scale (an fp8 cache
+ * with one scale; kv_scale a power of two, so the division is exact). */
+void synth_normal_e4m3(uint64_t seed, uint64_t tag, int64_t offset, int64_t n, double scale,
+                       double kv_scale, uint8_t* out) {
+  if (n <= 0) return;
+  uint64_t key = stream_key(seed, tag);
+#define PUT_E4M3(i, z) out[i] = e4m3_code((double)(float)(scale * (z)) / kv_scale)
+  FOR_EACH_NORMAL(key, offset, n, PUT_E4M3);
+#undef PUT_E4M3
+}
+
 /* out[i] = k * 2^-24 with k the top 24 bits of draw(offset + i): U[0,1), exact in fp32. */
 void synth_uniform_f32(uint64_t seed, uint64_t tag, int64_t offset, int64_t n, float* out) {
   uint64_t key = stream_key(seed, tag);

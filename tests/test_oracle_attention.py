@@ -171,3 +171,37 @@ def test_prefill_partial_block_is_mean_of_visible_members():
         assert np.array_equal(r["block_ids"], rp["block_ids"])
         assert np.array_equal(r["token_ids"], rp["token_ids"])
         assert (rp["token_ids"][rp["token_ids"] >= 0] < n_vis).all()
+
+
+def test_fp8_cache_rows_are_e4m3_values_times_one_scale():
+    """An fp8 cache row stands for E4M3(code) x kv_scale. Every E4M3 value is
+    exactly a bf16 value (3 mantissa bits of 7), so attending over fp8 rows
+    must equal attending over the bf16 bit patterns of the same values, scaled
+    once: a wrong code table, a scale applied twice or to the query, or window
+    rows left unscaled all break it. The scale is a power of two here, so the
+    bf16 patterns of the scaled values are exact too."""
+    rng = np.random.default_rng(81)
+    codes = rng.integers(0, 256, (300, 512), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C                # no NaN codes
+    win = rng.integers(0, 256, (40, 512), dtype=np.uint8)
+    win[(win & 0x7F) == 0x7F] = 0x41
+    q = synth.normal_bf16(81, 1, 0, 64 * 512, 1 / np.sqrt(512)).reshape(64, 512)
+    ids = np.array([5, 17, 299, -1, 0, 100], np.int64)
+    cfg = O.StepConfig(k_blocks=16, k_tokens=6)
+    for scale in (1.0, 2.0 ** -6, 8.0):
+        o8, l8 = O.attend_query(cfg, q, codes, ids, win, "fp8", scale)
+        vals = O.E4M3_TABLE[codes] * scale
+        wvals = O.E4M3_TABLE[win] * scale
+        bits = O.f32_to_bf16_rne(vals.astype(np.float32))
+        wbits = O.f32_to_bf16_rne(wvals.astype(np.float32))
+        assert np.array_equal(O.bf16_to_f64(bits), vals)  # exact in bf16
+        ob, lb = O.attend_query(cfg, q, bits, ids, wbits)
+        assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+    # a decode step over an fp8 cache attends over those values
+    inp = synth.decode_inputs([900, 33], 1, "bf16", seed=82, kv_fmt="fp8")
+    r = O.decode_sequence(O.StepConfig(k_blocks=16, k_tokens=64), inp, 0)
+    ids = r["token_ids_used"]
+    kv = np.concatenate([O.E4M3_TABLE[inp.latents[0][ids[ids >= 0]]],
+                         O.E4M3_TABLE[inp.swa[0][:int(inp.swa_len[0])]]]) * inp.kv_scale
+    o, lse = O.attend(O.bf16_to_f64(inp.q[0]), kv, O.StepConfig().tau)
+    assert np.array_equal(r["out"], o) and np.array_equal(r["lse"], lse)

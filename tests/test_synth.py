@@ -69,3 +69,15 @@ def test_decode_inputs_with_mxfp4_keys():
     assert abs(k.std() * np.sqrt(128) - 1) < 0.1
     pf = synth.prefill_inputs(20, 100, 2, "mxfp4", seed=4)
     assert pf.keys.data.shape == (64, 64) and pf.keys.fmt == "mxfp4"
+
+
+def test_fp8_cache_codes_match_the_oracle_encoder():
+    """synth's fp8 cache rows (its own C conversion) are the oracle's E4M3
+    encoding of the same fp32 normals divided by the cache scale."""
+    v = synth.normal_f32(5, 3, 100, 200000, 1 / np.sqrt(512))
+    for kv_scale in (2.0 ** -6, 2.0 ** -3, 1.0):
+        c = synth.normal_e4m3(5, 3, 100, 200000, 1 / np.sqrt(512), kv_scale)
+        assert np.array_equal(c, O.e4m3_encode(v.astype(np.float64) / kv_scale))
+    inp = synth.decode_inputs([300, 20], 1, "mxfp8", seed=6, kv_fmt="fp8")
+    assert inp.latents.dtype == np.uint8 and inp.swa.dtype == np.uint8
+    assert (inp.latents[1, 20:] == 0x7E).all()  # the poisoned tail: 448
