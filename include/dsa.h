@@ -96,7 +96,24 @@ typedef struct {
   int window;      /* sliding-window rows: 128 */
   int ratio;       /* positions per compressed latent: 1 or 2 */
   float sm_scale;  /* softmax scale tau; <= 0 selects 1/sqrt(latent_dim) */
+  int kv_fmt;      /* dsa_kv_fmt_t of the latents and window rows the attention reads */
+  float kv_scale;  /* DSA_KV_FP8_E4M3: a row holds code * kv_scale; finite, > 0 */
 } dsa_config_t;
+
+/* Storage of the latent cache and of the window rows (key = value rows of
+ * the attention). The serving pages run an fp8 KV cache (recipes.vllm.ai
+ * "DeepSeek-V4.1-Flash", serving configurations, --kv-cache-dtype fp8) and
+ * name no scale granularity; this library reads it as OCP E4M3 codes with one
+ * scale for the whole cache. fp8 rows are taken by dsa_sparse_attn_decode, its
+ * paged form and dsa_decode_step; the prefill, multi-query and append calls
+ * return DSA_ERR_UNSUPPORTED for them. The attention converts each code to f16
+ * exactly and takes the query to f16 with a power-of-two scale per head (exact
+ * unless an element is below 2^-24 of its head's largest), so its MMAs run on
+ * f16 operands; the probabilities are f16 too (bf16 with bf16 rows). */
+typedef enum {
+  DSA_KV_BF16 = 0,     /* bf16 rows of 512: 1024 bytes a row */
+  DSA_KV_FP8_E4M3 = 1  /* E4M3 codes, 512 bytes a row, standing for code * kv_scale */
+} dsa_kv_fmt_t;
 
 /*
  * Paged layout of a decode batch's caches (a block table, as serving engines

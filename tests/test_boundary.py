@@ -163,7 +163,13 @@ def test_attention_argument_errors(lib):
     bad = dsa.config()
     bad.latent_dim = 256
     assert call(c=bad) == 3
+    # the KV cache format: bf16 or E4M3 with a finite positive scale
+    assert call(c=dsa.config(kv_fmt=2)) == 1
+    assert call(c=dsa.config(kv_fmt=dsa.KV_FP8_E4M3, kv_scale=0.0)) == 1
+    assert call(c=dsa.config(kv_fmt=dsa.KV_FP8_E4M3, kv_scale=float("inf"))) == 1
+    assert call(c=dsa.config(kv_fmt=dsa.KV_FP8_E4M3, kv_scale=float("nan"))) == 1
     assert call(B=0) == 0
+    assert call(B=0, c=dsa.config(kv_fmt=dsa.KV_FP8_E4M3, kv_scale=0.5)) == 0
 
 
 def test_decode_step_argument_errors(lib):
@@ -208,6 +214,8 @@ def test_prefill_argument_errors(lib):
     assert call(ws=None) == 4
     assert call(wsb=4096) == 4
     assert call(nq=0) == 0
+    # an fp8 KV cache is a decode-only format
+    assert call(c=dsa.config(ratio=2, kv_fmt=dsa.KV_FP8_E4M3, kv_scale=1.0)) == 3
 
 
 def test_pool_argument_errors(lib):
@@ -291,6 +299,8 @@ def test_compress_append_argument_errors(lib):
     assert call(stride=99) == 1                         # latent rows a sequence < capacity
     assert call(new=_k(fmt=1, scales=A, stride=1)) == 1  # formats differ
     assert call(B=-1) == 1
+    # the append writes bf16 latents
+    assert call(c=dsa.config(ratio=2, kv_fmt=dsa.KV_FP8_E4M3, kv_scale=1.0)) == 3
 
 
 def test_hooks_and_self_test_argument_errors(lib):

@@ -419,6 +419,34 @@ def test_decode_step_split_paths_sharpened(B):
     check_step(inp, cfg, outs, range(B))
 
 
+@pytest.mark.parametrize("B,fmt", [(5, "mxfp8"), (30, "bf16"), (64, "mxfp4"), (100, "mxfp8")])
+def test_decode_step_fp8_kv_cache(B, fmt):
+    """An fp8 KV cache (latents and window rows as E4M3 codes times one
+    scale): the attention converts the rows to f16 as they land and takes Q to
+    f16 with a power-of-two scale per head. Split over 8, 4 and 2 CTAs a query
+    (B = 5, 30, 64) and, with fp8, over 2 in two waves at B = 100; sharpened
+    (q x 8, tau = 8) so the CTAs' running maxima differ, one window row made to
+    dominate head 0 in every fourth sequence, ragged lengths and a sequence
+    shorter than the window. Every sequence against the oracle."""
+    rng = np.random.default_rng(4000 + B)
+    T = [int(t) for t in rng.integers(900, 4000, B)]
+    T[0], T[-1] = 4000, 70
+    inp = synth.decode_inputs(T, 1, fmt, seed=90 + B, q_scale=8.0, kv_fmt="fp8",
+                              kv_scale=2.0 ** -6)
+    for b in range(0, B, 4):
+        s_ = int(rng.integers(0, inp.swa_len[b]))
+        qh = O.bf16_to_f64(inp.q[b, 0])
+        v = qh / np.sqrt((qh ** 2).sum()) * 0.6 / inp.kv_scale
+        inp.swa[b, s_] = O.e4m3_encode(v)
+    cfg = dsa.config(k_blocks=96, ratio=1, sm_scale=8.0, kv_fmt=dsa.KV_FP8_E4M3,
+                     kv_scale=inp.kv_scale)
+    d = DecodeOnDevice(inp, cfg)
+    d.pool()
+    outs = run_step(d, cfg)
+    assert d.status()[0] == 0
+    check_step(inp, cfg, outs, range(B))
+
+
 # ---------------------------------------------------------------------------
 # Prefill
 # ---------------------------------------------------------------------------

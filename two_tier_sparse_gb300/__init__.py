@@ -52,7 +52,11 @@ class Config(ctypes.Structure):
     _fields_ = [("n_heads", ctypes.c_int), ("latent_dim", ctypes.c_int),
                 ("n_idx_heads", ctypes.c_int), ("idx_dim", ctypes.c_int),
                 ("block", ctypes.c_int), ("k_blocks", ctypes.c_int), ("k_tokens", ctypes.c_int),
-                ("window", ctypes.c_int), ("ratio", ctypes.c_int), ("sm_scale", ctypes.c_float)]
+                ("window", ctypes.c_int), ("ratio", ctypes.c_int), ("sm_scale", ctypes.c_float),
+                ("kv_fmt", ctypes.c_int), ("kv_scale", ctypes.c_float)]
+
+
+KV_BF16, KV_FP8_E4M3 = 0, 1
 
 
 class _Pages(ctypes.Structure):
@@ -129,11 +133,15 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def config(k_blocks=2048, k_tokens=512, window=128, ratio=1, sm_scale=0.0) -> Config:
+def config(k_blocks=2048, k_tokens=512, window=128, ratio=1, sm_scale=0.0, kv_fmt=KV_BF16,
+           kv_scale=1.0) -> Config:
+    """kv_fmt: KV_BF16, or KV_FP8_E4M3 (latents and window rows as E4M3 codes
+    standing for code * kv_scale; decode attention and the decode step only)."""
     c = Config()
     load().dsa_default_config(ctypes.byref(c))
     c.k_blocks, c.k_tokens, c.window, c.ratio = k_blocks, k_tokens, window, ratio
     c.sm_scale = sm_scale
+    c.kv_fmt, c.kv_scale = kv_fmt, kv_scale
     return c
 
 

@@ -75,6 +75,10 @@ dsa_status_t check_config(const dsa_config_t* c) {
       !(c->sm_scale == c->sm_scale) || isinf(c->sm_scale)) {
     return DSA_ERR_INVALID_ARG;
   }
+  if (c->kv_fmt != DSA_KV_BF16 && c->kv_fmt != DSA_KV_FP8_E4M3) return DSA_ERR_INVALID_ARG;
+  if (c->kv_fmt == DSA_KV_FP8_E4M3 && !(c->kv_scale > 0.f && !isinf(c->kv_scale))) {
+    return DSA_ERR_INVALID_ARG;
+  }
   return DSA_OK;
 }
 
@@ -162,8 +166,9 @@ dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA
 // Launch shape of an attention call over n queries: split-KV over the most
 // CTAs per query (8, 4 or 2) whose n clusters are all resident at once, else
 // one; 64-row tiles for prefill chunks, 32-row tiles for decode.
+// An fp8 KV cache (decode only) is read by the split kernel alone: at least
+// two CTAs a query, in several waves when the batch is large.
 void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
-  (void)c;
   a.tile_rows = a.prefill ? 64 : 32;
   a.splits = 1;
   const int sms = device_sm_count();
@@ -173,6 +178,9 @@ void set_splits(AttnArgs& a, const dsa_config_t& c, int n) {
       break;
     }
   }
+  a.kv_fp8 = c.kv_fmt == DSA_KV_FP8_E4M3 ? 1 : 0;
+  a.kv_scale = c.kv_scale;
+  if (a.kv_fp8 && a.splits == 1) a.splits = 2;
 }
 
 #define DSA_TRY(expr)                  \
@@ -466,6 +474,8 @@ void dsa_default_config(dsa_config_t* c) {
   c->window = 128;
   c->ratio = 1;
   c->sm_scale = 0.f;
+  c->kv_fmt = DSA_KV_BF16;
+  c->kv_scale = 1.f;
 }
 
 const char* dsa_status_string(dsa_status_t s) {
@@ -766,6 +776,7 @@ dsa_status_t dsa_sparse_attn_prefill(const dsa_config_t* cfg, int n_q, int64_t c
                                      float* lse, int32_t* token_ids, void* workspace,
                                      size_t workspace_bytes, dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (cfg->kv_fmt != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;  // fp8 caches: decode only
   if (n_q < 0 || ctx_len < 0) return DSA_ERR_INVALID_ARG;
   const int64_t n_lat = (ctx_len + n_q) / cfg->ratio;
   if (n_lat > kMaxLatents) return DSA_ERR_INVALID_ARG;
@@ -828,6 +839,7 @@ dsa_status_t dsa_decode_multi(const dsa_config_t* cfg, int n_q, const int32_t* n
                               int32_t* token_ids, void* workspace, size_t workspace_bytes,
                               dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
+  if (cfg->kv_fmt != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;  // fp8 caches: single-query decode
   if (n_q < 1 || B < 0 || max_latents < 0 || max_latents > kMaxLatents ||
       latent_seq_stride_rows < max_latents || static_cast<int64_t>(B) * n_q > (1 << 30)) {
     return DSA_ERR_INVALID_ARG;
@@ -895,6 +907,7 @@ dsa_status_t dsa_compress_append(const dsa_config_t* cfg, int B, const int32_t* 
                                  dsa_stream_t stream) {
   DSA_TRY(check_config(cfg));
   if (cfg->ratio > 32) return DSA_ERR_UNSUPPORTED;
+  if (cfg->kv_fmt != DSA_KV_BF16) return DSA_ERR_UNSUPPORTED;  // it writes bf16 latents
   if (B < 0 || max_latents < 0 || max_latents > kMaxLatents || keys == nullptr ||
       pooled == nullptr || new_keys == nullptr) {
     return DSA_ERR_INVALID_ARG;

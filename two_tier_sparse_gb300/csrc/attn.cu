@@ -101,7 +101,9 @@ static_assert(kWgt + kMaxAttnSplits * kHeads * 4 <= kKV, "merge weights fit the 
 struct Misc {
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots], s_full[2], s_free[2], p_full[2], p_empty[2];
   uint64_t q_done, ids_ready;
+  uint64_t q_conv;                   // (fp8 cache) Q is in f16, scaled per head
   uint64_t o_done;                   // every MMA of the CTA has completed
+  alignas(16) float q_unscale[kHeads];  // (fp8 cache) kv_scale * 2^-e_h of head h
   uint32_t tmem_base;
   int abort;
   int n_sel;
@@ -146,7 +148,7 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 // p_i = 2^(scale z_i - m) (one fused multiply-add a score) packed as bf16
 // pairs into pk; returns sum_i p_i over the fp32 probabilities (four partial
 // sums)
-template <int R>
+template <int R, bool F16 = false>
 __device__ __forceinline__ float exp_pack(const float (&z)[R], float scale, float m,
                                           uint32_t (&pk)[R / 2]) {
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -154,10 +156,27 @@ __device__ __forceinline__ float exp_pack(const float (&z)[R], float scale, floa
   for (int i = 0; i < R; i += 2) {
     const float p0 = ex2_ftz(fmaf(z[i], scale, -m)), p1 = ex2_ftz(fmaf(z[i + 1], scale, -m));
     s4[(i >> 1) & 3] += p0 + p1;
-    const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
-    pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+    if constexpr (F16) {  // the PV operands of an fp8 cache are f16
+      const __half2 p2 = __floats2half2_rn(p0, p1);
+      pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+    } else {
+      const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
+      pk[i / 2] = *reinterpret_cast<const uint32_t*>(&p2);
+    }
   }
   return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
+// 8 E4M3 codes (two words, byte i = code i) -> 8 f16 (exact: every E4M3 value
+// is an f16 normal, subnormal or zero), element i in the low half of word i / 2.
+__device__ __forceinline__ uint4 e4m3x8_to_f16(uint2 c) {
+  uint4 r;
+  asm("{\n .reg .b16 a, b, c, d;\n mov.b32 {a, b}, %4;\n mov.b32 {c, d}, %5;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
+      " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n}\n"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(c.x), "r"(c.y));
+  return r;
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m,
@@ -197,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&misc->p_empty[i], 1);
     }
     mbar_init(&misc->q_done, 1);    // the TMA loads of Q (expect-tx arrival + 64 KB)
+    mbar_init(&misc->q_conv, 1);    // (fp8 cache) the math warps' conversion of Q
     mbar_init(&misc->ids_ready, 1);  // the math warps compacted the token ids
     mbar_init(&misc->o_done, 1);     // the PV issuer's last commit
     misc->abort = 0;
@@ -287,6 +307,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Compact the valid token ids (>= 0 and < n_vis) in order (math threads,
   // once the previous kernel's ids are final).
   if (tid < 128) {
+    if (a.kv_fp8) {
+      // An fp8 cache's rows become f16 operands, so Q goes to f16 too, in
+      // place, before the dependency wait (Q is an input): thread t takes head
+      // h = t / 2 in atoms 4 (t % 2) .. + 3 (the head's row of 8 chunks in
+      // each), scales the head by 2^e_h so that its largest element lies in
+      // [2^14, 2^15) (every bf16 element down to 2^-24 of it stays exact) and
+      // records kv_scale * 2^-e_h for the softmax.
+      wait_bar(&misc->q_done, 0u, misc, a.status);  // (a timeout is recorded)
+      const int h = tid >> 1;
+      const uint32_t qrow = sbase + kQ + static_cast<uint32_t>(4 * (tid & 1)) * (kHeads * 128) +
+                            static_cast<uint32_t>(h) * 128;
+      float amax = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const uint4 v = ld_shared_v4(qrow + (k >> 3) * (kHeads * 128) + (k & 7) * 16);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(vw[i] & 0xFFFF)),
+                                   fabsf(bf16_bits_to_float(vw[i] >> 16))));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      int e = 0;
+      if (amax > 0.f) {
+        const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+        e = min(126, max(-126, 14 - E));
+      }
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t addr = qrow + (k >> 3) * (kHeads * 128) + (k & 7) * 16;
+        const uint4 v = ld_shared_v4(addr);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 x = __floats2half2_rn(bf16_bits_to_float(vw[i] & 0xFFFF) * up,
+                                              bf16_bits_to_float(vw[i] >> 16) * up);
+          hw[i] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+        st_shared_v4(addr, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      }
+      if ((tid & 1) == 0) {
+        misc->q_unscale[h] = a.kv_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      }
+      fence_proxy_async_smem();  // the MMA reads Q through the async proxy
+      named_sync(kMathBar, 128);
+      if (tid == 0) mbar_arrive(&misc->q_conv);
+    }
     griddep_wait();
     const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
     constexpr int kPer = kMaxKTokens / 128;  // 4
@@ -393,22 +463,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunk lane of a row: atom lane / 8, 16-byte unit lane % 8; chunk
       // lane + 32: atom 4 + lane / 8, same unit
       const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
-#pragma unroll 4
-      for (int r = 0; r < kWarpRows; ++r) {
-        const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
-        const int row = kWarpRows * w + r;
-        const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
-        const uint32_t d1 = d0 + 4 * kAtomBytes;
-        if (arow >= 0) {
-          const uint16_t* src = (r0 + r < w_cnt ? a.swa : a.latents) + arow * kLatent + lane * 8;
-          cp_async_16(d0, src);
-          cp_async_16(d1, src + 256);
-        } else {
-          cp_async_16_zero(d0, a.latents);
-          cp_async_16_zero(d1, a.latents);
+      if (a.kv_fp8) {
+        // fp8 cache: lane l loads the row's codes [8 l, 8 l + 8) and
+        // [256 + 8 l, 256 + 8 l + 8), converts them to f16 and stores chunks
+        // l and l + 32, the places the bf16 copies fill (rows without a source:
+        // code 0, f16 zero). Eight rows' loads go out before the first store.
+        const uint8_t* lat8 = reinterpret_cast<const uint8_t*>(a.latents);
+        const uint8_t* swa8 = reinterpret_cast<const uint8_t*>(a.swa);
+#pragma unroll 1
+        for (int r8 = 0; r8 < kWarpRows; r8 += 8) {
+          uint2 lo[8], hi[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r8 + r);
+            lo[r] = make_uint2(0u, 0u);
+            hi[r] = make_uint2(0u, 0u);
+            if (arow >= 0) {
+              const uint8_t* src =
+                  (r0 + r8 + r < w_cnt ? swa8 : lat8) + arow * kLatent + lane * 8;
+              lo[r] = __ldg(reinterpret_cast<const uint2*>(src));
+              hi[r] = __ldg(reinterpret_cast<const uint2*>(src + 256));
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint32_t d0 = dstb + dcol + sw128_off(kWarpRows * w + r8 + r, lane & 7);
+            st_shared_v4(d0, e4m3x8_to_f16(lo[r]));
+            st_shared_v4(d0 + 4 * kAtomBytes, e4m3x8_to_f16(hi[r]));
+          }
         }
+        fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
+        mbar_arrive(&misc->kv_full[sl]);
+      } else {
+#pragma unroll 4
+        for (int r = 0; r < kWarpRows; ++r) {
+          const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r);
+          const int row = kWarpRows * w + r;
+          const uint32_t d0 = dstb + dcol + sw128_off(row, lane & 7);
+          const uint32_t d1 = d0 + 4 * kAtomBytes;
+          if (arow >= 0) {
+            const uint16_t* src = (r0 + r < w_cnt ? a.swa : a.latents) + arow * kLatent + lane * 8;
+            cp_async_16(d0, src);
+            cp_async_16(d1, src + 256);
+          } else {
+            cp_async_16_zero(d0, a.latents);
+            cp_async_16_zero(d1, a.latents);
+          }
+        }
+        cp_async_mbar_arrive_noinc(&misc->kv_full[sl]);
       }
-      cp_async_mbar_arrive_noinc(&misc->kv_full[sl]);
     }
     n_tiles_e = have_ids ? n_tiles : 0;
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -423,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // completed: its commit alone frees the tile's slot, and the PV issuer's
     // last commit means every MMA of the CTA has completed.
     if (lane == 0 && warp == kPvWarp) {
-      constexpr uint32_t idesc_o = mma_idesc(128, kHeads, true, true, false);
+      // f16 operands with an fp8 cache, bf16 otherwise
+      const uint32_t idesc_o = a.kv_fp8 ? mma_idesc(128, kHeads, false, true, false)
+                                        : mma_idesc(128, kHeads, true, true, false);
       for (int t = 0; t < n_tiles; ++t) {
         const int sb = t & 1;
         if (!wait_bar(&misc->p_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status)) {
@@ -451,8 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n_tiles > 0) mma_commit(&misc->o_done);  // arrives once every MMA has completed
     }
     if (lane == 0 && warp == kMmaWarp) {
-      constexpr uint32_t idesc_s = mma_idesc(128, kRows, true, false, false);
-      bool ok = n_tiles == 0 || wait_bar(&misc->q_done, 0u, misc, a.status);
+      const uint32_t idesc_s = a.kv_fp8 ? mma_idesc(128, kRows, false, false, false)
+                                        : mma_idesc(128, kRows, true, false, false);
+      // Q as loaded, or (fp8 cache) once the math warps have taken it to f16
+      bool ok = n_tiles == 0 ||
+                wait_bar(a.kv_fp8 ? &misc->q_conv : &misc->q_done, 0u, misc, a.status);
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int slot = t % kSlots, sb = t & 1;
         if (!wait_bar(&misc->kv_full[slot], static_cast<uint32_t>((t / kSlots) & 1), misc,
@@ -491,6 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // never part ways at a barrier.
     n_tiles_e = n_tiles;
     const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
+    // the softmax constant of this thread's head (fp8 cache: the head's Q
+    // scale undone and the cache scale applied)
+    const float sl = a.kv_fp8 ? a.scale_log2 * misc->q_unscale[tid & (kHeads - 1)] : a.scale_log2;
     // PV(j) is known complete through p_empty[j & 1], whose phases a thread
     // consumes in order (at most one phase ahead of its last wait), so a
     // parity wait is never more than one phase off; waiting on PV(j) early (to
@@ -511,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (ok) {
           load_scores<kRows>(la + 64 * sb, valid, z);
-          const float mt = max_scores<kRows>(z, a.scale_log2);
+          const float mt = max_scores<kRows>(z, sl);
           if (t == 0) {
             m_run = mt;
           } else if (mt > m_run + 8.f) {
@@ -554,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           uint32_t pk[kRows / 2];
           // the denominator sums the fp32 probabilities
-          l_run = l_run * alpha + exp_pack<kRows>(z, a.scale_log2, m_run, pk);
+          l_run = l_run * alpha + (a.kv_fp8 ? exp_pack<kRows, true>(z, sl, m_run, pk)
+                                            : exp_pack<kRows>(z, sl, m_run, pk));
           const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
           for (int c = 0; c < kRows / 8; ++c) {
@@ -623,7 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t inv_l_s = smem_u32(misc->inv_l);
     if (!paired) {
       if (warp < 2) {
-        misc->inv_l[tid] = l_run > 0.f ? 1.f / l_run : 0.f;
+        // (an fp8 cache's rows are code * kv_scale: O carries the scale)
+        misc->inv_l[tid] = l_run > 0.f ? (a.kv_fp8 ? a.kv_scale : 1.f) / l_run : 0.f;
         if (a.lse) {
           a.lse[static_cast<int64_t>(b) * kHeads + tid] =
               l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
@@ -719,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           wgt[q * kHeads + tid] = e;
           L = fmaf(e, x.y, L);
         }
-        const float inv_L = L > 0.f ? 1.f / L : 0.f;
+        // (an fp8 cache's rows are code * kv_scale: O carries the scale)
+        const float inv_L = L > 0.f ? (a.kv_fp8 ? a.kv_scale : 1.f) / L : 0.f;
 #pragma unroll 1
         for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
         if (a.lse && split == 0) {

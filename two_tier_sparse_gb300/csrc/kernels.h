@@ -262,6 +262,11 @@ struct AttnArgs {
   Paging pages;
   int64_t lat_rows;  // rows of the latent array (debug checks)
   int64_t swa_rows;  // rows of the window buffer (set by launch_attn; debug checks)
+  // fp8 KV cache (split kernel only): latents and window rows are E4M3 codes
+  // (512 bytes a row; the pointers above are then byte arrays) standing for
+  // code * kv_scale.
+  int kv_fp8;
+  float kv_scale;
   DeviceStatus* status;
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
