@@ -207,7 +207,8 @@ def cpu_oracle_rate(workload: str, n_seq: int, steps: int = 1):
     import synth
     spec = dict(synth.WORKLOADS[workload])
     assert spec.pop("kind") == "decode"
-    inp = synth.decode_inputs([spec["T"]] * n_seq, spec["ratio"], spec["key_fmt"], spec["seed"])
+    inp = synth.decode_inputs([spec["T"]] * n_seq, spec["ratio"], spec["key_fmt"], spec["seed"],
+                              kv_fmt=spec.get("kv_fmt", "bf16"))
     cfg = O.StepConfig(ratio=spec["ratio"])
     times = []
     for _ in range(steps):
@@ -399,9 +400,11 @@ def run_ours(args):
         B = args.batch
     # Every rank decodes its own batch: seeds differ per rank.
     t0 = time.time()
-    inp = synth.decode_inputs([T] * B, ratio, fmt, shard_seed(spec["seed"], rank))
+    kv_fmt = spec.get("kv_fmt", "bf16")
+    inp = synth.decode_inputs([T] * B, ratio, fmt, shard_seed(spec["seed"], rank), kv_fmt=kv_fmt)
     gen_s = time.time() - t0
-    cfg = dsa.config(ratio=ratio)
+    cfg = dsa.config(ratio=ratio, kv_fmt=dsa.KV_FP8_E4M3 if kv_fmt == "fp8" else dsa.KV_BF16,
+                     kv_scale=inp.kv_scale)
     cap = inp.cap
     L = int(inp.n_latents.max())
 
@@ -638,8 +641,10 @@ def run_ours(args):
     scan_avg_ms = float(np.mean(scan_ms)) if scan_ms else float("nan")
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = bytes_per_launch / (scan_avg_ms * 1e-3) / 1e9
-    # whole-step algorithmic bytes (keys scanned + latent rows gathered + window + q/out)
-    step_bytes = B * (blk_rows * row_bytes + tok_rows * row_bytes + 512 * 1024 + 128 * 1024
+    # whole-step algorithmic bytes (keys scanned + latent rows gathered + window + q/out;
+    # a latent or window row is 1024 bytes in bf16, 512 in fp8)
+    kv_row = 512 if kv_fmt == "fp8" else 1024
+    step_bytes = B * (blk_rows * row_bytes + tok_rows * row_bytes + 512 * kv_row + 128 * kv_row
                       + 64 * 512 * 2 * 2 + 16 * 128 * 2)
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "scan_traffic.json")
@@ -771,6 +776,7 @@ def run_ours(args):
                    "latents": L, "blocks": nb, "k_blocks": cfg.k_blocks,
                    "layout": f"paged, {page_rows}-token pages" if page_rows else "contiguous",
                    "k_tokens": cfg.k_tokens, "window": cfg.window, "key_fmt": fmt,
+                   "kv_fmt": kv_fmt,
                    "l2": L2Flush.DESCRIPTION,
                    "step_algorithmic_bytes": step_bytes,
                    "step_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,

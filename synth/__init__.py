@@ -440,6 +440,11 @@ WORKLOADS = {
     # block table (the paged layout serving engines use).
     "decode_b64_t131072_r1_mxfp8_paged64": dict(kind="decode", B=64, T=131072, ratio=1,
                                                 key_fmt="mxfp8", seed=2, page_rows=64),
+    # The same batch with an fp8 KV cache (latents and window rows as E4M3
+    # codes with one scale; recipes.vllm.ai "DeepSeek-V4.1-Flash", serving
+    # configurations, --kv-cache-dtype fp8).
+    "decode_b64_t131072_r1_mxfp8_fp8kv": dict(kind="decode", B=64, T=131072, ratio=1,
+                                              key_fmt="mxfp8", seed=2, kv_fmt="fp8"),
     # Multi-query decode: the 64 x 131072 batch with 5 queries a sequence (a
     # DSpark block of draft tokens verified in one pass).
     "decode_mq5_b64_t131072_r1_mxfp8": dict(kind="multi", B=64, n_q=5, T=131072, ratio=1,

@@ -184,7 +184,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
   return mbar_wait_abortable(bar, parity, &m->abort, st, SITE_ATTN);
 }
 
-template <int ROWS>
+template <int ROWS, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   using TS = TileShape<ROWS>;
@@ -307,56 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Compact the valid token ids (>= 0 and < n_vis) in order (math threads,
   // once the previous kernel's ids are final).
   if (tid < 128) {
-    if (a.kv_fp8) {
-      // An fp8 cache's rows become f16 operands, so Q goes to f16 too, in
-      // place, before the dependency wait (Q is an input): thread t takes head
-      // h = t / 2 in atoms 4 (t % 2) .. + 3 (the head's row of 8 chunks in
-      // each), scales the head by 2^e_h so that its largest element lies in
-      // [2^14, 2^15) (every bf16 element down to 2^-24 of it stays exact) and
-      // records kv_scale * 2^-e_h for the softmax.
-      wait_bar(&misc->q_done, 0u, misc, a.status);  // (a timeout is recorded)
-      const int h = tid >> 1;
-      const uint32_t qrow = sbase + kQ + static_cast<uint32_t>(4 * (tid & 1)) * (kHeads * 128) +
-                            static_cast<uint32_t>(h) * 128;
-      float amax = 0.f;
-#pragma unroll 4
-      for (int k = 0; k < 32; ++k) {
-        const uint4 v = ld_shared_v4(qrow + (k >> 3) * (kHeads * 128) + (k & 7) * 16);
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(vw[i] & 0xFFFF)),
-                                   fabsf(bf16_bits_to_float(vw[i] >> 16))));
-        }
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      int e = 0;
-      if (amax > 0.f) {
-        const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-        e = min(126, max(-126, 14 - E));
-      }
-      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-#pragma unroll 4
-      for (int k = 0; k < 32; ++k) {
-        const uint32_t addr = qrow + (k >> 3) * (kHeads * 128) + (k & 7) * 16;
-        const uint4 v = ld_shared_v4(addr);
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-        uint32_t hw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 x = __floats2half2_rn(bf16_bits_to_float(vw[i] & 0xFFFF) * up,
-                                              bf16_bits_to_float(vw[i] >> 16) * up);
-          hw[i] = *reinterpret_cast<const uint32_t*>(&x);
-        }
-        st_shared_v4(addr, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      }
-      if ((tid & 1) == 0) {
-        misc->q_unscale[h] = a.kv_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      }
-      fence_proxy_async_smem();  // the MMA reads Q through the async proxy
-      named_sync(kMathBar, 128);
-      if (tid == 0) mbar_arrive(&misc->q_conv);
-    }
     griddep_wait();
     const int32_t* tk = a.token_ids + static_cast<int64_t>(b) * a.k_tokens;
     constexpr int kPer = kMaxKTokens / 128;  // 4
@@ -402,6 +352,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 127) misc->n_sel = before;
     named_sync(kMathBar, 128);
     if (tid == 0) mbar_arrive(&misc->ids_ready);
+    if constexpr (FP8) {
+      // An fp8 cache's rows become f16 operands, so Q goes to f16 too, in
+      // place, once the ids are out (the loaders start on the tiles
+      // meanwhile; only the MMAs wait for it): thread t takes head
+      // h = t / 2 in atoms 4 (t % 2) .. + 3 (the head's row of 8 chunks in
+      // each), scales the head by 2^e_h so that its largest element lies in
+      // [2^14, 2^15) (every bf16 element down to 2^-24 of it stays exact) and
+      // records kv_scale * 2^-e_h for the softmax.
+      wait_bar(&misc->q_done, 0u, misc, a.status);  // (a timeout is recorded)
+      const int h = tid >> 1;
+      const uint32_t qrow = sbase + kQ + static_cast<uint32_t>(4 * (tid & 1)) * (kHeads * 128) +
+                            static_cast<uint32_t>(h) * 128;
+      // chunk k of the thread's 32 (atom k / 8); the order within a row is
+      // rotated by the head and the half so that the 8 lanes of a quarter
+      // warp touch 8 different 16-byte bank groups
+      auto qchunk = [&](int k) {
+        return qrow + static_cast<uint32_t>(k >> 3) * (kHeads * 128) +
+               static_cast<uint32_t>(((k & 7) + h + 4 * (tid & 1)) & 7) * 16;
+      };
+      float amax = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const uint4 v = ld_shared_v4(qchunk(k));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(vw[i] & 0xFFFF)),
+                                   fabsf(bf16_bits_to_float(vw[i] >> 16))));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      int e = 0;
+      if (amax > 0.f) {
+        const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+        e = min(126, max(-126, 14 - E));
+      }
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t addr = qchunk(k);
+        const uint4 v = ld_shared_v4(addr);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 x = __floats2half2_rn(bf16_bits_to_float(vw[i] & 0xFFFF) * up,
+                                              bf16_bits_to_float(vw[i] >> 16) * up);
+          hw[i] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+        st_shared_v4(addr, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      }
+      if ((tid & 1) == 0) {
+        misc->q_unscale[h] = a.kv_scale * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      }
+      fence_proxy_async_smem();  // the MMA reads Q through the async proxy
+      named_sync(kMathBar, 128);
+      if (tid == 0) mbar_arrive(&misc->q_conv);
+    }
   }
 
   // State the epilogue warps (math and loaders) share: the softmax statistics
@@ -422,6 +430,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp - kLoadWarp0;
     bool have_ids = false;
     int s_begin = 0, n_rows_cta = w_cnt, n_tiles = 0;
+    // An fp8 cache (32-row tiles: 8 rows a warp): lane l loads the codes
+    // [8 l, 8 l + 8) and [256 + 8 l, 256 + 8 l + 8) of each of its warp's rows
+    // into registers, and once the next tile's loads are out converts them to
+    // f16 and stores chunks l and l + 32 of the rows, the places the bf16
+    // copies fill (rows without a source: code 0, f16 zero). The load latency
+    // of one tile so overlaps the previous tile's conversion.
+    constexpr bool fp8 = FP8;
+    static_assert(!FP8 || kRows == 32, "an fp8 cache takes 32-row tiles");
+    const uint8_t* lat8 = reinterpret_cast<const uint8_t*>(a.latents);
+    const uint8_t* swa8 = reinterpret_cast<const uint8_t*>(a.swa);
+    // codes of even and of odd tiles (two register sets, so a tile's loads
+    // are never waited on before the next tile's are out)
+    uint2 alo[8], ahi[8], blo[8], bhi[8];
+    const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
+    auto fp8_load = [&](int r0t, int64_t arl, uint2 (&lo)[8], uint2 (&hi)[8]) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int64_t arow = __shfl_sync(0xFFFFFFFFu, arl, r);
+        lo[r] = make_uint2(0u, 0u);
+        hi[r] = make_uint2(0u, 0u);
+        if (arow >= 0) {
+          const uint8_t* src = (r0t + r < w_cnt ? swa8 : lat8) + arow * kLatent + lane * 8;
+          lo[r] = __ldg(reinterpret_cast<const uint2*>(src));
+          hi[r] = __ldg(reinterpret_cast<const uint2*>(src + 256));
+        }
+      }
+    };
+    auto fp8_store = [&](int tt, const uint2 (&clo)[8], const uint2 (&chi)[8]) -> bool {
+      const int slt = tt % kSlots;
+      if (tt >= kSlots &&
+          !wait_bar(&misc->kv_empty[slt], static_cast<uint32_t>(((tt / kSlots) - 1) & 1), misc,
+                    a.status)) {
+        return false;
+      }
+      const uint32_t db = sbase + kKV + slt * kSlotBytes;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t d0 = db + dcol + sw128_off(8 * w + r, lane & 7);
+        st_shared_v4(d0, e4m3x8_to_f16(clo[r]));
+        st_shared_v4(d0 + 4 * kAtomBytes, e4m3x8_to_f16(chi[r]));
+      }
+      fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
+      mbar_arrive(&misc->kv_full[slt]);
+      return true;
+    };
     for (int t = 0;; ++t) {
       const int g0 = t * kRows;
       if (!have_ids && g0 + kRows > w_cnt) {
@@ -437,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (have_ids && t >= n_tiles) break;
       const int sl = t % kSlots;
-      if (t >= kSlots &&
+      if (!fp8 && t >= kSlots &&
           !wait_bar(&misc->kv_empty[sl], static_cast<uint32_t>(((t / kSlots) - 1) & 1), misc,
                     a.status)) {
         ok = false;
@@ -460,40 +513,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // chunk lane of a row: atom lane / 8, 16-byte unit lane % 8; chunk
-      // lane + 32: atom 4 + lane / 8, same unit
-      const uint32_t dcol = static_cast<uint32_t>(lane >> 3) * kAtomBytes;
-      if (a.kv_fp8) {
-        // fp8 cache: lane l loads the row's codes [8 l, 8 l + 8) and
-        // [256 + 8 l, 256 + 8 l + 8), converts them to f16 and stores chunks
-        // l and l + 32, the places the bf16 copies fill (rows without a source:
-        // code 0, f16 zero). Eight rows' loads go out before the first store.
-        const uint8_t* lat8 = reinterpret_cast<const uint8_t*>(a.latents);
-        const uint8_t* swa8 = reinterpret_cast<const uint8_t*>(a.swa);
-#pragma unroll 1
-        for (int r8 = 0; r8 < kWarpRows; r8 += 8) {
-          uint2 lo[8], hi[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int64_t arow = __shfl_sync(0xFFFFFFFFu, arow_l, r8 + r);
-            lo[r] = make_uint2(0u, 0u);
-            hi[r] = make_uint2(0u, 0u);
-            if (arow >= 0) {
-              const uint8_t* src =
-                  (r0 + r8 + r < w_cnt ? swa8 : lat8) + arow * kLatent + lane * 8;
-              lo[r] = __ldg(reinterpret_cast<const uint2*>(src));
-              hi[r] = __ldg(reinterpret_cast<const uint2*>(src + 256));
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const uint32_t d0 = dstb + dcol + sw128_off(kWarpRows * w + r8 + r, lane & 7);
-            st_shared_v4(d0, e4m3x8_to_f16(lo[r]));
-            st_shared_v4(d0 + 4 * kAtomBytes, e4m3x8_to_f16(hi[r]));
-          }
+      // chunk lane of a row: atom lane / 8, 16-byte unit lane % 8 (dcol);
+      // chunk lane + 32: atom 4 + lane / 8, same unit
+      if constexpr (fp8) {
+        bool st_ok = true;
+        if ((t & 1) == 0) {
+          fp8_load(r0, arow_l, alo, ahi);
+          if (t > 0) st_ok = fp8_store(t - 1, blo, bhi);
+        } else {
+          fp8_load(r0, arow_l, blo, bhi);
+          st_ok = fp8_store(t - 1, alo, ahi);
         }
-        fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
-        mbar_arrive(&misc->kv_full[sl]);
+        if (!st_ok) {
+          ok = false;
+          break;
+        }
       } else {
 #pragma unroll 4
         for (int r = 0; r < kWarpRows; ++r) {
@@ -513,6 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_mbar_arrive_noinc(&misc->kv_full[sl]);
       }
     }
+    // (fp8) the last tile loaded
+    if constexpr (fp8) {
+      if (ok && have_ids && n_tiles > 0) {
+        if (!((n_tiles - 1) & 1 ? fp8_store(n_tiles - 1, blo, bhi)
+                                : fp8_store(n_tiles - 1, alo, ahi))) {
+          ok = false;
+        }
+      }
+    }
     n_tiles_e = have_ids ? n_tiles : 0;
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ---------------- MMA issuers ----------------
@@ -527,8 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // last commit means every MMA of the CTA has completed.
     if (lane == 0 && warp == kPvWarp) {
       // f16 operands with an fp8 cache, bf16 otherwise
-      const uint32_t idesc_o = a.kv_fp8 ? mma_idesc(128, kHeads, false, true, false)
-                                        : mma_idesc(128, kHeads, true, true, false);
+      constexpr uint32_t idesc_o = mma_idesc(128, kHeads, !FP8, true, false);
       for (int t = 0; t < n_tiles; ++t) {
         const int sb = t & 1;
         if (!wait_bar(&misc->p_full[sb], static_cast<uint32_t>((t >> 1) & 1), misc, a.status)) {
@@ -556,11 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n_tiles > 0) mma_commit(&misc->o_done);  // arrives once every MMA has completed
     }
     if (lane == 0 && warp == kMmaWarp) {
-      const uint32_t idesc_s = a.kv_fp8 ? mma_idesc(128, kRows, false, false, false)
-                                        : mma_idesc(128, kRows, true, false, false);
+      constexpr uint32_t idesc_s = mma_idesc(128, kRows, !FP8, false, false);
       // Q as loaded, or (fp8 cache) once the math warps have taken it to f16
       bool ok = n_tiles == 0 ||
-                wait_bar(a.kv_fp8 ? &misc->q_conv : &misc->q_done, 0u, misc, a.status);
+                wait_bar(FP8 ? &misc->q_conv : &misc->q_done, 0u, misc, a.status);
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int slot = t % kSlots, sb = t & 1;
         if (!wait_bar(&misc->kv_full[slot], static_cast<uint32_t>((t / kSlots) & 1), misc,
@@ -601,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t la = tmem_addr(tmem, static_cast<uint32_t>(32 * warp), 0);
     // the softmax constant of this thread's head (fp8 cache: the head's Q
     // scale undone and the cache scale applied)
-    const float sl = a.kv_fp8 ? a.scale_log2 * misc->q_unscale[tid & (kHeads - 1)] : a.scale_log2;
+    const float sl = FP8 ? a.scale_log2 * misc->q_unscale[tid & (kHeads - 1)] : a.scale_log2;
     // PV(j) is known complete through p_empty[j & 1], whose phases a thread
     // consumes in order (at most one phase ahead of its last wait), so a
     // parity wait is never more than one phase off; waiting on PV(j) early (to
@@ -665,8 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           uint32_t pk[kRows / 2];
           // the denominator sums the fp32 probabilities
-          l_run = l_run * alpha + (a.kv_fp8 ? exp_pack<kRows, true>(z, sl, m_run, pk)
-                                            : exp_pack<kRows>(z, sl, m_run, pk));
+          l_run = l_run * alpha + exp_pack<kRows, FP8>(z, sl, m_run, pk);
           const uint32_t pb = sbase + kP + sb * kPBytes;
 #pragma unroll
           for (int c = 0; c < kRows / 8; ++c) {
@@ -736,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!paired) {
       if (warp < 2) {
         // (an fp8 cache's rows are code * kv_scale: O carries the scale)
-        misc->inv_l[tid] = l_run > 0.f ? (a.kv_fp8 ? a.kv_scale : 1.f) / l_run : 0.f;
+        misc->inv_l[tid] = l_run > 0.f ? (FP8 ? a.kv_scale : 1.f) / l_run : 0.f;
         if (a.lse) {
           a.lse[static_cast<int64_t>(b) * kHeads + tid] =
               l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
@@ -833,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           L = fmaf(e, x.y, L);
         }
         // (an fp8 cache's rows are code * kv_scale: O carries the scale)
-        const float inv_L = L > 0.f ? (a.kv_fp8 ? a.kv_scale : 1.f) / L : 0.f;
+        const float inv_L = L > 0.f ? (FP8 ? a.kv_scale : 1.f) / L : 0.f;
 #pragma unroll 1
         for (int q = 0; q < S; ++q) wgt[q * kHeads + tid] *= inv_L;
         if (a.lse && split == 0) {
@@ -1456,7 +1496,7 @@ int attn_max_clusters(int splits) {
   int n = cache[dev][k].load(std::memory_order_relaxed);
   if (n > 0) return n;
   static std::atomic<int> smem_set[64]{};
-  if (ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set) !=
+  if (ensure_smem(reinterpret_cast<const void*>(attn_kernel<32, false>), kSmemBytes, smem_set) !=
       cudaSuccess) {
     return 0;
   }
@@ -1471,7 +1511,7 @@ int attn_max_clusters(int splits) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<32>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<32, false>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();  // clear the error the failed query left behind
     n = device_sm_count() / splits;
   }
@@ -1495,6 +1535,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       a.prefill ? (a.mq > 0 ? static_cast<uint64_t>(a.B / a.mq) * a.swa_seq_rows
                             : static_cast<uint64_t>(a.B) + a.window - 1)
                 : static_cast<uint64_t>(a.B) * a.window;
+  // an fp8 cache is read by the split kernel with 32-row tiles only
+  if (a.kv_fp8 && (a.splits == 1 || a.tile_rows != 32)) return cudaErrorInvalidValue;
   AttnArgs args = a;
   args.swa_rows = static_cast<int64_t>(wrows);
   if (a.splits == 1) {
@@ -1516,16 +1558,23 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   }
   if (a.tile_rows == 64) {
     static std::atomic<int> smem_set[64]{};
-    e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64>), kSmemBytes, smem_set);
+    e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<64, false>), kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_kernel<64>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
+    return launch_pdl(attn_kernel<64, false>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
                       a.splits, args, qmap);
   }
   if (a.tile_rows != 32) return cudaErrorInvalidValue;
   static std::atomic<int> smem_set[64]{};
-  e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32>), kSmemBytes, smem_set);
+  if (a.kv_fp8) {
+    static std::atomic<int> smem_set8[64]{};
+    e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32, true>), kSmemBytes, smem_set8);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_kernel<32, true>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
+                      a.splits, args, qmap);
+  }
+  e = ensure_smem(reinterpret_cast<const void*>(attn_kernel<32, false>), kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_kernel<32>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
+  return launch_pdl(attn_kernel<32, false>, dim3(a.B, a.splits), dim3(kThreads), kSmemBytes, s,
                     a.splits, args, qmap);
 }
 
