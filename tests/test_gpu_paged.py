@@ -112,9 +112,13 @@ def test_paged_decode_step_equals_contiguous(fmt, ratio, page_rows, k_blocks):
     check_step(inp, cfg, got, [0, 2, 4])
 
 
-def test_paged_attention_equals_contiguous():
-    inp = synth.decode_inputs([5000, 3001, 70], 1, "bf16", seed=72, q_scale=8.0)
-    cfg = dsa.config(sm_scale=8.0)
+@pytest.mark.parametrize("kv_fmt", ["bf16", "fp8"])
+def test_paged_attention_equals_contiguous(kv_fmt):
+    """Attention over a paged latent pool gives the bits of the contiguous
+    cache, with bf16 rows and with an fp8 cache (E4M3 codes, one scale)."""
+    inp = synth.decode_inputs([5000, 3001, 70], 1, "bf16", seed=72, q_scale=8.0, kv_fmt=kv_fmt)
+    cfg = dsa.config(sm_scale=8.0, kv_fmt=dsa.KV_FP8_E4M3 if kv_fmt == "fp8" else dsa.KV_BF16,
+                     kv_scale=inp.kv_scale)
     oc = oracle_cfg(cfg)
     refs = [O.decode_sequence(oc, inp, b) for b in range(inp.B)]
     ids = dev(np.stack([r["token_ids"] for r in refs]).astype(np.int32))
