@@ -125,7 +125,8 @@ typedef enum {
  * with R = page_rows for index keys and latents and R = page_rows / 8 for
  * block keys (a page of page_rows tokens holds page_rows / 8 blocks). So the
  * pools are laid out as [n_pages * R] rows of the cache's own row format
- * (latents: 512 bf16; keys: their dsa_fmt_t row, MX scales [n_pages * R, 4]).
+ * (latents: 512 bf16, or 512 E4M3 codes with an fp8 KV cache; keys: their dsa_fmt_t
+ * row, MX scales [n_pages * R, 4]).
  *   page_table:    device int32 [B, pages_per_seq]; an entry outside
  *                  [0, n_pages) is a device-detected error (DSA_ERR_DEVICE_CHECK,
  *                  the rows of that page are skipped)
@@ -244,9 +245,11 @@ dsa_status_t dsa_topk(const dsa_config_t* cfg, const void* q_idx, const float* w
  *     lse[b][h] = log sum_j exp(z_j)   (natural log; -inf when there are no rows).
  *   q:        device bf16 [B, 64, 512]
  *   latents:  device bf16, sequence b's row r at (b * latent_seq_stride_rows + r) * 512
+ *             (cfg->kv_fmt DSA_KV_FP8_E4M3: uint8 E4M3 codes, the same row layout)
  *   n_latents: device int32 [B]; an id >= n_latents[b] is flagged and skipped
  *   token_ids: device int32 [B, k_tokens], -1 entries are skipped
  *   swa:      device bf16 [B, window, 512]; slot s holds position T - swa_len[b] + s
+ *             (DSA_KV_FP8_E4M3: uint8 E4M3 codes [B, window, 512])
  *   swa_len:  device int32 [B], each in [0, window]
  *   out:      out, device bf16 [B, 64, 512]
  *   lse:      out (optional), device fp32 [B, 64]
@@ -261,7 +264,8 @@ dsa_status_t dsa_sparse_attn_decode(const dsa_config_t* cfg, const void* q, cons
 /*
  * dsa_sparse_attn_decode over a paged latent pool: latent id t of sequence b
  * is row page_table[b * pages_per_seq + t / page_rows] * page_rows + t % page_rows
- * of `latents` (bf16 [pages->n_pages * page_rows, 512]). Ids whose page entry
+ * of `latents` (bf16 [pages->n_pages * page_rows, 512], or E4M3 codes with an fp8 KV
+ * cache). Ids whose page entry
  * is out of range are skipped and reported like ids past n_latents.
  */
 dsa_status_t dsa_sparse_attn_decode_paged(const dsa_config_t* cfg, const void* q,
