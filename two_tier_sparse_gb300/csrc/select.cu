@@ -1018,10 +1018,13 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, int* launches) {
   // its own chunk (same order, same ids), so the second pass over the C * k
   // kept ids finds exactly the plain selection.
   if (a.tmp && !a.block_ids && a.k > 0) {
-    // As many chunks as keep the second pass at 16 candidates a thread (the
-    // 32-a-thread kernel spills), but enough for each chunk to fit a CTA.
+    // Enough chunks for each to fit a CTA, and for the B x C first-pass CTAs
+    // to fill the SMs (a cluster of CTAs takes the second pass's C x k ids),
+    // but at least as many as keep a one-CTA second pass at 16 candidates a
+    // thread (the 32-a-thread kernel spills).
     const int64_t c_fit = (a.n + kRegMax - 1) / kRegMax;
-    const int64_t c_pref = std::min<int64_t>(kRegMax / 2 / a.k, kMaxChunks);
+    const int64_t c_sms = std::max<int64_t>(1, device_sm_count() / std::max(1, a.B));
+    const int64_t c_pref = std::min<int64_t>(std::max<int64_t>(kRegMax / 2 / a.k, c_sms), kMaxChunks);
     const int64_t C = std::min<int64_t>(std::max(c_fit, c_pref), kRegMax / a.k);
     const int64_t chunk = (a.n + C - 1) / C;
     if (C >= 2 && chunk <= kRegMax && chunk > a.k) {
