@@ -14,7 +14,7 @@
 // each half has its own producer warp and load ring: small gathered boxes
 // stream at about twice the rate with two independent producers per SM. A
 // ring stage holds TPS of its half's tiles behind one TMA barrier (1 for bf16
-// keys, whose tiles are 32 KB; 2 or 4 for the narrower MXFP8 and MXFP4 tiles)
+// keys, whose tiles are 32 KB; 2 for the narrower MXFP8 and MXFP4 tiles)
 // because a TMA ring streams HBM fastest with about 32 KB per barrier.
 //   warps 0-1  producers: TMA tiled loads (128-byte swizzle) of the tiles' key
 //              rows: one box of 128 rows for block keys or a plain latent
@@ -91,6 +91,13 @@ struct Plan<DSA_FMT_MXFP4> {
 // Tiles per ring stage of a gathered (token-stage) scan over MX keys.
 #ifndef DSA_SCAN_GATHER_TPS
 #define DSA_SCAN_GATHER_TPS 2
+#endif
+// Tiles per ring stage of an MXFP4 scan, contiguous and gathered.
+#ifndef DSA_SCAN_MXFP4_TPS
+#define DSA_SCAN_MXFP4_TPS 2
+#endif
+#ifndef DSA_SCAN_MXFP4_GATHER_TPS
+#define DSA_SCAN_MXFP4_GATHER_TPS 2
 #endif
 
 // A ring stage: TPS tiles' codes (each 1024-byte aligned, as the 128-byte
@@ -906,8 +913,11 @@ cudaError_t launch_fmt(const ScanArgs& args, int num_sms, cudaStream_t s) {
 }  // namespace
 
 // Tiles per ring stage: bf16 tiles are 32 KB already; MXFP8 tiles (16.5 KB)
-// go two a stage and MXFP4 tiles (8.5 KB) four a stage over contiguous rows;
-// gathered scans take DSA_SCAN_GATHER_TPS MXFP8 tiles (twice as many MXFP4).
+// go two a stage, and so do MXFP4 tiles (8.5 KB): a stage is released only
+// once its last tile is converted, and four MXFP4 tiles a stage (two stages a
+// half) left the scans pipeline-bound at ~0.65 us a tile (the 64 x 131072
+// step 117.0 us against 103.8 with two a stage, three stages a half).
+// Gathered MXFP8 scans take DSA_SCAN_GATHER_TPS tiles a stage.
 cudaError_t launch_scan(const ScanArgs& args, int num_sms, cudaStream_t s) {
   const bool gather = args.mode == ROWS_GATHER || args.pages.table != nullptr;
   ScanArgs a = args;
@@ -919,8 +929,8 @@ cudaError_t launch_scan(const ScanArgs& args, int num_sms, cudaStream_t s) {
     return launch_fmt<DSA_FMT_MXFP8, 2>(a, num_sms, s);
   }
   if (a.fmt == DSA_FMT_MXFP4) {
-    if (gather) return launch_fmt<DSA_FMT_MXFP4, 2 * DSA_SCAN_GATHER_TPS>(a, num_sms, s);
-    return launch_fmt<DSA_FMT_MXFP4, 4>(a, num_sms, s);
+    if (gather) return launch_fmt<DSA_FMT_MXFP4, DSA_SCAN_MXFP4_GATHER_TPS>(a, num_sms, s);
+    return launch_fmt<DSA_FMT_MXFP4, DSA_SCAN_MXFP4_TPS>(a, num_sms, s);
   }
   return cudaErrorInvalidValue;
 }
