@@ -1,4 +1,4 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the
+"""Parity at the workloads' full sizes, in the launch configuration the
 benchmark times (dsa_decode_step with the pool tail update, dsa_sparse_attn_prefill).
 
 The oracle recomputes sampled sequences (decode) or sampled queries (prefill)
@@ -43,11 +43,14 @@ def check_all_sequences(inp, cfg, outs):
     ("decode_b64_t131072_r1_mxfp8", [0, 9, 18, 27, 37, 45, 54, 63]),
     ("decode_b8_t1048576_r1_mxfp8", [0, 3, 5, 7]),
     ("decode_b64_t131072_r1_mxfp4", [0, 21, 42, 63]),
+    ("decode_b64_t131072_r1_mxfp8_fp8kv", [0, 31, 63]),
 ])
 def test_decode_workload_full_size(workload, sample):
     spec = synth.WORKLOADS[workload]
     inp = synth.workload_inputs(workload)
-    cfg = dsa.config(ratio=spec["ratio"])
+    fp8 = spec.get("kv_fmt", "bf16") == "fp8"
+    cfg = dsa.config(ratio=spec["ratio"], kv_fmt=dsa.KV_FP8_E4M3 if fp8 else dsa.KV_BF16,
+                     kv_scale=inp.kv_scale)
     d = DecodeOnDevice(inp, cfg)
     d.pool()
     outs = run_step(d, cfg, update_pool=True)
